@@ -1,0 +1,141 @@
+"""CPU oracle for the Gated Delta Rule-2 recurrence -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The product library
+(``gated_delta_rule_166_b300``) never imports it, and nothing here imports the
+product: the two share no code.
+
+Two independent fp64 implementations of the same definition are provided:
+
+* :func:`forward` -- the plain sequential C loop in ``gdr2_oracle.c`` (threaded
+  over independent (batch, head) pairs), loaded through ctypes.
+* :func:`forward_np` -- a NumPy restatement that forms the d_k x d_k transition
+  matrix ``A_t = (I - k_t (b_t * k_t)^T) D_t`` explicitly every step.
+
+Both follow the update equation of the "Gated DeltaNet-2: Decoupling Erase and
+Write in Linear Attention" page (section "Gated Delta Rule-2 update equation")
+with the readout ``o_t = S_t^T q_t`` after the update.  Layouts: token tensors
+``[B, T, H, d]``, states ``[B, H, d_k, d_v]``.
+
+Every function is pinned by the ``-m "not gpu"`` tests (closed forms, brute
+force, hand-computed worked examples, reductions to KDA / Gated DeltaNet /
+(gated) linear attention, invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdr2_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libgdr2_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (plain -O2, no fast-math) into oracle/libgdr2_oracle.so."""
+    if force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    ):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+             "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.gdr2_oracle_forward.argtypes = [dp] * 9 + [ctypes.c_long] * 5 + [ctypes.c_int]
+        lib.gdr2_oracle_forward.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Exact upcast of a NumPy array or torch tensor (bf16/fp16/fp32/fp64) to a
+    C-contiguous float64 NumPy array."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor, possibly bf16
+        import torch
+
+        x = x.detach().to("cpu", torch.float64).contiguous().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def forward(q, k, v, b, w, g, S0=None, nthreads: int | None = None):
+    """Sequential fp64 recurrence (C).  Returns ``(o, S_T)`` as float64 arrays.
+
+    q, k, b, g: [B, T, H, dk]; v, w: [B, T, H, dv]; S0: [B, H, dk, dv] or None.
+    """
+    lib = _load()
+    q, k, v, b, w, g, S0 = (_f64(t) for t in (q, k, v, b, w, g, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", g, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        if t.shape != (B, T, H, d):
+            raise ValueError(f"{name} has shape {t.shape}, expected {(B, T, H, d)}")
+    if S0 is not None and S0.shape != (B, H, dk, dv):
+        raise ValueError(f"S0 has shape {S0.shape}, expected {(B, H, dk, dv)}")
+    o = np.empty((B, T, H, dv), dtype=np.float64)
+    ST = np.empty((B, H, dk, dv), dtype=np.float64)
+    rc = lib.gdr2_oracle_forward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(g), _ptr(S0),
+        _ptr(o), _ptr(ST), B, T, H, dk, dv,
+        int(nthreads if nthreads is not None else default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"gdr2_oracle_forward failed with code {rc}")
+    return o, ST
+
+
+def decode_step(q, k, v, b, w, g, S):
+    """One recurrence step per (batch, head).  Token tensors are [B, H, d];
+    S is [B, H, dk, dv].  Returns ``(o [B, H, dv], S_new)`` in float64.  This
+    is :func:`forward` with T = 1 (the decode step applies the same update)."""
+    q, k, v, b, w, g = (_f64(t)[:, None] for t in (q, k, v, b, w, g))
+    o, S_new = forward(q, k, v, b, w, g, S0=_f64(S))
+    return o[:, 0], S_new
+
+
+def forward_np(q, k, v, b, w, g, S0=None):
+    """Independent NumPy fp64 restatement: per step, form the d_k x d_k
+    transition ``A_t = (I - k_t (b_t * k_t)^T) diag(exp g_t)`` and apply
+    ``S_t = A_t S_{t-1} + k_t (w_t * v_t)^T``; read out ``o_t = S_t^T q_t``.
+    Vectorised over (batch, head); intended for small cases."""
+    q, k, v, b, w, g, S0 = (_f64(t) for t in (q, k, v, b, w, g, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    S = np.zeros((B, H, dk, dv)) if S0 is None else S0.copy()
+    eye = np.eye(dk)
+    o = np.empty((B, T, H, dv))
+    for t in range(T):
+        kt, bt, gt, qt = k[:, t], b[:, t], g[:, t], q[:, t]
+        erase = eye - kt[..., :, None] * (bt * kt)[..., None, :]      # I - k (b*k)^T
+        A = erase * np.exp(gt)[..., None, :]                           # (...) D_t
+        S = A @ S + kt[..., :, None] * (w[:, t] * v[:, t])[..., None, :]
+        o[:, t] = np.einsum("bhij,bhi->bhj", S, qt)
+    return o, S
