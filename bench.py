@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of the Gated Delta Rule-2 hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one gdr2_forward over the GDN-2 1.3B layer workload (B=4, H=16,
+T=4096, d_k=d_v=128, bf16 inputs, fp32 state, zero S0): 16,384 tokens per
+step.  The headline value is tokens/s with inputs resident in HBM (402 MB of
+inputs > the 126 MB L2, so no flush is needed between steps).  The same JSON
+line carries:
+
+* roofline: the prefill kernel's algorithmic bytes per launch / its mean
+  CUDA-event duration, against the measured HBM copy bandwidth;
+* decode: the in-place decode step (B=256, H=16, d=128, fp32 state of 268 MB)
+  over 1024 consecutive steps, in HBM GB/s, with its own roofline;
+* e2e: the same prefill through the public API from pinned host buffers, the
+  host->device copies of the step's inputs and the device->host copies of o
+  and S_T inside the timed region;
+* cpu_baseline: the fp64 CPU oracle (as it stands) on a bounded sample of the
+  same workload on the host cores;
+* clocks: nvidia-smi samples taken during the timed region.
+
+Under torchrun (N > 1) every rank runs its own independent batch (weak
+scaling, no collective on the data path); timing is bracketed by barriers and
+the slowest rank's time is reported.  ``--impl reference`` times the CPU
+oracle instead (rank 0 only) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "GDR-2 fwd tokens/sec at H16 d128 T4K (1×B300); % of roofline; decode GB/s"
+WORKLOAD = "gdn2_layer_T4096"
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+
+# --------------------------------------------------------------------------
+# algorithmic work per launch
+# --------------------------------------------------------------------------
+def prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=False, st=True):
+    """Bytes a perfect prefill must move: the six token inputs read once (esz
+    bytes each), o written once (osz bytes), S0 read (if given) and S_T
+    written once (fp32)."""
+    tok = B * T * H * (4 * dk + 2 * dv) * esz + B * T * H * dv * osz
+    state = B * H * dk * dv * 4
+    return tok + (state if s0 else 0) + (state if st else 0)
+
+
+def prefill_flops(B, T, H, dk, dv, C=64):
+    """Algorithmic flops of the chunked form per token-head:
+    6*dk*dv (three dk x dv state products) + 3*C*dk + 2*C*dv (the C x C
+    triangular intra-chunk products counted at half)."""
+    return B * T * H * (6 * dk * dv + 3 * C * dk + 2 * C * dv)
+
+
+def decode_bytes(B, H, dk, dv, esz=2, osz=4):
+    """Per decode step: the fp32 state read and written, six token inputs
+    read, o written."""
+    return B * H * (2 * dk * dv * 4 + (4 * dk + 2 * dv) * esz + dv * osz)
+
+
+# --------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_166_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel_key):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+def bench_prefill(gdr2, x, steps, warmup, world):
+    B, T, H, dk = x.q.shape
+    dv = x.v.shape[-1]
+    stream = torch.cuda.current_stream()
+    o = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        gdr2.forward(*x.tensors(), x.S0, o=o, S_T=ST)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        gdr2.forward(*x.tensors(), x.S0, o=o, S_T=ST)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    if gdr2.gdr2_device_status() != 0:
+        raise RuntimeError("device-side failure during the timed prefill")
+    return total_ms / steps, per_launch, steps
+
+
+def bench_decode(gdr2, steps=1024, pool=16, seed=5):
+    from gated_delta_rule_166_b300.inputs import DECODE_WORKLOAD, make_decode_state, make_decode_token
+
+    W = DECODE_WORKLOAD
+    B, H, dk, dv = W["B"], W["H"], W["dk"], W["dv"]
+    S = make_decode_state(B, H, dk, dv, seed=seed).cuda()
+    toks = [make_decode_token(B, H, dk, dv, seed=seed, step=s).to("cuda") for s in range(pool)]
+    o = torch.empty((B, H, dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for s in range(8):
+        gdr2.decode_step(*toks[s % pool].tensors(), S, o=o)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(steps):
+        gdr2.decode_step(*toks[s % pool].tensors(), S, o=o)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if gdr2.gdr2_device_status() != 0:
+        raise RuntimeError("device-side failure during decode")
+    ms = a.elapsed_time(b)
+    per_step_s = ms / 1e3 / steps
+    nbytes = decode_bytes(B, H, dk, dv)
+    return {"workload": f"decode B{B} H{H} d{dk} fp32 state, {steps} in-place steps",
+            "gbs": nbytes / per_step_s / 1e9, "us_per_step": per_step_s * 1e6,
+            "tokens_per_s": B * steps / (ms / 1e3), "bytes_per_step": nbytes,
+            "launches": steps, "input_pool": pool}
+
+
+def bench_e2e(gdr2, x_host, steps, warmup):
+    """Pinned host inputs -> device -> gdr2_forward -> o and S_T back to host."""
+    B, T, H, dk = x_host.q.shape
+    dv = x_host.v.shape[-1]
+    pinned = [t.pin_memory() for t in x_host.tensors()]
+    dev_in = [torch.empty_like(t, device="cuda") for t in pinned]
+    o_h = torch.empty((B, T, H, dv), dtype=torch.float32).pin_memory()
+    S_h = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+    o_d = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    S_d = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, d in zip(pinned, dev_in):
+            d.copy_(h, non_blocking=True)
+        gdr2.forward(*dev_in, None, o=o_d, S_T=S_d)
+        o_h.copy_(o_d, non_blocking=True)
+        S_h.copy_(S_d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+    return ms, h2d, d2h
+
+
+def oracle_sample(x, pairs):
+    """Run the oracle on the (batch, head) pairs in `pairs`; returns seconds,
+    token-heads processed and threads used."""
+    import oracle
+
+    idx_b = sorted({p[0] for p in pairs})
+    hs = sorted({p[1] for p in pairs})
+    sel = [t[idx_b][:, :, hs].contiguous() for t in x.tensors()]
+    S0 = None if x.S0 is None else x.S0[idx_b][:, hs].contiguous()
+    threads = min(oracle.default_threads(), len(idx_b) * len(hs))
+    oracle.build()
+    t = time.perf_counter()
+    oracle.forward(*sel, S0, nthreads=threads)
+    dt = time.perf_counter() - t
+    return dt, len(idx_b) * len(hs) * x.q.shape[1], threads
+
+
+def cpu_baseline(x, budget_s=15.0):
+    """Time the oracle on a bounded sample: whole sequences of as many heads
+    as fit ~budget_s, taken from batch 0 first."""
+    B, T, H, _ = x.q.shape
+    probe = [(0, 0)]
+    dt, th, _ = oracle_sample(x, probe)
+    rate1 = th / max(dt, 1e-6)                       # token-heads/s on one thread
+    import oracle
+
+    cores = oracle.default_threads()
+    n_pairs = max(1, min(B * H, int(budget_s * rate1 * cores / T)))
+    pairs = [(i // H, i % H) for i in range(n_pairs)]
+    if n_pairs >= H:                                 # whole batch rows
+        n_rows = n_pairs // H
+        pairs = [(bi, h) for bi in range(n_rows) for h in range(H)]
+    dt, tokheads, threads = oracle_sample(x, pairs)
+    return {"value": (tokheads / H) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(pairs)} of {B * H} (batch, head) sequences x {T} tokens "
+                      f"({tokheads} token-heads, {dt:.1f} s)"}
+
+
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from gated_delta_rule_166_b300.inputs import WORKLOADS, make_workload
+
+    cfg = WORKLOADS[WORKLOAD]
+    B, T, H, dk, dv = cfg["B"], cfg["T"], cfg["H"], cfg["dk"], cfg["dv"]
+    config = {"workload": f"{WORKLOAD}: B={B} H={H} T={T} d_k=d_v={dk}, bf16 inputs, "
+                          f"fp32 state and fp32 o, S0=0, chunk 64",
+              "global_batch": B, "seq_len": T, "heads": H, "head_dim": dk,
+              "l2": "inputs (402 MB) larger than L2 (126 MB); no flush"}
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return
+        x = make_workload(WORKLOAD)
+        # each step: the oracle over one batch row of whole sequences (16 heads x 4096 tokens)
+        pairs = [(0, h) for h in range(H)]
+        times, tokheads, threads = [], 0, 0
+        for s in range(args.steps):
+            row = s % B
+            dt, th, threads = oracle_sample(x, [(row, h) for h in range(H)])
+            times.append(dt)
+            tokheads = th
+        ms = 1e3 * sum(times) / len(times)
+        value = (tokheads / H) / (ms / 1e3)
+        sample = f"per step: batch row ({H} heads x {T} tokens) of {WORKLOAD}, fp64 oracle"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    world, rank, local = dist_setup(args)
+    import gated_delta_rule_166_b300 as gdr2
+
+    hbm_gbs, bf16_tflops, peak_src = load_peaks()
+    x_host = make_workload(WORKLOAD, seed=cfg["seed"] + rank)
+    x = x_host.to("cuda")
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        ms, per_launch, launches = bench_prefill(gdr2, x, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    ms_max = max_over_ranks(ms, world)
+    tokens = B * T
+    value = world * tokens / (ms_max / 1e3)
+
+    kern_ms = sum(per_launch) / len(per_launch)
+    nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=False, st=True)
+    nflops = prefill_flops(B, T, H, dk, dv)
+    achieved = nbytes / (kern_ms / 1e3) / 1e9
+    traffic = traffic_record("prefill_" + WORKLOAD)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": traffic,
+                "kernel": "gdr2 prefill", "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                "algorithmic_bytes_per_launch": nbytes,
+                "tflops": nflops / (kern_ms / 1e3) / 1e12,
+                "tensor_frac_of_bf16_peak": nflops / (kern_ms / 1e3) / 1e12 / bf16_tflops}
+
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded; distributions of the GDN-2 layer workload)",
+           "config": config, "roofline": roofline, "clocks": clocks,
+           "gpu_launches": launches}
+
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        out["e2e"] = {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": e2e_ms}
+    if not args.no_decode:
+        dec = bench_decode(gdr2)
+        dec["roofline"] = {"bound": "hbm", "achieved": dec["gbs"], "peak": hbm_gbs, "unit": "GB/s",
+                           "frac": dec["gbs"] / hbm_gbs,
+                           "traffic": traffic_record("decode_B256_H16_d128")}
+        out["decode"] = dec
+        out["gpu_launches"] = launches  # timed prefill region only; decode launches in out["decode"]
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(x_host)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,19 @@
+"""B300-native (sm_103a) Gated Delta Rule-2: chunked prefill and decode.
+
+    S_t = (I - k_t (b_t * k_t)^T) D_t S_{t-1} + k_t (w_t * v_t)^T,   o_t = S_t^T q_t
+
+The computation lives in libgdr2.so (hand-written CUDA, C ABI in
+include/gdr2.h); this package is its thin Python binding plus the seeded
+synthetic input generators used by the tests and the bench.
+"""
+from ._lib import (  # noqa: F401
+    GDR2Error,
+    GDR2LibraryError,
+    gdr2_decode_step,
+    gdr2_device_status,
+    gdr2_forward,
+    gdr2_version,
+)
+
+forward = gdr2_forward
+decode_step = gdr2_decode_step

@@ -1,0 +1,168 @@
+"""ctypes binding over libgdr2.so (the C ABI declared in include/gdr2.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their device pointers and the current CUDA stream are passed to
+the C entry points, and a non-zero status becomes an exception.  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU path.  If
+the library is missing the call fails loudly (GDR2LibraryError).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdr2.so")
+
+GDR2_F32, GDR2_BF16 = 0, 1
+_DTYPES = {torch.float32: GDR2_F32, torch.bfloat16: GDR2_BF16}
+_lib = None
+
+
+class GDR2LibraryError(RuntimeError):
+    """libgdr2.so is missing or cannot be loaded."""
+
+
+class GDR2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise GDR2LibraryError(
+                f"{LIB_PATH} not found: build it with `python -m gated_delta_rule_166_b300.build`")
+        try:
+            L = ctypes.CDLL(LIB_PATH)
+        except OSError as e:  # pragma: no cover
+            raise GDR2LibraryError(f"cannot load {LIB_PATH}: {e}") from e
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.gdr2_forward.argtypes = [vp] * 9 + [i64] * 5 + [ci, ci, vp]
+        L.gdr2_forward.restype = ci
+        L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
+        L.gdr2_decode_step.restype = ci
+        L.gdr2_device_status.argtypes = [vp]
+        L.gdr2_device_status.restype = ci
+        L.gdr2_status_string.argtypes = [ci]
+        L.gdr2_status_string.restype = ctypes.c_char_p
+        L.gdr2_version.argtypes = []
+        L.gdr2_version.restype = ci
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gdr2_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tokens(name, t, shape, dtype, device):
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gdr2_forward(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
+                 out_dtype=torch.float32, return_state: bool = True, stream=None):
+    """Chunked prefill.  q, k, b, log_decay: [B, T, H, dk]; v, w: [B, T, H, dv]
+    (all fp32 or all bf16, on one CUDA device); S0: [B, H, dk, dv] fp32 or None.
+    Returns ``(o, S_T)`` with o in ``out_dtype`` (fp32 by default, or bf16);
+    S_T is None when ``return_state`` is False.  ``o`` and ``S_T`` may be passed
+    in to reuse buffers (``S_T is S0`` updates in place)."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q and v must be [B, T, H, d]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_forward runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (B, T, H, d), dtype, dev)
+    if S0 is not None:
+        _check_tokens("S0", S0, (B, H, dk, dv), torch.float32, dev)
+    if o is None:
+        if out_dtype not in _DTYPES:
+            raise ValueError(f"unsupported out_dtype {out_dtype}")
+        o = torch.empty((B, T, H, dv), dtype=out_dtype, device=dev)
+    else:
+        if o.dtype not in _DTYPES:
+            raise ValueError(f"unsupported o dtype {o.dtype}")
+        _check_tokens("o", o, (B, T, H, dv), o.dtype, dev)
+    if S_T is None and return_state:
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    elif S_T is not None:
+        _check_tokens("S_T", S_T, (B, H, dk, dv), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().gdr2_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
+                                _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv,
+                                _DTYPES[dtype], _DTYPES[o.dtype],
+                                ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_forward")
+    return o, S_T
+
+
+def gdr2_decode_step(q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.float32,
+                     stream=None):
+    """One decode step, S updated in place.  q, k, b, log_decay: [B, H, dk];
+    v, w: [B, H, dv]; S: [B, H, dk, dv] fp32.  Returns o [B, H, dv] in
+    ``out_dtype`` (fp32 by default, or bf16)."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q and v must be [B, H, d]")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_decode_step runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (B, H, d), dtype, dev)
+    _check_tokens("S", S, (B, H, dk, dv), torch.float32, dev)
+    if o is None:
+        if out_dtype not in _DTYPES:
+            raise ValueError(f"unsupported out_dtype {out_dtype}")
+        o = torch.empty((B, H, dv), dtype=out_dtype, device=dev)
+    else:
+        if o.dtype not in _DTYPES:
+            raise ValueError(f"unsupported o dtype {o.dtype}")
+        _check_tokens("o", o, (B, H, dv), o.dtype, dev)
+    with torch.cuda.device(dev):
+        st = lib().gdr2_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
+                                    _ptr(S), _ptr(o), B, H, dk, dv, _DTYPES[dtype],
+                                    _DTYPES[o.dtype], ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_decode_step")
+    return o
+
+
+def gdr2_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side status."""
+    return lib().gdr2_device_status(ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gdr2_version() -> int:
+    return lib().gdr2_version()

@@ -1,0 +1,178 @@
+// C ABI of libgdr2: host-side validation, dispatch, and the device error word.
+#include <mutex>
+
+#include "gdr2.h"
+#include "gdr2_internal.cuh"
+
+namespace gdr2 {
+namespace {
+
+// Device word where bounded waits record a failure (kDevTimeout).  It lives in
+// the module's static device memory: nothing is allocated for it.
+__device__ int g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_addr[kMaxDevices] = {};
+int g_cc_ok[kMaxDevices] = {};   // 0 unknown, 1 sm_103, -1 other
+
+// Address of the error word on the current device (looked up once per device,
+// with that device current) and a check that the device is an sm_103 part.
+int device_setup(int** err_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR2_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_cc_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return GDR2_ERR_CUDA;
+        g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_cc_ok[dev] != 1) return GDR2_ERR_UNSUPPORTED;
+    if (!g_err_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return GDR2_ERR_CUDA;
+        g_err_addr[dev] = static_cast<int*>(p);
+    }
+    if (err_out) *err_out = g_err_addr[dev];
+    return GDR2_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool head_dim_ok(int64_t d) { return d == 32 || d == 64 || d == 128; }
+bool dtype_ok(int t) { return t == GDR2_F32 || t == GDR2_BF16; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+}  // namespace
+}  // namespace gdr2
+
+using namespace gdr2;
+
+extern "C" int gdr2_forward(const void* q, const void* k, const void* v,
+                            const void* b, const void* w, const void* log_decay,
+                            const float* S0, void* o, float* S_T,
+                            int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                            int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (B < 0 || T < 0 || H < 0) return GDR2_ERR_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
+    const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
+    const size_t osz = out_dtype == GDR2_F32 ? 4 : 2;
+    int64_t bth = 0, bh = 0, nk = 0, nv = 0, ns = 0;
+    if (!mul_ok(B, T, &bth) || !mul_ok(bth, H, &bth) || !mul_ok(B, H, &bh) ||
+        !mul_ok(bth, dk, &nk) || !mul_ok(bth, dv, &nv) || !mul_ok(bh, dk * dv, &ns) ||
+        nk > INT64_MAX / 4 || ns > INT64_MAX / 4)
+        return GDR2_ERR_SHAPE;
+    const bool has_tokens = bth > 0;
+    if (has_tokens && (!q || !k || !v || !b || !w || !log_decay || !o)) return GDR2_ERR_ARG;
+    for (const void* p : {q, k, v, b, w, log_decay, (const void*)S0, (const void*)o, (const void*)S_T})
+        if (p && !aligned16(p)) return GDR2_ERR_ALIGN;
+
+    const size_t bk = (size_t)nk * esz, bv = (size_t)nv * esz, bs = (size_t)ns * 4;
+    const size_t bo = (size_t)nv * osz;
+    const void* tok_in[6] = {q, k, b, log_decay, v, w};
+    const size_t tok_bytes[6] = {bk, bk, bk, bk, bv, bv};
+    if (has_tokens) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(o, bo, tok_in[i], tok_bytes[i])) return GDR2_ERR_ALIAS;
+        if (overlaps(o, bo, S0, bs) || overlaps(o, bo, S_T, bs)) return GDR2_ERR_ALIAS;
+    }
+    for (int i = 0; i < 6; ++i)
+        if (has_tokens && overlaps(S_T, bs, tok_in[i], tok_bytes[i])) return GDR2_ERR_ALIAS;
+    if (S_T && S0 && S_T != S0 && overlaps(S_T, bs, S0, bs)) return GDR2_ERR_ALIAS;
+
+    int* err = nullptr;
+    int st = device_setup(&err);
+    if (st != GDR2_OK) return st;
+    if (bh == 0) return GDR2_OK;
+
+    if (T == 0) {   // no tokens: S_T = S0 (or zeros)
+        if (!S_T) return GDR2_OK;
+        cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
+                                        : cudaMemcpyAsync(S_T, S0, bs, cudaMemcpyDeviceToDevice, stream))
+                           : cudaMemsetAsync(S_T, 0, bs, stream);
+        return e == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+    }
+
+    ForwardArgs a{q, k, v, b, w, log_decay, S0, o, S_T, B, T, H, dk, dv, in_dtype, out_dtype};
+    if (chunked_bf16_supports(a)) return launch_chunked_bf16(a, stream, err);
+    return launch_recurrent(a, stream);
+}
+
+extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,
+                                const void* b, const void* w, const void* log_decay,
+                                float* S, void* o,
+                                int64_t B, int64_t H, int64_t dk, int64_t dv,
+                                int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (B < 0 || H < 0) return GDR2_ERR_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
+    int64_t bh = 0, tmp = 0;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, dk * dv, &tmp) || tmp > INT64_MAX / 4 ||
+        bh > 0x7fffffffLL)
+        return GDR2_ERR_SHAPE;
+    if (bh > 0 && (!q || !k || !v || !b || !w || !log_decay || !S || !o)) return GDR2_ERR_ARG;
+    for (const void* p : {q, k, v, b, w, log_decay, (const void*)S, (const void*)o})
+        if (p && !aligned16(p)) return GDR2_ERR_ALIGN;
+    const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
+    const size_t osz = out_dtype == GDR2_F32 ? 4 : 2;
+    const size_t bk = (size_t)(bh * dk) * esz, bv = (size_t)(bh * dv) * esz, bs = (size_t)tmp * 4;
+    const size_t bo = (size_t)(bh * dv) * osz;
+    const void* ins[6] = {q, k, b, log_decay, v, w};
+    const size_t nb[6] = {bk, bk, bk, bk, bv, bv};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, bo, ins[i], nb[i]) || overlaps(S, bs, ins[i], nb[i])) return GDR2_ERR_ALIAS;
+    if (overlaps(o, bo, S, bs)) return GDR2_ERR_ALIAS;
+
+    int st = device_setup(nullptr);
+    if (st != GDR2_OK) return st;
+    if (bh == 0) return GDR2_OK;
+    DecodeArgs a{q, k, v, b, w, log_decay, S, o, B, H, dk, dv, in_dtype, out_dtype};
+    return launch_decode(a, stream);
+}
+
+extern "C" int gdr2_device_status(cudaStream_t stream) {
+    int* err = nullptr;
+    int st = device_setup(&err);
+    if (st != GDR2_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GDR2_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDR2_ERR_CUDA;
+    if (h != kDevOk) {
+        const int zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return GDR2_ERR_CUDA;
+        return GDR2_ERR_TIMEOUT;
+    }
+    return GDR2_OK;
+}
+
+extern "C" const char* gdr2_status_string(int status) {
+    switch (status) {
+        case GDR2_OK: return "GDR2_OK";
+        case GDR2_ERR_ARG: return "GDR2_ERR_ARG: null pointer or negative size";
+        case GDR2_ERR_SHAPE: return "GDR2_ERR_SHAPE: unsupported head dim or size overflow";
+        case GDR2_ERR_ALIGN: return "GDR2_ERR_ALIGN: pointer not 16-byte aligned";
+        case GDR2_ERR_UNSUPPORTED: return "GDR2_ERR_UNSUPPORTED: unknown dtype or device is not sm_103";
+        case GDR2_ERR_CUDA: return "GDR2_ERR_CUDA: a CUDA runtime call failed";
+        case GDR2_ERR_TIMEOUT: return "GDR2_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case GDR2_ERR_ALIAS: return "GDR2_ERR_ALIAS: output buffer overlaps another argument";
+        default: return "GDR2: unknown status";
+    }
+}
+
+extern "C" int gdr2_version(void) { return 100; }

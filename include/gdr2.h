@@ -1,0 +1,135 @@
+/*
+ * gdr2.h -- C ABI of the B300 (sm_103a) Gated Delta Rule-2 library (libgdr2.so).
+ *
+ * The operation ("Gated DeltaNet-2: Decoupling Erase and Write in Linear
+ * Attention" page, section "Gated Delta Rule-2 update equation", and the
+ * symbol table under it):
+ *
+ *     S_t = (I - k_t (b_t (.) k_t)^T) D_t S_{t-1} + k_t (w_t (.) v_t)^T
+ *     o_t = S_t^T q_t                       (readout after the update)
+ *
+ *   S_t       per-head d_k x d_v fast-weight memory, fp32 in this library
+ *   k_t, q_t  key / query, d_k channels (keys are expected L2-normalised by the
+ *             caller, as the page's symbol table states; nothing is normalised
+ *             or scaled inside)
+ *   b_t       erase gate over the d_k key channels   (used as given: no
+ *             sigmoid, no clamp -- the page's ablation widens it to [0, 2])
+ *   w_t       write gate over the d_v value channels (used as given)
+ *   D_t       diag(exp(log_decay_t)), log_decay_t over the d_k key channels
+ *
+ * Special cases named on the same page: b = w = one scalar gives KDA; a scalar
+ * decay in addition gives Gated DeltaNet.  Both run through the same calls.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *   row-major and contiguous, 16-byte aligned.  The caller owns every buffer;
+ *   the library allocates no device memory and keeps no pointer after return.
+ * - in_dtype selects the element type of the six token inputs and out_dtype
+ *   that of o: GDR2_F32 (float) or GDR2_BF16 (__nv_bfloat16).  States are
+ *   always fp32.  All arithmetic is fp32 (bf16 only as tensor-core operands
+ *   on the chunked bf16 path).  out_dtype = GDR2_F32 keeps o at accumulation
+ *   precision; GDR2_BF16 halves its bytes at the cost of one bf16 rounding
+ *   (relative 2^-9) per element.
+ * - Supported head dims: d_k, d_v in {32, 64, 128}.
+ * - Calls are asynchronous on `stream` (0 = legacy default stream): they
+ *   validate on the host, enqueue kernels and return.  Argument errors are
+ *   reported before anything is enqueued and leave every buffer untouched.
+ * - Device-side failures (a bounded wait that timed out) are recorded in a
+ *   per-library device word and reported by gdr2_device_status().
+ * - Nothing throws across the ABI; every call returns a gdr2_status.
+ */
+#ifndef GDR2_H_
+#define GDR2_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDR2_F32 = 0,
+    GDR2_BF16 = 1
+} gdr2_dtype;
+
+typedef enum {
+    GDR2_OK = 0,
+    GDR2_ERR_ARG = -1,          /* null pointer where one is required, negative size */
+    GDR2_ERR_SHAPE = -2,        /* head dims outside {32, 64, 128}, size overflow     */
+    GDR2_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned                   */
+    GDR2_ERR_UNSUPPORTED = -4,  /* unknown in/out dtype; device is not sm_103         */
+    GDR2_ERR_CUDA = -5,         /* a CUDA runtime call failed (launch, attribute)     */
+    GDR2_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up                 */
+    GDR2_ERR_ALIAS = -7         /* o overlaps an input, or S_T overlaps a token input */
+} gdr2_status;
+
+/*
+ * gdr2_forward -- chunked prefill over a whole sequence.
+ *
+ * Applies the update above for t = 0 .. T-1 to every (batch, head) pair,
+ * starting from S0, writes every o_t and (optionally) the final state.
+ * The page's "efficient implementation" section (WY form with decay
+ * absorption, chunkwise algorithm) describes the method used for bf16 inputs:
+ * fixed 64-token chunks, a per-chunk UT/WY transform with the cumulative
+ * channel decay folded into the rank-1 erase factors, and an fp32 state
+ * carried across chunks on chip.  fp32 inputs run a token-sequential fp32
+ * kernel.
+ *
+ *   q, k, b, log_decay : [B, T, H, dk]  (in_dtype)
+ *   v, w               : [B, T, H, dv]  (in_dtype)
+ *   S0                 : [B, H, dk, dv] fp32, or NULL for a zero initial state
+ *   o                  : [B, T, H, dv]  (out_dtype), written
+ *   S_T                : [B, H, dk, dv] fp32, written, or NULL (not stored)
+ *
+ * T = 0 is allowed: S_T receives S0 (or zeros) and o is untouched.
+ * S0 == S_T (in-place state update) is allowed; any other overlap between S_T
+ * or o and another argument is rejected with GDR2_ERR_ALIAS.
+ * Precondition (not checked): log_decay <= 0 and finite.
+ */
+int gdr2_forward(const void* q, const void* k, const void* v,
+                 const void* b, const void* w, const void* log_decay,
+                 const float* S0, void* o, float* S_T,
+                 int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                 int in_dtype, int out_dtype, cudaStream_t stream);
+
+/*
+ * gdr2_decode_step -- one autoregressive step for every (batch, head), the
+ * state updated in place (same equation, one token):
+ *
+ *     S' = D S,  r = S'^T (b (.) k),  p = S'^T q,  delta = w (.) v - r,
+ *     S  <- S' + k delta^T,           o = p + (k . q) delta  ( = S^T q )
+ *
+ *   q, k, b, log_decay : [B, H, dk]  (in_dtype)
+ *   v, w               : [B, H, dv]  (in_dtype)
+ *   S                  : [B, H, dk, dv] fp32, read and overwritten
+ *   o                  : [B, H, dv]  (out_dtype), written
+ *
+ * The fp32 state is streamed once from HBM and written once (128-bit
+ * accesses); o must not overlap any other argument.
+ */
+int gdr2_decode_step(const void* q, const void* k, const void* v,
+                     const void* b, const void* w, const void* log_decay,
+                     float* S, void* o,
+                     int64_t B, int64_t H, int64_t dk, int64_t dv,
+                     int in_dtype, int out_dtype, cudaStream_t stream);
+
+/*
+ * gdr2_device_status -- synchronises `stream`, then returns GDR2_OK, the
+ * recorded device-side failure (GDR2_ERR_TIMEOUT) or GDR2_ERR_CUDA if the
+ * stream reports a CUDA error.  Reading clears the recorded failure.
+ */
+int gdr2_device_status(cudaStream_t stream);
+
+/* Human-readable name of a gdr2_status value (static storage). */
+const char* gdr2_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int gdr2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR2_H_ */

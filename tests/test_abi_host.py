@@ -1,0 +1,111 @@
+"""The C ABI on the host: the library loads, exports every entry point that
+include/gdr2.h declares, and rejects bad arguments before touching a device.
+No CUDA device is needed: the pointers below are never dereferenced because
+validation fails first."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_166_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr2.h")
+
+OK, ARG, SHAPE, ALIGN, UNSUP, CUDA, TIMEOUT, ALIAS = 0, -1, -2, -3, -4, -5, -6, -7
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr2_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = _lib.lib()
+    names = declared_functions()
+    assert {"gdr2_forward", "gdr2_decode_step", "gdr2_device_status"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"libgdr2.so does not export {n}"
+
+
+def test_status_strings_and_version():
+    for s in (OK, ARG, SHAPE, ALIGN, UNSUP, CUDA, TIMEOUT, ALIAS):
+        assert _lib.status_string(s).startswith("GDR2")
+    assert _lib.gdr2_version() >= 100
+
+
+# fake, never-dereferenced device addresses (16-byte aligned, far apart)
+BASE = 1 << 40
+GAP = 1 << 32
+
+
+def fwd_args(B=1, T=4, H=2, dk=64, dv=64, dtype=1, out_dtype=0, **over):
+    p = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in
+         enumerate(["q", "k", "v", "b", "w", "g", "S0", "o", "ST"])}
+    p.update(over)
+    return ([p[n] for n in ["q", "k", "v", "b", "w", "g", "S0", "o", "ST"]]
+            + [B, T, H, dk, dv, dtype, out_dtype, None])
+
+
+def call_fwd(**kw):
+    return _lib.lib().gdr2_forward(*fwd_args(**kw))
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 64), (64, 96), (256, 128), (0, 32)])
+def test_forward_rejects_head_dims(dk, dv):
+    assert call_fwd(dk=dk, dv=dv) == SHAPE
+
+
+def test_forward_rejects_negative_sizes_and_dtype():
+    assert call_fwd(B=-1) == ARG
+    assert call_fwd(T=-3) == ARG
+    assert call_fwd(dtype=7) == UNSUP
+    assert call_fwd(out_dtype=3) == UNSUP
+
+
+def test_forward_rejects_null_token_pointer():
+    for n in ("q", "k", "v", "b", "w", "g", "o"):
+        assert call_fwd(**{n: None}) == ARG, n
+
+
+def test_forward_rejects_misaligned_pointer():
+    for n in ("q", "v", "S0", "o", "ST"):
+        assert call_fwd(**{n: ctypes.c_void_p(BASE + 7 * GAP + 8)}) == ALIGN, n
+
+
+def test_forward_rejects_aliasing():
+    # o overlapping q, o overlapping S0, S_T overlapping a token input, S_T straddling S0
+    assert call_fwd(o=ctypes.c_void_p(BASE)) == ALIAS
+    assert call_fwd(o=ctypes.c_void_p(BASE + 6 * GAP)) == ALIAS
+    assert call_fwd(ST=ctypes.c_void_p(BASE + 1 * GAP + 64)) == ALIAS
+    assert call_fwd(ST=ctypes.c_void_p(BASE + 6 * GAP + 16)) == ALIAS
+
+
+def test_forward_size_overflow():
+    assert call_fwd(B=1 << 40, T=1 << 30) == SHAPE
+
+
+def test_decode_rejects_bad_args():
+    L = _lib.lib()
+    p = [ctypes.c_void_p(BASE + i * GAP) for i in range(8)]
+    assert L.gdr2_decode_step(*p, 4, 2, 48, 64, 1, 0, None) == SHAPE
+    assert L.gdr2_decode_step(*p, -1, 2, 64, 64, 1, 0, None) == ARG
+    assert L.gdr2_decode_step(*p, 4, 2, 64, 64, 1, 5, None) == UNSUP
+    bad = list(p)
+    bad[6] = None  # S
+    assert L.gdr2_decode_step(*bad, 4, 2, 64, 64, 1, 0, None) == ARG
+    bad = list(p)
+    bad[7] = p[0]  # o aliases q
+    assert L.gdr2_decode_step(*bad, 4, 2, 64, 64, 1, 0, None) == ALIAS
+    bad = list(p)
+    bad[2] = ctypes.c_void_p(BASE + 2 * GAP + 4)
+    assert L.gdr2_decode_step(*bad, 4, 2, 64, 64, 1, 0, None) == ALIGN
+
+
+def test_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 2, 1, 32)
+    with pytest.raises(ValueError):
+        _lib.gdr2_forward(x, x, x, x, x, x)
