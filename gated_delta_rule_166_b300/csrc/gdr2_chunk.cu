@@ -14,8 +14,8 @@
 // with A_kk[r,i] = sum_j c_r[j] k_i[j] e^{G_r[j]-G_i[j]} (i < r) and
 // A_qk[r,i] = sum_j q_r[j] k_i[j] e^{G_r[j]-G_i[j]} (i <= r): the cumulative
 // channel decay sits inside the rank-1 erase factors.  With T = (I + A_kk)^-1
-// (UT transform), Cb = c*e^{G}, Qb = q*e^{G}, Kb = k*e^{G_C - G}, G_ = A_qk T:
-//     X = U - Cb S,   E = T X,   O = Qb S + G_ X,   S <- diag(e^{G_C}) S + Kb^T E.
+// (UT transform), Cb = c*e^{G}, Qb = q*e^{G}, Kb = k*e^{G_C - G}:
+//     X = U - Cb S,   E = T X,   O = Qb S + A_qk E,   S <- diag(e^{G_C}) S + Kb^T E.
 //
 // Overflow-free decay factors: e^{G_r - G_i} is formed as a product of two
 // factors about a reference m of the 16-token sub-chunk holding r (its 8th
@@ -26,7 +26,10 @@
 // tf32 (10-bit mantissa) and multiplied with kind::tf32 into fp32 TMEM
 // accumulators; bf16 operands (8-bit mantissa) are too coarse for the
 // max|err|/RMS <= 2e-2 bar (the output is a small residual of O(1) terms).
-// The triangular solve, decay factors and the state carry are fp32 on CUDA
+// X and E, whose rounding the later products amplify most, enter as a tf32
+// pair x = x_hi + x_lo (two MMAs each, x_lo = tf32(x - x_hi)).  The triangular
+// solve (16x16 diagonal blocks by forward substitution, then the off-diagonal
+// blocks level by level), decay factors and the state carry are fp32 on CUDA
 // cores.
 //
 // Work split: one CTA (512 threads, one per SM) per (batch*head, 64-column
@@ -56,23 +59,24 @@ constexpr uint32_t kRawQ = 0, kRawK = 16384, kRawB = 32768, kRawG = 49152;  // b
 constexpr uint32_t kRawV = 65536, kRawW = 73728;                            // bf16 [64][64]
 constexpr uint32_t kRawBytes = 81920;
 constexpr uint32_t kOpA = 81920;      // 64 KB: [Ct;Qt] -> solve staging -> [Cb;Qb] -> Kb^T
-constexpr uint32_t kOpB = 147456;     // 32 KB: K~ group columns -> [T;G_]
+constexpr uint32_t kOpB = 147456;     // 32 KB: K~ group columns -> [T; A_qk]
 constexpr uint32_t kSt = 180224;      // 32 KB: S^T operand  (64 rows j x 128 K)
-constexpr uint32_t kXE = 212992;      // 16 KB: X^T / E^T operand (64 rows j x 64 K); P1 scratch
+constexpr uint32_t kXE = 212992;      // 16 KB: K~ group 1 -> X^T / E^T operand (64 rows j x 64 K)
+constexpr uint32_t kLo = kOpA + 32768; // 16 KB: tf32 remainder of X^T / E^T (second half of kOpA)
 constexpr uint32_t kMisc = 229376;    // mbarriers, TMEM base, abort flag
 constexpr uint32_t kSmemBytes = kMisc + 64;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 // solve staging inside the kOpA area (padded fp32 rows)
 constexpr int kLd = 65;
-constexpr uint32_t kStAkk = kOpA, kStAqk = kOpA + 64 * kLd * 4, kStT = kOpA + 2 * 64 * kLd * 4;
-constexpr uint32_t kStP = kXE;        // 3 blocks of 16 x 17 floats during the solve
-// P1 scratch in the kXE area
-constexpr uint32_t kTot = kXE, kMid = kXE + 2048;
+constexpr uint32_t kStAkk = kOpA, kStT = kOpA + 64 * kLd * 4;
+constexpr uint32_t kStP = kOpA + 2 * 64 * kLd * 4;   // 3 blocks of 16 x 17 floats
+// P1 scratch inside the g tile once every g value is in registers
+constexpr uint32_t kTot = kRawG, kMid = kRawG + 2048;
 
 // ---- TMEM columns ------------------------------------------------------------
 constexpr uint32_t kTmA = 0;      // A_kk / A_qk raw products: 160 columns
-constexpr uint32_t kTmD1 = 160;   // [Cb S ; Qb S]          128 lanes x 64
-constexpr uint32_t kTmD2 = 224;   // [E ; G_ X]             128 lanes x 64
+constexpr uint32_t kTmD1 = 160;   // [Cb S ; Qb S], then rows 64..127 += A_qk E (= O)
+constexpr uint32_t kTmD2 = 224;   // [E ; A_qk X (unused)]  128 lanes x 64
 constexpr uint32_t kTmD3 = 288;   // Kb^T E                 128 lanes (key channel) x 64
 constexpr uint32_t kTmCols = 512;
 
@@ -201,12 +205,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // swizzled tiles in shared memory.  Issued by a single thread.
 __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, uint32_t a_rows,
                                          uint32_t b_base, uint32_t b_rows, int k_elems,
-                                         uint32_t idesc) {
+                                         uint32_t idesc, bool accumulate = false) {
     const int steps = k_elems / 8;   // tf32: 8 elements (32 bytes) per instruction
     for (int s = 0; s < steps; ++s) {
         const uint32_t kb = static_cast<uint32_t>(s) >> 2, kin = (static_cast<uint32_t>(s) & 3u) * 32u;
         mma_tf32(d_tmem, umma_desc(a_base + kb * a_rows * 128u + kin),
-                 umma_desc(b_base + kb * b_rows * 128u + kin), idesc, s > 0 ? 1u : 0u);
+                 umma_desc(b_base + kb * b_rows * 128u + kin), idesc, (s > 0 || accumulate) ? 1u : 0u);
     }
 }
 
@@ -326,36 +330,38 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
 
         // ---- P1: cumulative decay and the decay factors about each sub-chunk's reference
-        float Gm[16], rho[16], irho[16];
-        float acc = 0.f;
+        float rho[16], irho[16];
+        float gmu, emu, eCmu, gamma;
+        {
+            float Gm[16];
+            float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            acc += ld_bf16(sw_bf16(base + kRawG, 64, 16 * R + s, c));
-            Gm[s] = acc;
+            for (int s = 0; s < 16; ++s) {
+                acc += ld_bf16(sw_bf16(base + kRawG, 64, 16 * R + s, c));
+                Gm[s] = acc;
+            }
+            __syncthreads();   // every g value is in registers: the g tile becomes scratch
+            st_f32(base + kTot + (R * 128 + c) * 4, acc);
+            __syncthreads();
+            float pre = 0.f, gC = 0.f;
+#pragma unroll
+            for (int r2 = 0; r2 < 4; ++r2) {
+                const float t = ld_f32(base + kTot + (r2 * 128 + c) * 4);
+                gC += t;
+                if (r2 < R) pre += t;
+            }
+            gmu = Gm[7] + pre;
+            st_f32(base + kMid + (R * 128 + c) * 4, gmu);
+#pragma unroll
+            for (int s = 0; s < 16; ++s) {
+                const float d = Gm[s] + pre - gmu;
+                rho[s] = __expf(fminf(d, 80.f));
+                irho[s] = __expf(fminf(-d, 80.f));
+            }
+            emu = __expf(gmu);           // e^{G_m}       (<= 1)
+            eCmu = __expf(gC - gmu);     // e^{G_C - G_m} (<= 1)
+            gamma = __expf(gC);          // e^{G_C}
         }
-        st_f32(base + kTot + (R * 128 + c) * 4, acc);
-        __syncthreads();
-        float pre = 0.f, gC = 0.f;
-#pragma unroll
-        for (int r2 = 0; r2 < 4; ++r2) {
-            const float t = ld_f32(base + kTot + (r2 * 128 + c) * 4);
-            gC += t;
-            if (r2 < R) pre += t;
-        }
-#pragma unroll
-        for (int s = 0; s < 16; ++s) Gm[s] += pre;
-        const float gmu = Gm[7];
-        st_f32(base + kMid + (R * 128 + c) * 4, gmu);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float d = Gm[s] - gmu;
-            rho[s] = __expf(fminf(d, 80.f));
-            irho[s] = __expf(fminf(-d, 80.f));
-        }
-        const float emu = __expf(gmu);           // e^{G_m}      (<= 1)
-        const float eCmu = __expf(gC - gmu);     // e^{G_C - G_m} (<= 1)
-        const float gamma = __expf(gC);          // e^{G_C}
-
         // [Ct; Qt]: rows scaled by e^{G_r - G_m(r)}
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
@@ -368,125 +374,138 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         __syncthreads();   // kMid visible to all
 
-        // ---- intra-chunk products in three passes over the key-column groups.
-        // Group g holds k_i * e^{G_m(g) - G_i} for i < 16(g+1); the pass layout
-        // puts group 3 at TMEM column 0, groups 2 and 0 at 64, group 1 at 128.
-#pragma unroll 1
-        for (int pass = 0; pass < 3; ++pass) {
-            const int ga = pass == 0 ? 3 : (pass == 1 ? 2 : 1);
-            const int gb = pass == 1 ? 0 : -1;
+        // ---- intra-chunk products.  Key-column group g holds k_i * e^{G_m(g) - G_i}
+        // for i < 16(g+1).  Pass 0: group 3 (kOpB) -> TMEM columns 0..63 and
+        // group 1 (kXE) -> 128..159; pass 1: groups 2 and 0 (kOpB) -> 64..127.
+        auto put_group = [&](int grp, uint32_t buf, uint32_t rows, int row0) {
+            if (grp < R) return;
+            const float sc = grp == R ? 1.f : __expf(ld_f32(base + kMid + (grp * 128 + c) * 4) - gmu);
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const int grp = which == 0 ? ga : gb;
-                const int row0 = which == 0 ? 0 : 48;
-                if (grp >= R) {
-                    const float sc = grp == R ? 1.f : __expf(ld_f32(base + kMid + (grp * 128 + c) * 4) - gmu);
-#pragma unroll
-                    for (int s = 0; s < 16; ++s) {
-                        const int i = 16 * R + s;
-                        const float kv = ld_bf16(sw_bf16(base + kRawK, 64, i, c));
-                        st_f32(sw_f32(base + kOpB, 64, row0 + i, c), tf32r(kv * irho[s] * sc));
-                    }
-                }
+            for (int s = 0; s < 16; ++s) {
+                const int i = 16 * R + s;
+                const float kv = ld_bf16(sw_bf16(base + kRawK, 64, i, c));
+                st_f32(sw_f32(buf, rows, row0 + i, c), tf32r(kv * irho[s] * sc));
             }
-            sync_for_mma();
-            if (tid == 0) {
-                const uint32_t N = pass == 2 ? 32u : 64u;
-                mma_tile(tmem + kTmA + static_cast<uint32_t>(pass) * 64u, base + kOpA, 128, base + kOpB, 64,
-                         kDK, idesc_tf32(128, N));
-                mma_commit(bar_mma);
-            }
-            if (!mma_wait()) { failed = true; break; }
+        };
+        put_group(3, base + kOpB, 64, 0);
+        put_group(1, base + kXE, 32, 0);
+        sync_for_mma();
+        if (tid == 0) {
+            mma_tile(tmem + kTmA, base + kOpA, 128, base + kOpB, 64, kDK, idesc_tf32(128, 64));
+            mma_tile(tmem + kTmA + 128, base + kOpA, 128, base + kXE, 32, kDK, idesc_tf32(128, 32));
+            mma_commit(bar_mma);
         }
-        if (failed) break;
+        if (!mma_wait()) { failed = true; break; }
+        put_group(2, base + kOpB, 64, 0);
+        put_group(0, base + kOpB, 64, 48);
+        sync_for_mma();
+        if (tid == 0) {
+            mma_tile(tmem + kTmA + 64, base + kOpA, 128, base + kOpB, 64, kDK, idesc_tf32(128, 64));
+            mma_commit(bar_mma);
+        }
+        if (!mma_wait()) { failed = true; break; }
 
-        // ---- extract A_kk (strictly lower) and A_qk (lower) into padded fp32 staging
+        // ---- A_kk -> padded fp32 staging (solve input); A_qk -> rows 64..127 of the
+        // [T; A_qk] operand (tf32, zero above the diagonal).  T staging zeroed.
+        for (int e = tid; e < 1024; e += kThreads) {   // operand rows 64..127, both K-blocks
+            const uint32_t kb = static_cast<uint32_t>(e >> 9), rw = 64u + ((e >> 3) & 63), ch = e & 7;
+            asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(base + kOpB + kb * 16384u + rw * 128u + ch * 16u), "f"(0.f) : "memory");
+        }
+        for (int e = tid; e < 64 * kLd; e += kThreads) st_f32(base + kStT + e * 4, 0.f);
+        __syncthreads();
         {
-            const int r_lane = quarter * 32 + lane;   // TMEM lane = row of [Ct; Qt]
-            const bool is_q = r_lane >= 64;
-            const int rr = r_lane & 63;
+            const int q2 = quarter & 1;                 // lanes 0-15: group 2*q2, 16-31: group 2*q2+1
+            const int rr = q2 * 32 + lane;              // row of A_kk (quarters 0,1) or A_qk (2,3)
             const int Rr = rr >> 4;
-            const uint32_t stg = base + (is_q ? kStAqk : kStAkk);
-#pragma unroll 1
-            for (int piece = 0; piece < 10; ++piece) {
-                if ((piece & 3) != R && piece < 8) continue;  // pieces 0..7 split over R, 8..9 by R < 2
-                if (piece >= 8 && R != piece - 8) continue;
+            const bool is_q = quarter >= 2;
+            int pieces[2], np = 0;
+            if (q2 == 0) { if (R < 3) pieces[np++] = 7 + R; }
+            else { pieces[np++] = R; if (R + 4 < 7) pieces[np++] = R + 4; }
+            for (int pi = 0; pi < np; ++pi) {
                 float v[16];
-                tmem_ld16(tmem + lane_base + kTmA + static_cast<uint32_t>(piece) * 16u, v);
+                tmem_ld16(tmem + lane_base + kTmA + static_cast<uint32_t>(pieces[pi]) * 16u, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     int i;
-                    const int g = group_of_col(piece * 16 + e, &i);
-                    if (g == Rr && (is_q ? i <= rr : i < rr)) st_f32(stg + (rr * kLd + i) * 4, v[e]);
+                    const int g = group_of_col(pieces[pi] * 16 + e, &i);
+                    if (g != Rr) continue;
+                    if (!is_q) {
+                        if (i < rr) st_f32(base + kStAkk + (rr * kLd + i) * 4, v[e]);
+                    } else if (i <= rr) {
+                        st_f32(sw_f32(base + kOpB, 128, 64 + rr, i), tf32r(v[e]));
+                    }
                 }
             }
         }
         tc_fence_before();
         __syncthreads();
 
-        // ---- T = (I + A_kk)^-1: 16x16 diagonal blocks by forward substitution,
-        // then the off-diagonal blocks level by level.
-        for (int e = tid; e < 64 * kLd; e += kThreads) st_f32(base + kStT + e * 4, 0.f);
-        __syncthreads();
+        // ---- T = (I + A_kk)^-1.  16x16 diagonal blocks by column forward substitution
         if (tid < 64) {
-            const int blk = tid >> 4, col = tid & 15, o16 = 16 * blk;
-            float tc[16];
+            const int o16 = 16 * (tid >> 4), col = tid & 15;
+            float tcol[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) tc[r] = 0.f;
-            tc[col] = 1.f;
+            for (int r = 0; r < 16; ++r) tcol[r] = r == col ? 1.f : 0.f;
 #pragma unroll
             for (int r = 1; r < 16; ++r) {
-                if (r > col) {
-                    float sum = 0.f;
+                float sum = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 15; ++i)
-                        if (i >= col && i < r) sum = fmaf(ld_f32(base + kStAkk + ((o16 + r) * kLd + o16 + i) * 4), tc[i], sum);
-                    tc[r] = -sum;
-                }
+                for (int i = 0; i < r; ++i)
+                    sum = fmaf(ld_f32(base + kStAkk + ((o16 + r) * kLd + o16 + i) * 4), tcol[i], sum);
+                if (r > col) tcol[r] = -sum;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (r >= col) st_f32(base + kStT + ((o16 + r) * kLd + o16 + col) * 4, tc[r]);
+            for (int r = 0; r < 16; ++r) st_f32(base + kStT + ((o16 + r) * kLd + o16 + col) * 4, tcol[r]);
         }
         __syncthreads();
+        // off-diagonal blocks, level d = Rb - I:  T_{Rb,I} = -T_{Rb,Rb} sum_{J=I}^{Rb-1} A_{Rb,J} T_{J,I}
+        // one warp per block; lane -> row lane/2, columns 8*(lane&1) .. +7
 #pragma unroll 1
         for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;                 // blocks (Rb, Rb - d), Rb = d..3
-            // P = sum_{J=I}^{Rb-1} A_{Rb,J} T_{J,I}
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int bI = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int Rb = d + bI, I = bI;
-                float sum = 0.f;
-                for (int kk = 16 * I; kk < 16 * Rb; ++kk)
-                    sum = fmaf(ld_f32(base + kStAkk + ((16 * Rb + rr) * kLd + kk) * 4),
-                               ld_f32(base + kStT + (kk * kLd + 16 * I + cc) * 4), sum);
-                st_f32(base + kStP + (bI * 16 * 17 + rr * 17 + cc) * 4, sum);
+            const int rr = lane >> 1, c8 = 8 * (lane & 1);
+            const int bI = warp, Rb = d + warp;
+            if (warp < 4 - d) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) p[e] = 0.f;
+#pragma unroll 1
+                for (int J = bI; J < Rb; ++J) {
+#pragma unroll
+                    for (int k16 = 0; k16 < 16; ++k16) {
+                        const int kk = 16 * J + k16;
+                        const float a = ld_f32(base + kStAkk + ((16 * Rb + rr) * kLd + kk) * 4);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            p[e] = fmaf(a, ld_f32(base + kStT + (kk * kLd + 16 * bI + c8 + e) * 4), p[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st_f32(base + kStP + (bI * 16 * 17 + rr * 17 + c8 + e) * 4, p[e]);
             }
             __syncthreads();
-            // T_{Rb,I} = -T_{Rb,Rb} P
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int bI = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int Rb = d + bI, I = bI;
-                float sum = 0.f;
-                for (int kk = 0; kk <= rr; ++kk)
-                    sum = fmaf(ld_f32(base + kStT + ((16 * Rb + rr) * kLd + 16 * Rb + kk) * 4),
-                               ld_f32(base + kStP + (bI * 16 * 17 + kk * 17 + cc) * 4), sum);
-                st_f32(base + kStT + ((16 * Rb + rr) * kLd + 16 * I + cc) * 4, -sum);
+            if (warp < 4 - d) {
+                float t[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const float a = ld_f32(base + kStT + ((16 * Rb + rr) * kLd + 16 * Rb + kk) * 4);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        t[e] = fmaf(a, ld_f32(base + kStP + (bI * 16 * 17 + kk * 17 + c8 + e) * 4), t[e]);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st_f32(base + kStT + ((16 * Rb + rr) * kLd + 16 * bI + c8 + e) * 4, -t[e]);
             }
             __syncthreads();
         }
-        // [T; G_] operand (G_ = A_qk T), 128 rows x 64 K, into the kOpB area.
+        // T -> rows 0..63 of the [T; A_qk] operand
         {
             const int cc = tid & 63;
-#pragma unroll 1
+#pragma unroll
             for (int m = 0; m < 8; ++m) {
                 const int r = (tid >> 6) + 8 * m;
-                float gsum = 0.f;
-                for (int i = cc; i <= r; ++i)
-                    gsum = fmaf(ld_f32(base + kStAqk + (r * kLd + i) * 4), ld_f32(base + kStT + (i * kLd + cc) * 4), gsum);
-                const float tv = cc <= r ? ld_f32(base + kStT + (r * kLd + cc) * 4) : 0.f;
-                st_f32(sw_f32(base + kOpB, 128, r, cc), tf32r(tv));
-                st_f32(sw_f32(base + kOpB, 128, 64 + r, cc), tf32r(cc <= r ? gsum : 0.f));
+                st_f32(sw_f32(base + kOpB, 128, r, cc), tf32r(ld_f32(base + kStT + (r * kLd + cc) * 4)));
             }
         }
         __syncthreads();   // staging reads done before [Cb; Qb] overwrites the area
@@ -509,22 +528,18 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         if (!mma_wait()) { failed = true; break; }
 
-        // ---- X = U - Cb S (rows 0..63), keep Qb S (rows 64..127); Kb^T operand
-        float qs[16];
-        {
+        // ---- X = U - Cb S (rows 0..63) -> X^T operand as a tf32 pair; Kb^T operand
+        if (quarter < 2) {
             float v[16];
             tmem_ld16(tmem + lane_base + kTmD1 + static_cast<uint32_t>(R) * 16u, v);
             const int r = quarter * 32 + lane;
-            if (r < 64) {
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = 16 * R + jj;
-                    const float u = ld_bf16(sw_bf16(base + kRawW, 64, r, j)) * ld_bf16(sw_bf16(base + kRawV, 64, r, j));
-                    st_f32(sw_f32(base + kXE, 64, j, r), tf32r(u - v[jj]));
-                }
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) qs[jj] = v[jj];
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j = 16 * R + jj;
+                const float u = ld_bf16(sw_bf16(base + kRawW, 64, r, j)) * ld_bf16(sw_bf16(base + kRawV, 64, r, j));
+                const float x = u - v[jj], xh = tf32r(x);
+                st_f32(sw_f32(base + kXE, 64, j, r), xh);
+                st_f32(sw_f32(base + kLo, 64, j, r), tf32r(x - xh));
             }
         }
 #pragma unroll
@@ -534,46 +549,39 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             st_f32(sw_f32(base + kOpA, 128, c, r), tf32r(kv * eCmu * irho[s]));
         }
         sync_for_mma();
-        if (tid == 0) {
+        if (tid == 0) {   // MMA2: [T; A_qk] (X_hi + X_lo) -> rows 0..63 = E
             mma_tile(tmem + kTmD2, base + kOpB, 128, base + kXE, 64, kC, idesc_tf32(128, kDVT));
+            mma_tile(tmem + kTmD2, base + kOpB, 128, base + kLo, 64, kC, idesc_tf32(128, kDVT), true);
             mma_commit(bar_mma);
             if (n + 1 < nchunks) issue_loads(n + 1);   // every read of the raw tiles is done
         }
         if (!mma_wait()) { failed = true; break; }
 
-        // ---- E (rows 0..63) -> E^T operand; O = Qb S + G_ X (rows 64..127) -> o
-        {
+        // ---- E (rows 0..63) -> E^T operand as a tf32 pair
+        if (quarter < 2) {
             float v[16];
             tmem_ld16(tmem + lane_base + kTmD2 + static_cast<uint32_t>(R) * 16u, v);
             const int r = quarter * 32 + lane;
-            if (r < 64) {
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) st_f32(sw_f32(base + kXE, 64, 16 * R + jj, r), tf32r(v[jj]));
-            } else if (r - 64 < nv) {
-                const int64_t off = ((static_cast<int64_t>(bi) * T + t0 + (r - 64)) * prm.H + h) * prm.dv + j0 + 16 * R;
-                if (prm.out_bf16) {
-                    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 2)
-                        *reinterpret_cast<__nv_bfloat162*>(op + jj) =
-                            __floats2bfloat162_rn(qs[jj] + v[jj], qs[jj + 1] + v[jj + 1]);
-                } else {
-                    float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4)
-                        op[jj / 4] = make_float4(qs[jj] + v[jj], qs[jj + 1] + v[jj + 1], qs[jj + 2] + v[jj + 2],
-                                                 qs[jj + 3] + v[jj + 3]);
-                }
+            for (int jj = 0; jj < 16; ++jj) {
+                const float eh = tf32r(v[jj]);
+                st_f32(sw_f32(base + kXE, 64, 16 * R + jj, r), eh);
+                st_f32(sw_f32(base + kLo, 64, 16 * R + jj, r), tf32r(v[jj] - eh));
             }
         }
         sync_for_mma();
         if (tid == 0) {
+            // MMA3: Kb^T E -> D3.  MMA_O: [T; A_qk] E accumulated onto [Cb S; Qb S]:
+            // rows 64..127 become O = Qb S + A_qk E (rows 0..63 are not used).
             mma_tile(tmem + kTmD3, base + kOpA, 128, base + kXE, 64, kC, idesc_tf32(128, kDVT));
+            mma_tile(tmem + kTmD3, base + kOpA, 128, base + kLo, 64, kC, idesc_tf32(128, kDVT), true);
+            mma_tile(tmem + kTmD1, base + kOpB, 128, base + kXE, 64, kC, idesc_tf32(128, kDVT), true);
+            mma_tile(tmem + kTmD1, base + kOpB, 128, base + kLo, 64, kC, idesc_tf32(128, kDVT), true);
             mma_commit(bar_mma);
         }
         if (!mma_wait()) { failed = true; break; }
 
-        // ---- S <- diag(e^{G_C}) S + Kb^T E; refresh the S^T operand
+        // ---- S <- diag(e^{G_C}) S + Kb^T E; refresh the S^T operand; store O
         {
             float v[16];
             tmem_ld16(tmem + lane_base + kTmD3 + static_cast<uint32_t>(R) * 16u, v);
@@ -581,6 +589,24 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int jj = 0; jj < 16; ++jj) {
                 S[jj] = fmaf(gamma, S[jj], v[jj]);
                 st_f32(sw_f32(base + kSt, 64, 16 * R + jj, c), tf32r(S[jj]));
+            }
+        }
+        if (quarter >= 2) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + kTmD1 + static_cast<uint32_t>(R) * 16u, v);
+            const int r = quarter * 32 + lane - 64;
+            if (r < nv) {
+                const int64_t off = ((static_cast<int64_t>(bi) * T + t0 + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                if (prm.out_bf16) {
+                    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 2)
+                        *reinterpret_cast<__nv_bfloat162*>(op + jj) = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                } else {
+                    float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 4) op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                }
             }
         }
         tc_fence_before();
