@@ -335,6 +335,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling aid: run just one kernel's leg (no JSON line for decode-only)")
+    ap.add_argument("--decode-steps", type=int, default=1024)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -384,6 +387,12 @@ def main():
     x = x_host.to("cuda")
     torch.cuda.synchronize()
 
+    if args.only == "decode":
+        dec = bench_decode(gdr2, steps=args.decode_steps)
+        if rank == 0:
+            print(json.dumps({"decode": dec}))
+        return
+
     with ClockSampler(local) as clk:
         ms, per_launch, launches = bench_prefill(gdr2, x, args.steps, args.warmup, world)
     clocks = clk.summary()
@@ -410,6 +419,8 @@ def main():
            "config": config, "roofline": roofline, "clocks": clocks,
            "gpu_launches": launches}
 
+    if args.only == "prefill":
+        args.no_e2e = args.no_decode = args.no_cpu_baseline = True
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
@@ -417,7 +428,7 @@ def main():
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "ms_per_step": e2e_ms}
     if not args.no_decode:
-        dec = bench_decode(gdr2)
+        dec = bench_decode(gdr2, steps=args.decode_steps)
         dec["roofline"] = {"bound": "hbm", "achieved": dec["gbs"], "peak": hbm_gbs, "unit": "GB/s",
                            "frac": dec["gbs"] / hbm_gbs,
                            "traffic": traffic_record("decode_B256_H16_d128")}
