@@ -86,7 +86,12 @@ typedef enum {
  * T = 0 is allowed: S_T receives S0 (or zeros) and o is untouched.
  * S0 == S_T (in-place state update) is allowed; any other overlap between S_T
  * or o and another argument is rejected with GDR2_ERR_ALIAS.
- * Precondition (not checked): log_decay <= 0 and finite.
+ * Preconditions (not checked): log_decay <= 0 and finite.  The chunked bf16
+ * path forms per-channel decay factors about the middle token of each
+ * 16-token sub-chunk, each clamped at e^80: it is exact while the decay over
+ * any 8 consecutive tokens stays above e^-80 (log_decay above about -10 per
+ * token); below that, terms already smaller than e^-80 of the largest are
+ * flushed to zero.  The fp32 path and the decode step have no such limit.
  */
 int gdr2_forward(const void* q, const void* k, const void* v,
                  const void* b, const void* w, const void* log_decay,
