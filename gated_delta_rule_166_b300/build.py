@@ -22,6 +22,8 @@ LIB = os.path.join(PKG, "libgdr2.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
                      "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+# per-file extra flags
+FILE_FLAGS: dict = {}
 
 
 def _nvcc() -> str:
@@ -48,7 +50,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_v else []) + ["-c", src, "-o", obj]
+            cmd = ([nvcc] + NVCC_FLAGS + FILE_FLAGS.get(os.path.basename(src), []) +
+                   (["-Xptxas", "-v"] if ptxas_v else []) + ["-c", src, "-o", obj])
             jobs.append(cmd)
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:

@@ -1,6 +1,8 @@
 // Chunked Gated Delta Rule-2 prefill for bf16 inputs on sm_103a:
-// TMA-staged input tiles, tcgen05 tensor-core contractions with TMEM
-// accumulators, fp32 state carried on chip across chunks.
+// TMA-staged input tiles, tcgen05 tensor-core products with TMEM
+// accumulators and TMEM-resident operands, an fp32 state carried on chip
+// across chunks, and the state-independent work of chunk n+1 overlapped
+// with the state pass of chunk n.
 //
 // Method ("Gated DeltaNet-2: Decoupling Erase and Write in Linear Attention"
 // page: update equation, and the "efficient implementation" section's WY form
@@ -8,38 +10,50 @@
 // tokens r = 0..63 with chunk-initial state S (d_k x d_v), cumulative log
 // decay G_r = sum_{t<=r} g_t (per key channel), c_r = b_r * k_r,
 // u_r = w_r * v_r, the recurrence unrolls to
-//     S_r = diag(e^{G_r}) S + sum_{i<=r} diag(e^{G_r - G_i}) k_i e_i^T
 //     e_r = u_r - (c_r * e^{G_r})^T S - sum_{i<r} A_kk[r,i] e_i
 //     o_r = (q_r * e^{G_r})^T S + sum_{i<=r} A_qk[r,i] e_i
+//     S_C = diag(e^{G_C}) S + sum_i diag(e^{G_C - G_i}) k_i e_i^T
 // with A_kk[r,i] = sum_j c_r[j] k_i[j] e^{G_r[j]-G_i[j]} (i < r) and
 // A_qk[r,i] = sum_j q_r[j] k_i[j] e^{G_r[j]-G_i[j]} (i <= r): the cumulative
 // channel decay sits inside the rank-1 erase factors.  With T = (I + A_kk)^-1
-// (UT transform), Cb = c*e^{G}, Qb = q*e^{G}, Kb = k*e^{G_C - G}:
-//     X = U - Cb S,   E = T X,   O = Qb S + A_qk E,   S <- diag(e^{G_C}) S + Kb^T E.
+// (UT transform), Cb = c*e^{G}, Qb = q*e^{G}, Kb = k*e^{G_C - G},
+// W = T Cb and P = Qb - A_qk W, the chunk is
+//     [E; O] = [T; A_qk T] U + [-W; P] S,     S <- diag(e^{G_C}) S + Kb^T E.
+// Everything left of S is independent of the state, so the only products on
+// the chunk-to-chunk chain are [-W; P] S and Kb^T E.
 //
 // Overflow-free decay factors: e^{G_r - G_i} is formed as a product of two
-// factors about a reference m of the 16-token sub-chunk holding r (its 8th
-// token): e^{G_r - G_m} * e^{G_m - G_i}.  For i in an earlier sub-chunk both
-// factors are <= 1; inside the sub-chunk each spans at most 8 tokens of decay.
+// factors about a reference m, the 8th token of the 16-token sub-chunk
+// ("stripe") holding r: e^{G_r - G_m} * e^{G_m - G_i}.  Row r carries
+// e^{G_r - G_m}; column i is scaled once per stripe R >= stripe(i)
+// ("K-group" R).  For i in an earlier stripe both factors are <= 1; inside
+// the stripe each spans at most 8 tokens (clamped at e^80).
 //
-// Precision: every tensor-core operand is an fp32 value rounded to nearest
-// tf32 (10-bit mantissa) and multiplied with kind::tf32 into fp32 TMEM
-// accumulators; bf16 operands (8-bit mantissa) are too coarse for the
-// max|err|/RMS <= 2e-2 bar (the output is a small residual of O(1) terms).
-// X and E, whose rounding the later products amplify most, enter as a tf32
-// pair x = x_hi + x_lo (two MMAs each, x_lo = tf32(x - x_hi)).  The triangular
-// solve (16x16 diagonal blocks by forward substitution, then the off-diagonal
-// blocks level by level), decay factors and the state carry are fp32 on CUDA
-// cores.
+// Precision: tensor-core operands are tf32 (kind::tf32, fp32 accumulators);
+// U and E, whose rounding the later products amplify most, enter as a tf32
+// pair x = x_hi + x_lo (two products each).  Operands the tensor core reads
+// from TMEM (T, A_qk T, -W, P, Kb^T) are fp32 accumulator values taken as
+// tf32.  The triangular solve, decay factors and state update are fp32 on
+// CUDA cores.
 //
 // Work split: one CTA (512 threads, one per SM) per (batch*head, 64-column
-// d_v tile); the CTA walks the chunks of its sequence in order.  Thread
-// (c = tid % 128, R = tid / 128) owns key channel c of sub-chunk R in the
-// elementwise phases and TMEM lane c (or token row), columns 16R..16R+15 in
-// the epilogues.  Every operand lives in shared memory in the K-major
-// 128-byte-swizzled layout the tensor core reads.
+// d_v tile).  Thread (j = tid % 128, R = tid / 128) owns key channel j of
+// stripe R in the elementwise phases and TMEM lane j, columns 16R..16R+15 in
+// the accumulator phases (warp w may only touch TMEM lanes 32*(w%4)..+31,
+// and j = 32*(w%4) + lane).  Loop iteration `it` runs the state pass of chunk
+// it-1 and the state-independent preparation of chunk it:
+//   (a) chain MMAs [E;O] = A0 U + A1 S          (A0 = [T; A_qk T], A1 = [-W; P])
+//   (b) prep pass 1: raw tiles -> registers, decay factors, [Ct; Qt] and the
+//       K-groups in shared memory
+//   (c) chain epilogue: E -> E^T operand, O -> global; MMA2 Kb^T E; prep
+//       intra-chunk products [Ct; Qt] K-groups^T
+//   (e) chain: S <- gamma S + Kb^T E, S^T operand refreshed
+//   (f) prep: A_kk, A_qk out of TMEM, triangular solve, A0 = [I; A_qk] T,
+//       pass 2 (-Cb^T, Kb^T -> TMEM, U^T), A1 = A0 (-Cb^T), P += Qb.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -49,35 +63,58 @@
 namespace gdr2 {
 namespace {
 
-constexpr int kC = 64;        // chunk length
-constexpr int kDK = 128;      // key channels
-constexpr int kDVT = 64;      // value columns per CTA
-constexpr int kThreads = 512;
+constexpr int kC = 64;         // chunk length
+constexpr int kDK = 128;       // key channels
+constexpr int kDVT = 64;       // value columns per CTA
+constexpr int kSimt = 512;     // 16 warps: elementwise and accumulator phases
+constexpr int kThreads = kSimt + 128;  // + one warpgroup whose first thread issues TMA loads and MMAs
+// Registers: launched at 96 per thread (640 x 96 = 61440 in the CTA's pool); the
+// MMA warpgroup drops to 32 and the 16 elementwise warps rise to 112:
+// 512 x 112 + 128 x 32 = 61440 <= 61440, and per SM sub-partition (4 elementwise
+// warps + 1 MMA-group warp) 4 x 112 x 32 + 32 x 32 = 15360 <= 16384.
+constexpr int kRegsSimt = 112, kRegsMma = 32;
+static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96, "register pool");
 
-// ---- shared-memory map (bytes from a 1024-aligned base) -------------------
+// ---- shared-memory map (bytes from a 1024-aligned base) ------------------------
+// Every MMA operand is K-major with the 128-byte swizzle: K-blocks of 32 tf32,
+// each K-block `rows` x 128 B, 16-byte chunk index XOR (row % 8).
 constexpr uint32_t kRawQ = 0, kRawK = 16384, kRawB = 32768, kRawG = 49152;  // bf16 [2 kblk][64][64]
-constexpr uint32_t kRawV = 65536, kRawW = 73728;                            // bf16 [64][64]
-constexpr uint32_t kRawBytes = 81920;
-constexpr uint32_t kOpA = 81920;      // 64 KB: [Ct;Qt] -> solve staging -> [Cb;Qb] -> Kb^T
-constexpr uint32_t kOpB = 147456;     // 32 KB: K~ group columns -> [T; A_qk]
-constexpr uint32_t kSt = 180224;      // 32 KB: S^T operand  (64 rows j x 128 K)
-constexpr uint32_t kXE = 212992;      // 16 KB: K~ group 1 -> X^T / E^T operand (64 rows j x 64 K)
-constexpr uint32_t kLo = kOpA + 32768; // 16 KB: tf32 remainder of X^T / E^T (second half of kOpA)
-constexpr uint32_t kMisc = 229376;    // mbarriers, TMEM base, abort flag
-constexpr uint32_t kSmemBytes = kMisc + 64;
+constexpr uint32_t kG31 = 0;           // K-groups [G3 (64 rows) | G1 (32 rows)], 96 x 128 K (48 KB)
+constexpr uint32_t kOpA = 65536;       // [Ct; Qt]: 128 rows x 128 K (64 KB)
+constexpr uint32_t kG20 = 131072;      // K-groups [G2 (48 rows) | G0 (16 rows)], 64 x 128 K (32 KB)
+constexpr uint32_t kSt = 163840;       // S^T: 64 rows (d_v) x 128 K (d_k) (32 KB)
+constexpr uint32_t kEU = 196608;       // [U_hi^T; U_lo^T], later [E_hi^T; E_lo^T]: 128 rows x 64 K (32 KB)
+constexpr uint32_t kMisc = 229376;     // mbarriers, TMEM base
+constexpr uint32_t kSmemBytes = kMisc + 128;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
-// solve staging inside the kOpA area (padded fp32 rows)
-constexpr int kLd = 65;
-constexpr uint32_t kStAkk = kOpA, kStT = kOpA + 64 * kLd * 4;
-constexpr uint32_t kStP = kOpA + 2 * 64 * kLd * 4;   // 3 blocks of 16 x 17 floats
-// P1 scratch inside the g tile once every g value is in registers
-constexpr uint32_t kTot = kRawG, kMid = kRawG + 2048;
+// pass-1 exchange of per-stripe decay sums (inside [Ct; Qt] before it is written)
+constexpr uint32_t kXTot = kOpA, kXMid = kOpA + 2048;
+// phase (f) scratch inside kOpA .. kOpA + 96 KB (the intra-chunk product operands are dead)
+constexpr int kLd = 65;                              // padded fp32 row (floats)
+constexpr uint32_t kSL = kOpA;                       // A_kk staging  [64][65] fp32
+constexpr uint32_t kSTs = kOpA + 16640;              // T staging     [64][65] fp32
+constexpr uint32_t kIA = kOpA + 33792;               // [I; A_qk]: 128 rows x 64 K (32 KB)
+constexpr uint32_t kTT = kIA + 32768;                // T^T: 64 rows x 64 K (16 KB)
+constexpr uint32_t kSP = kTT + 16384;                // solve: 6 blocks M_{RJ} of 16 x 17 fp32
+constexpr uint32_t kCbT = kOpA;                      // -Cb^T: 128 rows x 64 K (32 KB), after the solve
+constexpr int kLq = 132;                             // padded Qb row (floats)
+constexpr uint32_t kQb = kOpA + 33792;               // Qb [64][132] fp32, after the A0 product
+static_assert(kSP + 6 * 16 * 17 * 4 <= kSt, "solve scratch");
+static_assert(kQb + 64 * kLq * 4 <= kSt, "Qb staging");
+static_assert(kG31 + 3 * 12288 + 12288 <= kOpA, "K-groups in the raw area");
+static_assert(kSmemAlloc <= 232448, "shared memory");
+// mbarriers (8 bytes each) inside kMisc
+enum : uint32_t { kBarTma = 0, kRdyChain, kRdyMma2, kRdyAP, kRdyA0, kRdyA1, kDoneC1, kDoneC2, kDoneP1,
+                  kDoneP2, kDoneP3, kNumBars };
+constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
 
-// ---- TMEM columns ------------------------------------------------------------
-constexpr uint32_t kTmA = 0;      // A_kk / A_qk raw products: 160 columns
-constexpr uint32_t kTmD1 = 160;   // [Cb S ; Qb S], then rows 64..127 += A_qk E (= O)
-constexpr uint32_t kTmD2 = 224;   // [E ; A_qk X (unused)]  128 lanes x 64
-constexpr uint32_t kTmD3 = 288;   // Kb^T E                 128 lanes (key channel) x 64
+// ---- TMEM columns ------------------------------------------------------------------
+constexpr uint32_t kTmA0 = 0;      // [T; A_qk T]   (A operand, K = 64 tokens)
+constexpr uint32_t kTmA1 = 64;     // [-W; P]       (A operand, K = 128 channels)
+constexpr uint32_t kTmAP = 64;     // intra-chunk products while A1 is free: [G3|G1] 64..159, [G2|G0] 160..223
+constexpr uint32_t kTmA2 = 224;    // Kb^T          (A operand, lanes = channels, K = 64 tokens)
+constexpr uint32_t kTmEO = 288;    // [E; O] as hi | lo halves (128 columns), then Kb^T E likewise
+constexpr uint32_t kTmS = 416;     // fp32 state S[j][j0 + c], lanes = key channels, 64 columns
 constexpr uint32_t kTmCols = 512;
 
 constexpr long long kWaitCycles = 4ll * 1000 * 1000 * 1000;   // ~2 s at 2 GHz
@@ -91,29 +128,10 @@ __device__ __forceinline__ float tf32r(float x) {   // round to nearest tf32
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return __uint_as_float(r);
 }
-__device__ __forceinline__ void st_f32(uint32_t addr, float v) {
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ float ld_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float ld_bf16(uint32_t addr) {
-    unsigned short h;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr) : "memory");
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-// 128-byte swizzled K-major layout, 4-byte elements: K-blocks of 32 elements,
-// each K-block `rows` x 128 B; 16-byte chunk index XOR (row % 8).
-__device__ __forceinline__ uint32_t sw_f32(uint32_t base, uint32_t rows, uint32_t row, uint32_t k) {
-    const uint32_t kb = k >> 5, kk = k & 31;
-    return base + kb * rows * 128u + row * 128u + ((((kk >> 2) ^ (row & 7u)) << 4) | ((kk & 3u) << 2));
-}
-// The same swizzle for the bf16 tiles TMA writes (64 elements per 128-B row).
-__device__ __forceinline__ uint32_t sw_bf16(uint32_t base, uint32_t rows, uint32_t row, uint32_t c) {
-    const uint32_t kb = c >> 6, cc = c & 63;
-    return base + kb * rows * 128u + row * 128u + ((((cc >> 3) ^ (row & 7u)) << 4) | ((cc & 7u) << 1));
+// Byte offset of element (row, k) of a K-major 128B-swizzled tf32 operand
+// whose K-blocks are `kstride` bytes apart.
+__device__ __forceinline__ uint32_t sw(uint32_t kstride, uint32_t row, uint32_t k) {
+    return (k >> 5) * kstride + row * 128u + ((((k & 31u) >> 2) ^ (row & 7u)) << 4) + ((k & 3u) << 2);
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -121,6 +139,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -143,6 +164,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Barrier over the 16 elementwise warps only (the MMA warp never joins it).
+__device__ __forceinline__ void simt_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ bool simt_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 512, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
 }
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             int c3, uint32_t bar) {
@@ -167,13 +202,22 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -186,9 +230,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// 32 lanes x 32 bit, 16 consecutive columns per thread.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 lanes x 32 bit, 16 consecutive columns per thread (no wait).
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -196,25 +239,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    tmem_ld16_nw(taddr, r);
+    tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-
-// One full-K tile product: D (+)= A[M x K] * B[N x K]^T, both K-major
-// swizzled tiles in shared memory.  Issued by a single thread.
-__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, uint32_t a_rows,
-                                         uint32_t b_base, uint32_t b_rows, int k_elems,
-                                         uint32_t idesc, bool accumulate = false) {
-    const int steps = k_elems / 8;   // tf32: 8 elements (32 bytes) per instruction
-    for (int s = 0; s < steps; ++s) {
-        const uint32_t kb = static_cast<uint32_t>(s) >> 2, kin = (static_cast<uint32_t>(s) & 3u) * 32u;
-        mma_tf32(d_tmem, umma_desc(a_base + kb * a_rows * 128u + kin),
-                 umma_desc(b_base + kb * b_rows * 128u + kin), idesc, (s > 0 || accumulate) ? 1u : 0u);
-    }
+// Sum of the two 64-column halves (hi and lo products) at columns c and c + 64.
+__device__ __forceinline__ void tmem_ld16_pair(uint32_t taddr, float (&v)[16]) {
+    uint32_t a[16], b[16];
+    tmem_ld16_nw(taddr, a);
+    tmem_ld16_nw(taddr + 64u, b);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]) + __uint_as_float(b[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t kstep(uint32_t base, uint32_t kstride, int s) {   // tf32 K-step s
+    return base + (static_cast<uint32_t>(s) >> 2) * kstride + (static_cast<uint32_t>(s) & 3u) * 32u;
 }
 
 struct ChunkParams {
+    const void* v;
+    const void* w;
     const float* S0;
     void* o;
     float* ST;
@@ -223,31 +287,27 @@ struct ChunkParams {
     int out_bf16;
 };
 
-// Column of the raw-product TMEM block holding A[r, i] for a row of
-// sub-chunk R: group 3 at 0, group 2 at 64, group 0 at 112, group 1 at 128.
-__device__ __forceinline__ int group_of_col(int col, int* i) {
-    if (col < 64) { *i = col; return 3; }
-    if (col < 112) { *i = col - 64; return 2; }
-    if (col < 128) { *i = col - 112; return 0; }
-    *i = col - 128;
-    return 1;
+// First TMEM column of K-group R in the intra-chunk product block.
+__device__ __forceinline__ uint32_t group_col(int R) {
+    return kTmAP + (R == 3 ? 0u : R == 1 ? 64u : R == 2 ? 96u : 144u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_g,
-             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
              const ChunkParams prm) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));   // generic pointer to the same base
-    const uint32_t bar_tma = base + kMisc, bar_mma = base + kMisc + 8;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kMisc + 16);
+    float* const F = reinterpret_cast<float*>(sgen);
+    const unsigned short* const H16 = reinterpret_cast<const unsigned short*>(sgen);
+    auto bar = [&](uint32_t i) { return base + kMisc + 8u * i; };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kTmemSlot);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int c = tid & 127;          // key channel (elementwise phases) / TMEM lane
-    const int R = tid >> 7;           // sub-chunk (elementwise) / 16-column piece (epilogues)
+    const int j = tid & 127;          // key channel (elementwise) / TMEM lane (accumulator phases)
+    const int R = (tid >> 7) & 3;     // stripe (elementwise) / 16-column block (accumulator phases)
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int bh = blockIdx.x;
     const int bi = bh / prm.H, h = bh % prm.H;
@@ -256,14 +316,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int nchunks = (T + kC - 1) / kC;
 
     if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+        for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         base + kMisc + 16),
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + kTmemSlot),
                      "r"(kTmCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -272,358 +330,477 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
 
-    auto issue_loads = [&](int n) {
-        const int t0 = n * kC;
-        mbar_expect_tx(bar_tma, kRawBytes);
-        tma_load_4d(base + kRawQ, &tm_q, 0, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawQ + 8192, &tm_q, 64, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawK, &tm_k, 0, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawK + 8192, &tm_k, 64, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawB, &tm_b, 0, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawB + 8192, &tm_b, 64, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawG, &tm_g, 0, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawG + 8192, &tm_g, 64, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawV, &tm_v, j0, h, t0, bi, bar_tma);
-        tma_load_4d(base + kRawW, &tm_w, j0, h, t0, bi, bar_tma);
-    };
-    if (tid == 0 && nchunks > 0) issue_loads(0);
-
-    // fp32 state: S[c][j0 + 16R + jj], jj = 0..15, kept in registers.
-    float S[16];
-    {
-        const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + c) * prm.dv + j0 + 16 * R
-                                 : nullptr;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            S[jj] = s0 ? s0[jj] : 0.f;
-            st_f32(sw_f32(base + kSt, 64, 16 * R + jj, c), tf32r(S[jj]));
+    if (warp >= kSimt / 32) {
+        // ================= MMA / TMA warpgroup: one elected thread ================
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
+        if (warp == kSimt / 32 && lane == 0) {
+            auto issue_loads = [&](int n) {
+                const int t0 = n * kC;
+                mbar_expect_tx(bar(kBarTma), 65536u);
+                tma_load_4d(base + kRawQ, &tm_q, 0, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawQ + 8192, &tm_q, 64, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawK, &tm_k, 0, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawK + 8192, &tm_k, 64, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawB, &tm_b, 0, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawB + 8192, &tm_b, 64, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawG, &tm_g, 0, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawG + 8192, &tm_g, 64, h, t0, bi, bar(kBarTma));
+            };
+            uint32_t ph_chain = 0, ph_mma2 = 0, ph_ap = 0, ph_a0 = 0, ph_a1 = 0, ph_p1 = 0;
+            int issued = 0;
+            bool ok = true;
+            if (nchunks > 0) { issue_loads(0); issued = 1; }
+#pragma unroll 1
+            for (int it = 0; it <= nchunks && ok; ++it) {
+                const bool has_prep = it < nchunks, has_chain = it > 0;
+                if (has_chain) {
+                    // [E; O] (hi | lo halves) = A0 [U_hi^T; U_lo^T] + A1 S^T, the d_k sum split over both halves
+                    ok = mbar_wait(bar(kRdyChain), ph_chain); ph_chain ^= 1u;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s)
+                        mma_ts(tmem + kTmEO, tmem + kTmA0 + 8u * s, umma_desc(kstep(base + kEU, 16384, s)),
+                               idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s) {
+                        mma_ts(tmem + kTmEO, tmem + kTmA1 + 8u * s, umma_desc(kstep(base + kSt, 8192, s)),
+                               idesc_tf32(128, kDVT), 1u);
+                        mma_ts(tmem + kTmEO + 64u, tmem + kTmA1 + 8u * (s + 8),
+                               umma_desc(kstep(base + kSt, 8192, s + 8)), idesc_tf32(128, kDVT), 1u);
+                    }
+                    mma_commit(bar(kDoneC1));
+                    // Kb^T [E_hi^T; E_lo^T] -> the same 128 columns
+                    ok = mbar_wait(bar(kRdyMma2), ph_mma2); ph_mma2 ^= 1u;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s)
+                        mma_ts(tmem + kTmEO, tmem + kTmA2 + 8u * s, umma_desc(kstep(base + kEU, 16384, s)),
+                               idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                    mma_commit(bar(kDoneC2));
+                }
+                if (has_prep) {
+                    // intra-chunk products [Ct; Qt] x [G3|G1]^T and x [G2|G0]^T, interleaved
+                    ok = mbar_wait(bar(kRdyAP), ph_ap); ph_ap ^= 1u;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < 16; ++s) {
+                        const uint64_t a = umma_desc(kstep(base + kOpA, 16384, s));
+                        mma_ss(tmem + kTmAP, a, umma_desc(kstep(base + kG31, 12288, s)), idesc_tf32(128, 96),
+                               s > 0 ? 1u : 0u);
+                        mma_ss(tmem + kTmAP + 96u, a, umma_desc(kstep(base + kG20, 8192, s)), idesc_tf32(128, 64),
+                               s > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(kDoneP1));
+                    ok = mbar_wait(bar(kDoneP1), ph_p1); ph_p1 ^= 1u;   // the raw area is free again
+                    if (!ok) break;
+                    if (it + 1 < nchunks) { issue_loads(it + 1); ++issued; }
+                    // A0 = [I; A_qk] T = [T; A_qk T]
+                    ok = mbar_wait(bar(kRdyA0), ph_a0); ph_a0 ^= 1u;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s)
+                        mma_ss(tmem + kTmA0, umma_desc(kstep(base + kIA, 16384, s)),
+                               umma_desc(kstep(base + kTT, 8192, s)), idesc_tf32(128, 64), s > 0 ? 1u : 0u);
+                    mma_commit(bar(kDoneP2));
+                    // A1 = A0 (-Cb^T) = [-W; -A_qk W]
+                    ok = mbar_wait(bar(kRdyA1), ph_a1); ph_a1 ^= 1u;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s)
+                        mma_ts(tmem + kTmA1, tmem + kTmA0 + 8u * s, umma_desc(kstep(base + kCbT, 16384, s)),
+                               idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                    mma_commit(bar(kDoneP3));
+                }
+            }
+            if (!ok) {
+                atomicExch(prm.err, kDevTimeout);
+                // a tile load may still be in flight: wait for it (bounded) before exiting
+                if (issued > 0) mbar_wait(bar(kBarTma), static_cast<uint32_t>((issued - 1) & 1));
+            }
         }
-    }
-
-    uint32_t mma_phase = 0;
-    int loads_done = 0;               // chunks whose raw tiles have arrived
-    bool failed = false;
-    auto mma_wait = [&]() -> bool {
-        const bool ok = mbar_wait(bar_mma, mma_phase);
-        mma_phase ^= 1u;
-        const bool bad = __syncthreads_or(!ok);
-        tc_fence_after();
-        return !bad;
-    };
-    // Make generic-proxy smem writes visible to the tensor core, then issue.
-    auto sync_for_mma = [&]() {
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    };
-
-    for (int n = 0; n < nchunks && !failed; ++n) {
-        const int t0 = n * kC;
-        const int nv = min(kC, T - t0);
+        __syncwarp();
+    } else {
+        // ================= 16 elementwise / accumulator warps ====================
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSimt));
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        // fp32 state slice S[j][j0 + 16R + jj], jj = 0..15, held in registers; S^T operand.
         {
-            const bool ok = mbar_wait(bar_tma, static_cast<uint32_t>(n & 1));
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            loads_done = n + 1;
+            const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R
+                                     : nullptr;
+            float S[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                S[jj] = s0 ? s0[jj] : 0.f;
+                F[(kSt + sw(8192, 16 * R + jj, j)) >> 2] = tf32r(S[jj]);
+            }
+            tmem_st16(tmem + lane_base + kTmS + static_cast<uint32_t>(16 * R), S);
+            tmem_st_wait();
         }
-
-        // ---- P1: cumulative decay and the decay factors about each sub-chunk's reference
-        float rho[16], irho[16];
-        float gmu, emu, eCmu, gamma;
-        {
-            float Gm[16];
-            float acc = 0.f;
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                acc += ld_bf16(sw_bf16(base + kRawG, 64, 16 * R + s, c));
-                Gm[s] = acc;
-            }
-            __syncthreads();   // every g value is in registers: the g tile becomes scratch
-            st_f32(base + kTot + (R * 128 + c) * 4, acc);
-            __syncthreads();
-            float pre = 0.f, gC = 0.f;
-#pragma unroll
-            for (int r2 = 0; r2 < 4; ++r2) {
-                const float t = ld_f32(base + kTot + (r2 * 128 + c) * 4);
-                gC += t;
-                if (r2 < R) pre += t;
-            }
-            gmu = Gm[7] + pre;
-            st_f32(base + kMid + (R * 128 + c) * 4, gmu);
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const float d = Gm[s] + pre - gmu;
-                rho[s] = __expf(fminf(d, 80.f));
-                irho[s] = __expf(fminf(-d, 80.f));
-            }
-            emu = __expf(gmu);           // e^{G_m}       (<= 1)
-            eCmu = __expf(gC - gmu);     // e^{G_C - G_m} (<= 1)
-            gamma = __expf(gC);          // e^{G_C}
-        }
-        // [Ct; Qt]: rows scaled by e^{G_r - G_m(r)}
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const int r = 16 * R + s;
-            const float kv = ld_bf16(sw_bf16(base + kRawK, 64, r, c));
-            const float bv = ld_bf16(sw_bf16(base + kRawB, 64, r, c));
-            const float qv = ld_bf16(sw_bf16(base + kRawQ, 64, r, c));
-            st_f32(sw_f32(base + kOpA, 128, r, c), tf32r(bv * kv * rho[s]));
-            st_f32(sw_f32(base + kOpA, 128, 64 + r, c), tf32r(qv * rho[s]));
-        }
-        __syncthreads();   // kMid visible to all
-
-        // ---- intra-chunk products.  Key-column group g holds k_i * e^{G_m(g) - G_i}
-        // for i < 16(g+1).  Pass 0: group 3 (kOpB) -> TMEM columns 0..63 and
-        // group 1 (kXE) -> 128..159; pass 1: groups 2 and 0 (kOpB) -> 64..127.
-        auto put_group = [&](int grp, uint32_t buf, uint32_t rows, int row0) {
-            if (grp < R) return;
-            const float sc = grp == R ? 1.f : __expf(ld_f32(base + kMid + (grp * 128 + c) * 4) - gmu);
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const int i = 16 * R + s;
-                const float kv = ld_bf16(sw_bf16(base + kRawK, 64, i, c));
-                st_f32(sw_f32(buf, rows, row0 + i, c), tf32r(kv * irho[s] * sc));
-            }
+        uint32_t ph_tma = 0, ph_c1 = 0, ph_c2 = 0, ph_p1 = 0, ph_p2 = 0, ph_p3 = 0;
+        bool failed = false;
+        float gamma_prev = 1.f;   // e^{G_C} of the chunk whose state pass comes next, channel j
+        auto wait_done = [&](uint32_t b, uint32_t& ph) -> bool {
+            const bool ok = mbar_wait(bar(b), ph);
+            ph ^= 1u;
+            const bool bad = simt_any(!ok);
+            tc_fence_after();
+            return !bad;
         };
-        put_group(3, base + kOpB, 64, 0);
-        put_group(1, base + kXE, 32, 0);
-        sync_for_mma();
-        if (tid == 0) {
-            mma_tile(tmem + kTmA, base + kOpA, 128, base + kOpB, 64, kDK, idesc_tf32(128, 64));
-            mma_tile(tmem + kTmA + 128, base + kOpA, 128, base + kXE, 32, kDK, idesc_tf32(128, 32));
-            mma_commit(bar_mma);
-        }
-        if (!mma_wait()) { failed = true; break; }
-        put_group(2, base + kOpB, 64, 0);
-        put_group(0, base + kOpB, 64, 48);
-        sync_for_mma();
-        if (tid == 0) {
-            mma_tile(tmem + kTmA + 64, base + kOpA, 128, base + kOpB, 64, kDK, idesc_tf32(128, 64));
-            mma_commit(bar_mma);
-        }
-        if (!mma_wait()) { failed = true; break; }
+        // Publish smem / TMEM writes of all 16 warps, then signal the MMA warp.
+        auto signal = [&](uint32_t b) {
+            fence_async_smem();
+            tc_fence_before();
+            simt_sync();
+            if (tid == 0) mbar_arrive(bar(b));
+        };
 
-        // ---- A_kk -> padded fp32 staging (solve input); A_qk -> rows 64..127 of the
-        // [T; A_qk] operand (tf32, zero above the diagonal).  T staging zeroed.
-        for (int e = tid; e < 1024; e += kThreads) {   // operand rows 64..127, both K-blocks
-            const uint32_t kb = static_cast<uint32_t>(e >> 9), rw = 64u + ((e >> 3) & 63), ch = e & 7;
-            asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(base + kOpB + kb * 16384u + rw * 128u + ch * 16u), "f"(0.f) : "memory");
-        }
-        for (int e = tid; e < 64 * kLd; e += kThreads) st_f32(base + kStT + e * 4, 0.f);
-        __syncthreads();
-        {
-            const int q2 = quarter & 1;                 // lanes 0-15: group 2*q2, 16-31: group 2*q2+1
-            const int rr = q2 * 32 + lane;              // row of A_kk (quarters 0,1) or A_qk (2,3)
-            const int Rr = rr >> 4;
-            const bool is_q = quarter >= 2;
-            int pieces[2], np = 0;
-            if (q2 == 0) { if (R < 3) pieces[np++] = 7 + R; }
-            else { pieces[np++] = R; if (R + 4 < 7) pieces[np++] = R + 4; }
-            for (int pi = 0; pi < np; ++pi) {
+        for (int it = 0; it <= nchunks && !failed; ++it) {
+            const bool has_prep = it < nchunks;
+            const bool has_chain = it > 0;
+            const int tp = it * kC;                  // first token of the prepared chunk
+            const int tc = (it - 1) * kC;            // first token of the chained chunk
+
+            // ---- (b) prep pass 1 -------------------------------------------------------
+            // This chunk's -Cb, Qb and Kb for the stripe's 16 tokens, kept until their
+            // buffers are free.  All three are bounded by 2 in magnitude and later rounded
+            // to tf32 (11 significant bits), so fp16 pairs carry them exactly enough.
+            __half2 cbp[8], qbp[8], kbp[8];
+            float gam = 1.f;
+            if (has_prep) {
+                float cr[16], qr[16], kr[16];     // c*rho, q*rho, k/rho
+                {
+                    const bool ok = mbar_wait(bar(kBarTma), ph_tma);
+                    ph_tma ^= 1u;
+                    if (simt_any(!ok)) { failed = true; break; }
+                }
+                // raw loads: element (token 16R+s, channel j) of a bf16 tile
+                const uint32_t cbase = (static_cast<uint32_t>(j) >> 6) * 8192u +
+                                       static_cast<uint32_t>(16 * R) * 128u + ((static_cast<uint32_t>(j) & 7u) << 1);
+                const uint32_t c8 = (static_cast<uint32_t>(j) & 63u) >> 3;
+                float Gl[16];
+                float acc = 0.f;
+#pragma unroll
+                for (int s = 0; s < 16; ++s) {
+                    const uint32_t off =
+                        cbase + static_cast<uint32_t>(s) * 128u + ((c8 ^ (static_cast<uint32_t>(s) & 7u)) << 4);
+                    acc += __uint_as_float(static_cast<uint32_t>(H16[(kRawG + off) >> 1]) << 16);
+                    Gl[s] = acc;
+                    const float kv = __uint_as_float(static_cast<uint32_t>(H16[(kRawK + off) >> 1]) << 16);
+                    cr[s] = __uint_as_float(static_cast<uint32_t>(H16[(kRawB + off) >> 1]) << 16) * kv;
+                    qr[s] = __uint_as_float(static_cast<uint32_t>(H16[(kRawQ + off) >> 1]) << 16);
+                    kr[s] = kv;
+                }
+                F[(kXTot >> 2) + R * 128 + j] = acc;
+                F[(kXMid >> 2) + R * 128 + j] = Gl[7];
+                simt_sync();   // raw tiles fully read; stripe sums visible
+                float gmid[4];
+                float gC = 0.f;
+#pragma unroll
+                for (int r2 = 0; r2 < 4; ++r2) {
+                    gmid[r2] = gC + F[(kXMid >> 2) + r2 * 128 + j];
+                    gC += F[(kXTot >> 2) + r2 * 128 + j];
+                }
+                const float gm = gmid[R];
+                const float em = __expf(gm);          // e^{G_m}        (<= 1)
+                const float ecm = __expf(gC - gm);    // e^{G_C - G_m}  (<= 1)
+                gam = __expf(gC);                     // e^{G_C}
+#pragma unroll
+                for (int s = 0; s < 16; ++s) {
+                    const float d = Gl[s] - Gl[7];
+                    const float rho = __expf(fminf(d, 80.f)), irho = __expf(fminf(-d, 80.f));
+                    cr[s] *= rho;
+                    qr[s] *= rho;
+                    kr[s] *= irho;
+                }
+                simt_sync();   // exchange reads done before [Ct; Qt] overwrites it
+#pragma unroll
+                for (int s = 0; s < 16; ++s) {
+                    const uint32_t r = static_cast<uint32_t>(16 * R + s);
+                    F[(kOpA + sw(16384, r, j)) >> 2] = tf32r(cr[s]);
+                    F[(kOpA + sw(16384, 64u + r, j)) >> 2] = tf32r(qr[s]);
+                }
+                // K-groups: this stripe's tokens scaled to each later stripe's reference
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (g < R) continue;
+                    const float sc = g == R ? 1.f : __expf(gmid[g] - gm);
+                    const uint32_t gb = g == 3 ? kG31 : g == 1 ? kG31 : kG20;
+                    const uint32_t ks = g == 3 || g == 1 ? 12288u : 8192u;
+                    const uint32_t r0 = g == 1 ? 64u : g == 0 ? 48u : 0u;
+#pragma unroll
+                    for (int s = 0; s < 16; ++s)
+                        F[(gb + sw(ks, r0 + static_cast<uint32_t>(16 * R + s), j)) >> 2] = tf32r(kr[s] * sc);
+                }
+#pragma unroll
+                for (int s = 0; s < 16; s += 2) {
+                    cbp[s / 2] = __floats2half2_rn(-cr[s] * em, -cr[s + 1] * em);
+                    qbp[s / 2] = __floats2half2_rn(qr[s] * em, qr[s + 1] * em);
+                    kbp[s / 2] = __floats2half2_rn(kr[s] * ecm, kr[s + 1] * ecm);
+                }
+                signal(kRdyAP);
+            }
+
+            // w, v of the prepared chunk (consumed after the state pass) for U = w * v: token tu, d_v columns 8*cu .. +7
+            const int tu = tid & 63, cu = tid >> 6;
+            uint4 vraw = make_uint4(0, 0, 0, 0), wraw = vraw;
+            if (has_prep && tp + tu < T) {
+                const int64_t off = ((static_cast<int64_t>(bi) * T + tp + tu) * prm.H + h) * prm.dv + j0 + 8 * cu;
+                vraw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(prm.v) + off);
+                wraw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(prm.w) + off);
+            }
+
+            // ---- (c) chain: E -> [E_hi^T; E_lo^T], O -> global ---------------------------
+            if (has_chain) {
+                if (!wait_done(kDoneC1, ph_c1)) { failed = true; break; }
                 float v[16];
-                tmem_ld16(tmem + lane_base + kTmA + static_cast<uint32_t>(pieces[pi]) * 16u, v);
+                tmem_ld16_pair(tmem + lane_base + kTmEO + static_cast<uint32_t>(16 * R), v);
+                if (quarter < 2) {
+                    const uint32_t r = static_cast<uint32_t>(j);       // token of the chained chunk
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    int i;
-                    const int g = group_of_col(pieces[pi] * 16 + e, &i);
-                    if (g != Rr) continue;
-                    if (!is_q) {
-                        if (i < rr) st_f32(base + kStAkk + (rr * kLd + i) * 4, v[e]);
-                    } else if (i <= rr) {
-                        st_f32(sw_f32(base + kOpB, 128, 64 + rr, i), tf32r(v[e]));
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const uint32_t n = static_cast<uint32_t>(16 * R + jj);
+                        const float eh = tf32r(v[jj]);
+                        F[(kEU + sw(16384, n, r)) >> 2] = eh;
+                        F[(kEU + sw(16384, 64u + n, r)) >> 2] = tf32r(v[jj] - eh);
                     }
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- T = (I + A_kk)^-1.  16x16 diagonal blocks by column forward substitution
-        if (tid < 64) {
-            const int o16 = 16 * (tid >> 4), col = tid & 15;
-            float tcol[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) tcol[r] = r == col ? 1.f : 0.f;
-#pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                float sum = 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i)
-                    sum = fmaf(ld_f32(base + kStAkk + ((o16 + r) * kLd + o16 + i) * 4), tcol[i], sum);
-                if (r > col) tcol[r] = -sum;
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) st_f32(base + kStT + ((o16 + r) * kLd + o16 + col) * 4, tcol[r]);
-        }
-        __syncthreads();
-        // off-diagonal blocks, level d = Rb - I:  T_{Rb,I} = -T_{Rb,Rb} sum_{J=I}^{Rb-1} A_{Rb,J} T_{J,I}
-        // one warp per block; lane -> row lane/2, columns 8*(lane&1) .. +7
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            const int rr = lane >> 1, c8 = 8 * (lane & 1);
-            const int bI = warp, Rb = d + warp;
-            if (warp < 4 - d) {
-                float p[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) p[e] = 0.f;
-#pragma unroll 1
-                for (int J = bI; J < Rb; ++J) {
-#pragma unroll
-                    for (int k16 = 0; k16 < 16; ++k16) {
-                        const int kk = 16 * J + k16;
-                        const float a = ld_f32(base + kStAkk + ((16 * Rb + rr) * kLd + kk) * 4);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            p[e] = fmaf(a, ld_f32(base + kStT + (kk * kLd + 16 * bI + c8 + e) * 4), p[e]);
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) st_f32(base + kStP + (bI * 16 * 17 + rr * 17 + c8 + e) * 4, p[e]);
-            }
-            __syncthreads();
-            if (warp < 4 - d) {
-                float t[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t[e] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const float a = ld_f32(base + kStT + ((16 * Rb + rr) * kLd + 16 * Rb + kk) * 4);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        t[e] = fmaf(a, ld_f32(base + kStP + (bI * 16 * 17 + kk * 17 + c8 + e) * 4), t[e]);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) st_f32(base + kStT + ((16 * Rb + rr) * kLd + 16 * bI + c8 + e) * 4, -t[e]);
-            }
-            __syncthreads();
-        }
-        // T -> rows 0..63 of the [T; A_qk] operand
-        {
-            const int cc = tid & 63;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int r = (tid >> 6) + 8 * m;
-                st_f32(sw_f32(base + kOpB, 128, r, cc), tf32r(ld_f32(base + kStT + (r * kLd + cc) * 4)));
-            }
-        }
-        __syncthreads();   // staging reads done before [Cb; Qb] overwrites the area
-
-        // ---- [Cb; Qb] = [c * e^{G}; q * e^{G}] rows, then MMA1: [Cb S ; Qb S]
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const int r = 16 * R + s;
-            const float eg = rho[s] * emu;
-            const float kv = ld_bf16(sw_bf16(base + kRawK, 64, r, c));
-            const float bv = ld_bf16(sw_bf16(base + kRawB, 64, r, c));
-            const float qv = ld_bf16(sw_bf16(base + kRawQ, 64, r, c));
-            st_f32(sw_f32(base + kOpA, 128, r, c), tf32r(bv * kv * eg));
-            st_f32(sw_f32(base + kOpA, 128, 64 + r, c), tf32r(qv * eg));
-        }
-        sync_for_mma();
-        if (tid == 0) {
-            mma_tile(tmem + kTmD1, base + kOpA, 128, base + kSt, 64, kDK, idesc_tf32(128, kDVT));
-            mma_commit(bar_mma);
-        }
-        if (!mma_wait()) { failed = true; break; }
-
-        // ---- X = U - Cb S (rows 0..63) -> X^T operand as a tf32 pair; Kb^T operand
-        if (quarter < 2) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + kTmD1 + static_cast<uint32_t>(R) * 16u, v);
-            const int r = quarter * 32 + lane;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int j = 16 * R + jj;
-                const float u = ld_bf16(sw_bf16(base + kRawW, 64, r, j)) * ld_bf16(sw_bf16(base + kRawV, 64, r, j));
-                const float x = u - v[jj], xh = tf32r(x);
-                st_f32(sw_f32(base + kXE, 64, j, r), xh);
-                st_f32(sw_f32(base + kLo, 64, j, r), tf32r(x - xh));
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const int r = 16 * R + s;
-            const float kv = ld_bf16(sw_bf16(base + kRawK, 64, r, c));
-            st_f32(sw_f32(base + kOpA, 128, c, r), tf32r(kv * eCmu * irho[s]));
-        }
-        sync_for_mma();
-        if (tid == 0) {   // MMA2: [T; A_qk] (X_hi + X_lo) -> rows 0..63 = E
-            mma_tile(tmem + kTmD2, base + kOpB, 128, base + kXE, 64, kC, idesc_tf32(128, kDVT));
-            mma_tile(tmem + kTmD2, base + kOpB, 128, base + kLo, 64, kC, idesc_tf32(128, kDVT), true);
-            mma_commit(bar_mma);
-            if (n + 1 < nchunks) issue_loads(n + 1);   // every read of the raw tiles is done
-        }
-        if (!mma_wait()) { failed = true; break; }
-
-        // ---- E (rows 0..63) -> E^T operand as a tf32 pair
-        if (quarter < 2) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + kTmD2 + static_cast<uint32_t>(R) * 16u, v);
-            const int r = quarter * 32 + lane;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const float eh = tf32r(v[jj]);
-                st_f32(sw_f32(base + kXE, 64, 16 * R + jj, r), eh);
-                st_f32(sw_f32(base + kLo, 64, 16 * R + jj, r), tf32r(v[jj] - eh));
-            }
-        }
-        sync_for_mma();
-        if (tid == 0) {
-            // MMA3: Kb^T E -> D3.  MMA_O: [T; A_qk] E accumulated onto [Cb S; Qb S]:
-            // rows 64..127 become O = Qb S + A_qk E (rows 0..63 are not used).
-            mma_tile(tmem + kTmD3, base + kOpA, 128, base + kXE, 64, kC, idesc_tf32(128, kDVT));
-            mma_tile(tmem + kTmD3, base + kOpA, 128, base + kLo, 64, kC, idesc_tf32(128, kDVT), true);
-            mma_tile(tmem + kTmD1, base + kOpB, 128, base + kXE, 64, kC, idesc_tf32(128, kDVT), true);
-            mma_tile(tmem + kTmD1, base + kOpB, 128, base + kLo, 64, kC, idesc_tf32(128, kDVT), true);
-            mma_commit(bar_mma);
-        }
-        if (!mma_wait()) { failed = true; break; }
-
-        // ---- S <- diag(e^{G_C}) S + Kb^T E; refresh the S^T operand; store O
-        {
-            float v[16];
-            tmem_ld16(tmem + lane_base + kTmD3 + static_cast<uint32_t>(R) * 16u, v);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                S[jj] = fmaf(gamma, S[jj], v[jj]);
-                st_f32(sw_f32(base + kSt, 64, 16 * R + jj, c), tf32r(S[jj]));
-            }
-        }
-        if (quarter >= 2) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + kTmD1 + static_cast<uint32_t>(R) * 16u, v);
-            const int r = quarter * 32 + lane - 64;
-            if (r < nv) {
-                const int64_t off = ((static_cast<int64_t>(bi) * T + t0 + r) * prm.H + h) * prm.dv + j0 + 16 * R;
-                if (prm.out_bf16) {
-                    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 2)
-                        *reinterpret_cast<__nv_bfloat162*>(op + jj) = __floats2bfloat162_rn(v[jj], v[jj + 1]);
                 } else {
-                    float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+                    const int r = j - 64;
+                    if (tc + r < T) {
+                        const int64_t off =
+                            ((static_cast<int64_t>(bi) * T + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                        if (prm.out_bf16) {
+                            __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
+                            uint4 pk[2];
+                            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4) op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                            for (int jj = 0; jj < 16; jj += 2) {
+                                __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                                pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
+                            }
+                            reinterpret_cast<uint4*>(op)[0] = pk[0];
+                            reinterpret_cast<uint4*>(op)[1] = pk[1];
+                        } else {
+                            float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+#pragma unroll
+                            for (int jj = 0; jj < 16; jj += 4)
+                                op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                        }
+                    }
                 }
+                signal(kRdyMma2);
+            }
+
+            // ---- (e) chain: S <- gamma S + Kb^T E; then this chunk's Kb^T and U operands ---
+            if (has_chain) {
+                if (!wait_done(kDoneC2, ph_c2)) { failed = true; break; }
+                uint32_t a[16], b[16], c[16];
+                tmem_ld16_nw(tmem + lane_base + kTmEO + static_cast<uint32_t>(16 * R), a);
+                tmem_ld16_nw(tmem + lane_base + kTmEO + 64u + static_cast<uint32_t>(16 * R), b);
+                tmem_ld16_nw(tmem + lane_base + kTmS + static_cast<uint32_t>(16 * R), c);
+                tmem_ld_wait();
+                float S[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    S[jj] = fmaf(gamma_prev, __uint_as_float(c[jj]), __uint_as_float(a[jj]) + __uint_as_float(b[jj]));
+                    F[(kSt + sw(8192, static_cast<uint32_t>(16 * R + jj), j)) >> 2] = tf32r(S[jj]);
+                }
+                tmem_st16(tmem + lane_base + kTmS + static_cast<uint32_t>(16 * R), S);
+                tmem_st_wait();
+            }
+            if (has_prep) {
+                float kb[16];
+#pragma unroll
+                for (int s = 0; s < 16; s += 2) {
+                    const float2 f = __half22float2(kbp[s / 2]);
+                    kb[s] = f.x;
+                    kb[s + 1] = f.y;
+                }
+                tmem_st16(tmem + lane_base + kTmA2 + static_cast<uint32_t>(16 * R), kb);
+                const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vraw);
+                const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(&wraw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float u = __bfloat162float(vb[e]) * __bfloat162float(wb[e]);
+                    const float uh = tf32r(u);
+                    const uint32_t n = static_cast<uint32_t>(8 * cu + e);
+                    F[(kEU + sw(16384, n, static_cast<uint32_t>(tu))) >> 2] = uh;
+                    F[(kEU + sw(16384, 64u + n, static_cast<uint32_t>(tu))) >> 2] = tf32r(u - uh);
+                }
+                tmem_st_wait();
+            }
+
+            // ---- (f) prep: A_kk, A_qk; solve; A0; -Cb^T; A1; P ---------------------------
+            if (has_prep) {
+                if (!wait_done(kDoneP1, ph_p1)) { failed = true; break; }
+                // A_kk -> fp32 staging (strictly lower part), A_qk -> rows 64..127 of [I; A_qk]
+                // (tf32, zero above the diagonal), identity -> rows 0..63.  Warp: TMEM lane
+                // quarter, K range [16R, 16R + 16).
+                {
+                    const int m = j;                          // TMEM lane = product row
+                    const int r = m & 63;                     // token row within the chunk
+                    const int s0 = 2 * (quarter & 1);         // the two stripes of this quarter
+                    uint32_t ra[16], rb[16];
+                    if (R <= s0) tmem_ld16_nw(tmem + lane_base + group_col(s0) + 16u * R, ra);
+                    if (R <= s0 + 1) tmem_ld16_nw(tmem + lane_base + group_col(s0 + 1) + 16u * R, rb);
+                    tmem_ld_wait();
+                    const int rs = r >> 4;
+                    const bool have = R <= rs;
+                    float out[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        out[e] = have ? __uint_as_float(rs == s0 ? ra[e] : rb[e]) : 0.f;
+                    if (m < 64) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int i = 16 * R + e;
+                            if (i < r) F[(kSL >> 2) + r * kLd + i] = out[e];
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const int i = 16 * R + e;
+                            *reinterpret_cast<float4*>(sgen + kIA + sw(16384, r, i)) =
+                                make_float4(i == r ? 1.f : 0.f, i + 1 == r ? 1.f : 0.f, i + 2 == r ? 1.f : 0.f,
+                                            i + 3 == r ? 1.f : 0.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const int i = 16 * R + e;
+                            *reinterpret_cast<float4*>(sgen + kIA + sw(16384, m, i)) =
+                                make_float4(i <= r ? tf32r(out[e]) : 0.f, i + 1 <= r ? tf32r(out[e + 1]) : 0.f,
+                                            i + 2 <= r ? tf32r(out[e + 2]) : 0.f, i + 3 <= r ? tf32r(out[e + 3]) : 0.f);
+                        }
+                    }
+                }
+                // T above the diagonal blocks is zero
+                for (int e = tid; e < 6 * 256; e += kSimt) {
+                    const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                    const int Rb = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+                    const int Ib = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+                    F[(kSTs >> 2) + (16 * Rb + rr) * kLd + 16 * Ib + cc] = 0.f;
+                }
+                tc_fence_before();
+                simt_sync();
+
+                // ---- T = (I + A_kk)^-1: 16x16 diagonal blocks by column forward substitution
+                const float* L = F + (kSL >> 2);
+                float* Ts = F + (kSTs >> 2);
+                float* SP = F + (kSP >> 2);
+                if (tid < 64) {
+                    const int o16 = 16 * (tid >> 4), col = tid & 15;
+                    float tcol[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) tcol[r] = r == col ? 1.f : 0.f;
+#pragma unroll
+                    for (int r = 1; r < 16; ++r) {
+                        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < r; ++i) {
+                            const float a = L[(o16 + r) * kLd + o16 + i];
+                            if (i & 1) s1 = fmaf(a, tcol[i], s1); else s0 = fmaf(a, tcol[i], s0);
+                        }
+                        if (r > col) tcol[r] = -(s0 + s1);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) Ts[(o16 + r) * kLd + o16 + col] = tcol[r];
+                }
+                simt_sync();
+                // off-diagonal blocks: with M_{RJ} = T_{RR} A_{RJ} (R > J),
+                //   T_{RI} = -sum_{J=I}^{R-1} M_{RJ} T_{JI}, level by level (R - I = 1, 2, 3).
+                // M_{RJ} is stored as block p = R(R-1)/2 + J (16 x 17 floats each).
+                for (int e = tid; e < 6 * 256; e += kSimt) {
+                    const int p = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                    const int Rb = p == 0 ? 1 : p < 3 ? 2 : 3, Jb = p - Rb * (Rb - 1) / 2;
+                    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        a[x & 3] = fmaf(Ts[(16 * Rb + rr) * kLd + 16 * Rb + x], L[(16 * Rb + x) * kLd + 16 * Jb + cc], a[x & 3]);
+                    SP[p * 272 + rr * 17 + cc] = (a[0] + a[1]) + (a[2] + a[3]);
+                }
+                simt_sync();
+#pragma unroll
+                for (int d = 1; d < 4; ++d) {
+                    for (int e = tid; e < (4 - d) * 256; e += kSimt) {
+                        const int Ib = e >> 8, Rb = Ib + d, rr = (e >> 4) & 15, cc = e & 15;
+                        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int Jd = 0; Jd < d; ++Jd) {
+                            const int Jb = Ib + Jd, p = Rb * (Rb - 1) / 2 + Jb;
+#pragma unroll
+                            for (int x = 0; x < 16; ++x)
+                                a[x & 3] = fmaf(SP[p * 272 + rr * 17 + x], Ts[(16 * Jb + x) * kLd + 16 * Ib + cc], a[x & 3]);
+                        }
+                        Ts[(16 * Rb + rr) * kLd + 16 * Ib + cc] = -((a[0] + a[1]) + (a[2] + a[3]));
+                    }
+                    simt_sync();
+                }
+                // T^T operand: row n (column of T), K = k (row of T)
+                {
+                    const int n = tid & 63, k0 = (tid >> 6) * 8;
+                    float t8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = tf32r(Ts[(k0 + e) * kLd + n]);
+                    *reinterpret_cast<float4*>(sgen + kTT + sw(8192, n, k0)) = make_float4(t8[0], t8[1], t8[2], t8[3]);
+                    *reinterpret_cast<float4*>(sgen + kTT + sw(8192, n, k0 + 4)) =
+                        make_float4(t8[4], t8[5], t8[6], t8[7]);
+                }
+                signal(kRdyA0);
+                // -Cb^T operand (overlaps the A0 product; the solve staging is dead)
+#pragma unroll
+                for (int s = 0; s < 16; s += 4) {
+                    const uint32_t r = static_cast<uint32_t>(16 * R + s);
+                    const float2 a = __half22float2(cbp[s / 2]), b2 = __half22float2(cbp[s / 2 + 1]);
+                    *reinterpret_cast<float4*>(sgen + kCbT + sw(16384, static_cast<uint32_t>(j), r)) =
+                        make_float4(a.x, a.y, b2.x, b2.y);
+                }
+                if (!wait_done(kDoneP2, ph_p2)) { failed = true; break; }   // A0 ready; [I; A_qk], T^T free
+                signal(kRdyA1);
+                // Qb staging (overlaps the A1 product)
+#pragma unroll
+                for (int s = 0; s < 16; s += 2) {
+                    const float2 f = __half22float2(qbp[s / 2]);
+                    F[(kQb >> 2) + (16 * R + s) * kLq + j] = f.x;
+                    F[(kQb >> 2) + (16 * R + s + 1) * kLq + j] = f.y;
+                }
+                gamma_prev = gam;
+                if (!wait_done(kDoneP3, ph_p3)) { failed = true; break; }
+                // P = Qb - A_qk W on lanes 64..127 of A1 (columns 32R .. 32R + 31)
+                if (quarter >= 2) {
+                    const int r = j - 64;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t col = static_cast<uint32_t>(32 * R + 16 * half);
+                        float v[16];
+                        tmem_ld16(tmem + lane_base + kTmA1 + col, v);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const float4 qb = *reinterpret_cast<const float4*>(sgen + kQb + (r * kLq + col + e) * 4);
+                            v[e] += qb.x; v[e + 1] += qb.y; v[e + 2] += qb.z; v[e + 3] += qb.w;
+                        }
+                        tmem_st16(tmem + lane_base + kTmA1 + col, v);
+                    }
+                    tmem_st_wait();
+                }
+                signal(kRdyChain);   // A0, A1, A2, [U_hi^T; U_lo^T] and S^T ready for the next state pass
             }
         }
-        tc_fence_before();
-        __syncthreads();
-    }
 
-    if (failed) {
-        if (tid == 0) {
-            atomicExch(prm.err, kDevTimeout);
-            // a tile load may still be in flight: wait for it (bounded) before exiting
-            if (loads_done < nchunks) mbar_wait(bar_tma, static_cast<uint32_t>(loads_done & 1));
-        }
-    } else if (prm.ST) {
-        float* st = prm.ST + (static_cast<int64_t>(bh) * kDK + c) * prm.dv + j0 + 16 * R;
+        if (failed) {
+            if (tid == 0) atomicExch(prm.err, kDevTimeout);
+        } else if (prm.ST) {
+            float* st = prm.ST + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R;
+            float S[16];
+            tmem_ld16(tmem + lane_base + kTmS + static_cast<uint32_t>(16 * R), S);
 #pragma unroll
-        for (int jj = 0; jj < 16; jj += 4)
-            *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+            for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -673,10 +850,9 @@ bool chunked_bf16_supports(const ForwardArgs& a) {
 }
 
 int launch_chunked_bf16(const ForwardArgs& a, cudaStream_t stream, int* err) {
-    CUtensorMap mq, mk, mb, mg, mv, mw;
+    CUtensorMap mq, mk, mb, mg;
     if (!make_map(&mq, a.q, a.B, a.T, a.H, a.dk) || !make_map(&mk, a.k, a.B, a.T, a.H, a.dk) ||
-        !make_map(&mb, a.b, a.B, a.T, a.H, a.dk) || !make_map(&mg, a.g, a.B, a.T, a.H, a.dk) ||
-        !make_map(&mv, a.v, a.B, a.T, a.H, a.dv) || !make_map(&mw, a.w, a.B, a.T, a.H, a.dv))
+        !make_map(&mb, a.b, a.B, a.T, a.H, a.dk) || !make_map(&mg, a.g, a.B, a.T, a.H, a.dk))
         return GDR2_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -685,10 +861,10 @@ int launch_chunked_bf16(const ForwardArgs& a, cudaStream_t stream, int* err) {
                                         static_cast<int>(kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
-    ChunkParams prm{a.S0, a.o, a.ST, err, static_cast<int>(a.T), static_cast<int>(a.H),
+    ChunkParams prm{a.v, a.w, a.S0, a.o, a.ST, err, static_cast<int>(a.T), static_cast<int>(a.H),
                     static_cast<int>(a.dv), a.out_dtype == GDR2_BF16 ? 1 : 0};
     const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
-    chunk_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, mv, mw, prm);
+    chunk_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 
