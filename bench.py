@@ -163,17 +163,31 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------
 def dist_setup(args):
+    """One process per GPU (torchrun env vars); NCCL on GPUs, gloo without."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
+
+
+def rank_seed(base_seed, rank):
+    """Weak scaling: every rank draws its own independent batch."""
+    return base_seed + rank
+
+
+def aggregate_tokens_per_s(tokens_per_rank, ms_max, world):
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
 
 
 def barrier(world):
@@ -188,7 +202,8 @@ def max_over_ranks(x, world):
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -383,7 +398,7 @@ def main():
     import gated_delta_rule_166_b300 as gdr2
 
     hbm_gbs, bf16_tflops, peak_src = load_peaks()
-    x_host = make_workload(WORKLOAD, seed=cfg["seed"] + rank)
+    x_host = make_workload(WORKLOAD, seed=rank_seed(cfg["seed"], rank))
     x = x_host.to("cuda")
     torch.cuda.synchronize()
 
@@ -398,7 +413,7 @@ def main():
     clocks = clk.summary()
     ms_max = max_over_ranks(ms, world)
     tokens = B * T
-    value = world * tokens / (ms_max / 1e3)
+    value = aggregate_tokens_per_s(tokens, ms_max, world)
 
     kern_ms = sum(per_launch) / len(per_launch)
     nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=False, st=True)
@@ -424,7 +439,7 @@ def main():
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
-        out["e2e"] = {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+        out["e2e"] = {"value": aggregate_tokens_per_s(tokens, e2e_ms, world), "unit": "tokens/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "ms_per_step": e2e_ms}
     if not args.no_decode:
