@@ -90,17 +90,19 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 // pass-1 exchange of per-stripe decay sums (inside [Ct; Qt] before it is written)
 constexpr uint32_t kXTot = kOpA, kXMid = kOpA + 2048;
 // phase (f) scratch inside kOpA .. kOpA + 96 KB (the intra-chunk product operands are dead)
-constexpr int kLd = 65;                              // padded fp32 row (floats)
+constexpr int kLd = 65;                              // A_kk staging row (floats)
+constexpr int kLt = 68;                              // T staging row (floats; rows 16-byte aligned)
 constexpr uint32_t kSL = kOpA;                       // A_kk staging  [64][65] fp32
-constexpr uint32_t kSTs = kOpA + 16640;              // T staging     [64][65] fp32
-constexpr uint32_t kIA = kOpA + 33792;               // [I; A_qk]: 128 rows x 64 K (32 KB)
+constexpr uint32_t kSTs = kOpA + 16640;              // T staging     [64][68] fp32
+constexpr uint32_t kSP = kOpA + 34048;               // solve: 6 blocks M_{RJ} of 16 x 17 fp32
+constexpr uint32_t kIA = kOpA + 40960;               // [I; A_qk]: 128 rows x 64 K (32 KB)
 constexpr uint32_t kTT = kIA + 32768;                // T^T: 64 rows x 64 K (16 KB)
-constexpr uint32_t kSP = kTT + 16384;                // solve: 6 blocks M_{RJ} of 16 x 17 fp32
 constexpr uint32_t kCbT = kOpA;                      // -Cb^T: 128 rows x 64 K (32 KB), after the solve
 constexpr int kLq = 132;                             // padded Qb row (floats)
-constexpr uint32_t kQb = kOpA + 33792;               // Qb [64][132] fp32, after the A0 product
-static_assert(kSP + 6 * 16 * 17 * 4 <= kSt, "solve scratch");
-static_assert(kQb + 64 * kLq * 4 <= kSt, "Qb staging");
+constexpr uint32_t kQb = kOpA + 40960;               // Qb [64][132] fp32, after the A0 product
+static_assert(kSTs + 64 * kLt * 4 <= kSP && kSP + 6 * 16 * 17 * 4 <= kIA, "solve scratch");
+static_assert(kTT + 16384 <= kSt && kQb + 64 * kLq * 4 <= kSt, "phase (f) scratch");
+static_assert(kCbT + 32768 <= kIA, "-Cb^T below [I; A_qk]");
 static_assert(kG31 + 3 * 12288 + 12288 <= kOpA, "K-groups in the raw area");
 static_assert(kSmemAlloc <= 232448, "shared memory");
 // mbarriers (8 bytes each) inside kMisc
@@ -347,7 +349,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 tma_load_4d(base + kRawG, &tm_g, 0, h, t0, bi, bar(kBarTma));
                 tma_load_4d(base + kRawG + 8192, &tm_g, 64, h, t0, bi, bar(kBarTma));
             };
-            uint32_t ph_chain = 0, ph_mma2 = 0, ph_ap = 0, ph_a0 = 0, ph_a1 = 0, ph_p1 = 0;
+            uint32_t ph_chain = 0, ph_mma2 = 0, ph_ap = 0, ph_a0 = 0, ph_a1 = 0, ph_c1 = 0;
             int issued = 0;
             bool ok = true;
             if (nchunks > 0) { issue_loads(0); issued = 1; }
@@ -371,19 +373,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                umma_desc(kstep(base + kSt, 8192, s + 8)), idesc_tf32(128, kDVT), 1u);
                     }
                     mma_commit(bar(kDoneC1));
-                    // Kb^T [E_hi^T; E_lo^T] -> the same 128 columns
-                    ok = mbar_wait(bar(kRdyMma2), ph_mma2); ph_mma2 ^= 1u;
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int s = 0; s < 8; ++s)
-                        mma_ts(tmem + kTmEO, tmem + kTmA2 + 8u * s, umma_desc(kstep(base + kEU, 16384, s)),
-                               idesc_tf32(128, 128), s > 0 ? 1u : 0u);
-                    mma_commit(bar(kDoneC2));
                 }
                 if (has_prep) {
-                    // intra-chunk products [Ct; Qt] x [G3|G1]^T and x [G2|G0]^T, interleaved
+                    // intra-chunk products [Ct; Qt] x [G3|G1]^T and x [G2|G0]^T, interleaved.
+                    // Their accumulator overlaps A1, which the state pass above reads: wait
+                    // for that pass to complete first.
                     ok = mbar_wait(bar(kRdyAP), ph_ap); ph_ap ^= 1u;
+                    if (ok && has_chain) ok = mbar_wait(bar(kDoneC1), ph_c1);
+                    if (has_chain) ph_c1 ^= 1u;
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll 1
@@ -395,13 +392,26 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                s > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(kDoneP1));
-                    ok = mbar_wait(bar(kDoneP1), ph_p1); ph_p1 ^= 1u;   // the raw area is free again
+                }
+                if (has_chain) {
+                    // Kb^T [E_hi^T; E_lo^T] -> the same 128 columns
+                    ok = mbar_wait(bar(kRdyMma2), ph_mma2); ph_mma2 ^= 1u;
                     if (!ok) break;
-                    if (it + 1 < nchunks) { issue_loads(it + 1); ++issued; }
-                    // A0 = [I; A_qk] T = [T; A_qk T]
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s)
+                        mma_ts(tmem + kTmEO, tmem + kTmA2 + 8u * s, umma_desc(kstep(base + kEU, 16384, s)),
+                               idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                    mma_commit(bar(kDoneC2));
+                }
+                if (has_prep) {
+                    // A0 = [I; A_qk] T = [T; A_qk T].  By this signal the elementwise warps
+                    // have read the K-group 3 tile (for Kb^T) and the products are done: the
+                    // raw area may take the next chunk's tiles.
                     ok = mbar_wait(bar(kRdyA0), ph_a0); ph_a0 ^= 1u;
                     if (!ok) break;
                     tc_fence_after();
+                    if (it + 1 < nchunks) { issue_loads(it + 1); ++issued; }
 #pragma unroll 1
                     for (int s = 0; s < 8; ++s)
                         mma_ss(tmem + kTmA0, umma_desc(kstep(base + kIA, 16384, s)),
@@ -683,7 +693,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
                     const int Rb = blk < 3 ? 0 : blk < 5 ? 1 : 2;
                     const int Ib = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
-                    F[(kSTs >> 2) + (16 * Rb + rr) * kLd + 16 * Ib + cc] = 0.f;
+                    F[(kSTs >> 2) + (16 * Rb + rr) * kLt + 16 * Ib + cc] = 0.f;
                 }
                 tc_fence_before();
                 simt_sync();
@@ -708,35 +718,46 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         if (r > col) tcol[r] = -(s0 + s1);
                     }
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) Ts[(o16 + r) * kLd + o16 + col] = tcol[r];
+                    for (int r = 0; r < 16; ++r) Ts[(o16 + r) * kLt + o16 + col] = tcol[r];
                 }
                 simt_sync();
                 // off-diagonal blocks: with M_{RJ} = T_{RR} A_{RJ} (R > J),
                 //   T_{RI} = -sum_{J=I}^{R-1} M_{RJ} T_{JI}, level by level (R - I = 1, 2, 3).
-                // M_{RJ} is stored as block p = R(R-1)/2 + J (16 x 17 floats each).
-                for (int e = tid; e < 6 * 256; e += kSimt) {
-                    const int p = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                // M_{RJ} is stored as block p = R(R-1)/2 + J (16 x 17 floats each).  Each
+                // thread computes 4 adjacent columns of one row.
+                if (tid < 6 * 64) {
+                    const int p = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
                     const int Rb = p == 0 ? 1 : p < 3 ? 2 : 3, Jb = p - Rb * (Rb - 1) / 2;
-                    float a[4] = {0.f, 0.f, 0.f, 0.f};
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        a[x & 3] = fmaf(Ts[(16 * Rb + rr) * kLd + 16 * Rb + x], L[(16 * Rb + x) * kLd + 16 * Jb + cc], a[x & 3]);
-                    SP[p * 272 + rr * 17 + cc] = (a[0] + a[1]) + (a[2] + a[3]);
+                    for (int x = 0; x < 16; ++x) {
+                        const float t = Ts[(16 * Rb + rr) * kLt + 16 * Rb + x];
+                        const float* lr = L + (16 * Rb + x) * kLd + 16 * Jb + c4;
+                        a0 = fmaf(t, lr[0], a0); a1 = fmaf(t, lr[1], a1);
+                        a2 = fmaf(t, lr[2], a2); a3 = fmaf(t, lr[3], a3);
+                    }
+                    float* mp = SP + p * 272 + rr * 17 + c4;
+                    mp[0] = a0; mp[1] = a1; mp[2] = a2; mp[3] = a3;
                 }
                 simt_sync();
 #pragma unroll
                 for (int d = 1; d < 4; ++d) {
-                    for (int e = tid; e < (4 - d) * 256; e += kSimt) {
-                        const int Ib = e >> 8, Rb = Ib + d, rr = (e >> 4) & 15, cc = e & 15;
-                        float a[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (tid < (4 - d) * 64) {
+                        const int Ib = tid >> 6, Rb = Ib + d, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int Jd = 0; Jd < d; ++Jd) {
                             const int Jb = Ib + Jd, p = Rb * (Rb - 1) / 2 + Jb;
 #pragma unroll
-                            for (int x = 0; x < 16; ++x)
-                                a[x & 3] = fmaf(SP[p * 272 + rr * 17 + x], Ts[(16 * Jb + x) * kLd + 16 * Ib + cc], a[x & 3]);
+                            for (int x = 0; x < 16; ++x) {
+                                const float m = SP[p * 272 + rr * 17 + x];
+                                const float4 tv = *reinterpret_cast<const float4*>(Ts + (16 * Jb + x) * kLt + 16 * Ib + c4);
+                                acc.x = fmaf(m, tv.x, acc.x); acc.y = fmaf(m, tv.y, acc.y);
+                                acc.z = fmaf(m, tv.z, acc.z); acc.w = fmaf(m, tv.w, acc.w);
+                            }
                         }
-                        Ts[(16 * Rb + rr) * kLd + 16 * Ib + cc] = -((a[0] + a[1]) + (a[2] + a[3]));
+                        *reinterpret_cast<float4*>(Ts + (16 * Rb + rr) * kLt + 16 * Ib + c4) =
+                            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                     }
                     simt_sync();
                 }
@@ -745,7 +766,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const int n = tid & 63, k0 = (tid >> 6) * 8;
                     float t8[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = tf32r(Ts[(k0 + e) * kLd + n]);
+                    for (int e = 0; e < 8; ++e) t8[e] = tf32r(Ts[(k0 + e) * kLt + n]);
                     *reinterpret_cast<float4*>(sgen + kTT + sw(8192, n, k0)) = make_float4(t8[0], t8[1], t8[2], t8[3]);
                     *reinterpret_cast<float4*>(sgen + kTT + sw(8192, n, k0 + 4)) =
                         make_float4(t8[4], t8[5], t8[6], t8[7]);
