@@ -44,6 +44,8 @@ def lib():
         vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.gdr2_forward.argtypes = [vp] * 9 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward.restype = ci
+        L.gdr2_forward_varlen.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, vp]
+        L.gdr2_forward_varlen.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
         L.gdr2_decode_step.restype = ci
         L.gdr2_device_status.argtypes = [vp]
@@ -121,6 +123,53 @@ def gdr2_forward(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
                                 ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
         raise GDR2Error(st, "gdr2_forward")
+    return o, S_T
+
+
+def gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, o=None, S_T=None,
+                        out_dtype=torch.float32, return_state: bool = True, stream=None):
+    """Prefill over N packed sequences of different lengths.  q, k, b,
+    log_decay: [total_T, H, dk]; v, w: [total_T, H, dv]; cu_seqlens: int32
+    [N + 1] on the same device (sequence n owns rows cu_seqlens[n] ..
+    cu_seqlens[n+1] - 1); S0: [N, H, dk, dv] fp32 or None.  Returns
+    ``(o [total_T, H, dv], S_T [N, H, dk, dv])``."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q and v must be [total_T, H, d]")
+    total, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_forward_varlen runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (total, H, d), dtype, dev)
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D tensor of N + 1 offsets")
+    _check_tokens("cu_seqlens", cu_seqlens, cu_seqlens.shape, torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    if S0 is not None:
+        _check_tokens("S0", S0, (N, H, dk, dv), torch.float32, dev)
+    if o is None:
+        if out_dtype not in _DTYPES:
+            raise ValueError(f"unsupported out_dtype {out_dtype}")
+        o = torch.empty((total, H, dv), dtype=out_dtype, device=dev)
+    else:
+        if o.dtype not in _DTYPES:
+            raise ValueError(f"unsupported o dtype {o.dtype}")
+        _check_tokens("o", o, (total, H, dv), o.dtype, dev)
+    if S_T is None and return_state:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    elif S_T is not None:
+        _check_tokens("S_T", S_T, (N, H, dk, dv), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().gdr2_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
+                                       _ptr(S0), _ptr(o), _ptr(S_T), _ptr(cu_seqlens), N, total, H,
+                                       dk, dv, _DTYPES[dtype], _DTYPES[o.dtype],
+                                       ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_forward_varlen")
     return o, S_T
 
 

@@ -62,45 +62,49 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
 
 using namespace gdr2;
 
-extern "C" int gdr2_forward(const void* q, const void* k, const void* v,
-                            const void* b, const void* w, const void* log_decay,
-                            const float* S0, void* o, float* S_T,
-                            int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
-                            int in_dtype, int out_dtype, cudaStream_t stream) {
-    if (B < 0 || T < 0 || H < 0) return GDR2_ERR_ARG;
+namespace {
+
+// Shared by the fixed-length and the packed-sequence prefill: N sequences of
+// `total` token rows in all; cu (device, N + 1 offsets) or null for N x T rows.
+int forward_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
+                 const void* log_decay, const float* S0, void* o, float* S_T, const int32_t* cu,
+                 int64_t N, int64_t T, int64_t total, int64_t H, int64_t dk, int64_t dv, int in_dtype,
+                 int out_dtype, cudaStream_t stream) {
+    if (N < 0 || T < 0 || total < 0 || H < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
     const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
     const size_t osz = out_dtype == GDR2_F32 ? 4 : 2;
-    int64_t bth = 0, bh = 0, nk = 0, nv = 0, ns = 0;
-    if (!mul_ok(B, T, &bth) || !mul_ok(bth, H, &bth) || !mul_ok(B, H, &bh) ||
-        !mul_ok(bth, dk, &nk) || !mul_ok(bth, dv, &nv) || !mul_ok(bh, dk * dv, &ns) ||
-        nk > INT64_MAX / 4 || ns > INT64_MAX / 4)
+    int64_t rows = 0, bh = 0, nk = 0, nv = 0, ns = 0;
+    if (!mul_ok(total, H, &rows) || !mul_ok(N, H, &bh) || !mul_ok(rows, dk, &nk) || !mul_ok(rows, dv, &nv) ||
+        !mul_ok(bh, dk * dv, &ns) || nk > INT64_MAX / 4 || ns > INT64_MAX / 4)
         return GDR2_ERR_SHAPE;
-    const bool has_tokens = bth > 0;
+    const bool has_tokens = rows > 0;
     if (has_tokens && (!q || !k || !v || !b || !w || !log_decay || !o)) return GDR2_ERR_ARG;
     for (const void* p : {q, k, v, b, w, log_decay, (const void*)S0, (const void*)o, (const void*)S_T})
         if (p && !aligned16(p)) return GDR2_ERR_ALIGN;
+    if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u)) return GDR2_ERR_ALIGN;
 
     const size_t bk = (size_t)nk * esz, bv = (size_t)nv * esz, bs = (size_t)ns * 4;
-    const size_t bo = (size_t)nv * osz;
+    const size_t bo = (size_t)nv * osz, bc = cu ? (size_t)(N + 1) * 4 : 0;
     const void* tok_in[6] = {q, k, b, log_decay, v, w};
     const size_t tok_bytes[6] = {bk, bk, bk, bk, bv, bv};
     if (has_tokens) {
         for (int i = 0; i < 6; ++i)
             if (overlaps(o, bo, tok_in[i], tok_bytes[i])) return GDR2_ERR_ALIAS;
-        if (overlaps(o, bo, S0, bs) || overlaps(o, bo, S_T, bs)) return GDR2_ERR_ALIAS;
+        if (overlaps(o, bo, S0, bs) || overlaps(o, bo, S_T, bs) || overlaps(o, bo, cu, bc)) return GDR2_ERR_ALIAS;
     }
     for (int i = 0; i < 6; ++i)
         if (has_tokens && overlaps(S_T, bs, tok_in[i], tok_bytes[i])) return GDR2_ERR_ALIAS;
     if (S_T && S0 && S_T != S0 && overlaps(S_T, bs, S0, bs)) return GDR2_ERR_ALIAS;
+    if (overlaps(S_T, bs, cu, bc)) return GDR2_ERR_ALIAS;
 
     int* err = nullptr;
     int st = device_setup(&err);
     if (st != GDR2_OK) return st;
     if (bh == 0) return GDR2_OK;
 
-    if (T == 0) {   // no tokens: S_T = S0 (or zeros)
+    if (!has_tokens) {   // no tokens at all: S_T = S0 (or zeros)
         if (!S_T) return GDR2_OK;
         cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
                                         : cudaMemcpyAsync(S_T, S0, bs, cudaMemcpyDeviceToDevice, stream))
@@ -108,9 +112,34 @@ extern "C" int gdr2_forward(const void* q, const void* k, const void* v,
         return e == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
     }
 
-    ForwardArgs a{q, k, v, b, w, log_decay, S0, o, S_T, B, T, H, dk, dv, in_dtype, out_dtype};
+    ForwardArgs a{q, k, v, b, w, log_decay, S0, o, S_T, N, T, H, dk, dv,
+                  reinterpret_cast<const int*>(cu), total, in_dtype, out_dtype};
     if (chunked_bf16_supports(a)) return launch_chunked_bf16(a, stream, err);
     return launch_recurrent(a, stream);
+}
+
+}  // namespace
+
+extern "C" int gdr2_forward(const void* q, const void* k, const void* v,
+                            const void* b, const void* w, const void* log_decay,
+                            const float* S0, void* o, float* S_T,
+                            int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                            int in_dtype, int out_dtype, cudaStream_t stream) {
+    int64_t total = 0;
+    if (B >= 0 && T >= 0 && !mul_ok(B, T, &total)) return GDR2_ERR_SHAPE;
+    return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, nullptr, B, T, total, H, dk, dv, in_dtype,
+                        out_dtype, stream);
+}
+
+extern "C" int gdr2_forward_varlen(const void* q, const void* k, const void* v,
+                                   const void* b, const void* w, const void* log_decay,
+                                   const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
+                                   int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                   int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (N > 0 && !cu_seqlens) return GDR2_ERR_ARG;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
+    return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, cu_seqlens, N, 0, total_T, H, dk, dv,
+                        in_dtype, out_dtype, stream);
 }
 
 extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,

@@ -285,7 +285,9 @@ struct ChunkParams {
     void* o;
     float* ST;
     int* err;
-    int T, H, dv;
+    const int* cu;      // sequence start offsets [N + 1] (packed sequences), or null: all of length T
+    int T, H, dv;       // T: the common length when cu is null
+    int total;          // token rows in the packed [total, H, d] tensors
     int out_bf16;
 };
 
@@ -312,9 +314,19 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int R = (tid >> 7) & 3;     // stripe (elementwise) / 16-column block (accumulator phases)
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int bh = blockIdx.x;
-    const int bi = bh / prm.H, h = bh % prm.H;
+    const int seq = bh / prm.H, h = bh % prm.H;
     const int j0 = blockIdx.y * kDVT;
-    const int T = prm.T;
+    // This sequence's token rows [tok0, tok0 + T) of the packed [total, H, d] tensors.
+    int tok0, T;
+    if (prm.cu) {   // offsets clamped to [0, total] and made non-decreasing
+        const int a = min(max(prm.cu[seq], 0), prm.total);
+        const int e = min(max(prm.cu[seq + 1], a), prm.total);
+        tok0 = a;
+        T = e - a;
+    } else {
+        tok0 = seq * prm.T;
+        T = prm.T;
+    }
     const int nchunks = (T + kC - 1) / kC;
 
     if (tid == 0) {
@@ -340,14 +352,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             auto issue_loads = [&](int n) {
                 const int t0 = n * kC;
                 mbar_expect_tx(bar(kBarTma), 65536u);
-                tma_load_4d(base + kRawQ, &tm_q, 0, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawQ + 8192, &tm_q, 64, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawK, &tm_k, 0, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawK + 8192, &tm_k, 64, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawB, &tm_b, 0, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawB + 8192, &tm_b, 64, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawG, &tm_g, 0, h, t0, bi, bar(kBarTma));
-                tma_load_4d(base + kRawG + 8192, &tm_g, 64, h, t0, bi, bar(kBarTma));
+                tma_load_4d(base + kRawQ, &tm_q, 0, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawQ + 8192, &tm_q, 64, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawK, &tm_k, 0, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawK + 8192, &tm_k, 64, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawB, &tm_b, 0, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawB + 8192, &tm_b, 64, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawG, &tm_g, 0, h, tok0 + t0, 0, bar(kBarTma));
+                tma_load_4d(base + kRawG + 8192, &tm_g, 64, h, tok0 + t0, 0, bar(kBarTma));
             };
             uint32_t ph_chain = 0, ph_mma2 = 0, ph_ap = 0, ph_a0 = 0, ph_a1 = 0, ph_c1 = 0;
             int issued = 0;
@@ -495,15 +507,19 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint32_t c8 = (static_cast<uint32_t>(j) & 63u) >> 3;
                 float Gl[16];
                 float acc = 0.f;
+                // tokens past the sequence end (the next sequence's rows, or the zero fill
+                // past the tensor) enter as q = k = b = log_decay = 0
+                const int nvalid = T - tp - 16 * R;
 #pragma unroll
                 for (int s = 0; s < 16; ++s) {
                     const uint32_t off =
                         cbase + static_cast<uint32_t>(s) * 128u + ((c8 ^ (static_cast<uint32_t>(s) & 7u)) << 4);
-                    acc += __uint_as_float(static_cast<uint32_t>(H16[(kRawG + off) >> 1]) << 16);
+                    const uint32_t live = s < nvalid ? 0xFFFFFFFFu : 0u;
+                    acc += __uint_as_float((static_cast<uint32_t>(H16[(kRawG + off) >> 1]) << 16) & live);
                     Gl[s] = acc;
-                    const float kv = __uint_as_float(static_cast<uint32_t>(H16[(kRawK + off) >> 1]) << 16);
+                    const float kv = __uint_as_float((static_cast<uint32_t>(H16[(kRawK + off) >> 1]) << 16) & live);
                     cr[s] = __uint_as_float(static_cast<uint32_t>(H16[(kRawB + off) >> 1]) << 16) * kv;
-                    qr[s] = __uint_as_float(static_cast<uint32_t>(H16[(kRawQ + off) >> 1]) << 16);
+                    qr[s] = __uint_as_float((static_cast<uint32_t>(H16[(kRawQ + off) >> 1]) << 16) & live);
                     kr[s] = kv;
                 }
                 F[(kXTot >> 2) + R * 128 + j] = acc;
@@ -560,7 +576,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int tu = tid & 63, cu = tid >> 6;
             uint4 vraw = make_uint4(0, 0, 0, 0), wraw = vraw;
             if (has_prep && tp + tu < T) {
-                const int64_t off = ((static_cast<int64_t>(bi) * T + tp + tu) * prm.H + h) * prm.dv + j0 + 8 * cu;
+                const int64_t off = ((static_cast<int64_t>(tok0) + tp + tu) * prm.H + h) * prm.dv + j0 + 8 * cu;
                 vraw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(prm.v) + off);
                 wraw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(prm.w) + off);
             }
@@ -583,7 +599,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const int r = j - 64;
                     if (tc + r < T) {
                         const int64_t off =
-                            ((static_cast<int64_t>(bi) * T + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                            ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
                         if (prm.out_bf16) {
                             __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
                             uint4 pk[2];
@@ -866,14 +882,17 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, 
 }  // namespace
 
 bool chunked_bf16_supports(const ForwardArgs& a) {
-    return a.in_dtype == GDR2_BF16 && a.dk == kDK && (a.dv == 64 || a.dv == 128) && a.T > 0 &&
-           a.T < (1ll << 31) && a.B < (1ll << 31) && a.B * a.H < (1ll << 31) && get_encode() != nullptr;
+    const int64_t total = a.cu ? a.total : a.B * a.T;
+    return a.in_dtype == GDR2_BF16 && a.dk == kDK && (a.dv == 64 || a.dv == 128) && total > 0 &&
+           total < (1ll << 31) && a.B * a.H < (1ll << 31) && get_encode() != nullptr;
 }
 
 int launch_chunked_bf16(const ForwardArgs& a, cudaStream_t stream, int* err) {
+    // token tensors as one packed [1, total, H, d] sequence; each CTA reads its own rows
+    const int64_t total = a.cu ? a.total : a.B * a.T;
     CUtensorMap mq, mk, mb, mg;
-    if (!make_map(&mq, a.q, a.B, a.T, a.H, a.dk) || !make_map(&mk, a.k, a.B, a.T, a.H, a.dk) ||
-        !make_map(&mb, a.b, a.B, a.T, a.H, a.dk) || !make_map(&mg, a.g, a.B, a.T, a.H, a.dk))
+    if (!make_map(&mq, a.q, 1, total, a.H, a.dk) || !make_map(&mk, a.k, 1, total, a.H, a.dk) ||
+        !make_map(&mb, a.b, 1, total, a.H, a.dk) || !make_map(&mg, a.g, 1, total, a.H, a.dk))
         return GDR2_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -882,8 +901,8 @@ int launch_chunked_bf16(const ForwardArgs& a, cudaStream_t stream, int* err) {
                                         static_cast<int>(kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
-    ChunkParams prm{a.v, a.w, a.S0, a.o, a.ST, err, static_cast<int>(a.T), static_cast<int>(a.H),
-                    static_cast<int>(a.dv), a.out_dtype == GDR2_BF16 ? 1 : 0};
+    ChunkParams prm{a.v, a.w, a.S0, a.o, a.ST, err, a.cu, static_cast<int>(a.T), static_cast<int>(a.H),
+                    static_cast<int>(a.dv), static_cast<int>(total), a.out_dtype == GDR2_BF16 ? 1 : 0};
     const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
     chunk_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;

@@ -24,7 +24,9 @@ struct ForwardArgs {
     const float* S0;
     void* o;
     float* ST;
-    int64_t B, T, H, dk, dv;
+    int64_t B, T, H, dk, dv;   // B sequences; T their common length when cu is null
+    const int* cu;             // packed sequences: start offsets [B + 1] on the device, or null
+    int64_t total;             // token rows of the packed tensors (cu != null)
     int in_dtype;        // GDR2_F32 / GDR2_BF16: q, k, v, b, w, log_decay
     int out_dtype;       // GDR2_F32 / GDR2_BF16: o
 };

@@ -29,14 +29,26 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                  const Tin* __restrict__ v, const Tin* __restrict__ b,
                  const Tin* __restrict__ w, const Tin* __restrict__ g,
                  const float* __restrict__ S0, Tout* __restrict__ o,
-                 float* __restrict__ ST, int64_t T, int H, int dv) {
+                 float* __restrict__ ST, int64_t Tfix, int H, int dv,
+                 const int* __restrict__ cu, int64_t total) {
     constexpr int RPL = DK / 32;          // key rows per lane
     constexpr int CPW = kDVT / kNW;       // value columns per warp
     __shared__ float sq[kTB][DK], sk[kTB][DK], sc[kTB][DK], sa[kTB][DK];
     __shared__ float su[kTB][kDVT], so[kTB][kDVT], skq[kTB];
 
     const int64_t bh = blockIdx.x;
-    const int64_t bi = bh / H, h = bh % H;
+    const int64_t seq = bh / H, h = bh % H;
+    // this sequence's token rows [tok0, tok0 + T) of the packed [total, H, d] tensors
+    int64_t tok0, T;
+    if (cu) {   // offsets clamped to [0, total] and made non-decreasing
+        const int64_t a = min(max(static_cast<int64_t>(cu[seq]), int64_t(0)), total);
+        const int64_t e = min(max(static_cast<int64_t>(cu[seq + 1]), a), total);
+        tok0 = a;
+        T = e - a;
+    } else {
+        tok0 = seq * Tfix;
+        T = Tfix;
+    }
     const int j0 = blockIdx.y * kDVT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int jw = warp * CPW;            // first column of this warp within the tile
@@ -55,7 +67,7 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         for (int e = threadIdx.x; e < kTB * DK; e += blockDim.x) {
             const int tt = e / DK, i = e % DK;
             if (tt < n) {
-                const int64_t off = ((bi * T + t0 + tt) * H + h) * DK + i;
+                const int64_t off = ((tok0 + t0 + tt) * H + h) * DK + i;
                 const float kv = to_f32(k[off]);
                 sq[tt][i] = to_f32(q[off]);
                 sk[tt][i] = kv;
@@ -66,7 +78,7 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         for (int e = threadIdx.x; e < kTB * kDVT; e += blockDim.x) {
             const int tt = e / kDVT, j = e % kDVT;
             if (tt < n) {
-                const int64_t off = ((bi * T + t0 + tt) * H + h) * dv + j0 + j;
+                const int64_t off = ((tok0 + t0 + tt) * H + h) * dv + j0 + j;
                 su[tt][j] = to_f32(w[off]) * to_f32(v[off]);
             }
         }
@@ -106,7 +118,7 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         __syncthreads();
         for (int e = threadIdx.x; e < n * kDVT; e += blockDim.x) {
             const int tt = e / kDVT, j = e % kDVT;
-            const int64_t off = ((bi * T + t0 + tt) * H + h) * dv + j0 + j;
+            const int64_t off = ((tok0 + t0 + tt) * H + h) * dv + j0 + j;
             o[off] = from_f32<Tout>(so[tt][j]);
         }
         __syncthreads();
@@ -128,7 +140,8 @@ int launch_typed(const ForwardArgs& a, cudaStream_t stream) {
     auto args = [&](auto kern) {
         kern<<<grid, block, 0, stream>>>(
             (const Tin*)a.q, (const Tin*)a.k, (const Tin*)a.v, (const Tin*)a.b,
-            (const Tin*)a.w, (const Tin*)a.g, a.S0, (Tout*)a.o, a.ST, a.T, (int)a.H, (int)a.dv);
+            (const Tin*)a.w, (const Tin*)a.g, a.S0, (Tout*)a.o, a.ST, a.T, (int)a.H, (int)a.dv, a.cu,
+            a.total);
     };
     switch (a.dk) {
         case 32: args(recurrent_kernel<Tin, Tout, 32>); break;

@@ -100,6 +100,36 @@ int gdr2_forward(const void* q, const void* k, const void* v,
                  int in_dtype, int out_dtype, cudaStream_t stream);
 
 /*
+ * gdr2_forward_varlen -- gdr2_forward over N packed sequences of different
+ * lengths (the serving layout): sequence n owns token rows
+ * [cu_seqlens[n], cu_seqlens[n+1]) of the packed tensors and its own initial
+ * and final state.  Each sequence is an independent recurrence, so the result
+ * for sequence n equals gdr2_forward on that sequence alone.
+ *
+ *   q, k, b, log_decay : [total_T, H, dk]  (in_dtype)
+ *   v, w               : [total_T, H, dv]  (in_dtype)
+ *   cu_seqlens         : [N + 1] int32 DEVICE offsets, non-decreasing, with
+ *                        cu_seqlens[0] = 0 and cu_seqlens[N] = total_T.  The
+ *                        kernels clamp each offset to [0, total_T] and each end
+ *                        to at least its start, so malformed offsets cannot
+ *                        cause out-of-range accesses (they give empty or
+ *                        truncated sequences instead).
+ *   S0                 : [N, H, dk, dv] fp32, or NULL (zeros)
+ *   o                  : [total_T, H, dv] (out_dtype), written for every row
+ *                        that belongs to a sequence
+ *   S_T                : [N, H, dk, dv] fp32, or NULL
+ *
+ * An empty sequence gives S_T = S0 (or zeros).  Errors and aliasing rules are
+ * those of gdr2_forward; o and S_T must not overlap cu_seqlens, and a null
+ * cu_seqlens with N > 0 is GDR2_ERR_ARG.
+ */
+int gdr2_forward_varlen(const void* q, const void* k, const void* v,
+                        const void* b, const void* w, const void* log_decay,
+                        const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
+                        int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                        int in_dtype, int out_dtype, cudaStream_t stream);
+
+/*
  * gdr2_decode_step -- one autoregressive step for every (batch, head), the
  * state updated in place (same equation, one token):
  *

@@ -109,3 +109,21 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 2, 1, 32)
     with pytest.raises(ValueError):
         _lib.gdr2_forward(x, x, x, x, x, x)
+
+
+def varlen_args(N=3, total=10, H=2, dk=64, dv=64, dtype=1, out_dtype=0, **over):
+    names = ["q", "k", "v", "b", "w", "g", "S0", "o", "ST", "cu"]
+    p = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in enumerate(names)}
+    p.update(over)
+    return [p[n] for n in names] + [N, total, H, dk, dv, dtype, out_dtype, None]
+
+
+def test_varlen_rejects_bad_args():
+    L = _lib.lib()
+    assert L.gdr2_forward_varlen(*varlen_args(cu=None)) == ARG
+    assert L.gdr2_forward_varlen(*varlen_args(cu=ctypes.c_void_p(BASE + 9 * GAP + 2))) == ALIGN
+    assert L.gdr2_forward_varlen(*varlen_args(o=ctypes.c_void_p(BASE + 9 * GAP))) == ALIAS   # o over cu
+    assert L.gdr2_forward_varlen(*varlen_args(ST=ctypes.c_void_p(BASE + 9 * GAP))) == ALIAS  # S_T over cu
+    assert L.gdr2_forward_varlen(*varlen_args(dk=48)) == SHAPE
+    assert L.gdr2_forward_varlen(*varlen_args(N=-1)) == ARG
+    assert L.gdr2_forward_varlen(*varlen_args(total=1 << 31)) == SHAPE
