@@ -84,25 +84,26 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files):
+    """Hash of the kernel sources a traffic record was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_166_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_record(kernel_key):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    """dram bytes per launch from the committed ncu summary (profiles/traffic.json),
+    if it was taken on the kernel's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel_key)
     except Exception:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(rec.get("sources", [])):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -344,7 +345,7 @@ def cpu_baseline(x, budget_s=15.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")

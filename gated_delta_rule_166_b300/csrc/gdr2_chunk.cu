@@ -27,7 +27,8 @@
 // ("stripe") holding r: e^{G_r - G_m} * e^{G_m - G_i}.  Row r carries
 // e^{G_r - G_m}; column i is scaled once per stripe R >= stripe(i)
 // ("K-group" R).  For i in an earlier stripe both factors are <= 1; inside
-// the stripe each spans at most 8 tokens (clamped at e^80).
+// the stripe each spans at most 8 tokens, and with per-token log decays
+// floored at -10 it stays within e^{+-80}.
 //
 // Precision: tensor-core operands are tf32 (kind::tf32, fp32 accumulators);
 // U and E, whose rounding the later products amplify most, enter as a tf32
@@ -120,6 +121,11 @@ constexpr uint32_t kTmS = 416;     // fp32 state S[j][j0 + c], lanes = key chann
 constexpr uint32_t kTmCols = 512;
 
 constexpr long long kWaitCycles = 4ll * 1000 * 1000 * 1000;   // ~2 s at 2 GHz
+// Per-token log decays below this are taken as this value: a factor spanning the
+// 8 tokens either side of a stripe's reference then stays within e^{+-80}.  The
+// decay factor e^{-10} = 4.5e-5 instead of a smaller one changes the state carried
+// across such a token by at most 4.5e-5 of itself.
+constexpr float kMinLogDecay = -10.f;
 
 // ---- PTX helpers ---------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -515,7 +521,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const uint32_t off =
                         cbase + static_cast<uint32_t>(s) * 128u + ((c8 ^ (static_cast<uint32_t>(s) & 7u)) << 4);
                     const uint32_t live = s < nvalid ? 0xFFFFFFFFu : 0u;
-                    acc += __uint_as_float((static_cast<uint32_t>(H16[(kRawG + off) >> 1]) << 16) & live);
+                    acc += fmaxf(__uint_as_float((static_cast<uint32_t>(H16[(kRawG + off) >> 1]) << 16) & live),
+                                 kMinLogDecay);
                     Gl[s] = acc;
                     const float kv = __uint_as_float((static_cast<uint32_t>(H16[(kRawK + off) >> 1]) << 16) & live);
                     cr[s] = __uint_as_float(static_cast<uint32_t>(H16[(kRawB + off) >> 1]) << 16) * kv;

@@ -88,10 +88,11 @@ typedef enum {
  * or o and another argument is rejected with GDR2_ERR_ALIAS.
  * Preconditions (not checked): log_decay <= 0 and finite.  The chunked bf16
  * path forms per-channel decay factors about the middle token of each
- * 16-token sub-chunk, each clamped at e^80: it is exact while the decay over
- * any 8 consecutive tokens stays above e^-80 (log_decay above about -10 per
- * token); below that, terms already smaller than e^-80 of the largest are
- * flushed to zero.  The fp32 path and the decode step have no such limit.
+ * 16-token sub-chunk and takes log_decay values below -10 as -10 (a per-token
+ * decay factor of 4.5e-5 instead of a smaller one, e.g. a hard reset at
+ * -inf): the state carried across such a token then differs from the exact
+ * one by at most 4.5e-5 of itself.  The fp32 path and the decode step use
+ * log_decay as given.
  */
 int gdr2_forward(const void* q, const void* k, const void* v,
                  const void* b, const void* w, const void* log_decay,

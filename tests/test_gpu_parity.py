@@ -74,3 +74,19 @@ def test_bf16_output_mode(name):
     x = make_prefill_inputs(2, 300, 4, 128, 128, dtype=torch.bfloat16, seed=5,
                             decay_regime="mixed", s0_std=0.3)
     compare(x, "mixed (bf16 o)", out_dtype=torch.bfloat16)
+
+
+def test_extreme_decays_and_resets():
+    """Per-token log decays far below the chunked path's floor of -10 (-30, and
+    -1e4 as a hard reset) stay within the bar: the floor changes the state
+    carried across such a token by at most e^-10 of itself."""
+    x = make_prefill_inputs(2, 400, 3, 128, 128, dtype=torch.bfloat16, seed=91, decay_regime="slow",
+                            s0_std=0.5)
+    gen = torch.Generator().manual_seed(92)
+    g = x.log_decay.float()
+    hard = torch.rand(g.shape, generator=gen) < 0.05
+    g[hard] = -30.0
+    reset = torch.rand(g.shape[:3], generator=gen) < 0.02          # whole-token resets
+    g[reset] = -1e4
+    x.log_decay = g.to(torch.bfloat16)
+    compare(x, "extreme decays")
