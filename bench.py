@@ -241,6 +241,8 @@ def bench_prefill(gdr2, x, steps, warmup, world):
 
 
 def bench_decode(gdr2, steps=1024, pool=16, seed=5):
+    """1024 in-place decode steps, launched eagerly and replayed from one CUDA
+    graph (the launch-bound inner loop of serving); GB/s from the graph replay."""
     from gated_delta_rule_166_b300.inputs import DECODE_WORKLOAD, make_decode_state, make_decode_token
 
     W = DECODE_WORKLOAD
@@ -248,23 +250,38 @@ def bench_decode(gdr2, steps=1024, pool=16, seed=5):
     S = make_decode_state(B, H, dk, dv, seed=seed).cuda()
     toks = [make_decode_token(B, H, dk, dv, seed=seed, step=s).to("cuda") for s in range(pool)]
     o = torch.empty((B, H, dv), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-    for s in range(8):
-        gdr2.decode_step(*toks[s % pool].tensors(), S, o=o)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for s in range(8):
+            gdr2.decode_step(*toks[s % pool].tensors(), S, o=o)
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for s in range(steps):
-        gdr2.decode_step(*toks[s % pool].tensors(), S, o=o)
-    b.record(stream)
+
+    def timed(fn):
+        stream = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    ms_eager = timed(lambda: [gdr2.decode_step(*toks[s % pool].tensors(), S, o=o) for s in range(steps)])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for s in range(steps):
+            gdr2.decode_step(*toks[s % pool].tensors(), S, o=o)
+    graph.replay()
     torch.cuda.synchronize()
+    ms = timed(graph.replay)
     if gdr2.gdr2_device_status() != 0:
         raise RuntimeError("device-side failure during decode")
-    ms = a.elapsed_time(b)
-    per_step_s = ms / 1e3 / steps
     nbytes = decode_bytes(B, H, dk, dv)
-    return {"workload": f"decode B{B} H{H} d{dk} fp32 state, {steps} in-place steps",
+    per_step_s = ms / 1e3 / steps
+    return {"workload": f"decode B{B} H{H} d{dk} fp32 state, {steps} in-place steps (one CUDA graph)",
             "gbs": nbytes / per_step_s / 1e9, "us_per_step": per_step_s * 1e6,
+            "gbs_eager_launches": nbytes / (ms_eager / 1e3 / steps) / 1e9,
             "tokens_per_s": B * steps / (ms / 1e3), "bytes_per_step": nbytes,
             "launches": steps, "input_pool": pool}
 
