@@ -90,3 +90,17 @@ def test_extreme_decays_and_resets():
     g[reset] = -1e4
     x.log_decay = g.to(torch.bfloat16)
     compare(x, "extreme decays")
+
+
+# The carry-exercising variants at the full shapes of the GDN-2 layer and
+# long-context workloads: slow, zero and mixed decays with a non-zero S0 keep
+# the chunk-to-chunk state and S0 visible in o and S_T over every chunk.
+@pytest.mark.parametrize("regime", ["slow", "zero", "mixed"])
+def test_full_size_carry_variants_layer(regime):
+    x = make_workload("gdn2_layer_T4096", decay_regime=regime, s0_std=0.02)
+    compare(x, f"gdn2_layer_T4096 {regime}")
+
+
+def test_full_size_carry_variant_long():
+    x = make_workload("long_T65536", decay_regime="slow")
+    compare(x, "long_T65536 slow")
