@@ -89,8 +89,11 @@ def kernel_source_hash(files):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_166_b300", "csrc")
     for name in sorted(files):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+        except OSError:
+            return None
     return h.hexdigest()[:16]
 
 
@@ -103,7 +106,8 @@ def traffic_record(kernel_key):
             rec = json.load(f).get(kernel_key)
     except Exception:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash(rec.get("sources", [])):
+    current = kernel_source_hash(rec.get("sources", [])) if rec else None
+    if not rec or current is None or rec.get("source_hash") != current:
         return None
     return rec.get("dram_bytes_per_launch")
 

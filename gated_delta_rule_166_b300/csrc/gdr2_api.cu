@@ -114,7 +114,18 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
 
     ForwardArgs a{q, k, v, b, w, log_decay, S0, o, S_T, N, T, H, dk, dv,
                   reinterpret_cast<const int*>(cu), total, in_dtype, out_dtype};
-    if (chunked_bf16_supports(a)) return launch_chunked_bf16(a, stream, err);
+    if (two_kernel_supports(a)) {
+        // Workspace for the per-chunk operands, stream-ordered from the device's
+        // default memory pool and released on the same stream.
+        const int64_t chunks = prep_chunk_bound(a);
+        void* ws = nullptr;
+        if (cudaMallocAsync(&ws, prep_workspace_bytes(chunks, H, N), stream) != cudaSuccess) return GDR2_ERR_CUDA;
+        const PrepSlots s = prep_carve(ws, chunks, H);
+        int rc = launch_prep(a, s, chunks, stream, err);
+        if (rc == GDR2_OK) rc = launch_state(a, s, chunks, stream, err);
+        if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
+        return rc;
+    }
     return launch_recurrent(a, stream);
 }
 

@@ -44,7 +44,36 @@ struct DecodeArgs {
 // of the library's error word (bounded waits record failures there).
 int launch_recurrent(const ForwardArgs& a, cudaStream_t stream);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
-int launch_chunked_bf16(const ForwardArgs& a, cudaStream_t stream, int* err);
-bool chunked_bf16_supports(const ForwardArgs& a);
+
+// ---- two-kernel chunked prefill (bf16 inputs, d_k = 128) --------------------------
+// The preparation kernel writes, for every 64-token chunk of every (sequence,
+// head), the state-independent operands of that chunk into one workspace slot;
+// the state kernel then carries the state across the chunks of each sequence.
+// Slot index = (global chunk) * H + head, where a sequence's chunks are
+// numbered consecutively from chunk_base[sequence].
+constexpr int kPrepC = 64;     // chunk length
+constexpr int kPrepDK = 128;   // key channels
+// The fp16 arrays are laid out for 16-byte loads whose 32 lanes read 512
+// contiguous bytes in the state kernel: 8 consecutive tokens (-Cb, Kb) or 8
+// consecutive key channels (Qb) per 16-byte group.
+struct PrepSlots {
+    float* a0;         // [slots][128][64]  [T; A_qk T] (rows 0..63 T, 64..127 A_qk T), tf32-rounded fp32
+    uint16_t* cbt;     // [slots][8][128][8]  -Cb: [token / 8][key channel][token % 8], fp16
+    uint16_t* kbt;     // [slots][8][128][8]  Kb, same layout
+    uint16_t* qb;      // [slots][16][64][8]  Qb: [channel / 8][token][channel % 8], fp16
+    float* gam;        // [slots][128]        e^{G_C} per key channel
+    int* chunk_base;   // [N + 1] first global chunk of each packed sequence (null: fixed length)
+};
+constexpr size_t kSlotBytes = 64 * 128 * 4 + 3 * 64 * 128 * 2 + 128 * 4;
+// Global chunks of a call: exact for fixed-length sequences, an upper bound
+// (ceil(total / 64) + N) for packed ones.
+int64_t prep_chunk_bound(const ForwardArgs& a);
+// Workspace bytes for `chunks` global chunks and N sequences; carve() lays the
+// arrays out in `ws` (256-byte aligned).
+size_t prep_workspace_bytes(int64_t chunks, int64_t H, int64_t N);
+PrepSlots prep_carve(void* ws, int64_t chunks, int64_t H);
+int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err);
+int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err);
+bool two_kernel_supports(const ForwardArgs& a);
 
 }  // namespace gdr2

@@ -1,0 +1,583 @@
+// Chunked Gated Delta Rule-2 prefill, part 2 of 2: the chunk-to-chunk state
+// pass, one CTA per (sequence*head, 64-column d_v tile).
+//
+// Method ("Gated DeltaNet-2: Decoupling Erase and Write in Linear Attention"
+// page, "efficient implementation" section: chunkwise algorithm).  With the
+// state-independent operands of each chunk read from its workspace slot
+// (written by the preparation kernel), the chunk with initial state S is
+//     A1 = [T; A_qk T] (-Cb) + [0; Qb] = [-W; P]
+//     [E; O] = [T; A_qk T] U + A1 S,            U = w * v
+//     S <- diag(e^{G_C}) S + Kb^T E
+// The products run on tcgen05 tensor cores (kind::tf32, fp32 accumulators in
+// TMEM); U and E enter as tf32 pairs x = x_hi + x_lo.  Every thread keeps its
+// 16 entries of the fp32 state in registers for the whole sequence.
+//
+// Only A1 S, the E read-out, Kb^T E and the state update are on the
+// chunk-to-chunk chain.  [T; A_qk T] U of the next chunk is issued while the
+// state update runs and A1 of the next chunk while E is read out, so the
+// state-independent products overlap the chain.
+//
+// Operands: [T; A_qk T] (two buffers) and the v, w tiles (two buffers) are
+// TMA-loaded into shared memory; A1 and Kb^T are TMEM-resident A operands;
+// S^T, U^T, E^T and -Cb^T are shared-memory B operands.
+//
+// Work split: 640 threads.  One thread of the last warpgroup issues the TMA
+// loads and all MMAs.  Warp w < 16 owns TMEM lane quarter q = w % 4 (lanes
+// 32q..32q+31) and column block R = w / 4; thread j = tid % 128 is TMEM lane j
+// and key channel j.  Warps of quarters 0-1 read E out (token rows 0..63),
+// warps of quarters 2-3 write O and complete P.  Warps signal the MMA thread
+// through mbarriers (one arrival per warp), so no CTA-wide barrier sits on the
+// chain.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "gdr2.h"
+#include "gdr2_internal.cuh"
+#include "gdr2_tc.cuh"
+
+namespace gdr2 {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = kPrepC;
+constexpr int kDK = kPrepDK;
+constexpr int kDVT = 64;                // value columns per CTA
+constexpr int kSimt = 512;
+constexpr int kThreads = kSimt + 128;
+constexpr int kRegsSimt = 112, kRegsMma = 32;
+static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96, "register pool");
+
+// ---- shared memory (bytes from a 1024-aligned base); K-major, 128-byte swizzle ----
+constexpr uint32_t kA0 = 0;            // two buffers of [T; A_qk T]: 128 rows x 64 K (32 KB each)
+constexpr uint32_t kVW = 65536;        // two buffers of {v, w} bf16 tiles [64 tokens][64 d_v] (16 KB each)
+constexpr uint32_t kCbT = 98304;       // -Cb^T: 128 rows (channels) x 64 K (tokens)
+constexpr uint32_t kSt = 131072;       // S^T: 64 rows (d_v) x 128 K (channels)
+constexpr uint32_t kU = 163840;        // [U_hi^T; U_lo^T]: 128 rows x 64 K (tokens)
+constexpr uint32_t kE = 196608;        // [E_hi^T; E_lo^T]: 128 rows x 64 K (tokens)
+constexpr uint32_t kMisc = 229376;
+enum : uint32_t {
+    kBarA0 = 0, kBarA0b, kBarVW, kBarVWb,         // TMA completions
+    kRdyA1, kRdyU, kRdyChain, kRdyMma2,            // elementwise warps -> MMA thread
+    kDoneC1, kDoneC2, kDoneP3,                     // MMA commits
+    kNumBars
+};
+constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
+constexpr uint32_t kAbort = kTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kMisc + 128;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+static_assert(kAbort + 4 <= kSmemBytes, "misc area");
+static_assert(kSmemAlloc <= 232448, "shared memory");
+
+// ---- TMEM columns ------------------------------------------------------------------
+constexpr uint32_t kTmA1 = 0;      // [-W; P] (A operand, K = 128 channels)
+constexpr uint32_t kTmA2 = 128;    // Kb^T (A operand: lanes = channels, K = 64 tokens)
+constexpr uint32_t kTmEO = 192;    // [E; O] as two 64-column halves (hi | lo products)
+constexpr uint32_t kTmD2 = 320;    // Kb^T E as two 64-column halves
+constexpr int kTmCols = 512;
+
+struct StateParams {
+    PrepSlots s;
+    const float* S0;
+    void* o;
+    float* ST;
+    int* err;
+    const int* cu;
+    int T, H, dv, total, nchunks;   // nchunks: chunks per sequence when cu is null
+    int chunk_bound;                // global chunks with a workspace slot
+    int out_bf16;
+};
+
+// Element (token t, column n) of a TMA-loaded bf16 [64][64] tile (128-byte rows, swizzled).
+__device__ __forceinline__ uint32_t vw_off(int t, int n) {
+    return static_cast<uint32_t>(t) * 128u + ((static_cast<uint32_t>(n >> 3) ^ (static_cast<uint32_t>(t) & 7u)) << 4) +
+           (static_cast<uint32_t>(n & 7) << 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_v,
+             const __grid_constant__ CUtensorMap tm_w, const StateParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));
+    float* const F = reinterpret_cast<float*>(sgen);
+    auto bar = [&](uint32_t i) { return base + kMisc + 8u * i; };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + kAbort);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int j = tid & 127;
+    const int R = (tid >> 7) & 3;
+    const int quarter = warp & 3;
+    const int bh = blockIdx.x;
+    const int seq = bh / prm.H, h = bh % prm.H;
+    const int j0 = blockIdx.y * kDVT;
+    int tok0, T, cb0;
+    if (prm.cu) {
+        const int a = min(max(prm.cu[seq], 0), prm.total);
+        const int e = min(max(prm.cu[seq + 1], a), prm.total);
+        tok0 = a;
+        T = e - a;
+        cb0 = prm.s.chunk_base[seq];
+    } else {
+        tok0 = seq * prm.T;
+        T = prm.T;
+        cb0 = seq * prm.nchunks;
+    }
+    // Well-formed offsets never reach the slot bound; overlapping malformed ones
+    // can, and their chunks past it are not run (the sequence is truncated).
+    const int n = min((T + kC - 1) / kC, max(prm.chunk_bound - cb0, 0));
+    auto slot = [&](int c) { return static_cast<int64_t>(cb0 + c) * prm.H + h; };
+
+    if (tid == 0) {
+        for (uint32_t i = 0; i < kNumBars; ++i) {
+            const uint32_t cnt = (i == kRdyA1 || i == kRdyU || i == kRdyChain) ? 16u : i == kRdyMma2 ? 8u : 1u;
+            mbar_init(bar(i), cnt);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_async_smem();
+    }
+    if (warp == 0) tmem_alloc<kTmCols>(base + kTmemSlot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= kSimt / 32) {
+        // ================= TMA / MMA warpgroup: one elected thread =================
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
+        if (warp == kSimt / 32 && lane == 0) {
+            // TMA batches issued per barrier kBarA0 + i (i = 0..3): any (bit i of iss_any) and
+            // the parity of their count (bit i of iss_par); bit-packed to stay in registers
+            uint32_t iss_any = 0, iss_par = 0;
+            auto load_a0 = [&](int c) {
+                const uint32_t b = bar(kBarA0 + (c & 1));
+                const uint32_t dst = base + kA0 + static_cast<uint32_t>(c & 1) * 32768u;
+                const int row = static_cast<int>(slot(c) * 128);
+                mbar_expect_tx(b, 32768u);
+                tma_load_2d(dst, &tm_a0, 0, row, b);
+                tma_load_2d(dst + 16384u, &tm_a0, 32, row, b);
+                iss_any |= 1u << (c & 1);
+                iss_par ^= 1u << (c & 1);
+            };
+            auto load_vw = [&](int c) {
+                const uint32_t b = bar(kBarVW + (c & 1));
+                const uint32_t dst = base + kVW + static_cast<uint32_t>(c & 1) * 16384u;
+                const int row = tok0 + c * kC;
+                mbar_expect_tx(b, 16384u);
+                tma_load_4d(dst, &tm_v, j0, h, row, 0, b);
+                tma_load_4d(dst + 8192u, &tm_w, j0, h, row, 0, b);
+                iss_any |= 4u << (c & 1);
+                iss_par ^= 4u << (c & 1);
+            };
+            auto wait = [&](uint32_t b, uint32_t& ph) {
+                const bool ok = mbar_wait_ab(bar(b), ph, abort_flag);
+                ph ^= 1u;
+                return ok;
+            };
+            uint32_t ph_a0 = 0, ph_a1 = 0, ph_u = 0, ph_chain = 0, ph_mma2 = 0, ph_c1 = 0;   // ph_a0: bit per buffer
+            // A1(c) = [T; A_qk T](c) (-Cb^T)(c)
+            auto issue_a1 = [&](int c) {
+                if (!wait(kRdyA1, ph_a1)) return false;
+                const uint32_t bit = 1u << (c & 1);
+                const bool landed = mbar_wait_ab(bar(kBarA0 + (c & 1)), (ph_a0 & bit) ? 1u : 0u, abort_flag);
+                ph_a0 ^= bit;
+                if (!landed) return false;
+                tc_fence_after();
+                const uint32_t a0 = base + kA0 + static_cast<uint32_t>(c & 1) * 32768u;
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s)
+                    mma_ss(tmem + kTmA1, umma_desc(kstep(a0, 16384, s)), umma_desc(kstep(base + kCbT, 16384, s)),
+                           idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                mma_commit(bar(kDoneP3));
+                return true;
+            };
+            // [E; O](c) halves := [T; A_qk T](c) [U_hi^T; U_lo^T](c)
+            auto issue_u = [&](int c) {
+                if (!wait(kRdyU, ph_u)) return false;
+                tc_fence_after();
+                const uint32_t a0 = base + kA0 + static_cast<uint32_t>(c & 1) * 32768u;
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s)
+                    mma_ss(tmem + kTmEO, umma_desc(kstep(a0, 16384, s)), umma_desc(kstep(base + kU, 16384, s)),
+                           idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                return true;
+            };
+            bool ok = true;
+            if (n > 0) {
+                load_a0(0);
+                load_vw(0);
+                if (n > 1) { load_a0(1); load_vw(1); }
+                ok = issue_a1(0) && issue_u(0);
+                if (ok && n > 2) load_vw(2);
+            }
+#pragma unroll 1
+            for (int c = 0; c < n && ok; ++c) {
+                // chain: [E; O] += A1 S^T, the d_k sum split over both halves
+                if (!(ok = wait(kRdyChain, ph_chain))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {
+                    mma_ts(tmem + kTmEO, tmem + kTmA1 + 8u * s, umma_desc(kstep(base + kSt, 8192, s)),
+                           idesc_tf32(128, kDVT), 1u);
+                    mma_ts(tmem + kTmEO + 64u, tmem + kTmA1 + 8u * (s + 8), umma_desc(kstep(base + kSt, 8192, s + 8)),
+                           idesc_tf32(128, kDVT), 1u);
+                }
+                mma_commit(bar(kDoneC1));
+                if (c + 1 < n) {
+                    // A1 of the next chunk once this pass has read A1 (runs during the E read-out)
+                    if (!(ok = wait(kDoneC1, ph_c1))) break;
+                    if (!(ok = issue_a1(c + 1))) break;
+                    // every product reading [T; A_qk T](c) is done: its buffer takes chunk c + 2
+                    if (c + 2 < n) load_a0(c + 2);
+                }
+                // chain: Kb^T [E_hi^T; E_lo^T]
+                if (!(ok = wait(kRdyMma2, ph_mma2))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s)
+                    mma_ts(tmem + kTmD2, tmem + kTmA2 + 8u * s, umma_desc(kstep(base + kE, 16384, s)),
+                           idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                mma_commit(bar(kDoneC2));
+                if (c + 1 < n) {
+                    // next chunk's U product (runs during the state update); the v, w
+                    // buffer it was computed from takes chunk c + 3
+                    if (!(ok = issue_u(c + 1))) break;
+                    if (c + 3 < n) load_vw(c + 3);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicExch(prm.err, kDevTimeout);
+                // tile loads may still be in flight: wait for them (bounded) before exiting
+                for (int b = 0; b < 4; ++b)
+                    if ((iss_any >> b) & 1u) mbar_wait(bar(kBarA0 + b), ((iss_par >> b) & 1u) ^ 1u);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= 16 elementwise / accumulator warps ====================
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSimt));
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const bool e_warp = quarter < 2;
+        // fp32 state S[j][j0 + 16R + jj] in registers; the S^T operand in shared memory
+        float S[16];
+        {
+            const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R
+                                     : nullptr;
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4) {
+                const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[jj] = x.x; S[jj + 1] = x.y; S[jj + 2] = x.z; S[jj + 3] = x.w;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) F[(kSt + sw(8192, 16 * R + jj, j)) >> 2] = tf32r(S[jj]);
+        }
+        bool failed = false;
+        uint32_t ph_c1 = 0, ph_c2 = 0, ph_p3 = 0, ph_vw0 = 0, ph_vw1 = 0;
+        auto wait = [&](uint32_t b, uint32_t& ph) {
+            const bool ok = mbar_wait_ab(bar(b), ph, abort_flag);
+            ph ^= 1u;
+            tc_fence_after();
+            return ok;
+        };
+        // Publish this warp's shared-memory / TMEM writes, then one arrival.
+        auto arrive = [&](uint32_t b) {
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(b));
+        };
+        // Workspace operands of chunk c (zeros past the sequence's chunks).
+        struct Ops {
+            uint4 cb[2];   // -Cb, channel j, tokens 16R..16R+15
+            uint4 kb[2];   // Kb, same
+            uint4 qb[4];   // Qb, token j - 64, channels 32R..32R+31 (quarters 2-3)
+            float gam;     // e^{G_C}, channel j
+        };
+        auto ld_cb = [&](int c, uint4 (&x)[2], const uint16_t* arr) {
+            if (c < n) {
+                const uint4* p = reinterpret_cast<const uint4*>(arr + slot(c) * (kDK * kC) + ((2 * R) * kDK + j) * 8);
+                x[0] = p[0];
+                x[1] = p[kDK];
+            } else {
+                x[0] = x[1] = make_uint4(0, 0, 0, 0);
+            }
+        };
+        auto ld_qb = [&](int c, uint4 (&x)[4]) {
+            if (c < n && !e_warp) {
+                const uint4* p = reinterpret_cast<const uint4*>(prm.s.qb + slot(c) * (kC * kDK) +
+                                                                ((4 * R) * kC + (j - 64)) * 8);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = p[k * kC];
+            }
+        };
+        // -Cb^T of one chunk -> its operand (channel row j, tokens 16R..16R+15)
+        auto put_cb = [&](const uint4 (&x)[2]) {
+            const __half2* hc = reinterpret_cast<const __half2*>(x);
+#pragma unroll
+            for (int s = 0; s < 16; s += 4) {
+                const float2 a = __half22float2(hc[s / 2]), b2 = __half22float2(hc[s / 2 + 1]);
+                *reinterpret_cast<float4*>(sgen + kCbT + sw(16384, static_cast<uint32_t>(j),
+                                                             static_cast<uint32_t>(16 * R + s))) =
+                    make_float4(a.x, a.y, b2.x, b2.y);
+            }
+        };
+        // U^T of chunk c from its v, w tile: d_v column un, tokens 8*ut .. 8*ut + 7
+        const int un = tid & 63, ut = tid >> 6;
+        auto put_u = [&](int c) {
+            const uint8_t* tv = sgen + kVW + static_cast<uint32_t>(c & 1) * 16384u;
+            const int tp = c * kC;
+            float hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * ut + e;
+                const uint32_t off = vw_off(t, un);
+                const float vv = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + off)) << 16);
+                const float ww =
+                    __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + 8192 + off)) << 16);
+                const float u = tp + t < T ? vv * ww : 0.f;   // rows past the sequence end
+                hi[e] = tf32r(u);
+                lo[e] = tf32r(u - hi[e]);
+            }
+            const uint32_t k0 = static_cast<uint32_t>(8 * ut);
+            *reinterpret_cast<float4*>(sgen + kU + sw(16384, un, k0)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<float4*>(sgen + kU + sw(16384, un, k0 + 4)) = make_float4(hi[4], hi[5], hi[6], hi[7]);
+            *reinterpret_cast<float4*>(sgen + kU + sw(16384, 64 + un, k0)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<float4*>(sgen + kU + sw(16384, 64 + un, k0 + 4)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
+        };
+        // Kb^T of one chunk -> TMEM (lane j, columns 16R..16R+15)
+        auto put_kb = [&](const uint4 (&x)[2]) {
+            const __half2* hk = reinterpret_cast<const __half2*>(x);
+            float kb[16];
+#pragma unroll
+            for (int s = 0; s < 16; s += 2) {
+                const float2 f = __half22float2(hk[s / 2]);
+                kb[s] = f.x;
+                kb[s + 1] = f.y;
+            }
+            tmem_st16(tmem + lane_base + kTmA2 + static_cast<uint32_t>(16 * R), kb);
+            tmem_st_wait();
+        };
+        // P = Qb - A_qk W on lanes 64..127 of A1 (columns 32R .. 32R + 31)
+        auto add_qb = [&](const uint4 (&x)[4]) {
+            const __half2* hq = reinterpret_cast<const __half2*>(x);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t col = static_cast<uint32_t>(32 * R + 16 * half);
+                float v[16];
+                tmem_ld16(tmem + lane_base + kTmA1 + col, v);
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const float2 q2 = __half22float2(hq[(16 * half + e) / 2]);
+                    v[e] += q2.x;
+                    v[e + 1] += q2.y;
+                }
+                tmem_st16(tmem + lane_base + kTmA1 + col, v);
+            }
+            tmem_st_wait();
+        };
+
+        Ops cur;
+        if (n > 0) {
+            // ---- prologue: operands of chunk 0, and -Cb^T of chunk 1 ------------------
+            uint4 cb0v[2], kb0v[2], qb0v[4];
+            ld_cb(0, cb0v, prm.s.cbt);
+            ld_cb(0, kb0v, prm.s.kbt);
+            ld_qb(0, qb0v);
+            put_cb(cb0v);
+            arrive(kRdyA1);                                       // A1(0)
+            if (!wait(kBarVW, ph_vw0)) failed = true;
+            if (!failed) {
+                put_u(0);
+                arrive(kRdyU);                                    // [T; A_qk T] U (0)
+                ld_cb(1, cur.cb, prm.s.cbt);
+                if (!wait(kDoneP3, ph_p3)) failed = true;
+            }
+            if (!failed) {
+                if (!e_warp) add_qb(qb0v);
+                if (n > 1) {
+                    put_cb(cur.cb);
+                    arrive(kRdyA1);                               // A1(1)
+                }
+                put_kb(kb0v);
+                arrive(kRdyChain);                                // chain of chunk 0
+            }
+        }
+
+        for (int c = 0; c < n && !failed; ++c) {
+            const int tc = c * kC;
+            // workspace operands used later in this iteration (their latency hides
+            // behind the E read-out)
+            ld_cb(c + 2, cur.cb, prm.s.cbt);
+            ld_cb(c + 1, cur.kb, prm.s.kbt);
+            ld_qb(c + 1, cur.qb);
+            cur.gam = prm.s.gam[slot(c) * kDK + j];
+
+            // ---- chain: E -> [E_hi^T; E_lo^T] (quarters 0-1), O -> global (quarters 2-3) ----
+            if (!wait(kDoneC1, ph_c1)) { failed = true; break; }
+            {
+                float v[16];
+                tmem_ld16_pair(tmem + lane_base + kTmEO + static_cast<uint32_t>(16 * R), v);
+                if (e_warp) {
+                    const uint32_t r = static_cast<uint32_t>(j);   // token row of the chunk
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const uint32_t nn = static_cast<uint32_t>(16 * R + jj);
+                        const float eh = tf32r(v[jj]);
+                        F[(kE + sw(16384, nn, r)) >> 2] = eh;
+                        F[(kE + sw(16384, 64u + nn, r)) >> 2] = tf32r(v[jj] - eh);
+                    }
+                    arrive(kRdyMma2);
+                } else {
+                    const int r = j - 64;
+                    if (tc + r < T) {
+                        const int64_t off =
+                            ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                        if (prm.out_bf16) {
+                            __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
+                            uint4 pk[2];
+                            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                            for (int jj = 0; jj < 16; jj += 2) {
+                                __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                                pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
+                            }
+                            reinterpret_cast<uint4*>(op)[0] = pk[0];
+                            reinterpret_cast<uint4*>(op)[1] = pk[1];
+                        } else {
+                            float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+#pragma unroll
+                            for (int jj = 0; jj < 16; jj += 4)
+                                op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                        }
+                    }
+                }
+            }
+            if (c + 1 < n) {
+                // ---- next chunk: U^T operand (its product overwrites [E; O] after this) --------
+                const bool odd = (c + 1) & 1;
+                if (!wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
+                put_u(c + 1);
+                arrive(kRdyU);
+                // ---- next chunk: P on A1, then -Cb^T of chunk c + 2 ------------------------
+                if (!wait(kDoneP3, ph_p3)) { failed = true; break; }
+                if (!e_warp) add_qb(cur.qb);
+                if (c + 2 < n) {
+                    put_cb(cur.cb);
+                    arrive(kRdyA1);
+                }
+            }
+            // ---- chain: S <- gamma S + Kb^T E; S^T operand; next chunk's Kb^T ----------------
+            if (!wait(kDoneC2, ph_c2)) { failed = true; break; }
+            {
+                uint32_t a[16], b[16];
+                tmem_ld16_nw(tmem + lane_base + kTmD2 + static_cast<uint32_t>(16 * R), a);
+                tmem_ld16_nw(tmem + lane_base + kTmD2 + 64u + static_cast<uint32_t>(16 * R), b);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    S[jj] = fmaf(cur.gam, S[jj], __uint_as_float(a[jj]) + __uint_as_float(b[jj]));
+                    F[(kSt + sw(8192, static_cast<uint32_t>(16 * R + jj), j)) >> 2] = tf32r(S[jj]);
+                }
+            }
+            if (c + 1 < n) {
+                put_kb(cur.kb);
+                arrive(kRdyChain);
+            }
+        }
+
+        if (failed) {
+            *abort_flag = 1;
+            if (lane == 0) atomicExch(prm.err, kDevTimeout);
+        } else if (prm.ST) {
+            float* st = prm.ST + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R;
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<kTmCols>(tmem);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [T; A_qk T] of all slots as a 2-D fp32 map (64 columns, slots*128 rows);
+// box 32 x 128 with the 128-byte swizzle: one K-block of the A operand.
+bool make_a0_map(CUtensorMap* m, const float* a0, int64_t slots) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(slots * 128)};
+    const cuuint64_t strides[1] = {64 * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(a0), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Packed [1, total, H, dv] bf16 values as a 4-D map (dv, H, total, 1); box
+// (64, 1, 64, 1), 128-byte swizzle; rows past the tensor read as zeros.
+bool make_value_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int64_t dv) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(total), 1};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(dv * 2), static_cast<cuuint64_t>(H * dv * 2),
+                                   static_cast<cuuint64_t>(total * H * dv * 2)};
+    const cuuint32_t box[4] = {64, 1, 64, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err) {
+    const int64_t total = a.cu ? a.total : a.B * a.T;
+    const int64_t slots = chunks * a.H;
+    if (slots * 128 >= (1ll << 31) || chunks >= (1ll << 31)) return GDR2_ERR_SHAPE;
+    CUtensorMap ma0, mv, mw;
+    if (!make_a0_map(&ma0, s.a0, slots > 0 ? slots : 1) || !make_value_map(&mv, a.v, total, a.H, a.dv) ||
+        !make_value_map(&mw, a.w, total, a.H, a.dv))
+        return GDR2_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemAlloc));
+    });
+    if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
+    StateParams prm{s, a.S0, a.o, a.ST, err, a.cu, static_cast<int>(a.T), static_cast<int>(a.H),
+                    static_cast<int>(a.dv), static_cast<int>(total),
+                    a.cu ? 0 : static_cast<int>((a.T + kC - 1) / kC), static_cast<int>(chunks),
+                    a.out_dtype == GDR2_BF16 ? 1 : 0};
+    const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
+    state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(ma0, mv, mw, prm);
+    return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
+}  // namespace gdr2

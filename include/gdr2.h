@@ -23,8 +23,13 @@
  * Conventions shared by every call
  * --------------------------------
  * - All tensor pointers are DEVICE pointers on the current CUDA device,
- *   row-major and contiguous, 16-byte aligned.  The caller owns every buffer;
- *   the library allocates no device memory and keeps no pointer after return.
+ *   row-major and contiguous, 16-byte aligned.  The caller owns every buffer
+ *   and the library keeps no pointer after return.  The chunked bf16 prefill
+ *   (gdr2_forward, gdr2_forward_varlen with bf16 inputs and d_k = 128) takes a
+ *   workspace of 82,432 bytes per (64-token chunk, head) -- the per-chunk
+ *   operands its two kernels exchange -- from the device's default
+ *   stream-ordered memory pool (cudaMallocAsync on `stream`) and releases it
+ *   on the same stream; no other call allocates device memory.
  * - in_dtype selects the element type of the six token inputs and out_dtype
  *   that of o: GDR2_F32 (float) or GDR2_BF16 (__nv_bfloat16).  States are
  *   always fp32.  All arithmetic is fp32 (bf16 only as tensor-core operands
@@ -71,11 +76,11 @@ typedef enum {
  * Applies the update above for t = 0 .. T-1 to every (batch, head) pair,
  * starting from S0, writes every o_t and (optionally) the final state.
  * The page's "efficient implementation" section (WY form with decay
- * absorption, chunkwise algorithm) describes the method used for bf16 inputs:
- * fixed 64-token chunks, a per-chunk UT/WY transform with the cumulative
- * channel decay folded into the rank-1 erase factors, and an fp32 state
- * carried across chunks on chip.  fp32 inputs run a token-sequential fp32
- * kernel.
+ * absorption, chunkwise algorithm) describes the method used for bf16 inputs
+ * with d_k = 128: fixed 64-token chunks, a per-chunk UT/WY transform with the
+ * cumulative channel decay folded into the rank-1 erase factors (computed for
+ * all chunks in parallel), and an fp32 state carried across the chunks of a
+ * sequence on chip.  Other inputs run a token-sequential fp32 kernel.
  *
  *   q, k, b, log_decay : [B, T, H, dk]  (in_dtype)
  *   v, w               : [B, T, H, dv]  (in_dtype)
