@@ -64,21 +64,21 @@ constexpr uint32_t kRawQ = 0, kRawK = 16384, kRawB = 32768, kRawG = 49152;  // b
 constexpr uint32_t kG31 = 0;           // K-groups [G3 (64 rows) | G1 (32 rows)] over the raw tiles (48 KB)
 constexpr uint32_t kOpA = 65536;       // [Ct; Qt]: 128 rows x 128 K (64 KB)
 constexpr uint32_t kG20 = 131072;      // K-groups [G2 (48 rows) | G0 (16 rows)] (32 KB)
-constexpr uint32_t kMisc = 163840;     // mbarriers, TMEM slot
+constexpr uint32_t kIA = 163840;       // [I; A_qk]: 128 rows x 64 K (32 KB)
+constexpr uint32_t kTT = 196608;       // T^T: 64 rows x 64 K (16 KB)
+constexpr uint32_t kMisc = 212992;     // mbarriers, TMEM slot
 constexpr uint32_t kSmemBytes = kMisc + 128;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr uint32_t kXTot = kOpA, kXMid = kOpA + 2048;   // per-stripe decay sums (before [Ct; Qt])
-// solve scratch inside kOpA .. (the intra-chunk product operands are dead by then)
+// solve scratch inside the [Ct; Qt] area (dead once the intra-chunk products are done)
 constexpr int kLd = 65;                   // A_kk staging row (floats)
 constexpr int kLt = 68;                   // T staging row (floats; rows 16-byte aligned)
 constexpr uint32_t kSL = kOpA;            // A_kk staging  [64][65] fp32
 constexpr uint32_t kSTs = kOpA + 16640;   // T staging     [64][68] fp32
 constexpr uint32_t kSP = kOpA + 34048;    // M_{RJ} blocks, 6 x 16 x 17 fp32
-constexpr uint32_t kIA = kOpA + 40960;    // [I; A_qk]: 128 rows x 64 K (32 KB)
-constexpr uint32_t kTT = kIA + 32768;     // T^T: 64 rows x 64 K (16 KB)
-static_assert(kSTs + 64 * kLt * 4 <= kSP && kSP + 6 * 16 * 17 * 4 <= kIA, "solve scratch");
-static_assert(kTT + 16384 <= kMisc, "solve scratch inside the operand area");
+static_assert(kSTs + 64 * kLt * 4 <= kSP && kSP + 6 * 16 * 17 * 4 <= kG20, "solve scratch");
 static_assert(kG31 + 4 * 12288 <= kOpA, "K-groups in the raw area");
+static_assert(kSmemAlloc <= 232448, "shared memory");
 enum : uint32_t { kBarTma = 0, kRdyAP, kRdyA0, kDoneP1, kDoneP2, kNumBars };
 constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
 
@@ -100,38 +100,48 @@ struct PrepParams {
     const int* cu;        // packed sequences: [N + 1] token offsets, or null
     int N, T, H, total;   // T: common length when cu is null
     int nchunks;          // chunks per sequence when cu is null
+    int nitems;           // work items = global chunk bound x H; item = slot index
     int* err;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-            const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_g,
-            const PrepParams prm) {
-    // ---- which (sequence, chunk, head) ------------------------------------------------
-    const int gc = blockIdx.x, h = blockIdx.y;
-    int tok0, T, c;
+// Work item `it` = (global chunk it / H, head it % H), its slot index.  False for
+// items past the last real chunk (packed sequences: the chunk count is a bound).
+struct Item {
+    int tok0, T, tp, h;
+};
+__device__ __forceinline__ bool locate(const PrepParams& prm, int it, Item& x) {
+    const int gc = it / prm.H;
+    x.h = it - gc * prm.H;
     if (prm.cu) {
         const int* cb = prm.s.chunk_base;
-        if (gc >= cb[prm.N]) return;                 // past the last chunk (the grid is a bound)
-        int lo = 0, hi = prm.N;                      // last sequence with cb[seq] <= gc
+        if (gc >= cb[prm.N]) return false;
+        int lo = 0, hi = prm.N;   // last sequence with cb[seq] <= gc
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (cb[mid] <= gc) lo = mid; else hi = mid;
         }
         const int a = min(max(prm.cu[lo], 0), prm.total);
         const int e = min(max(prm.cu[lo + 1], a), prm.total);
-        tok0 = a;
-        T = e - a;
-        c = gc - cb[lo];
+        x.tok0 = a;
+        x.T = e - a;
+        x.tp = (gc - cb[lo]) * kC;
     } else {
         const int seq = gc / prm.nchunks;
-        c = gc - seq * prm.nchunks;
-        tok0 = seq * prm.T;
-        T = prm.T;
+        x.tok0 = seq * prm.T;
+        x.T = prm.T;
+        x.tp = (gc - seq * prm.nchunks) * kC;
     }
-    const int tp = c * kC;                           // first token of the chunk
-    const int64_t slot = static_cast<int64_t>(gc) * prm.H + h;
+    return true;
+}
 
+// Persistent: CTA b handles items b, b + gridDim.x, ...  The next item's tiles load
+// while this item's solve runs, its [T; A_qk T] is written out while the next
+// item's intra-chunk products run, and the next item's pass 1 overlaps this
+// item's [T; A_qk T] product.
+__global__ void __launch_bounds__(kThreads, 1)
+prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_g,
+            const PrepParams prm) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));
@@ -145,6 +155,12 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int j = tid & 127;
     const int R = (tid >> 7) & 3;
     const int quarter = warp & 3;
+    // next real item after `it` (or nitems)
+    auto next_item = [&](int it, Item& x) {
+        for (it += gridDim.x; it < prm.nitems; it += gridDim.x)
+            if (locate(prm, it, x)) return it;
+        return prm.nitems;
+    };
 
     if (tid == 0) {
         for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
@@ -156,25 +172,35 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    Item first;
+    const int it0 = (static_cast<int>(blockIdx.x) < prm.nitems && locate(prm, blockIdx.x, first))
+                        ? static_cast<int>(blockIdx.x)
+                        : next_item(blockIdx.x, first);
 
     if (warp >= kSimt / 32) {
         // ================= TMA / MMA warpgroup: one elected thread =================
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
         if (warp == kSimt / 32 && lane == 0) {
+            auto load = [&](const Item& x) {
+                mbar_expect_tx(bar(kBarTma), 65536u);
+                const int row = x.tok0 + x.tp;
+                tma_load_4d(base + kRawQ, &tm_q, 0, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawQ + 8192, &tm_q, 64, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawK, &tm_k, 0, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawK + 8192, &tm_k, 64, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawB, &tm_b, 0, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawB + 8192, &tm_b, 64, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawG, &tm_g, 0, x.h, row, 0, bar(kBarTma));
+                tma_load_4d(base + kRawG + 8192, &tm_g, 64, x.h, row, 0, bar(kBarTma));
+            };
             bool ok = true;
-            mbar_expect_tx(bar(kBarTma), 65536u);
-            const int row = tok0 + tp;
-            tma_load_4d(base + kRawQ, &tm_q, 0, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawQ + 8192, &tm_q, 64, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawK, &tm_k, 0, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawK + 8192, &tm_k, 64, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawB, &tm_b, 0, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawB + 8192, &tm_b, 64, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawG, &tm_g, 0, h, row, 0, bar(kBarTma));
-            tma_load_4d(base + kRawG + 8192, &tm_g, 64, h, row, 0, bar(kBarTma));
-            // intra-chunk products [Ct; Qt] x [G3|G1]^T and x [G2|G0]^T
-            ok = mbar_wait(bar(kRdyAP), 0);
-            if (ok) {
+            uint32_t ph = 0;      // phase of this item's barriers
+            int loads = 0;        // tile loads issued
+            if (it0 < prm.nitems) { load(first); ++loads; }
+#pragma unroll 1
+            for (int it = it0; it < prm.nitems && ok; ph ^= 1u) {
+                // intra-chunk products [Ct; Qt] x [G3|G1]^T and x [G2|G0]^T
+                if (!(ok = mbar_wait(bar(kRdyAP), ph))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int s = 0; s < 16; ++s) {
@@ -185,19 +211,25 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                            s > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(kDoneP1));
+                // the products have read the K-groups over the raw tiles: next item's tiles
+                if (!(ok = mbar_wait(bar(kDoneP1), ph))) break;
+                Item nx;
+                const int nit = next_item(it, nx);
+                if (nit < prm.nitems) { load(nx); ++loads; }
                 // [T; A_qk T] = [I; A_qk] T
-                ok = mbar_wait(bar(kRdyA0), 0);
-            }
-            if (ok) {
+                if (!(ok = mbar_wait(bar(kRdyA0), ph))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s)
                     mma_ss(tmem + kTmA0, umma_desc(kstep(base + kIA, 16384, s)),
                            umma_desc(kstep(base + kTT, 8192, s)), idesc_tf32(128, 64), s > 0 ? 1u : 0u);
                 mma_commit(bar(kDoneP2));
-            } else {
+                it = nit;
+            }
+            if (!ok) {
                 atomicExch(prm.err, kDevTimeout);
-                mbar_wait(bar(kBarTma), 0);   // the tile loads may still be in flight
+                // the last tile load may still be in flight (bounded wait)
+                if (loads > 0) mbar_wait(bar(kBarTma), static_cast<uint32_t>((loads - 1) & 1));
             }
         }
         __syncwarp();
@@ -206,8 +238,8 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSimt));
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         bool failed = false;
-        auto wait_done = [&](uint32_t b) -> bool {
-            const bool ok = mbar_wait(bar(b), 0);
+        auto wait_done = [&](uint32_t b, uint32_t ph) -> bool {
+            const bool ok = mbar_wait(bar(b), ph);
             const bool bad = simt_any(!ok);
             tc_fence_after();
             return !bad;
@@ -218,14 +250,27 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             simt_sync();
             if (tid == 0) mbar_arrive(bar(b));
         };
+        // [T; A_qk T] of a finished item -> its slot (tf32-rounded)
+        auto write_a0 = [&](int64_t slot) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + kTmA0 + static_cast<uint32_t>(16 * R), v);
+            float4* dst = reinterpret_cast<float4*>(prm.s.a0 + slot * (128 * kC) + j * kC + 16 * R);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                dst[e / 4] = make_float4(tf32r(v[e]), tf32r(v[e + 1]), tf32r(v[e + 2]), tf32r(v[e + 3]));
+        };
 
-        // ---- pass 1: raw tiles -> decay factors, [Ct; Qt], K-groups, -Cb, Qb, Kb ----------
-        do {
-            float cr[16], qr[16], kr[16];   // c*rho, q*rho, k/rho
+        uint32_t ph = 0;
+        int prev = -1;
+        Item cur = first;
+#pragma unroll 1
+        for (int it = it0; it < prm.nitems && !failed; ph ^= 1u) {
+            const int T = cur.T, tp = cur.tp;
+            const int64_t slot = it;
+            // ---- pass 1: raw tiles -> decay factors, [Ct; Qt], K-groups, -Cb, Qb, Kb --------
             {
-                const bool ok = mbar_wait(bar(kBarTma), 0);
-                if (simt_any(!ok)) { failed = true; break; }
-            }
+                float cr[16], qr[16], kr[16];   // c*rho, q*rho, k/rho
+                if (!wait_done(kBarTma, ph)) { failed = true; break; }
             // element (token 16R+s, channel j) of a bf16 tile
             const uint32_t cbase = (static_cast<uint32_t>(j) >> 6) * 8192u +
                                    static_cast<uint32_t>(16 * R) * 128u + ((static_cast<uint32_t>(j) & 7u) << 1);
@@ -313,11 +358,14 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 for (int s = 0; s < 16; ++s) dq[s * 8] = __float2half_rn(qr[s] * em);
                 if (R == 0) prm.s.gam[slot * kDK + j] = __expf(gC);
             }
-        } while (false);
-
-        // ---- A_kk, A_qk out of TMEM; T = (I + A_kk)^-1; [I; A_qk] and T^T operands ---------
-        if (!failed && !wait_done(kDoneP1)) failed = true;
-        if (!failed) {
+            }
+            // ---- the previous item's [T; A_qk T] out (overlaps this item's products) -------
+            if (prev >= 0) {
+                if (!wait_done(kDoneP2, ph ^ 1u)) { failed = true; break; }
+                write_a0(prev);
+            }
+            // ---- A_kk, A_qk out of TMEM; T = (I + A_kk)^-1; [I; A_qk] and T^T operands -------
+            if (!wait_done(kDoneP1, ph)) { failed = true; break; }
             {
                 const int m = j;                          // TMEM lane = product row
                 const int r = m & 63;                     // token row within the chunk
@@ -435,16 +483,14 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     make_float4(t8[4], t8[5], t8[6], t8[7]);
             }
             signal(kRdyA0);
+            prev = it;
+            Item nx;
+            it = next_item(it, nx);
+            cur = nx;
         }
-        // ---- [T; A_qk T] -> the slot (tf32-rounded) ----------------------------------
-        if (!failed && !wait_done(kDoneP2)) failed = true;
-        if (!failed) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + kTmA0 + static_cast<uint32_t>(16 * R), v);
-            float4* dst = reinterpret_cast<float4*>(prm.s.a0 + slot * (128 * kC) + j * kC + 16 * R);
-#pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                dst[e / 4] = make_float4(tf32r(v[e]), tf32r(v[e + 1]), tf32r(v[e + 2]), tf32r(v[e + 3]));
+        if (!failed && prev >= 0) {
+            if (wait_done(kDoneP2, ph ^ 1u)) write_a0(prev);
+            else failed = true;
         }
         if (failed && tid == 0) atomicExch(prm.err, kDevTimeout);
     }
@@ -576,9 +622,17 @@ int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaSt
                                                   s.chunk_base);
         if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
     }
+    const int64_t nitems = chunks * a.H;
+    if (nitems >= (1ll << 31)) return GDR2_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return GDR2_ERR_CUDA;
     PrepParams prm{s, a.cu, static_cast<int>(a.B), static_cast<int>(a.T), static_cast<int>(a.H),
-                   static_cast<int>(total), a.cu ? 0 : static_cast<int>((a.T + kC - 1) / kC), err};
-    const dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(a.H));
+                   static_cast<int>(total), a.cu ? 0 : static_cast<int>((a.T + kC - 1) / kC),
+                   static_cast<int>(nitems), err};
+    // persistent: one CTA per SM, each looping over its items
+    const unsigned grid = static_cast<unsigned>(nitems < sms ? nitems : sms);
     prep_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }

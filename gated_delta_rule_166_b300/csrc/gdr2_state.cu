@@ -17,9 +17,10 @@
 // state update runs and A1 of the next chunk while E is read out, so the
 // state-independent products overlap the chain.
 //
-// Operands: [T; A_qk T] (two buffers) and the v, w tiles (two buffers) are
-// TMA-loaded into shared memory; A1 and Kb^T are TMEM-resident A operands;
-// S^T, U^T, E^T and -Cb^T are shared-memory B operands.
+// Operands: [T; A_qk T], A1 and Kb^T are TMEM-resident A operands (so every
+// product reads one operand from shared memory); S^T, U^T, E^T and -Cb^T are
+// shared-memory B operands; the v, w tiles (two buffers) arrive by TMA and O
+// leaves through a shared-memory tile and a TMA store.
 //
 // Work split: 640 threads.  One thread of the last warpgroup issues the TMA
 // loads and all MMAs.  Warp w < 16 owns TMEM lane quarter q = w % 4 (lanes
@@ -52,16 +53,17 @@ constexpr int kRegsSimt = 112, kRegsMma = 32;
 static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96, "register pool");
 
 // ---- shared memory (bytes from a 1024-aligned base); K-major, 128-byte swizzle ----
-constexpr uint32_t kA0 = 0;            // two buffers of [T; A_qk T]: 128 rows x 64 K (32 KB each)
-constexpr uint32_t kVW = 65536;        // two buffers of {v, w} bf16 tiles [64 tokens][64 d_v] (16 KB each)
-constexpr uint32_t kCbT = 98304;       // -Cb^T: 128 rows (channels) x 64 K (tokens)
-constexpr uint32_t kSt = 131072;       // S^T: 64 rows (d_v) x 128 K (channels)
-constexpr uint32_t kU = 163840;        // [U_hi^T; U_lo^T]: 128 rows x 64 K (tokens)
-constexpr uint32_t kE = 196608;        // [E_hi^T; E_lo^T]: 128 rows x 64 K (tokens)
-constexpr uint32_t kMisc = 229376;
+constexpr uint32_t kVW = 0;            // two buffers of {v, w} bf16 tiles [64 tokens][64 d_v] (16 KB each)
+constexpr uint32_t kCbT = 32768;       // -Cb^T: 128 rows (channels) x 64 K (tokens)
+constexpr uint32_t kSt = 65536;        // S^T: 64 rows (d_v) x 128 K (channels)
+constexpr uint32_t kU = 98304;         // [U_hi^T; U_lo^T]: 128 rows x 64 K (tokens)
+constexpr uint32_t kE = 131072;        // [E_hi^T; E_lo^T]: 128 rows x 64 K (tokens)
+constexpr uint32_t kO = 163840;        // O tile for the TMA store: [64 tokens][64 d_v] (16 KB)
+constexpr uint32_t kMisc = 180224;
 enum : uint32_t {
-    kBarA0 = 0, kBarA0b, kBarVW, kBarVWb,         // TMA completions
-    kRdyA1, kRdyU, kRdyChain, kRdyMma2,            // elementwise warps -> MMA thread
+    kBarVW = 0, kBarVWb,                                    // TMA completions
+    kRdyA1, kRdyA0, kRdyU, kEOFree, kRdyChain, kRdyMma2,    // elementwise warps -> MMA thread
+    kOFull, kOFree,                                         // O tile: written / stored
     kDoneC1, kDoneC2, kDoneP3,                     // MMA commits
     kNumBars
 };
@@ -77,6 +79,7 @@ constexpr uint32_t kTmA1 = 0;      // [-W; P] (A operand, K = 128 channels)
 constexpr uint32_t kTmA2 = 128;    // Kb^T (A operand: lanes = channels, K = 64 tokens)
 constexpr uint32_t kTmEO = 192;    // [E; O] as two 64-column halves (hi | lo products)
 constexpr uint32_t kTmD2 = 320;    // Kb^T E as two 64-column halves
+constexpr uint32_t kTmA0 = 448;    // [T; A_qk T] (A operand, K = 64 tokens)
 constexpr int kTmCols = 512;
 
 struct StateParams {
@@ -98,8 +101,8 @@ __device__ __forceinline__ uint32_t vw_off(int t, int n) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_v,
-             const __grid_constant__ CUtensorMap tm_w, const StateParams prm) {
+state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+             const __grid_constant__ CUtensorMap tm_o, const StateParams prm) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));
@@ -135,7 +138,11 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
 
     if (tid == 0) {
         for (uint32_t i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kRdyA1 || i == kRdyU || i == kRdyChain) ? 16u : i == kRdyMma2 ? 8u : 1u;
+            // one arrival per warp: 8 E warps (A1, U, Kb^T E operands), 8 O warps ([E; O]
+            // read out), all 16 ([T; A_qk T] and the chain)
+            const uint32_t cnt = (i == kRdyChain || i == kRdyA0) ? 16u
+                                 : (i == kRdyA1 || i == kRdyU || i == kEOFree || i == kRdyMma2 || i == kOFull) ? 8u
+                                                                                                             : 1u;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
@@ -152,19 +159,9 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
         // ================= TMA / MMA warpgroup: one elected thread =================
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
         if (warp == kSimt / 32 && lane == 0) {
-            // TMA batches issued per barrier kBarA0 + i (i = 0..3): any (bit i of iss_any) and
+            // TMA batches issued per barrier kBarVW + i (i = 0, 1): any (bit i of iss_any) and
             // the parity of their count (bit i of iss_par); bit-packed to stay in registers
             uint32_t iss_any = 0, iss_par = 0;
-            auto load_a0 = [&](int c) {
-                const uint32_t b = bar(kBarA0 + (c & 1));
-                const uint32_t dst = base + kA0 + static_cast<uint32_t>(c & 1) * 32768u;
-                const int row = static_cast<int>(slot(c) * 128);
-                mbar_expect_tx(b, 32768u);
-                tma_load_2d(dst, &tm_a0, 0, row, b);
-                tma_load_2d(dst + 16384u, &tm_a0, 32, row, b);
-                iss_any |= 1u << (c & 1);
-                iss_par ^= 1u << (c & 1);
-            };
             auto load_vw = [&](int c) {
                 const uint32_t b = bar(kBarVW + (c & 1));
                 const uint32_t dst = base + kVW + static_cast<uint32_t>(c & 1) * 16384u;
@@ -172,48 +169,41 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
                 mbar_expect_tx(b, 16384u);
                 tma_load_4d(dst, &tm_v, j0, h, row, 0, b);
                 tma_load_4d(dst + 8192u, &tm_w, j0, h, row, 0, b);
-                iss_any |= 4u << (c & 1);
-                iss_par ^= 4u << (c & 1);
+                iss_any |= 1u << (c & 1);
+                iss_par ^= 1u << (c & 1);
             };
             auto wait = [&](uint32_t b, uint32_t& ph) {
                 const bool ok = mbar_wait_ab(bar(b), ph, abort_flag);
                 ph ^= 1u;
                 return ok;
             };
-            uint32_t ph_a0 = 0, ph_a1 = 0, ph_u = 0, ph_chain = 0, ph_mma2 = 0, ph_c1 = 0;   // ph_a0: bit per buffer
+            uint32_t ph_a0 = 0, ph_a1 = 0, ph_u = 0, ph_eo = 0, ph_chain = 0, ph_mma2 = 0, ph_c1 = 0;
             // A1(c) = [T; A_qk T](c) (-Cb^T)(c)
-            auto issue_a1 = [&](int c) {
-                if (!wait(kRdyA1, ph_a1)) return false;
-                const uint32_t bit = 1u << (c & 1);
-                const bool landed = mbar_wait_ab(bar(kBarA0 + (c & 1)), (ph_a0 & bit) ? 1u : 0u, abort_flag);
-                ph_a0 ^= bit;
-                if (!landed) return false;
+            auto issue_a1 = [&]() {
+                if (!wait(kRdyA1, ph_a1) || !wait(kRdyA0, ph_a0)) return false;
                 tc_fence_after();
-                const uint32_t a0 = base + kA0 + static_cast<uint32_t>(c & 1) * 32768u;
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s)
-                    mma_ss(tmem + kTmA1, umma_desc(kstep(a0, 16384, s)), umma_desc(kstep(base + kCbT, 16384, s)),
+                    mma_ts(tmem + kTmA1, tmem + kTmA0 + 8u * s, umma_desc(kstep(base + kCbT, 16384, s)),
                            idesc_tf32(128, 128), s > 0 ? 1u : 0u);
                 mma_commit(bar(kDoneP3));
                 return true;
             };
             // [E; O](c) halves := [T; A_qk T](c) [U_hi^T; U_lo^T](c)
-            auto issue_u = [&](int c) {
-                if (!wait(kRdyU, ph_u)) return false;
+            auto issue_u = [&]() {
+                if (!wait(kRdyU, ph_u) || !wait(kEOFree, ph_eo)) return false;
                 tc_fence_after();
-                const uint32_t a0 = base + kA0 + static_cast<uint32_t>(c & 1) * 32768u;
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s)
-                    mma_ss(tmem + kTmEO, umma_desc(kstep(a0, 16384, s)), umma_desc(kstep(base + kU, 16384, s)),
+                    mma_ts(tmem + kTmEO, tmem + kTmA0 + 8u * s, umma_desc(kstep(base + kU, 16384, s)),
                            idesc_tf32(128, 128), s > 0 ? 1u : 0u);
                 return true;
             };
             bool ok = true;
             if (n > 0) {
-                load_a0(0);
                 load_vw(0);
-                if (n > 1) { load_a0(1); load_vw(1); }
-                ok = issue_a1(0) && issue_u(0);
+                if (n > 1) load_vw(1);
+                ok = issue_a1() && issue_u();
                 if (ok && n > 2) load_vw(2);
             }
 #pragma unroll 1
@@ -232,9 +222,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
                 if (c + 1 < n) {
                     // A1 of the next chunk once this pass has read A1 (runs during the E read-out)
                     if (!(ok = wait(kDoneC1, ph_c1))) break;
-                    if (!(ok = issue_a1(c + 1))) break;
-                    // every product reading [T; A_qk T](c) is done: its buffer takes chunk c + 2
-                    if (c + 2 < n) load_a0(c + 2);
+                    if (!(ok = issue_a1())) break;
                 }
                 // chain: Kb^T [E_hi^T; E_lo^T]
                 if (!(ok = wait(kRdyMma2, ph_mma2))) break;
@@ -247,7 +235,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
                 if (c + 1 < n) {
                     // next chunk's U product (runs during the state update); the v, w
                     // buffer it was computed from takes chunk c + 3
-                    if (!(ok = issue_u(c + 1))) break;
+                    if (!(ok = issue_u())) break;
                     if (c + 3 < n) load_vw(c + 3);
                 }
             }
@@ -255,18 +243,51 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
                 *abort_flag = 1;
                 atomicExch(prm.err, kDevTimeout);
                 // tile loads may still be in flight: wait for them (bounded) before exiting
-                for (int b = 0; b < 4; ++b)
-                    if ((iss_any >> b) & 1u) mbar_wait(bar(kBarA0 + b), ((iss_par >> b) & 1u) ^ 1u);
+                for (int b = 0; b < 2; ++b)
+                    if ((iss_any >> b) & 1u) mbar_wait(bar(kBarVW + b), ((iss_par >> b) & 1u) ^ 1u);
             }
+        } else if (warp == kSimt / 32 + 1 && lane == 0) {
+            // O tile stores: one per chunk that lies wholly inside the sequence
+            uint32_t ph_full = 0;
+            mbar_arrive(bar(kOFree));   // the tile starts free
+#pragma unroll 1
+            for (int c = 0; (c + 1) * kC <= T && c < n; ++c) {
+                if (!mbar_wait_ab(bar(kOFull), ph_full, abort_flag)) break;
+                ph_full ^= 1u;
+                const int row = tok0 + c * kC;
+                tma_store_4d(&tm_o, base + kO, j0, h, row, 0);
+                if (!prm.out_bf16) tma_store_4d(&tm_o, base + kO + 8192u, j0 + 32, h, row, 0);
+                bulk_commit();
+                bulk_wait_read();           // the tile has been read: it may take the next chunk
+                mbar_arrive(bar(kOFree));
+            }
+            bulk_wait_all();
         }
         __syncwarp();
     } else {
         // ================= 16 elementwise / accumulator warps ====================
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSimt));
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        // Quarters 0-1 ("E warps", lanes 0..63 = token rows of E) read E out and build the
+        // next chunks' U^T and -Cb^T operands while Kb^T E runs; quarters 2-3 ("O warps")
+        // write O and complete P.  All warps update their state slice and Kb^T.
         const bool e_warp = quarter < 2;
+        const int et = ((warp >> 2) * 2 + (warp & 1)) * 32 + lane;   // 0..255 within each group
+        // Shared-memory byte offset of element (row, k) of an operand with K-blocks `kstride`
+        // apart, for this thread's k (its TMEM lane) and rows row0 + jj: the swizzle term
+        // depends on jj % 8 only, so it is (xk ^ (jj % 8)) << 4 with xk = (k % 32) / 4.
+        auto lane_col = [&](uint32_t kstride, uint32_t k) {
+            return (k >> 5) * kstride + ((k & 3u) << 2);
+        };
+        const uint32_t xk4 = ((static_cast<uint32_t>(j) & 31u) >> 2) << 4;
         // fp32 state S[j][j0 + 16R + jj] in registers; the S^T operand in shared memory
         float S[16];
+        const uint32_t st_base = kSt + lane_col(8192, static_cast<uint32_t>(j)) + static_cast<uint32_t>(16 * R) * 128u;
+        auto put_st = [&]() {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+                *reinterpret_cast<float*>(sgen + st_base + jj * 128 + (xk4 ^ ((jj & 7) << 4))) = tf32r(S[jj]);
+        };
         {
             const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R
                                      : nullptr;
@@ -275,11 +296,10 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
                 const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[jj] = x.x; S[jj + 1] = x.y; S[jj + 2] = x.z; S[jj + 3] = x.w;
             }
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) F[(kSt + sw(8192, 16 * R + jj, j)) >> 2] = tf32r(S[jj]);
+            put_st();
         }
         bool failed = false;
-        uint32_t ph_c1 = 0, ph_c2 = 0, ph_p3 = 0, ph_vw0 = 0, ph_vw1 = 0;
+        uint32_t ph_c1 = 0, ph_c2 = 0, ph_p3 = 0, ph_vw0 = 0, ph_vw1 = 0, ph_of = 0;
         auto wait = [&](uint32_t b, uint32_t& ph) {
             const bool ok = mbar_wait_ab(bar(b), ph, abort_flag);
             ph ^= 1u;
@@ -293,65 +313,67 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(b));
         };
-        // Workspace operands of chunk c (zeros past the sequence's chunks).
-        struct Ops {
-            uint4 cb[2];   // -Cb, channel j, tokens 16R..16R+15
-            uint4 kb[2];   // Kb, same
-            uint4 qb[4];   // Qb, token j - 64, channels 32R..32R+31 (quarters 2-3)
-            float gam;     // e^{G_C}, channel j
+        // x = hi + lo with hi = x truncated to tf32 and lo = x - hi exactly; the tensor
+        // core then reads lo truncated, which keeps about 21 significant bits of x.
+        auto split = [](float x, float& hi, float& lo) {
+            hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+            lo = x - hi;
         };
-        auto ld_cb = [&](int c, uint4 (&x)[2], const uint16_t* arr) {
-            if (c < n) {
-                const uint4* p = reinterpret_cast<const uint4*>(arr + slot(c) * (kDK * kC) + ((2 * R) * kDK + j) * 8);
-                x[0] = p[0];
-                x[1] = p[kDK];
-            } else {
-                x[0] = x[1] = make_uint4(0, 0, 0, 0);
-            }
-        };
-        auto ld_qb = [&](int c, uint4 (&x)[4]) {
-            if (c < n && !e_warp) {
-                const uint4* p = reinterpret_cast<const uint4*>(prm.s.qb + slot(c) * (kC * kDK) +
-                                                                ((4 * R) * kC + (j - 64)) * 8);
+        // E warps: -Cb^T rows (channels) ej, tokens 32*eh .. 32*eh + 31
+        const int ej = et & 127, eh = et >> 7;
+        auto ld_cb = [&](int c, uint4 (&x)[4]) {
+            if (c < n && e_warp) {
+                const uint4* p =
+                    reinterpret_cast<const uint4*>(prm.s.cbt + slot(c) * (kDK * kC) + ((4 * eh) * kDK + ej) * 8);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) x[k] = p[k * kC];
+                for (int g = 0; g < 4; ++g) x[g] = p[g * kDK];
             }
         };
-        // -Cb^T of one chunk -> its operand (channel row j, tokens 16R..16R+15)
-        auto put_cb = [&](const uint4 (&x)[2]) {
+        auto put_cb = [&](const uint4 (&x)[4]) {
             const __half2* hc = reinterpret_cast<const __half2*>(x);
+            const uint32_t xr4 = ((static_cast<uint32_t>(ej) & 7u) << 4);
+            const uint32_t rb = kCbT + static_cast<uint32_t>(eh) * 16384u + static_cast<uint32_t>(ej) * 128u;
 #pragma unroll
-            for (int s = 0; s < 16; s += 4) {
+            for (int s = 0; s < 32; s += 4) {
                 const float2 a = __half22float2(hc[s / 2]), b2 = __half22float2(hc[s / 2 + 1]);
-                *reinterpret_cast<float4*>(sgen + kCbT + sw(16384, static_cast<uint32_t>(j),
-                                                             static_cast<uint32_t>(16 * R + s))) =
+                *reinterpret_cast<float4*>(sgen + rb + ((static_cast<uint32_t>(s >> 2) << 4) ^ xr4)) =
                     make_float4(a.x, a.y, b2.x, b2.y);
             }
         };
-        // U^T of chunk c from its v, w tile: d_v column un, tokens 8*ut .. 8*ut + 7
-        const int un = tid & 63, ut = tid >> 6;
+        // E warps: U^T of chunk c from its v, w tile: d_v column un, tokens 16*ut .. 16*ut + 15
+        const int un = et & 63, ut = et >> 6;
         auto put_u = [&](int c) {
             const uint8_t* tv = sgen + kVW + static_cast<uint32_t>(c & 1) * 16384u;
-            const int tp = c * kC;
-            float hi[8], lo[8];
+            const int tvalid = T - c * kC - 16 * ut;   // tokens past the sequence end give U = 0
+            const uint32_t xr4 = (static_cast<uint32_t>(un) & 7u) << 4;
+            const uint32_t rb = kU + static_cast<uint32_t>(ut >> 1) * 16384u + static_cast<uint32_t>(un) * 128u;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = 8 * ut + e;
-                const uint32_t off = vw_off(t, un);
-                const float vv = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + off)) << 16);
-                const float ww =
-                    __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + 8192 + off)) << 16);
-                const float u = tp + t < T ? vv * ww : 0.f;   // rows past the sequence end
-                hi[e] = tf32r(u);
-                lo[e] = tf32r(u - hi[e]);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 16 * ut + 4 * q4 + e;
+                    const uint32_t off = vw_off(t, un);
+                    const float vv =
+                        __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + off)) << 16);
+                    const float ww =
+                        __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + 8192 + off)) << 16);
+                    split(4 * q4 + e < tvalid ? vv * ww : 0.f, hi[e], lo[e]);
+                }
+                // K chunk (16*ut + 4*q4) % 32 / 4 of rows un (hi) and 64 + un (lo)
+                const uint32_t cofs = ((static_cast<uint32_t>((ut & 1) * 4 + q4) << 4) ^ xr4);
+                *reinterpret_cast<float4*>(sgen + rb + cofs) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4*>(sgen + rb + 8192u + cofs) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
-            const uint32_t k0 = static_cast<uint32_t>(8 * ut);
-            *reinterpret_cast<float4*>(sgen + kU + sw(16384, un, k0)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4*>(sgen + kU + sw(16384, un, k0 + 4)) = make_float4(hi[4], hi[5], hi[6], hi[7]);
-            *reinterpret_cast<float4*>(sgen + kU + sw(16384, 64 + un, k0)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<float4*>(sgen + kU + sw(16384, 64 + un, k0 + 4)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
         };
-        // Kb^T of one chunk -> TMEM (lane j, columns 16R..16R+15)
+        // all warps: Kb (channel j, tokens 16R..16R+15) -> TMEM Kb^T
+        auto ld_kb = [&](int c, uint4 (&x)[2]) {
+            if (c < n) {
+                const uint4* p = reinterpret_cast<const uint4*>(prm.s.kbt + slot(c) * (kDK * kC) + ((2 * R) * kDK + j) * 8);
+                x[0] = p[0];
+                x[1] = p[kDK];
+            }
+        };
         auto put_kb = [&](const uint4 (&x)[2]) {
             const __half2* hk = reinterpret_cast<const __half2*>(x);
             float kb[16];
@@ -364,7 +386,15 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
             tmem_st16(tmem + lane_base + kTmA2 + static_cast<uint32_t>(16 * R), kb);
             tmem_st_wait();
         };
-        // P = Qb - A_qk W on lanes 64..127 of A1 (columns 32R .. 32R + 31)
+        // O warps: P = Qb - A_qk W on lanes 64..127 of A1 (token j - 64, columns 32R .. 32R + 31)
+        auto ld_qb = [&](int c, uint4 (&x)[4]) {
+            if (c < n && !e_warp) {
+                const uint4* p = reinterpret_cast<const uint4*>(prm.s.qb + slot(c) * (kC * kDK) +
+                                                                ((4 * R) * kC + (j - 64)) * 8);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = p[k * kC];
+            }
+        };
         auto add_qb = [&](const uint4 (&x)[4]) {
             const __half2* hq = reinterpret_cast<const __half2*>(x);
 #pragma unroll
@@ -383,94 +413,154 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
             tmem_st_wait();
         };
 
-        Ops cur;
-        if (n > 0) {
-            // ---- prologue: operands of chunk 0, and -Cb^T of chunk 1 ------------------
-            uint4 cb0v[2], kb0v[2], qb0v[4];
-            ld_cb(0, cb0v, prm.s.cbt);
-            ld_cb(0, kb0v, prm.s.kbt);
-            ld_qb(0, qb0v);
-            put_cb(cb0v);
-            arrive(kRdyA1);                                       // A1(0)
-            if (!wait(kBarVW, ph_vw0)) failed = true;
-            if (!failed) {
-                put_u(0);
-                arrive(kRdyU);                                    // [T; A_qk T] U (0)
-                ld_cb(1, cur.cb, prm.s.cbt);
-                if (!wait(kDoneP3, ph_p3)) failed = true;
-            }
-            if (!failed) {
-                if (!e_warp) add_qb(qb0v);
-                if (n > 1) {
-                    put_cb(cur.cb);
-                    arrive(kRdyA1);                               // A1(1)
+        // all warps: [T; A_qk T] row j, columns 16R..16R+15 -> TMEM
+        auto ld_a0 = [&](int c, float (&x)[16]) {
+            if (c < n) {
+                const float4* p = reinterpret_cast<const float4*>(prm.s.a0 + slot(c) * (128 * kC) + j * kC + 16 * R);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 f = p[e];
+                    x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
                 }
-                put_kb(kb0v);
+            }
+        };
+        auto put_a0 = [&](const float (&x)[16]) {
+            tmem_st16(tmem + lane_base + kTmA0 + static_cast<uint32_t>(16 * R), x);
+            tmem_st_wait();
+        };
+
+        uint4 cbr[4], kbr[2], qbr[4];
+        float a0r[16];
+        float gam = 1.f;
+        if (n > 0) {
+            // ---- prologue: operands of chunk 0, and -Cb^T of chunk 1 ----------------------
+            ld_a0(0, a0r);
+            put_a0(a0r);
+            arrive(kRdyA0);
+            ld_cb(0, cbr);
+            ld_kb(0, kbr);
+            ld_qb(0, qbr);
+            if (e_warp) {
+                put_cb(cbr);
+                arrive(kRdyA1);                                   // A1(0)
+                ld_cb(1, cbr);
+                if (!wait(kBarVW, ph_vw0)) failed = true;
+                if (!failed) {
+                    put_u(0);
+                    arrive(kRdyU);                                // [T; A_qk T] U (0)
+                }
+            } else {
+                arrive(kEOFree);                                  // [E; O] free for chunk 0's U product
+            }
+            if (!failed && !wait(kDoneP3, ph_p3)) failed = true;
+            if (!failed) {
+                if (e_warp) {
+                    if (n > 1) {
+                        put_cb(cbr);
+                        arrive(kRdyA1);                           // A1(1)
+                    }
+                } else {
+                    add_qb(qbr);
+                }
+                put_kb(kbr);
                 arrive(kRdyChain);                                // chain of chunk 0
             }
         }
 
         for (int c = 0; c < n && !failed; ++c) {
             const int tc = c * kC;
-            // workspace operands used later in this iteration (their latency hides
-            // behind the E read-out)
-            ld_cb(c + 2, cur.cb, prm.s.cbt);
-            ld_cb(c + 1, cur.kb, prm.s.kbt);
-            ld_qb(c + 1, cur.qb);
-            cur.gam = prm.s.gam[slot(c) * kDK + j];
+            // workspace operands used later in this iteration
+            ld_cb(c + 2, cbr);
+            ld_kb(c + 1, kbr);
+            ld_qb(c + 1, qbr);
+            ld_a0(c + 1, a0r);
+            gam = prm.s.gam[slot(c) * kDK + j];
 
-            // ---- chain: E -> [E_hi^T; E_lo^T] (quarters 0-1), O -> global (quarters 2-3) ----
             if (!wait(kDoneC1, ph_c1)) { failed = true; break; }
-            {
+            // the products that read [T; A_qk T](c) are done: next chunk's into TMEM
+            if (c + 1 < n) {
+                put_a0(a0r);
+                arrive(kRdyA0);
+            }
+            if (e_warp) {
+                // ---- chain: E -> [E_hi^T; E_lo^T] --------------------------------------------
                 float v[16];
                 tmem_ld16_pair(tmem + lane_base + kTmEO + static_cast<uint32_t>(16 * R), v);
-                if (e_warp) {
-                    const uint32_t r = static_cast<uint32_t>(j);   // token row of the chunk
+                const uint32_t rb = kE + lane_col(16384, static_cast<uint32_t>(j)) + static_cast<uint32_t>(16 * R) * 128u;
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const uint32_t nn = static_cast<uint32_t>(16 * R + jj);
-                        const float eh = tf32r(v[jj]);
-                        F[(kE + sw(16384, nn, r)) >> 2] = eh;
-                        F[(kE + sw(16384, 64u + nn, r)) >> 2] = tf32r(v[jj] - eh);
-                    }
-                    arrive(kRdyMma2);
-                } else {
-                    const int r = j - 64;
-                    if (tc + r < T) {
-                        const int64_t off =
-                            ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
-                        if (prm.out_bf16) {
-                            __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
-                            uint4 pk[2];
-                            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
-#pragma unroll
-                            for (int jj = 0; jj < 16; jj += 2) {
-                                __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
-                                pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
-                            }
-                            reinterpret_cast<uint4*>(op)[0] = pk[0];
-                            reinterpret_cast<uint4*>(op)[1] = pk[1];
-                        } else {
-                            float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
-#pragma unroll
-                            for (int jj = 0; jj < 16; jj += 4)
-                                op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
-                        }
+                for (int jj = 0; jj < 16; ++jj) {
+                    float eh, el;
+                    split(v[jj], eh, el);
+                    const uint32_t a = rb + jj * 128 + (xk4 ^ ((jj & 7) << 4));
+                    *reinterpret_cast<float*>(sgen + a) = eh;
+                    *reinterpret_cast<float*>(sgen + a + 8192u) = el;
+                }
+                arrive(kRdyMma2);
+                if (c + 1 < n) {
+                    // ---- next chunk: U^T operand ------------------------------------------
+                    const bool odd = (c + 1) & 1;
+                    if (!wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
+                    put_u(c + 1);
+                    arrive(kRdyU);
+                    // ---- -Cb^T of chunk c + 2 once A1(c + 1) has read its buffer ------------
+                    if (!wait(kDoneP3, ph_p3)) { failed = true; break; }
+                    if (c + 2 < n) {
+                        put_cb(cbr);
+                        arrive(kRdyA1);
                     }
                 }
-            }
-            if (c + 1 < n) {
-                // ---- next chunk: U^T operand (its product overwrites [E; O] after this) --------
-                const bool odd = (c + 1) & 1;
-                if (!wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
-                put_u(c + 1);
-                arrive(kRdyU);
-                // ---- next chunk: P on A1, then -Cb^T of chunk c + 2 ------------------------
-                if (!wait(kDoneP3, ph_p3)) { failed = true; break; }
-                if (!e_warp) add_qb(cur.qb);
-                if (c + 2 < n) {
-                    put_cb(cur.cb);
-                    arrive(kRdyA1);
+            } else {
+                // ---- O -> global ---------------------------------------------------------------
+                float v[16];
+                tmem_ld16_pair(tmem + lane_base + kTmEO + static_cast<uint32_t>(16 * R), v);
+                if (c + 1 < n) arrive(kEOFree);
+                const int r = j - 64;
+                if (tc + kC <= T) {
+                    // whole chunk inside the sequence: O tile -> shared memory -> one TMA store
+                    if (!wait(kOFree, ph_of)) { failed = true; break; }
+                    if (prm.out_bf16) {
+                        uint4 pk[2];
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 2) {
+                            __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                            pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            *reinterpret_cast<uint4*>(sgen + kO + r * 128 + ((((2 * R + q) ^ (r & 7)) & 7) << 4)) = pk[q];
+                    } else {
+                        const uint32_t tb = kO + static_cast<uint32_t>(R >> 1) * 8192u + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<float4*>(sgen + tb + ((((4 * (R & 1) + q) ^ (r & 7)) & 7) << 4)) =
+                                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                    arrive(kOFull);
+                } else if (tc + r < T) {   // the sequence's last, partial chunk: row by row
+                    const int64_t off = ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                    if (prm.out_bf16) {
+                        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
+                        uint4 pk[2];
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 2) {
+                            __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                            pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
+                        }
+                        reinterpret_cast<uint4*>(op)[0] = pk[0];
+                        reinterpret_cast<uint4*>(op)[1] = pk[1];
+                    } else {
+                        float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 4)
+                            op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                    }
+                }
+                if (c + 1 < n) {
+                    // ---- next chunk: P on A1 ----------------------------------------------------
+                    if (!wait(kDoneP3, ph_p3)) { failed = true; break; }
+                    add_qb(qbr);
                 }
             }
             // ---- chain: S <- gamma S + Kb^T E; S^T operand; next chunk's Kb^T ----------------
@@ -481,13 +571,11 @@ state_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ 
                 tmem_ld16_nw(tmem + lane_base + kTmD2 + 64u + static_cast<uint32_t>(16 * R), b);
                 tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    S[jj] = fmaf(cur.gam, S[jj], __uint_as_float(a[jj]) + __uint_as_float(b[jj]));
-                    F[(kSt + sw(8192, static_cast<uint32_t>(16 * R + jj), j)) >> 2] = tf32r(S[jj]);
-                }
+                for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(gam, S[jj], __uint_as_float(a[jj]) + __uint_as_float(b[jj]));
+                put_st();
             }
             if (c + 1 < n) {
-                put_kb(cur.kb);
+                put_kb(kbr);
                 arrive(kRdyChain);
             }
         }
@@ -524,33 +612,22 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// [T; A_qk T] of all slots as a 2-D fp32 map (64 columns, slots*128 rows);
-// box 32 x 128 with the 128-byte swizzle: one K-block of the A operand.
-bool make_a0_map(CUtensorMap* m, const float* a0, int64_t slots) {
+// Packed [1, total, H, dv] token rows (bf16 or fp32) as a 4-D map (dv, H, total, 1);
+// box (128 bytes of d_v, 1, 64 tokens, 1) with the 128-byte swizzle.  Loads past
+// the tensor read zeros; stores past it are dropped.
+bool make_row_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int64_t dv, bool f32) {
     auto enc = get_encode();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(slots * 128)};
-    const cuuint64_t strides[1] = {64 * 4};
-    const cuuint32_t box[2] = {32, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(a0), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Packed [1, total, H, dv] bf16 values as a 4-D map (dv, H, total, 1); box
-// (64, 1, 64, 1), 128-byte swizzle; rows past the tensor read as zeros.
-bool make_value_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int64_t dv) {
-    auto enc = get_encode();
-    if (!enc) return false;
+    const cuuint64_t esz = f32 ? 4 : 2;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(total), 1};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(dv * 2), static_cast<cuuint64_t>(H * dv * 2),
-                                   static_cast<cuuint64_t>(total * H * dv * 2)};
-    const cuuint32_t box[4] = {64, 1, 64, 1};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(dv) * esz, static_cast<cuuint64_t>(H * dv) * esz,
+                                   static_cast<cuuint64_t>(total * H * dv) * esz};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), 1, 64, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -560,9 +637,9 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaS
     const int64_t total = a.cu ? a.total : a.B * a.T;
     const int64_t slots = chunks * a.H;
     if (slots * 128 >= (1ll << 31) || chunks >= (1ll << 31)) return GDR2_ERR_SHAPE;
-    CUtensorMap ma0, mv, mw;
-    if (!make_a0_map(&ma0, s.a0, slots > 0 ? slots : 1) || !make_value_map(&mv, a.v, total, a.H, a.dv) ||
-        !make_value_map(&mw, a.w, total, a.H, a.dv))
+    CUtensorMap mv, mw, mo;
+    if (!make_row_map(&mv, a.v, total, a.H, a.dv, false) || !make_row_map(&mw, a.w, total, a.H, a.dv, false) ||
+        !make_row_map(&mo, a.o, total, a.H, a.dv, a.out_dtype != GDR2_BF16))
         return GDR2_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -576,7 +653,7 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaS
                     a.cu ? 0 : static_cast<int>((a.T + kC - 1) / kC), static_cast<int>(chunks),
                     a.out_dtype == GDR2_BF16 ? 1 : 0};
     const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
-    state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(ma0, mv, mw, prm);
+    state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 
