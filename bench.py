@@ -9,8 +9,9 @@ step.  The headline value is tokens/s with inputs resident in HBM (402 MB of
 inputs > the 126 MB L2, so no flush is needed between steps).  The same JSON
 line carries:
 
-* roofline: the prefill kernel's algorithmic bytes per launch / its mean
-  CUDA-event duration, against the measured HBM copy bandwidth;
+* roofline: the prefill's algorithmic bytes per call / the call's mean
+  CUDA-event duration (both of its kernels: the chunk-parallel preparation
+  kernel and the state kernel), against the measured HBM copy bandwidth;
 * decode: the in-place decode step (B=256, H=16, d=128, fp32 state of 268 MB)
   over 1024 consecutive steps, in HBM GB/s, with its own roofline;
 * e2e: the same prefill through the public API from pinned host buffers, the
@@ -241,7 +242,8 @@ def bench_prefill(gdr2, x, steps, warmup, world):
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if gdr2.gdr2_device_status() != 0:
         raise RuntimeError("device-side failure during the timed prefill")
-    return total_ms / steps, per_launch, steps
+    # each bf16 gdr2_forward launches two kernels: preparation, then the state pass
+    return total_ms / steps, per_launch, 2 * steps
 
 
 def bench_decode(gdr2, steps=1024, pool=16, seed=5):
@@ -454,7 +456,8 @@ def main():
     traffic = traffic_record("prefill_" + WORKLOAD)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "traffic": traffic,
-                "kernel": "gdr2 prefill", "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                "kernel": "gdr2 prefill: prep_kernel + state_kernel per call",
+                "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": nbytes,
                 "tflops": nflops / (kern_ms / 1e3) / 1e12,
                 "tensor_frac_of_bf16_peak": nflops / (kern_ms / 1e3) / 1e12 / bf16_tflops}
