@@ -12,10 +12,12 @@ from ._lib import (  # noqa: F401
     gdr2_decode_step,
     gdr2_device_status,
     gdr2_forward,
+    gdr2_forward_noalloc,
     gdr2_forward_varlen,
     gdr2_version,
 )
 
 forward = gdr2_forward
 forward_varlen = gdr2_forward_varlen
+forward_noalloc = gdr2_forward_noalloc
 decode_step = gdr2_decode_step

@@ -44,6 +44,8 @@ def lib():
         vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.gdr2_forward.argtypes = [vp] * 9 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward.restype = ci
+        L.gdr2_forward_noalloc.argtypes = [vp] * 9 + [i64] * 5 + [ci, ci, vp]
+        L.gdr2_forward_noalloc.restype = ci
         L.gdr2_forward_varlen.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward_varlen.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
@@ -90,13 +92,27 @@ def gdr2_forward(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
     Returns ``(o, S_T)`` with o in ``out_dtype`` (fp32 by default, or bf16);
     S_T is None when ``return_state`` is False.  ``o`` and ``S_T`` may be passed
     in to reuse buffers (``S_T is S0`` updates in place)."""
+    return _forward("gdr2_forward", q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream)
+
+
+def gdr2_forward_noalloc(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
+                         out_dtype=torch.float32, return_state: bool = True, stream=None):
+    """gdr2_forward through the entry point that allocates no device memory (its
+    workspace is a fixed array inside the library; see include/gdr2.h), for
+    callers that may not allocate at call time.  The outputs ``o`` (and ``S_T``
+    when requested) are still allocated here unless passed in."""
+    return _forward("gdr2_forward_noalloc", q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state,
+                    stream)
+
+
+def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream):
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q and v must be [B, T, H, d]")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dtype, dev = q.dtype, q.device
     if dev.type != "cuda":
-        raise ValueError("gdr2_forward runs on CUDA tensors only")
+        raise ValueError(f"{entry} runs on CUDA tensors only")
     if dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
@@ -117,12 +133,12 @@ def gdr2_forward(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
     elif S_T is not None:
         _check_tokens("S_T", S_T, (B, H, dk, dv), torch.float32, dev)
     with torch.cuda.device(dev):
-        st = lib().gdr2_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
-                                _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv,
-                                _DTYPES[dtype], _DTYPES[o.dtype],
-                                ctypes.c_void_p(_stream_handle(stream)))
+        st = getattr(lib(), entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
+                                   _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv,
+                                   _DTYPES[dtype], _DTYPES[o.dtype],
+                                   ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
-        raise GDR2Error(st, "gdr2_forward")
+        raise GDR2Error(st, entry)
     return o, S_T
 
 

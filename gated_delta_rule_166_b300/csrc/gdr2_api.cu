@@ -39,6 +39,27 @@ int device_setup(int** err_out) {
     return GDR2_OK;
 }
 
+// Scratch of gdr2_forward_noalloc: file-scope device memory that every device
+// loading the library holds until exit, shared by all calls of that entry point.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per device
+// with that device current (the host-side name of the array is not a device address).
+int scratch_setup(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR2_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDR2_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return GDR2_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -69,7 +90,7 @@ namespace {
 int forward_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
                  const void* log_decay, const float* S0, void* o, float* S_T, const int32_t* cu,
                  int64_t N, int64_t T, int64_t total, int64_t H, int64_t dk, int64_t dv, int in_dtype,
-                 int out_dtype, cudaStream_t stream) {
+                 int out_dtype, cudaStream_t stream, bool noalloc = false) {
     if (N < 0 || T < 0 || total < 0 || H < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
@@ -114,6 +135,32 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
 
     ForwardArgs a{q, k, v, b, w, log_decay, S0, o, S_T, N, T, H, dk, dv,
                   reinterpret_cast<const int*>(cu), total, in_dtype, out_dtype};
+    if (noalloc && two_kernel_supports(a)) {
+        // The same two kernels over chunk ranges whose operands fit the scratch; the
+        // state between ranges is carried in S_T (or, when the caller wants no S_T,
+        // in the scratch).
+        void* scratch = nullptr;
+        if ((st = scratch_setup(&scratch)) != GDR2_OK) return st;
+        const int64_t nch = (T + 63) / 64;
+        const size_t carry = S_T ? 0 : (static_cast<size_t>(ns) * 4 + 255) / 256 * 256;
+        int64_t cpiece = 0;
+        while (cpiece < nch && carry + prep_workspace_bytes(N * (cpiece + 1), H, N) <= kNoAllocScratchBytes)
+            ++cpiece;
+        if (cpiece == 0) return GDR2_ERR_SCRATCH;
+        float* state = S_T ? S_T : reinterpret_cast<float*>(scratch);
+        const PrepSlots s = prep_carve(static_cast<uint8_t*>(scratch) + carry, N * cpiece, H);
+        for (int64_t c0 = 0; c0 < nch; c0 += cpiece) {
+            const int64_t cp = nch - c0 < cpiece ? nch - c0 : cpiece;
+            ForwardArgs ap = a;
+            ap.S0 = c0 == 0 ? S0 : state;
+            ap.ST = state;
+            int rc = launch_prep(ap, s, N * cp, static_cast<int>(c0), static_cast<int>(cp), stream, err);
+            if (rc == GDR2_OK)
+                rc = launch_state(ap, s, N * cp, static_cast<int>(c0), static_cast<int>(cp), stream, err);
+            if (rc != GDR2_OK) return rc;
+        }
+        return GDR2_OK;
+    }
     if (two_kernel_supports(a)) {
         // Workspace for the per-chunk operands, stream-ordered from the device's
         // default memory pool and released on the same stream.
@@ -121,8 +168,9 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         void* ws = nullptr;
         if (cudaMallocAsync(&ws, prep_workspace_bytes(chunks, H, N), stream) != cudaSuccess) return GDR2_ERR_CUDA;
         const PrepSlots s = prep_carve(ws, chunks, H);
-        int rc = launch_prep(a, s, chunks, stream, err);
-        if (rc == GDR2_OK) rc = launch_state(a, s, chunks, stream, err);
+        const int cpiece = static_cast<int>((T + 63) / 64);
+        int rc = launch_prep(a, s, chunks, 0, cpiece, stream, err);
+        if (rc == GDR2_OK) rc = launch_state(a, s, chunks, 0, cpiece, stream, err);
         if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
         return rc;
     }
@@ -151,6 +199,17 @@ extern "C" int gdr2_forward_varlen(const void* q, const void* k, const void* v,
     if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
     return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, cu_seqlens, N, 0, total_T, H, dk, dv,
                         in_dtype, out_dtype, stream);
+}
+
+extern "C" int gdr2_forward_noalloc(const void* q, const void* k, const void* v,
+                                    const void* b, const void* w, const void* log_decay,
+                                    const float* S0, void* o, float* S_T,
+                                    int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                    int in_dtype, int out_dtype, cudaStream_t stream) {
+    int64_t total = 0;
+    if (B >= 0 && T >= 0 && !mul_ok(B, T, &total)) return GDR2_ERR_SHAPE;
+    return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, nullptr, B, T, total, H, dk, dv, in_dtype,
+                        out_dtype, stream, /*noalloc=*/true);
 }
 
 extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,
@@ -209,6 +268,8 @@ extern "C" const char* gdr2_status_string(int status) {
         case GDR2_ERR_ALIGN: return "GDR2_ERR_ALIGN: pointer not 16-byte aligned";
         case GDR2_ERR_UNSUPPORTED: return "GDR2_ERR_UNSUPPORTED: unknown dtype or device is not sm_103";
         case GDR2_ERR_CUDA: return "GDR2_ERR_CUDA: a CUDA runtime call failed";
+        case GDR2_ERR_SCRATCH:
+            return "GDR2_ERR_SCRATCH: B*H too large for the no-allocation scratch (gdr2_forward_noalloc)";
         case GDR2_ERR_TIMEOUT: return "GDR2_ERR_TIMEOUT: a bounded device-side wait gave up";
         case GDR2_ERR_ALIAS: return "GDR2_ERR_ALIAS: output buffer overlaps another argument";
         default: return "GDR2: unknown status";

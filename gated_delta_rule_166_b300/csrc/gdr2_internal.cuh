@@ -72,8 +72,14 @@ int64_t prep_chunk_bound(const ForwardArgs& a);
 // arrays out in `ws` (256-byte aligned).
 size_t prep_workspace_bytes(int64_t chunks, int64_t H, int64_t N);
 PrepSlots prep_carve(void* ws, int64_t chunks, int64_t H);
-int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err);
-int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err);
+// Fixed-length calls may run chunks [c0, c0 + cpiece) of every sequence (the
+// slots then hold only those chunks, `chunks` = N * cpiece); the state kernel
+// starts from a.S0 and leaves the state after the range in a.ST.  Packed calls
+// ignore c0 and cpiece.
+int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
+                int* err);
+int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
+                 int* err);
 bool two_kernel_supports(const ForwardArgs& a);
 
 }  // namespace gdr2

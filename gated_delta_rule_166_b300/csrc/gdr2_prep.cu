@@ -99,7 +99,8 @@ struct PrepParams {
     PrepSlots s;
     const int* cu;        // packed sequences: [N + 1] token offsets, or null
     int N, T, H, total;   // T: common length when cu is null
-    int nchunks;          // chunks per sequence when cu is null
+    int nchunks;          // chunks per sequence in this launch when cu is null
+    int c0;               // first chunk of each sequence in this launch (cu null)
     int nitems;           // work items = global chunk bound x H; item = slot index
     int* err;
 };
@@ -126,9 +127,11 @@ __device__ __forceinline__ bool locate(const PrepParams& prm, int it, Item& x) {
         x.T = e - a;
         x.tp = (gc - cb[lo]) * kC;
     } else {
+        // chunks c0 .. c0 + nchunks - 1 of every sequence: token offsets relative to
+        // the first of them
         const int seq = gc / prm.nchunks;
-        x.tok0 = seq * prm.T;
-        x.T = prm.T;
+        x.tok0 = seq * prm.T + prm.c0 * kC;
+        x.T = prm.T - prm.c0 * kC;
         x.tp = (gc - seq * prm.nchunks) * kC;
     }
     return true;
@@ -602,7 +605,8 @@ PrepSlots prep_carve(void* ws, int64_t chunks, int64_t H) {
     return s;
 }
 
-int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err) {
+int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
+                int* err) {
     const int64_t total = a.cu ? a.total : a.B * a.T;
     if (chunks <= 0) return GDR2_OK;
     if (chunks >= (1ll << 31)) return GDR2_ERR_SHAPE;
@@ -629,8 +633,7 @@ int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaSt
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return GDR2_ERR_CUDA;
     PrepParams prm{s, a.cu, static_cast<int>(a.B), static_cast<int>(a.T), static_cast<int>(a.H),
-                   static_cast<int>(total), a.cu ? 0 : static_cast<int>((a.T + kC - 1) / kC),
-                   static_cast<int>(nitems), err};
+                   static_cast<int>(total), a.cu ? 0 : cpiece, a.cu ? 0 : c0, static_cast<int>(nitems), err};
     // persistent: one CTA per SM, each looping over its items
     const unsigned grid = static_cast<unsigned>(nitems < sms ? nitems : sms);
     prep_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);

@@ -89,7 +89,8 @@ struct StateParams {
     float* ST;
     int* err;
     const int* cu;
-    int T, H, dv, total, nchunks;   // nchunks: chunks per sequence when cu is null
+    int T, H, dv, total, nchunks;   // nchunks: chunks per sequence in this launch when cu is null
+    int c0;                         // first chunk of each sequence in this launch (cu null)
     int chunk_bound;                // global chunks with a workspace slot
     int out_bf16;
 };
@@ -127,13 +128,15 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         T = e - a;
         cb0 = prm.s.chunk_base[seq];
     } else {
-        tok0 = seq * prm.T;
-        T = prm.T;
+        // chunks c0 .. c0 + nchunks - 1: token offsets relative to the first of them
+        tok0 = seq * prm.T + prm.c0 * kC;
+        T = prm.T - prm.c0 * kC;
         cb0 = seq * prm.nchunks;
     }
     // Well-formed offsets never reach the slot bound; overlapping malformed ones
     // can, and their chunks past it are not run (the sequence is truncated).
-    const int n = min((T + kC - 1) / kC, max(prm.chunk_bound - cb0, 0));
+    int n = min((T + kC - 1) / kC, max(prm.chunk_bound - cb0, 0));
+    if (!prm.cu) n = min(n, prm.nchunks);
     auto slot = [&](int c) { return static_cast<int64_t>(cb0 + c) * prm.H + h; };
 
     if (tid == 0) {
@@ -633,7 +636,8 @@ bool make_row_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int
 
 }  // namespace
 
-int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaStream_t stream, int* err) {
+int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
+                 int* err) {
     const int64_t total = a.cu ? a.total : a.B * a.T;
     const int64_t slots = chunks * a.H;
     if (slots * 128 >= (1ll << 31) || chunks >= (1ll << 31)) return GDR2_ERR_SHAPE;
@@ -650,7 +654,7 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, cudaS
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     StateParams prm{s, a.S0, a.o, a.ST, err, a.cu, static_cast<int>(a.T), static_cast<int>(a.H),
                     static_cast<int>(a.dv), static_cast<int>(total),
-                    a.cu ? 0 : static_cast<int>((a.T + kC - 1) / kC), static_cast<int>(chunks),
+                    a.cu ? 0 : cpiece, a.cu ? 0 : c0, static_cast<int>(chunks),
                     a.out_dtype == GDR2_BF16 ? 1 : 0};
     const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
     state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, prm);

@@ -67,7 +67,8 @@ typedef enum {
     GDR2_ERR_UNSUPPORTED = -4,  /* unknown in/out dtype; device is not sm_103         */
     GDR2_ERR_CUDA = -5,         /* a CUDA runtime call failed (launch, attribute)     */
     GDR2_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up                 */
-    GDR2_ERR_ALIAS = -7         /* o overlaps an input, or S_T overlaps a token input */
+    GDR2_ERR_ALIAS = -7,        /* o overlaps an input, or S_T overlaps a token input */
+    GDR2_ERR_SCRATCH = -8       /* gdr2_forward_noalloc: B*H exceeds its fixed scratch */
 } gdr2_status;
 
 /*
@@ -134,6 +135,38 @@ int gdr2_forward_varlen(const void* q, const void* k, const void* v,
                         const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
                         int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
                         int in_dtype, int out_dtype, cudaStream_t stream);
+
+/*
+ * gdr2_forward_noalloc -- gdr2_forward that allocates no device memory.
+ *
+ * The page has no counterpart to this call; it exists for callers that must
+ * not allocate at call time: a serving runtime that reserves all device memory
+ * when it starts and forbids allocations on its request path, or an embedding
+ * host whose memory is managed by someone else and that may not draw from the
+ * device's stream-ordered pool (which gdr2_forward uses for its workspace).
+ *
+ * Same arguments, layouts, results and error codes as gdr2_forward.  For bf16
+ * inputs with d_k = 128 the two prefill kernels run over ranges of chunks
+ * whose per-chunk operands fit a fixed 64 MiB device array inside the library
+ * (file-scope memory that every GPU which loads the library holds until the
+ * process exits): a range covers min(all, floor(scratch / (B*H*82,432 B)))
+ * chunks of every sequence, and the state is carried between ranges in S_T (in
+ * the scratch when S_T is NULL).  B*H above about 800 (fewer when S_T is NULL)
+ * returns GDR2_ERR_SCRATCH before anything is enqueued.  Other inputs run the
+ * token-sequential kernel, which needs no scratch.
+ *
+ * Every call shares the one array per device: two calls that overlap on the
+ * GPU (on different streams, or from different host threads without ordering)
+ * race on it and give wrong results; calls on one stream are ordered and safe.
+ * Nothing in the array needs to start at zero: each call writes every byte it
+ * reads.  The first call on a device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ */
+int gdr2_forward_noalloc(const void* q, const void* k, const void* v,
+                         const void* b, const void* w, const void* log_decay,
+                         const float* S0, void* o, float* S_T,
+                         int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                         int in_dtype, int out_dtype, cudaStream_t stream);
 
 /*
  * gdr2_decode_step -- one autoregressive step for every (batch, head), the

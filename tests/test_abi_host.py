@@ -13,7 +13,7 @@ from gated_delta_rule_166_b300 import _lib
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdr2.h")
 
-OK, ARG, SHAPE, ALIGN, UNSUP, CUDA, TIMEOUT, ALIAS = 0, -1, -2, -3, -4, -5, -6, -7
+OK, ARG, SHAPE, ALIGN, UNSUP, CUDA, TIMEOUT, ALIAS, SCRATCH = 0, -1, -2, -3, -4, -5, -6, -7, -8
 
 
 def declared_functions():
@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    for s in (OK, ARG, SHAPE, ALIGN, UNSUP, CUDA, TIMEOUT, ALIAS):
+    for s in (OK, ARG, SHAPE, ALIGN, UNSUP, CUDA, TIMEOUT, ALIAS, SCRATCH):
         assert _lib.status_string(s).startswith("GDR2")
     assert _lib.gdr2_version() >= 100
 
