@@ -57,7 +57,8 @@ constexpr int kPrepDK = 128;   // key channels
 // contiguous bytes in the state kernel: 8 consecutive tokens (-Cb, Kb) or 8
 // consecutive key channels (Qb) per 16-byte group.
 struct PrepSlots {
-    float* a0;         // [slots][128][64]  [T; A_qk T] (rows 0..63 T, 64..127 A_qk T), tf32-rounded fp32
+    float* a0;         // [slots][4][128][16]  [T; A_qk T] as 16-column blocks: [col / 16][row][col % 16]
+                       // (rows 0..63 T, 64..127 A_qk T), tf32-rounded fp32
     uint16_t* cbt;     // [slots][8][128][8]  -Cb: [token / 8][key channel][token % 8], fp16
     uint16_t* kbt;     // [slots][8][128][8]  Kb, same layout
     uint16_t* qb;      // [slots][16][64][8]  Qb: [channel / 8][token][channel % 8], fp16

@@ -257,7 +257,7 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         auto write_a0 = [&](int64_t slot) {
             float v[16];
             tmem_ld16(tmem + lane_base + kTmA0 + static_cast<uint32_t>(16 * R), v);
-            float4* dst = reinterpret_cast<float4*>(prm.s.a0 + slot * (128 * kC) + j * kC + 16 * R);
+            float4* dst = reinterpret_cast<float4*>(prm.s.a0 + slot * (128 * kC) + (R * 128 + j) * 16);
 #pragma unroll
             for (int e = 0; e < 16; e += 4)
                 dst[e / 4] = make_float4(tf32r(v[e]), tf32r(v[e + 1]), tf32r(v[e + 2]), tf32r(v[e + 3]));
@@ -354,11 +354,20 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 *reinterpret_cast<uint4*>(prm.s.cbt + o1) = sc4[1];
                 *reinterpret_cast<uint4*>(prm.s.kbt + o0) = sk4[0];
                 *reinterpret_cast<uint4*>(prm.s.kbt + o1) = sk4[1];
-                // [channel / 8][token][channel % 8]
-                __half* dq = reinterpret_cast<__half*>(prm.s.qb) + slot * (kC * kDK) + ((j >> 3) * kC + 16 * R) * 8 +
-                             (j & 7);
+                // [channel / 8][token][channel % 8], two channels per 4-byte store: lanes j
+                // (even) and j + 1 swap halves so that the even lane stores tokens 0..7 and
+                // the odd lane tokens 8..15 of the channel pair
+                {
+                    const bool odd = j & 1;
+                    __half2* dq = reinterpret_cast<__half2*>(reinterpret_cast<__half*>(prm.s.qb) + slot * (kC * kDK) +
+                                                             ((j >> 3) * kC + 16 * R + (odd ? 8 : 0)) * 8 + (j & 6));
 #pragma unroll
-                for (int s = 0; s < 16; ++s) dq[s * 8] = __float2half_rn(qr[s] * em);
+                    for (int s = 0; s < 8; ++s) {
+                        const float mine_lo = qr[s] * em, mine_hi = qr[s + 8] * em;
+                        const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_lo : mine_hi, 1);
+                        dq[s * 4] = odd ? __floats2half2_rn(other, mine_hi) : __floats2half2_rn(mine_lo, other);
+                    }
+                }
                 if (R == 0) prm.s.gam[slot * kDK + j] = __expf(gC);
             }
             }

@@ -62,7 +62,7 @@ constexpr uint32_t kO = 163840;        // O tile for the TMA store: [64 tokens][
 constexpr uint32_t kMisc = 180224;
 enum : uint32_t {
     kBarVW = 0, kBarVWb,                                    // TMA completions
-    kRdyA1, kRdyA0, kRdyU, kEOFree, kRdyChain, kRdyMma2,    // elementwise warps -> MMA thread
+    kRdyA1, kRdyA0, kRdyU, kRdyChain, kRdyMma2,             // elementwise warps -> MMA thread
     kOFull, kOFree,                                         // O tile: written / stored
     kDoneC1, kDoneC2, kDoneP3,                     // MMA commits
     kNumBars
@@ -141,10 +141,10 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
 
     if (tid == 0) {
         for (uint32_t i = 0; i < kNumBars; ++i) {
-            // one arrival per warp: 8 E warps (A1, U, Kb^T E operands), 8 O warps ([E; O]
-            // read out), all 16 ([T; A_qk T] and the chain)
+            // one arrival per warp: 8 E warps (the Kb^T E operand), 8 O warps (A1, U
+            // operands, O tile), all 16 ([T; A_qk T] and the chain)
             const uint32_t cnt = (i == kRdyChain || i == kRdyA0) ? 16u
-                                 : (i == kRdyA1 || i == kRdyU || i == kEOFree || i == kRdyMma2 || i == kOFull) ? 8u
+                                 : (i == kRdyA1 || i == kRdyU || i == kRdyMma2 || i == kOFull) ? 8u
                                                                                                              : 1u;
             mbar_init(bar(i), cnt);
         }
@@ -180,7 +180,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 ph ^= 1u;
                 return ok;
             };
-            uint32_t ph_a0 = 0, ph_a1 = 0, ph_u = 0, ph_eo = 0, ph_chain = 0, ph_mma2 = 0, ph_c1 = 0;
+            uint32_t ph_a0 = 0, ph_a1 = 0, ph_u = 0, ph_chain = 0, ph_mma2 = 0, ph_c1 = 0;
             // A1(c) = [T; A_qk T](c) (-Cb^T)(c)
             auto issue_a1 = [&]() {
                 if (!wait(kRdyA1, ph_a1) || !wait(kRdyA0, ph_a0)) return false;
@@ -194,7 +194,9 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
             };
             // [E; O](c) halves := [T; A_qk T](c) [U_hi^T; U_lo^T](c)
             auto issue_u = [&]() {
-                if (!wait(kRdyU, ph_u) || !wait(kEOFree, ph_eo)) return false;
+                // the E warps finished reading [E; O] before Kb^T E was issued; the O
+                // warps signal U after reading their half
+                if (!wait(kRdyU, ph_u)) return false;
                 tc_fence_after();
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s)
@@ -271,9 +273,10 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         // ================= 16 elementwise / accumulator warps ====================
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSimt));
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        // Quarters 0-1 ("E warps", lanes 0..63 = token rows of E) read E out and build the
-        // next chunks' U^T and -Cb^T operands while Kb^T E runs; quarters 2-3 ("O warps")
-        // write O and complete P.  All warps update their state slice and Kb^T.
+        // Quarters 0-1 ("E warps", lanes 0..63 = token rows of E) read E out, the chain's
+        // critical step; quarters 2-3 ("O warps") write O, complete P and build the next
+        // chunks' U^T and -Cb^T operands while Kb^T E runs.  All warps update their state
+        // slice, Kb^T and [T; A_qk T].
         const bool e_warp = quarter < 2;
         const int et = ((warp >> 2) * 2 + (warp & 1)) * 32 + lane;   // 0..255 within each group
         // Shared-memory byte offset of element (row, k) of an operand with K-blocks `kstride`
@@ -322,10 +325,10 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
             hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
             lo = x - hi;
         };
-        // E warps: -Cb^T rows (channels) ej, tokens 32*eh .. 32*eh + 31
+        // O warps: -Cb^T rows (channels) ej, tokens 32*eh .. 32*eh + 31
         const int ej = et & 127, eh = et >> 7;
         auto ld_cb = [&](int c, uint4 (&x)[4]) {
-            if (c < n && e_warp) {
+            if (c < n && !e_warp) {
                 const uint4* p =
                     reinterpret_cast<const uint4*>(prm.s.cbt + slot(c) * (kDK * kC) + ((4 * eh) * kDK + ej) * 8);
 #pragma unroll
@@ -343,7 +346,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                     make_float4(a.x, a.y, b2.x, b2.y);
             }
         };
-        // E warps: U^T of chunk c from its v, w tile: d_v column un, tokens 16*ut .. 16*ut + 15
+        // O warps: U^T of chunk c from its v, w tile: d_v column un, tokens 16*ut .. 16*ut + 15
         const int un = et & 63, ut = et >> 6;
         auto put_u = [&](int c) {
             const uint8_t* tv = sgen + kVW + static_cast<uint32_t>(c & 1) * 16384u;
@@ -419,7 +422,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         // all warps: [T; A_qk T] row j, columns 16R..16R+15 -> TMEM
         auto ld_a0 = [&](int c, float (&x)[16]) {
             if (c < n) {
-                const float4* p = reinterpret_cast<const float4*>(prm.s.a0 + slot(c) * (128 * kC) + j * kC + 16 * R);
+                const float4* p = reinterpret_cast<const float4*>(prm.s.a0 + slot(c) * (128 * kC) + (R * 128 + j) * 16);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float4 f = p[e];
@@ -443,7 +446,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
             ld_cb(0, cbr);
             ld_kb(0, kbr);
             ld_qb(0, qbr);
-            if (e_warp) {
+            if (!e_warp) {
                 put_cb(cbr);
                 arrive(kRdyA1);                                   // A1(0)
                 ld_cb(1, cbr);
@@ -452,19 +455,16 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                     put_u(0);
                     arrive(kRdyU);                                // [T; A_qk T] U (0)
                 }
-            } else {
-                arrive(kEOFree);                                  // [E; O] free for chunk 0's U product
-            }
-            if (!failed && !wait(kDoneP3, ph_p3)) failed = true;
-            if (!failed) {
-                if (e_warp) {
+                if (!failed && !wait(kDoneP3, ph_p3)) failed = true;
+                if (!failed) {
+                    add_qb(qbr);
                     if (n > 1) {
                         put_cb(cbr);
                         arrive(kRdyA1);                           // A1(1)
                     }
-                } else {
-                    add_qb(qbr);
                 }
+            }
+            if (!failed) {
                 put_kb(kbr);
                 arrive(kRdyChain);                                // chain of chunk 0
             }
@@ -499,24 +499,10 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                     *reinterpret_cast<float*>(sgen + a + 8192u) = el;
                 }
                 arrive(kRdyMma2);
-                if (c + 1 < n) {
-                    // ---- next chunk: U^T operand ------------------------------------------
-                    const bool odd = (c + 1) & 1;
-                    if (!wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
-                    put_u(c + 1);
-                    arrive(kRdyU);
-                    // ---- -Cb^T of chunk c + 2 once A1(c + 1) has read its buffer ------------
-                    if (!wait(kDoneP3, ph_p3)) { failed = true; break; }
-                    if (c + 2 < n) {
-                        put_cb(cbr);
-                        arrive(kRdyA1);
-                    }
-                }
             } else {
                 // ---- O -> global ---------------------------------------------------------------
                 float v[16];
                 tmem_ld16_pair(tmem + lane_base + kTmEO + static_cast<uint32_t>(16 * R), v);
-                if (c + 1 < n) arrive(kEOFree);
                 const int r = j - 64;
                 if (tc + kC <= T) {
                     // whole chunk inside the sequence: O tile -> shared memory -> one TMA store
@@ -561,9 +547,18 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                     }
                 }
                 if (c + 1 < n) {
-                    // ---- next chunk: P on A1 ----------------------------------------------------
+                    // ---- next chunk: U^T operand (its product overwrites [E; O] after this) -----
+                    const bool odd = (c + 1) & 1;
+                    if (!wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
+                    put_u(c + 1);
+                    arrive(kRdyU);
+                    // ---- next chunk: P on A1, then -Cb^T of chunk c + 2 into the freed buffer -----
                     if (!wait(kDoneP3, ph_p3)) { failed = true; break; }
                     add_qb(qbr);
+                    if (c + 2 < n) {
+                        put_cb(cbr);
+                        arrive(kRdyA1);
+                    }
                 }
             }
             // ---- chain: S <- gamma S + Kb^T E; S^T operand; next chunk's Kb^T ----------------
