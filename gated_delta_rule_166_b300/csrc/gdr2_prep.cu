@@ -61,12 +61,13 @@ static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96
 // ---- shared memory (bytes from a 1024-aligned base) ------------------------------
 // MMA operands are K-major with the 128-byte swizzle (K-blocks of 32 tf32).
 constexpr uint32_t kRawQ = 0, kRawK = 16384, kRawB = 32768, kRawG = 49152;  // bf16 [2 kblk][64][64]
-constexpr uint32_t kG31 = 0;           // K-groups [G3 (64 rows) | G1 (32 rows)] over the raw tiles (48 KB)
-constexpr uint32_t kOpA = 65536;       // [Ct; Qt]: 128 rows x 128 K (64 KB)
-constexpr uint32_t kG20 = 131072;      // K-groups [G2 (48 rows) | G0 (16 rows)] (32 KB)
-constexpr uint32_t kIA = 163840;       // [I; A_qk]: 128 rows x 64 K (32 KB)
-constexpr uint32_t kTT = 196608;       // T^T: 64 rows x 64 K (16 KB)
-constexpr uint32_t kMisc = 212992;     // mbarriers, TMEM slot
+// K-groups [G3 (64 rows) | G1 (32) | G2 (48) | G0 (16)]: one 160-row operand (K-blocks
+// 20 KB apart), written over the raw tiles once pass 1 has read them
+constexpr uint32_t kKG = 0, kKGStride = 20480;
+constexpr uint32_t kOpA = 81920;       // [Ct; Qt]: 128 rows x 128 K (64 KB)
+constexpr uint32_t kIA = 147456;       // [I; A_qk]: 128 rows x 64 K (32 KB)
+constexpr uint32_t kTT = 180224;       // T^T: 64 rows x 64 K (16 KB)
+constexpr uint32_t kMisc = 196608;     // mbarriers, TMEM slot
 constexpr uint32_t kSmemBytes = kMisc + 128;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr uint32_t kXTot = kOpA, kXMid = kOpA + 2048;   // per-stripe decay sums (before [Ct; Qt])
@@ -76,15 +77,15 @@ constexpr int kLt = 68;                   // T staging row (floats; rows 16-byte
 constexpr uint32_t kSL = kOpA;            // A_kk staging  [64][65] fp32
 constexpr uint32_t kSTs = kOpA + 16640;   // T staging     [64][68] fp32
 constexpr uint32_t kSP = kOpA + 34048;    // M_{RJ} blocks, 6 x 16 x 17 fp32
-static_assert(kSTs + 64 * kLt * 4 <= kSP && kSP + 6 * 16 * 17 * 4 <= kG20, "solve scratch");
-static_assert(kG31 + 4 * 12288 <= kOpA, "K-groups in the raw area");
+static_assert(kSTs + 64 * kLt * 4 <= kSP && kSP + 6 * 16 * 17 * 4 <= kOpA + 65536, "solve scratch");
+static_assert(kKG + 4 * kKGStride <= kOpA && kRawG + 16384 <= kOpA, "K-groups over the raw tiles");
 static_assert(kSmemAlloc <= 232448, "shared memory");
 enum : uint32_t { kBarTma = 0, kRdyAP, kRdyA0, kDoneP1, kDoneP2, kNumBars };
 constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
 
 // ---- TMEM columns ---------------------------------------------------------------
 constexpr uint32_t kTmA0 = 0;     // [T; A_qk T]: 128 lanes x 64 columns
-constexpr uint32_t kTmAP = 64;    // intra-chunk products: [G3|G1] 64..159, [G2|G0] 160..223
+constexpr uint32_t kTmAP = 64;    // intra-chunk products [Ct; Qt] x [G3|G1|G2|G0]^T: columns 64..223
 constexpr int kTmCols = 256;
 
 constexpr float kMinLogDecay = -10.f;
@@ -202,17 +203,13 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (it0 < prm.nitems) { load(first); ++loads; }
 #pragma unroll 1
             for (int it = it0; it < prm.nitems && ok; ph ^= 1u) {
-                // intra-chunk products [Ct; Qt] x [G3|G1]^T and x [G2|G0]^T
+                // intra-chunk products [Ct; Qt] x [G3|G1|G2|G0]^T
                 if (!(ok = mbar_wait(bar(kRdyAP), ph))) break;
                 tc_fence_after();
 #pragma unroll 1
-                for (int s = 0; s < 16; ++s) {
-                    const uint64_t a = umma_desc(kstep(base + kOpA, 16384, s));
-                    mma_ss(tmem + kTmAP, a, umma_desc(kstep(base + kG31, 12288, s)), idesc_tf32(128, 96),
-                           s > 0 ? 1u : 0u);
-                    mma_ss(tmem + kTmAP + 96u, a, umma_desc(kstep(base + kG20, 8192, s)), idesc_tf32(128, 64),
-                           s > 0 ? 1u : 0u);
-                }
+                for (int s = 0; s < 16; ++s)
+                    mma_ss(tmem + kTmAP, umma_desc(kstep(base + kOpA, 16384, s)),
+                           umma_desc(kstep(base + kKG, kKGStride, s)), idesc_tf32(128, 160), s > 0 ? 1u : 0u);
                 mma_commit(bar(kDoneP1));
                 // the products have read the K-groups over the raw tiles: next item's tiles
                 if (!(ok = mbar_wait(bar(kDoneP1), ph))) break;
@@ -328,14 +325,11 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int g = 0; g < 4; ++g) {
                 if (g < R) continue;
                 const float sc = g == R ? 1.f : __expf(gmid[g] - gm);
-                const uint32_t gb = g == 3 ? kG31 : g == 1 ? kG31 : kG20;
-                const uint32_t ks = g == 3 || g == 1 ? 12288u : 8192u;
-                const uint32_t r0 = g == 1 ? 64u : g == 0 ? 48u : 0u;
+                const uint32_t r0 = g == 3 ? 0u : g == 1 ? 64u : g == 2 ? 96u : 144u;   // = group_col(g) - kTmAP
 #pragma unroll
                 for (int s = 0; s < 16; ++s)
-                    F[(gb + sw(ks, r0 + static_cast<uint32_t>(16 * R + s), j)) >> 2] = tf32r(kr[s] * sc);
+                    F[(kKG + sw(kKGStride, r0 + static_cast<uint32_t>(16 * R + s), j)) >> 2] = tf32r(kr[s] * sc);
             }
-            signal(kRdyAP);
             // -Cb^T, Kb^T (channel rows) and Qb (token rows) as fp16 into the slot
             {
                 __half2 cbp[8], kbp[8];
@@ -370,6 +364,7 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 if (R == 0) prm.s.gam[slot * kDK + j] = __expf(gC);
             }
+                signal(kRdyAP);
             }
             // ---- the previous item's [T; A_qk T] out (overlaps this item's products) -------
             if (prev >= 0) {
