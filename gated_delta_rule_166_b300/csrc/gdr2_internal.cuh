@@ -57,15 +57,15 @@ constexpr int kPrepDK = 128;   // key channels
 // contiguous bytes in the state kernel: 8 consecutive tokens (-Cb, Kb) or 8
 // consecutive key channels (Qb) per 16-byte group.
 struct PrepSlots {
-    float* a0;         // [slots][4][128][16]  [T; A_qk T] as 16-column blocks: [col / 16][row][col % 16]
-                       // (rows 0..63 T, 64..127 A_qk T), tf32-rounded fp32
+    uint16_t* a0;      // [slots][4][128][16]  [T; A_qk T] as fp16 in 16-column blocks:
+                       // [col / 16][row][col % 16] (rows 0..63 T, 64..127 A_qk T)
     uint16_t* cbt;     // [slots][8][128][8]  -Cb: [token / 8][key channel][token % 8], fp16
     uint16_t* kbt;     // [slots][8][128][8]  Kb, same layout
     uint16_t* qb;      // [slots][16][64][8]  Qb: [channel / 8][token][channel % 8], fp16
     float* gam;        // [slots][128]        e^{G_C} per key channel
     int* chunk_base;   // [N + 1] first global chunk of each packed sequence (null: fixed length)
 };
-constexpr size_t kSlotBytes = 64 * 128 * 4 + 3 * 64 * 128 * 2 + 128 * 4;
+constexpr size_t kSlotBytes = 4 * 64 * 128 * 2 + 128 * 4;
 // Global chunks of a call: exact for fixed-length sequences, an upper bound
 // (ceil(total / 64) + N) for packed ones.
 int64_t prep_chunk_bound(const ForwardArgs& a);

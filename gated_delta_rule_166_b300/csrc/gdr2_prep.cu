@@ -13,7 +13,7 @@
 // Kb = k e^{G_C - G}, W = T Cb, P = Qb - A_qk W and U = w * v.  Everything but
 // U and S depends on q, k, b and g of the chunk alone; this kernel computes
 // it for every (chunk, head) at once and writes one workspace slot:
-//     [T; A_qk T] (fp32), -Cb^T, Kb^T, Qb (fp16), e^{G_C} (fp32).
+//     [T; A_qk T], -Cb^T, Kb^T, Qb (fp16), e^{G_C} (fp32).
 // The state kernel forms [-W; P] = [T; A_qk T](-Cb) + [0; Qb] on the tensor
 // core and runs the chunk-to-chunk chain.
 //
@@ -250,14 +250,18 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             simt_sync();
             if (tid == 0) mbar_arrive(bar(b));
         };
-        // [T; A_qk T] of a finished item -> its slot (tf32-rounded)
+        // [T; A_qk T] of a finished item -> its slot as fp16 (the 11 significant bits of
+        // the tf32 operand it becomes)
         auto write_a0 = [&](int64_t slot) {
             float v[16];
             tmem_ld16(tmem + lane_base + kTmA0 + static_cast<uint32_t>(16 * R), v);
-            float4* dst = reinterpret_cast<float4*>(prm.s.a0 + slot * (128 * kC) + (R * 128 + j) * 16);
+            uint4 pk[2];
+            __half2* ph = reinterpret_cast<__half2*>(pk);
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                dst[e / 4] = make_float4(tf32r(v[e]), tf32r(v[e + 1]), tf32r(v[e + 2]), tf32r(v[e + 3]));
+            for (int e = 0; e < 16; e += 2) ph[e / 2] = __floats2half2_rn(v[e], v[e + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(prm.s.a0 + slot * (128 * kC) + (R * 128 + j) * 16);
+            dst[0] = pk[0];
+            dst[1] = pk[1];
         };
 
         uint32_t ph = 0;
@@ -600,7 +604,7 @@ PrepSlots prep_carve(void* ws, int64_t chunks, int64_t H) {
         return r;
     };
     PrepSlots s;
-    s.a0 = reinterpret_cast<float*>(take(n * 64 * 128 * 4));
+    s.a0 = reinterpret_cast<uint16_t*>(take(n * 64 * 128 * 2));
     s.cbt = reinterpret_cast<uint16_t*>(take(n * 64 * 128 * 2));
     s.kbt = reinterpret_cast<uint16_t*>(take(n * 64 * 128 * 2));
     s.qb = reinterpret_cast<uint16_t*>(take(n * 64 * 128 * 2));

@@ -54,12 +54,12 @@ static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96
 
 // ---- shared memory (bytes from a 1024-aligned base); K-major, 128-byte swizzle ----
 constexpr uint32_t kVW = 0;            // two buffers of {v, w} bf16 tiles [64 tokens][64 d_v] (16 KB each)
-constexpr uint32_t kCbT = 32768;       // -Cb^T: 128 rows (channels) x 64 K (tokens)
-constexpr uint32_t kSt = 65536;        // S^T: 64 rows (d_v) x 128 K (channels)
-constexpr uint32_t kU = 98304;         // [U_hi^T; U_lo^T]: 128 rows x 64 K (tokens)
-constexpr uint32_t kE = 131072;        // [E_hi^T; E_lo^T]: 128 rows x 64 K (tokens)
-constexpr uint32_t kO = 163840;        // O tile for the TMA store: [64 tokens][64 d_v] (16 KB)
-constexpr uint32_t kMisc = 180224;
+constexpr uint32_t kCbT = 32768;       // -Cb^T fp16: 128 rows (channels) x 64 K (tokens), one 128 B K-block
+constexpr uint32_t kSt = 49152;        // S^T tf32: 64 rows (d_v) x 128 K (channels)
+constexpr uint32_t kU = 81920;         // [U_hi^T; U_lo^T] fp16: 128 rows x 64 K (tokens)
+constexpr uint32_t kE = 98304;         // [E_hi^T; E_lo^T] tf32: 128 rows x 64 K (tokens)
+constexpr uint32_t kO = 131072;        // O tile for the TMA store: [64 tokens][64 d_v] (16 KB)
+constexpr uint32_t kMisc = 147456;
 enum : uint32_t {
     kBarVW = 0, kBarVWb,                                    // TMA completions
     kRdyA1, kRdyA0, kRdyU, kRdyChain, kRdyMma2,             // elementwise warps -> MMA thread
@@ -79,7 +79,7 @@ constexpr uint32_t kTmA1 = 0;      // [-W; P] (A operand, K = 128 channels)
 constexpr uint32_t kTmA2 = 128;    // Kb^T (A operand: lanes = channels, K = 64 tokens)
 constexpr uint32_t kTmEO = 192;    // [E; O] as two 64-column halves (hi | lo products)
 constexpr uint32_t kTmD2 = 320;    // Kb^T E as two 64-column halves
-constexpr uint32_t kTmA0 = 448;    // [T; A_qk T] (A operand, K = 64 tokens)
+constexpr uint32_t kTmA0 = 448;    // [T; A_qk T] fp16 pairs (A operand, K = 64 tokens in 32 columns)
 constexpr int kTmCols = 512;
 
 struct StateParams {
@@ -186,9 +186,9 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 if (!wait(kRdyA1, ph_a1) || !wait(kRdyA0, ph_a0)) return false;
                 tc_fence_after();
 #pragma unroll 1
-                for (int s = 0; s < 8; ++s)
-                    mma_ts(tmem + kTmA1, tmem + kTmA0 + 8u * s, umma_desc(kstep(base + kCbT, 16384, s)),
-                           idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                for (int s = 0; s < 4; ++s)   // kind::f16, K = 16 per step
+                    mma_ts_f16(tmem + kTmA1, tmem + kTmA0 + 8u * s, umma_desc(base + kCbT + 32u * s),
+                               idesc_f16(128, 128), s > 0 ? 1u : 0u);
                 mma_commit(bar(kDoneP3));
                 return true;
             };
@@ -199,9 +199,9 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 if (!wait(kRdyU, ph_u)) return false;
                 tc_fence_after();
 #pragma unroll 1
-                for (int s = 0; s < 8; ++s)
-                    mma_ts(tmem + kTmEO, tmem + kTmA0 + 8u * s, umma_desc(kstep(base + kU, 16384, s)),
-                           idesc_tf32(128, 128), s > 0 ? 1u : 0u);
+                for (int s = 0; s < 4; ++s)   // kind::f16, K = 16 per step
+                    mma_ts_f16(tmem + kTmEO, tmem + kTmA0 + 8u * s, umma_desc(base + kU + 32u * s),
+                               idesc_f16(128, 128), s > 0 ? 1u : 0u);
                 return true;
             };
             bool ok = true;
@@ -335,41 +335,47 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 for (int g = 0; g < 4; ++g) x[g] = p[g * kDK];
             }
         };
+        // the fp16 operand row holds all 64 tokens in 128 bytes: 16-byte chunk = 8 tokens
         auto put_cb = [&](const uint4 (&x)[4]) {
-            const __half2* hc = reinterpret_cast<const __half2*>(x);
-            const uint32_t xr4 = ((static_cast<uint32_t>(ej) & 7u) << 4);
-            const uint32_t rb = kCbT + static_cast<uint32_t>(eh) * 16384u + static_cast<uint32_t>(ej) * 128u;
+            const uint32_t rb = kCbT + static_cast<uint32_t>(ej) * 128u;
 #pragma unroll
-            for (int s = 0; s < 32; s += 4) {
-                const float2 a = __half22float2(hc[s / 2]), b2 = __half22float2(hc[s / 2 + 1]);
-                *reinterpret_cast<float4*>(sgen + rb + ((static_cast<uint32_t>(s >> 2) << 4) ^ xr4)) =
-                    make_float4(a.x, a.y, b2.x, b2.y);
-            }
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4*>(sgen + rb + (((static_cast<uint32_t>(4 * eh + g)) ^ (static_cast<uint32_t>(ej) & 7u)) << 4)) = x[g];
         };
         // O warps: U^T of chunk c from its v, w tile: d_v column un, tokens 16*ut .. 16*ut + 15
         const int un = et & 63, ut = et >> 6;
+        // u = hi + lo as an fp16 pair (22 significant bits); the fp16 operand row holds all
+        // 64 tokens in 128 bytes, 8 tokens per 16-byte chunk
         auto put_u = [&](int c) {
             const uint8_t* tv = sgen + kVW + static_cast<uint32_t>(c & 1) * 16384u;
             const int tvalid = T - c * kC - 16 * ut;   // tokens past the sequence end give U = 0
-            const uint32_t xr4 = (static_cast<uint32_t>(un) & 7u) << 4;
-            const uint32_t rb = kU + static_cast<uint32_t>(ut >> 1) * 16384u + static_cast<uint32_t>(un) * 128u;
+            const uint32_t rb = kU + static_cast<uint32_t>(un) * 128u;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float hi[4], lo[4];
+            for (int q8 = 0; q8 < 2; ++q8) {
+                uint4 hk, lk;
+                __half2* hh = reinterpret_cast<__half2*>(&hk);
+                __half2* lh = reinterpret_cast<__half2*>(&lk);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 16 * ut + 4 * q4 + e;
-                    const uint32_t off = vw_off(t, un);
-                    const float vv =
-                        __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + off)) << 16);
-                    const float ww =
-                        __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + 8192 + off)) << 16);
-                    split(4 * q4 + e < tvalid ? vv * ww : 0.f, hi[e], lo[e]);
+                for (int e = 0; e < 8; e += 2) {
+                    float u[2];
+#pragma unroll
+                    for (int f = 0; f < 2; ++f) {
+                        const int t = 16 * ut + 8 * q8 + e + f;
+                        const uint32_t off = vw_off(t, un);
+                        const float vv =
+                            __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + off)) << 16);
+                        const float ww = __uint_as_float(
+                            static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + 8192 + off)) << 16);
+                        u[f] = 8 * q8 + e + f < tvalid ? vv * ww : 0.f;
+                    }
+                    const __half2 h2 = __floats2half2_rn(u[0], u[1]);
+                    const float2 hf = __half22float2(h2);
+                    hh[e / 2] = h2;
+                    lh[e / 2] = __floats2half2_rn(u[0] - hf.x, u[1] - hf.y);
                 }
-                // K chunk (16*ut + 4*q4) % 32 / 4 of rows un (hi) and 64 + un (lo)
-                const uint32_t cofs = ((static_cast<uint32_t>((ut & 1) * 4 + q4) << 4) ^ xr4);
-                *reinterpret_cast<float4*>(sgen + rb + cofs) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4*>(sgen + rb + 8192u + cofs) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+                const uint32_t cofs = (static_cast<uint32_t>(2 * ut + q8) ^ (static_cast<uint32_t>(un) & 7u)) << 4;
+                *reinterpret_cast<uint4*>(sgen + rb + cofs) = hk;
+                *reinterpret_cast<uint4*>(sgen + rb + 64u * 128u + cofs) = lk;
             }
         };
         // all warps: Kb (channel j, tokens 16R..16R+15) -> TMEM Kb^T
@@ -420,23 +426,22 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         };
 
         // all warps: [T; A_qk T] row j, columns 16R..16R+15 -> TMEM
-        auto ld_a0 = [&](int c, float (&x)[16]) {
+        // fp16 pairs: column 8R + e holds tokens 16R + 2e (low half) and 16R + 2e + 1
+        auto ld_a0 = [&](int c, uint32_t (&x)[8]) {
             if (c < n) {
-                const float4* p = reinterpret_cast<const float4*>(prm.s.a0 + slot(c) * (128 * kC) + (R * 128 + j) * 16);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 f = p[e];
-                    x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
-                }
+                const uint4* p = reinterpret_cast<const uint4*>(prm.s.a0 + slot(c) * (128 * kC) + (R * 128 + j) * 16);
+                const uint4 a = p[0], b = p[1];
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
             }
         };
-        auto put_a0 = [&](const float (&x)[16]) {
-            tmem_st16(tmem + lane_base + kTmA0 + static_cast<uint32_t>(16 * R), x);
+        auto put_a0 = [&](const uint32_t (&x)[8]) {
+            tmem_st8(tmem + lane_base + kTmA0 + static_cast<uint32_t>(8 * R), x);
             tmem_st_wait();
         };
 
         uint4 cbr[4], kbr[2], qbr[4];
-        float a0r[16];
+        uint32_t a0r[8];
         float gam = 1.f;
         if (n > 0) {
             // ---- prologue: operands of chunk 0, and -Cb^T of chunk 1 ----------------------

@@ -26,7 +26,7 @@
  *   row-major and contiguous, 16-byte aligned.  The caller owns every buffer
  *   and the library keeps no pointer after return.  The chunked bf16 prefill
  *   (gdr2_forward, gdr2_forward_varlen with bf16 inputs and d_k = 128) takes a
- *   workspace of 82,432 bytes per (64-token chunk, head) -- the per-chunk
+ *   workspace of 66,048 bytes per (64-token chunk, head) -- the per-chunk
  *   operands its two kernels exchange -- from the device's default
  *   stream-ordered memory pool (cudaMallocAsync on `stream`) and releases it
  *   on the same stream; no other call allocates device memory.
@@ -149,9 +149,9 @@ int gdr2_forward_varlen(const void* q, const void* k, const void* v,
  * inputs with d_k = 128 the two prefill kernels run over ranges of chunks
  * whose per-chunk operands fit a fixed 64 MiB device array inside the library
  * (file-scope memory that every GPU which loads the library holds until the
- * process exits): a range covers min(all, floor(scratch / (B*H*82,432 B)))
+ * process exits): a range covers min(all, floor(scratch / (B*H*66,048 B)))
  * chunks of every sequence, and the state is carried between ranges in S_T (in
- * the scratch when S_T is NULL).  B*H above about 800 (fewer when S_T is NULL)
+ * the scratch when S_T is NULL).  B*H above about 1000 (fewer when S_T is NULL)
  * returns GDR2_ERR_SCRATCH before anything is enqueued.  Other inputs run the
  * token-sequential kernel, which needs no scratch.
  *
