@@ -29,11 +29,11 @@
 // and Kb are bounded by |b k| and |q|, |k| and are later used at tf32
 // precision, so fp16 (the same 11 significant bits) carries them.
 //
-// Work split: one CTA (640 threads, one per SM) per (chunk, head).  Thread
-// (j = tid % 128, R = tid / 128) of the first 512 owns key channel j of stripe R
-// in the elementwise phases and TMEM lane j, columns 16R..16R+15 in the
-// accumulator phases; one thread of the last warpgroup issues the TMA loads and
-// tcgen05 MMAs.
+// Work split: one persistent CTA (640 threads) per SM.  In pass 1 thread
+// (jp = tid % 64, hs = tid / 64) of the first 512 owns key channels 2jp, 2jp + 1
+// over the 8 tokens of half-stripe hs; in the accumulator phases thread
+// (j = tid % 128, R = tid / 128) owns TMEM lane j, columns 16R..16R+15.  One
+// thread of the last warpgroup issues the TMA loads and tcgen05 MMAs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -70,7 +70,7 @@ constexpr uint32_t kTT = 180224;       // T^T: 64 rows x 64 K (16 KB)
 constexpr uint32_t kMisc = 196608;     // mbarriers, TMEM slot
 constexpr uint32_t kSmemBytes = kMisc + 128;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
-constexpr uint32_t kXTot = kOpA, kXMid = kOpA + 2048;   // per-stripe decay sums (before [Ct; Qt])
+constexpr uint32_t kXTot = kOpA;   // per-half-stripe decay sums, 8 x 128 fp32 (before [Ct; Qt])
 // solve scratch inside the [Ct; Qt] area (dead once the intra-chunk products are done)
 constexpr int kLd = 65;                   // A_kk staging row (floats)
 constexpr int kLt = 68;                   // T staging row (floats; rows 16-byte aligned)
@@ -272,102 +272,119 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int T = cur.T, tp = cur.tp;
             const int64_t slot = it;
             // ---- pass 1: raw tiles -> decay factors, [Ct; Qt], K-groups, -Cb, Qb, Kb --------
+            // Thread (jp = tid % 64, hs = tid / 64) owns key channels 2jp and 2jp + 1 over tokens
+            // 8hs .. 8hs + 7 (half hs % 2 of stripe hs / 2): 32-bit raw loads and 64-bit
+            // operand stores carry both channels.
             {
-                float cr[16], qr[16], kr[16];   // c*rho, q*rho, k/rho
+                const int jp = tid & 63, hs = tid >> 6, Rs = hs >> 1, hf = hs & 1;
+                const uint32_t ch = 2u * static_cast<uint32_t>(jp);
+                float cr[2][8], qr[2][8], kr[2][8];   // [channel][token]: c*rho, q*rho, k/rho
                 if (!wait_done(kBarTma, ph)) { failed = true; break; }
-            // element (token 16R+s, channel j) of a bf16 tile
-            const uint32_t cbase = (static_cast<uint32_t>(j) >> 6) * 8192u +
-                                   static_cast<uint32_t>(16 * R) * 128u + ((static_cast<uint32_t>(j) & 7u) << 1);
-            const uint32_t c8 = (static_cast<uint32_t>(j) & 63u) >> 3;
-            float Gl[16];
-            float acc = 0.f;
-            // tokens past the sequence end enter as q = k = b = log_decay = 0
-            const int nvalid = T - tp - 16 * R;
+                // element (token 8hs + s, channels ch, ch + 1) of a bf16 tile: one 32-bit word
+                const uint32_t cbase = (ch >> 6) * 8192u + static_cast<uint32_t>(8 * hs) * 128u + ((ch & 7u) << 1);
+                const uint32_t c8 = (ch & 63u) >> 3;
+                float Gl[2][8];
+                float acc0 = 0.f, acc1 = 0.f;
+                // tokens past the sequence end enter as q = k = b = log_decay = 0
+                const int nvalid = T - tp - 8 * hs;
 #pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const uint32_t off =
-                    cbase + static_cast<uint32_t>(s) * 128u + ((c8 ^ (static_cast<uint32_t>(s) & 7u)) << 4);
-                const uint32_t live = s < nvalid ? 0xFFFFFFFFu : 0u;
-                acc += fmaxf(__uint_as_float((static_cast<uint32_t>(H16[(kRawG + off) >> 1]) << 16) & live),
-                             kMinLogDecay);
-                Gl[s] = acc;
-                const float kv = __uint_as_float((static_cast<uint32_t>(H16[(kRawK + off) >> 1]) << 16) & live);
-                cr[s] = __uint_as_float(static_cast<uint32_t>(H16[(kRawB + off) >> 1]) << 16) * kv;
-                qr[s] = __uint_as_float((static_cast<uint32_t>(H16[(kRawQ + off) >> 1]) << 16) & live);
-                kr[s] = kv;
-            }
-            F[(kXTot >> 2) + R * 128 + j] = acc;
-            F[(kXMid >> 2) + R * 128 + j] = Gl[7];
-            simt_sync();   // raw tiles fully read; stripe sums visible
-            float gmid[4];
-            float gC = 0.f;
-#pragma unroll
-            for (int r2 = 0; r2 < 4; ++r2) {
-                gmid[r2] = gC + F[(kXMid >> 2) + r2 * 128 + j];
-                gC += F[(kXTot >> 2) + r2 * 128 + j];
-            }
-            const float gm = gmid[R];
-            const float em = __expf(gm);          // e^{G_m}        (<= 1)
-            const float ecm = __expf(gC - gm);    // e^{G_C - G_m}  (<= 1)
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const float d = Gl[s] - Gl[7];
-                const float rho = __expf(fminf(d, 80.f)), irho = __expf(fminf(-d, 80.f));
-                cr[s] *= rho;
-                qr[s] *= rho;
-                kr[s] *= irho;
-            }
-            simt_sync();   // exchange reads done before [Ct; Qt] overwrites it
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const uint32_t r = static_cast<uint32_t>(16 * R + s);
-                F[(kOpA + sw(16384, r, j)) >> 2] = tf32r(cr[s]);
-                F[(kOpA + sw(16384, 64u + r, j)) >> 2] = tf32r(qr[s]);
-            }
-            // K-groups: this stripe's tokens scaled to each later stripe's reference
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (g < R) continue;
-                const float sc = g == R ? 1.f : __expf(gmid[g] - gm);
-                const uint32_t r0 = g == 3 ? 0u : g == 1 ? 64u : g == 2 ? 96u : 144u;   // = group_col(g) - kTmAP
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    F[(kKG + sw(kKGStride, r0 + static_cast<uint32_t>(16 * R + s), j)) >> 2] = tf32r(kr[s] * sc);
-            }
-            // -Cb^T, Kb^T (channel rows) and Qb (token rows) as fp16 into the slot
-            {
-                __half2 cbp[8], kbp[8];
-#pragma unroll
-                for (int s = 0; s < 16; s += 2) {
-                    cbp[s / 2] = __floats2half2_rn(-cr[s] * em, -cr[s + 1] * em);
-                    kbp[s / 2] = __floats2half2_rn(kr[s] * ecm, kr[s + 1] * ecm);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = cbase + static_cast<uint32_t>(s) * 128u + ((c8 ^ static_cast<uint32_t>(s)) << 4);
+                    const uint32_t live = s < nvalid ? 0xFFFFFFFFu : 0u;
+                    const uint32_t g2 = *reinterpret_cast<const uint32_t*>(sgen + kRawG + off) & live;
+                    const uint32_t k2 = *reinterpret_cast<const uint32_t*>(sgen + kRawK + off) & live;
+                    const uint32_t b2 = *reinterpret_cast<const uint32_t*>(sgen + kRawB + off);
+                    const uint32_t q2 = *reinterpret_cast<const uint32_t*>(sgen + kRawQ + off) & live;
+                    acc0 += fmaxf(__uint_as_float(g2 << 16), kMinLogDecay);
+                    acc1 += fmaxf(__uint_as_float(g2 & 0xFFFF0000u), kMinLogDecay);
+                    Gl[0][s] = acc0;
+                    Gl[1][s] = acc1;
+                    const float k0 = __uint_as_float(k2 << 16), k1 = __uint_as_float(k2 & 0xFFFF0000u);
+                    cr[0][s] = __uint_as_float(b2 << 16) * k0;
+                    cr[1][s] = __uint_as_float(b2 & 0xFFFF0000u) * k1;
+                    qr[0][s] = __uint_as_float(q2 << 16);
+                    qr[1][s] = __uint_as_float(q2 & 0xFFFF0000u);
+                    kr[0][s] = k0;
+                    kr[1][s] = k1;
                 }
-                // [token / 8][channel][token % 8]: this thread's tokens 16R..16R+15 are
-                // groups 2R and 2R + 1
-                const int64_t o0 = slot * (kDK * kC) + ((2 * R) * kDK + j) * 8;
-                const int64_t o1 = o0 + kDK * 8;
-                const uint4* sc4 = reinterpret_cast<const uint4*>(cbp);
-                const uint4* sk4 = reinterpret_cast<const uint4*>(kbp);
-                *reinterpret_cast<uint4*>(prm.s.cbt + o0) = sc4[0];
-                *reinterpret_cast<uint4*>(prm.s.cbt + o1) = sc4[1];
-                *reinterpret_cast<uint4*>(prm.s.kbt + o0) = sk4[0];
-                *reinterpret_cast<uint4*>(prm.s.kbt + o1) = sk4[1];
-                // [channel / 8][token][channel % 8], two channels per 4-byte store: lanes j
-                // (even) and j + 1 swap halves so that the even lane stores tokens 0..7 and
-                // the odd lane tokens 8..15 of the channel pair
-                {
-                    const bool odd = j & 1;
-                    __half2* dq = reinterpret_cast<__half2*>(reinterpret_cast<__half*>(prm.s.qb) + slot * (kC * kDK) +
-                                                             ((j >> 3) * kC + 16 * R + (odd ? 8 : 0)) * 8 + (j & 6));
+                // half-stripe totals -> every thread: G at each stripe's reference token (the
+                // last token of its first half) and G_C, per channel
+                float* const xt = F + (kXTot >> 2);
+                xt[hs * 128 + ch] = acc0;
+                xt[hs * 128 + ch + 1] = acc1;
+                simt_sync();   // raw tiles fully read; totals visible
+                float gmid0[4], gmid1[4], gC0 = 0.f, gC1 = 0.f;
 #pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const float mine_lo = qr[s] * em, mine_hi = qr[s + 8] * em;
-                        const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_lo : mine_hi, 1);
-                        dq[s * 4] = odd ? __floats2half2_rn(other, mine_hi) : __floats2half2_rn(mine_lo, other);
+                for (int h2 = 0; h2 < 8; ++h2) {
+                    gC0 += xt[h2 * 128 + ch];
+                    gC1 += xt[h2 * 128 + ch + 1];
+                    if (!(h2 & 1)) {
+                        gmid0[h2 >> 1] = gC0;
+                        gmid1[h2 >> 1] = gC1;
                     }
                 }
-                if (R == 0) prm.s.gam[slot * kDK + j] = __expf(gC);
-            }
+                const float gm0 = gmid0[Rs], gm1 = gmid1[Rs];
+                const float em0 = __expf(gm0), em1 = __expf(gm1);                  // e^{G_m}        (<= 1)
+                const float ecm0 = __expf(gC0 - gm0), ecm1 = __expf(gC1 - gm1);    // e^{G_C - G_m}  (<= 1)
+                // G_r - G_m within the stripe: the first half ends at m, the second starts after it
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const float d0 = hf ? Gl[0][s] : Gl[0][s] - Gl[0][7];
+                    const float d1 = hf ? Gl[1][s] : Gl[1][s] - Gl[1][7];
+                    const float rho0 = __expf(fminf(d0, 80.f)), irho0 = __expf(fminf(-d0, 80.f));
+                    const float rho1 = __expf(fminf(d1, 80.f)), irho1 = __expf(fminf(-d1, 80.f));
+                    cr[0][s] *= rho0; qr[0][s] *= rho0; kr[0][s] *= irho0;
+                    cr[1][s] *= rho1; qr[1][s] *= rho1; kr[1][s] *= irho1;
+                }
+                simt_sync();   // exchange reads done before [Ct; Qt] overwrites it
+                const uint32_t row0 = static_cast<uint32_t>(8 * hs);   // this half-stripe's first token row
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t r = row0 + static_cast<uint32_t>(s);
+                    *reinterpret_cast<float2*>(sgen + kOpA + sw(16384, r, ch)) =
+                        make_float2(tf32r(cr[0][s]), tf32r(cr[1][s]));
+                    *reinterpret_cast<float2*>(sgen + kOpA + sw(16384, 64u + r, ch)) =
+                        make_float2(tf32r(qr[0][s]), tf32r(qr[1][s]));
+                }
+                // K-groups: this half-stripe's tokens scaled to each later stripe's reference
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (g < Rs) continue;
+                    const float sc0 = g == Rs ? 1.f : __expf(gmid0[g] - gm0);
+                    const float sc1 = g == Rs ? 1.f : __expf(gmid1[g] - gm1);
+                    const uint32_t r0 = g == 3 ? 0u : g == 1 ? 64u : g == 2 ? 96u : 144u;   // = group_col(g) - kTmAP
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        *reinterpret_cast<float2*>(sgen + kKG + sw(kKGStride, r0 + row0 + static_cast<uint32_t>(s), ch)) =
+                            make_float2(tf32r(kr[0][s] * sc0), tf32r(kr[1][s] * sc1));
+                }
+                // -Cb, Kb as fp16 [token / 8][channel][token % 8] (this half-stripe is token group
+                // hs), Qb as [channel / 8][token][channel % 8], e^{G_C}: into the slot
+                {
+                    uint4 cb[2], kb[2];
+                    __half2* pc = reinterpret_cast<__half2*>(cb);
+                    __half2* pk = reinterpret_cast<__half2*>(kb);
+#pragma unroll
+                    for (int s = 0; s < 8; s += 2) {
+                        pc[s / 2] = __floats2half2_rn(-cr[0][s] * em0, -cr[0][s + 1] * em0);
+                        pc[4 + s / 2] = __floats2half2_rn(-cr[1][s] * em1, -cr[1][s + 1] * em1);
+                        pk[s / 2] = __floats2half2_rn(kr[0][s] * ecm0, kr[0][s + 1] * ecm0);
+                        pk[4 + s / 2] = __floats2half2_rn(kr[1][s] * ecm1, kr[1][s + 1] * ecm1);
+                    }
+                    const int64_t o = slot * (kDK * kC) + (static_cast<int64_t>(hs) * kDK + ch) * 8;
+                    uint4* dc = reinterpret_cast<uint4*>(prm.s.cbt + o);
+                    uint4* dk = reinterpret_cast<uint4*>(prm.s.kbt + o);
+                    dc[0] = cb[0]; dc[1] = cb[1];
+                    dk[0] = kb[0]; dk[1] = kb[1];
+                    __half2* dq = reinterpret_cast<__half2*>(reinterpret_cast<__half*>(prm.s.qb) + slot * (kC * kDK) +
+                                                             ((ch >> 3) * kC + 8 * hs) * 8 + (ch & 7u));
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) dq[s * 4] = __floats2half2_rn(qr[0][s] * em0, qr[1][s] * em1);
+                    if (hs == 0) {
+                        prm.s.gam[slot * kDK + ch] = __expf(gC0);
+                        prm.s.gam[slot * kDK + ch + 1] = __expf(gC1);
+                    }
+                }
                 signal(kRdyAP);
             }
             // ---- the previous item's [T; A_qk T] out (overlaps this item's products) -------

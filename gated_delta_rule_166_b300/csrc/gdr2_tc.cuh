@@ -14,10 +14,12 @@ constexpr long long kWaitCycles = 4ll * 1000 * 1000 * 1000;   // ~2 s at 2 GHz
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ float tf32r(float x) {   // round to nearest tf32
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+// Round to the nearest tf32 value (10 explicit mantissa bits), ties away from zero,
+// on the integer pipe: adding half a unit of the 11th significant bit to the
+// magnitude bits and clearing the 13 bits below it rounds the significand and
+// carries into the exponent where needed (finite x well below the fp32 maximum).
+__device__ __forceinline__ float tf32r(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 // Byte offset of element (row, k) of a K-major 128B-swizzled tf32 operand
 // whose 32-element K-blocks are `kstride` bytes apart.
