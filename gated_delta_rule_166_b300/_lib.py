@@ -46,6 +46,8 @@ def lib():
         L.gdr2_forward.restype = ci
         L.gdr2_forward_noalloc.argtypes = [vp] * 9 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward_noalloc.restype = ci
+        L.gdr2_forward_segmented.argtypes = [vp] * 9 + [i64] * 5 + [ci, ci, i64, vp]
+        L.gdr2_forward_segmented.restype = ci
         L.gdr2_forward_varlen.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward_varlen.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
@@ -86,12 +88,20 @@ def _check_tokens(name, t, shape, dtype, device):
 
 
 def gdr2_forward(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
-                 out_dtype=torch.float32, return_state: bool = True, stream=None):
+                 out_dtype=torch.float32, return_state: bool = True, stream=None, segments=None):
     """Chunked prefill.  q, k, b, log_decay: [B, T, H, dk]; v, w: [B, T, H, dv]
     (all fp32 or all bf16, on one CUDA device); S0: [B, H, dk, dv] fp32 or None.
     Returns ``(o, S_T)`` with o in ``out_dtype`` (fp32 by default, or bf16);
     S_T is None when ``return_state`` is False.  ``o`` and ``S_T`` may be passed
-    in to reuse buffers (``S_T is S0`` updates in place)."""
+    in to reuse buffers (``S_T is S0`` updates in place).  ``segments`` (an int)
+    fixes the number of sequence segments of the chunk-parallel scan
+    (gdr2_forward_segmented; 1 = the sequential state pass); None leaves the
+    choice to the library."""
+    if segments is not None:
+        if int(segments) < 0:
+            raise ValueError("segments must be >= 0")
+        return _forward("gdr2_forward_segmented", q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state,
+                        stream, extra=(int(segments),))
     return _forward("gdr2_forward", q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream)
 
 
@@ -105,7 +115,7 @@ def gdr2_forward_noalloc(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
                     stream)
 
 
-def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream):
+def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream, extra=()):
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q and v must be [B, T, H, d]")
     B, T, H, dk = q.shape
@@ -135,7 +145,7 @@ def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_stat
     with torch.cuda.device(dev):
         st = getattr(lib(), entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
                                    _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv,
-                                   _DTYPES[dtype], _DTYPES[o.dtype],
+                                   _DTYPES[dtype], _DTYPES[o.dtype], *extra,
                                    ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
         raise GDR2Error(st, entry)

@@ -60,6 +60,37 @@ int scratch_setup(void** out) {
     return GDR2_OK;
 }
 
+int g_sm_count[kMaxDevices] = {};
+
+// Streaming multiprocessors of the current device (looked up once per device).
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_sm_count[dev] && cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        g_sm_count[dev] = 0;
+    return g_sm_count[dev];
+}
+
+// Segments per sequence for the chunk-parallel scan when the caller leaves the
+// choice to the library: the most segments (each of at least kMinSegChunks chunks)
+// whose value and transfer tiles still fit one CTA per SM in a single wave.  The
+// state pass is a chain of dependent steps per chunk, so splitting the sequences
+// pays only while the unsplit pass leaves SMs idle.
+constexpr int64_t kMinSegChunks = 16;
+int auto_segments(int64_t BH, int64_t dv, int64_t nch) {
+    const int64_t sms = sm_count();
+    const int64_t tv = dv / 64, tk = kPrepDK / 64;
+    int G = 1;
+    for (int64_t g = 2; g <= 64; ++g) {
+        if (g * BH * tv + (g - 1) * BH * tk > sms || nch < g * kMinSegChunks) break;
+        G = static_cast<int>(g);
+    }
+    return G;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -90,8 +121,8 @@ namespace {
 int forward_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
                  const void* log_decay, const float* S0, void* o, float* S_T, const int32_t* cu,
                  int64_t N, int64_t T, int64_t total, int64_t H, int64_t dk, int64_t dv, int in_dtype,
-                 int out_dtype, cudaStream_t stream, bool noalloc = false) {
-    if (N < 0 || T < 0 || total < 0 || H < 0) return GDR2_ERR_ARG;
+                 int out_dtype, cudaStream_t stream, bool noalloc = false, int64_t segments = 0) {
+    if (N < 0 || T < 0 || total < 0 || H < 0 || segments < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
     const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
@@ -162,18 +193,57 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         return GDR2_OK;
     }
     if (two_kernel_supports(a)) {
-        // Workspace for the per-chunk operands, stream-ordered from the device's
-        // default memory pool and released on the same stream.
+        // Segments of the chunk-parallel scan (fixed-length sequences only).
+        const int64_t nch = (T + 63) / 64;
+        SegArgs seg;
+        if (!cu) {
+            int64_t G = segments > 0 ? (segments < nch ? segments : nch) : auto_segments(bh, dv, nch);
+            int64_t L = (nch + G - 1) / G;
+            L += L & 1;              // even: 128-row tiles of the correction stay in one segment
+            G = (nch + L - 1) / L;   // no empty segment
+            if (G > 1) {
+                seg.G = static_cast<int>(G);
+                seg.L = static_cast<int>(L);
+                seg.Tr = T - L * 64;
+            }
+        } else if (segments > 1) {
+            return GDR2_ERR_UNSUPPORTED;
+        }
+        // Workspace for the per-chunk operands (and the segments' maps and partial
+        // outputs), stream-ordered from the device's default memory pool and released
+        // on the same stream.
         const int64_t chunks = prep_chunk_bound(a);
+        const size_t wsb = round256(prep_workspace_bytes(chunks, H, N));
+        size_t nb_state = 0, nb_m = 0, nb_o32 = 0, nb_r = 0;
+        if (seg.G > 1) {
+            nb_state = round256(static_cast<size_t>(N * seg.G * H) * dk * dv * 4);   // also sT
+            nb_m = round256(static_cast<size_t>(N * seg.G * H) * dk * dk * 4);
+            nb_o32 = round256(static_cast<size_t>(N * seg.Tr * H) * dv * 4);
+            nb_r = round256(static_cast<size_t>(N * seg.Tr * H) * dk * 4);
+        }
         void* ws = nullptr;
-        if (cudaMallocAsync(&ws, prep_workspace_bytes(chunks, H, N), stream) != cudaSuccess) return GDR2_ERR_CUDA;
+        if (cudaMallocAsync(&ws, wsb + 2 * nb_state + nb_m + nb_o32 + nb_r, stream) != cudaSuccess)
+            return GDR2_ERR_CUDA;
         const PrepSlots s = prep_carve(ws, chunks, H);
-        const int cpiece = static_cast<int>((T + 63) / 64);
+        if (seg.G > 1) {
+            uint8_t* p = static_cast<uint8_t*>(ws) + wsb;
+            seg.seg_state = reinterpret_cast<float*>(p);
+            seg.sT = reinterpret_cast<float*>(p + nb_state);
+            seg.seg_m = reinterpret_cast<float*>(p + 2 * nb_state);
+            seg.o32 = reinterpret_cast<float*>(p + 2 * nb_state + nb_m);
+            seg.r = reinterpret_cast<float*>(p + 2 * nb_state + nb_m + nb_o32);
+        }
+        const int cpiece = static_cast<int>(nch);
         int rc = launch_prep(a, s, chunks, 0, cpiece, stream, err);
-        if (rc == GDR2_OK) rc = launch_state(a, s, chunks, 0, cpiece, stream, err);
+        if (rc == GDR2_OK) rc = launch_state(a, s, chunks, 0, cpiece, stream, err, seg);
+        if (seg.G > 1) {
+            if (rc == GDR2_OK) rc = launch_scan(a, seg, stream);
+            if (rc == GDR2_OK) rc = launch_correct(a, seg, stream, err);
+        }
         if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
         return rc;
     }
+    if (segments > 1) return GDR2_ERR_UNSUPPORTED;
     return launch_recurrent(a, stream);
 }
 
@@ -210,6 +280,18 @@ extern "C" int gdr2_forward_noalloc(const void* q, const void* k, const void* v,
     if (B >= 0 && T >= 0 && !mul_ok(B, T, &total)) return GDR2_ERR_SHAPE;
     return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, nullptr, B, T, total, H, dk, dv, in_dtype,
                         out_dtype, stream, /*noalloc=*/true);
+}
+
+extern "C" int gdr2_forward_segmented(const void* q, const void* k, const void* v,
+                                      const void* b, const void* w, const void* log_decay,
+                                      const float* S0, void* o, float* S_T,
+                                      int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                      int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream) {
+    int64_t total = 0;
+    if (B >= 0 && T >= 0 && !mul_ok(B, T, &total)) return GDR2_ERR_SHAPE;
+    if (segments < 0) return GDR2_ERR_ARG;
+    return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, nullptr, B, T, total, H, dk, dv, in_dtype,
+                        out_dtype, stream, /*noalloc=*/false, segments);
 }
 
 extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,

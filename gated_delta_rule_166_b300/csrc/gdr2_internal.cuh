@@ -79,8 +79,27 @@ PrepSlots prep_carve(void* ws, int64_t chunks, int64_t H);
 // ignore c0 and cpiece.
 int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
                 int* err);
+// Chunk-parallel scan over segments of the sequences (fixed-length calls with
+// c0 = 0): G segments of L chunks per sequence, L even (the last may be shorter,
+// none is empty).  The state kernel then runs every segment at once: value tiles from S0
+// (segment 0) or zero, transfer tiles from the identity with U = 0; launch_scan
+// chains the segments' affine maps S -> M S + N and launch_correct adds each later
+// segment's start-state term S_start^T r_t to its o rows.  G = 1: no segments.
+struct SegArgs {
+    int G = 1, L = 0;
+    int64_t Tr = 0;              // T - L * 64: rows per sequence of o32 and r
+    float* seg_state = nullptr;  // [B][H][G][d_k][dv] value tiles' end states
+    float* seg_m = nullptr;      // [B][H][G][d_k][d_k] transfer tiles' end states (g >= 1)
+    float* o32 = nullptr;        // [B * Tr][H][dv] o of segments g >= 1 from a zero start
+    float* r = nullptr;          // [B * Tr][H][d_k] r_t = M_t^T q_t of segments g >= 1
+    float* sT = nullptr;         // [B][H][G][dv][d_k] S_start(g)^T (g >= 1)
+};
 int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
-                 int* err);
+                 int* err, const SegArgs& seg = SegArgs{});
+// S_start of every segment and the final state (into a.ST when non-null); then o of
+// segments g >= 1 = o32 + S_start^T r in the output dtype.
+int launch_scan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream);
+int launch_correct(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream, int* err);
 bool two_kernel_supports(const ForwardArgs& a);
 
 }  // namespace gdr2

@@ -93,6 +93,19 @@ struct StateParams {
     int c0;                         // first chunk of each sequence in this launch (cu null)
     int chunk_bound;                // global chunks with a workspace slot
     int out_bf16;
+    // Segmented pass (fixed-length sequences, G > 1): blockIdx.x = (sequence * G + g) * H
+    // + head runs chunks g*L .. g*L + L - 1.  Value tiles of segment 0 start from S0
+    // and write o; those of later segments start from zero and write fp32 rows to
+    // o32.  Transfer tiles (blockIdx.y >= dv / 64, segments g >= 1) start from the
+    // identity columns j0.. of d_k with U = 0 and write r_t = M_t^T q_t to r.  Every
+    // tile leaves its end state in seg_state ([sequence][head][g][d_k][dv], value) or
+    // seg_m ([sequence][head][g][d_k][d_k], transfer).
+    int G, L;
+    int Tr;                         // rows per sequence of o32 and r: T - L * 64
+    float* seg_state;
+    float* seg_m;
+    float* o32;                     // [N * Tr][H][dv] fp32
+    float* r;                       // [N * Tr][H][d_k] fp32
 };
 
 // Element (token t, column n) of a TMA-loaded bf16 [64][64] tile (128-byte rows, swizzled).
@@ -103,7 +116,18 @@ __device__ __forceinline__ uint32_t vw_off(int t, int n) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
-             const __grid_constant__ CUtensorMap tm_o, const StateParams prm) {
+             const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_o32,
+             const __grid_constant__ CUtensorMap tm_r, const StateParams prm) {
+    // segment, tile kind and output routing (uniform over the CTA)
+    const int ntv = prm.dv / kDVT;
+    const bool mtile = static_cast<int>(blockIdx.y) >= ntv;
+    const int h = static_cast<int>(blockIdx.x) % prm.H;
+    const int sg = static_cast<int>(blockIdx.x) / prm.H;
+    const int seq = sg / prm.G, g = sg % prm.G;
+    if (mtile && g == 0) return;   // segment 0 starts from S0 itself: no transfer needed
+    const int bh = seq * prm.H + h;
+    const int j0 = (mtile ? static_cast<int>(blockIdx.y) - ntv : static_cast<int>(blockIdx.y)) * kDVT;
+
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));
@@ -117,9 +141,6 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
     const int j = tid & 127;
     const int R = (tid >> 7) & 3;
     const int quarter = warp & 3;
-    const int bh = blockIdx.x;
-    const int seq = bh / prm.H, h = bh % prm.H;
-    const int j0 = blockIdx.y * kDVT;
     int tok0, T, cb0;
     if (prm.cu) {
         const int a = min(max(prm.cu[seq], 0), prm.total);
@@ -128,15 +149,21 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         T = e - a;
         cb0 = prm.s.chunk_base[seq];
     } else {
-        // chunks c0 .. c0 + nchunks - 1: token offsets relative to the first of them
-        tok0 = seq * prm.T + prm.c0 * kC;
-        T = prm.T - prm.c0 * kC;
-        cb0 = seq * prm.nchunks;
+        // chunks c0 + g L .. c0 + nchunks - 1: token offsets relative to the first of them
+        tok0 = seq * prm.T + (prm.c0 + g * prm.L) * kC;
+        T = prm.T - (prm.c0 + g * prm.L) * kC;
+        cb0 = seq * prm.nchunks + g * prm.L;
     }
     // Well-formed offsets never reach the slot bound; overlapping malformed ones
     // can, and their chunks past it are not run (the sequence is truncated).
     int n = min((T + kC - 1) / kC, max(prm.chunk_bound - cb0, 0));
-    if (!prm.cu) n = min(n, prm.nchunks);
+    if (!prm.cu) n = min(n, min(prm.nchunks - g * prm.L, prm.L));
+    // o rows: the caller's o (whole sequence, or segment 0), else fp32 scratch rows
+    const bool to_o = prm.G == 1 || (!mtile && g == 0);
+    const CUtensorMap* const om = to_o ? &tm_o : (mtile ? &tm_r : &tm_o32);
+    const bool obf16 = to_o && prm.out_bf16;
+    const int ow = mtile ? kDK : prm.dv;
+    const int orow0 = to_o ? tok0 : seq * prm.Tr + (g - 1) * prm.L * kC;
     auto slot = [&](int c) { return static_cast<int64_t>(cb0 + c) * prm.H + h; };
 
     if (tid == 0) {
@@ -166,6 +193,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
             // the parity of their count (bit i of iss_par); bit-packed to stay in registers
             uint32_t iss_any = 0, iss_par = 0;
             auto load_vw = [&](int c) {
+                if (mtile) return;   // U = 0: no v, w tiles
                 const uint32_t b = bar(kBarVW + (c & 1));
                 const uint32_t dst = base + kVW + static_cast<uint32_t>(c & 1) * 16384u;
                 const int row = tok0 + c * kC;
@@ -259,9 +287,9 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
             for (int c = 0; (c + 1) * kC <= T && c < n; ++c) {
                 if (!mbar_wait_ab(bar(kOFull), ph_full, abort_flag)) break;
                 ph_full ^= 1u;
-                const int row = tok0 + c * kC;
-                tma_store_4d(&tm_o, base + kO, j0, h, row, 0);
-                if (!prm.out_bf16) tma_store_4d(&tm_o, base + kO + 8192u, j0 + 32, h, row, 0);
+                const int row = orow0 + c * kC;
+                tma_store_4d(om, base + kO, j0, h, row, 0);
+                if (!obf16) tma_store_4d(om, base + kO + 8192u, j0 + 32, h, row, 0);
                 bulk_commit();
                 bulk_wait_read();           // the tile has been read: it may take the next chunk
                 mbar_arrive(bar(kOFree));
@@ -295,12 +323,19 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 *reinterpret_cast<float*>(sgen + st_base + jj * 128 + (xk4 ^ ((jj & 7) << 4))) = tf32r(S[jj]);
         };
         {
-            const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R
-                                     : nullptr;
+            // S0 for the whole sequence or segment 0, zero for later segments' value
+            // tiles, identity columns for transfer tiles
+            const float* s0 = prm.S0 && !mtile && g == 0
+                                  ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R
+                                  : nullptr;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
                 const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[jj] = x.x; S[jj + 1] = x.y; S[jj + 2] = x.z; S[jj + 3] = x.w;
+            }
+            if (mtile) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) S[jj] = j == j0 + 16 * R + jj ? 1.f : 0.f;
             }
             put_st();
         }
@@ -366,7 +401,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                             __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + off)) << 16);
                         const float ww = __uint_as_float(
                             static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tv + 8192 + off)) << 16);
-                        u[f] = 8 * q8 + e + f < tvalid ? vv * ww : 0.f;
+                        u[f] = !mtile && 8 * q8 + e + f < tvalid ? vv * ww : 0.f;
                     }
                     const __half2 h2 = __floats2half2_rn(u[0], u[1]);
                     const float2 hf = __half22float2(h2);
@@ -455,7 +490,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 put_cb(cbr);
                 arrive(kRdyA1);                                   // A1(0)
                 ld_cb(1, cbr);
-                if (!wait(kBarVW, ph_vw0)) failed = true;
+                if (!mtile && !wait(kBarVW, ph_vw0)) failed = true;
                 if (!failed) {
                     put_u(0);
                     arrive(kRdyU);                                // [T; A_qk T] U (0)
@@ -512,7 +547,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 if (tc + kC <= T) {
                     // whole chunk inside the sequence: O tile -> shared memory -> one TMA store
                     if (!wait(kOFree, ph_of)) { failed = true; break; }
-                    if (prm.out_bf16) {
+                    if (obf16) {
                         uint4 pk[2];
                         uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
@@ -532,8 +567,8 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                     }
                     arrive(kOFull);
                 } else if (tc + r < T) {   // the sequence's last, partial chunk: row by row
-                    const int64_t off = ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
-                    if (prm.out_bf16) {
+                    const int64_t off = ((static_cast<int64_t>(orow0) + tc + r) * prm.H + h) * ow + j0 + 16 * R;
+                    if (obf16) {
                         __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
                         uint4 pk[2];
                         uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
@@ -545,7 +580,8 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                         reinterpret_cast<uint4*>(op)[0] = pk[0];
                         reinterpret_cast<uint4*>(op)[1] = pk[1];
                     } else {
-                        float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+                        float* const ob = to_o ? static_cast<float*>(prm.o) : (mtile ? prm.r : prm.o32);
+                        float4* op = reinterpret_cast<float4*>(ob + off);
 #pragma unroll
                         for (int jj = 0; jj < 16; jj += 4)
                             op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
@@ -554,7 +590,7 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
                 if (c + 1 < n) {
                     // ---- next chunk: U^T operand (its product overwrites [E; O] after this) -----
                     const bool odd = (c + 1) & 1;
-                    if (!wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
+                    if (!mtile && !wait(odd ? kBarVWb : kBarVW, odd ? ph_vw1 : ph_vw0)) { failed = true; break; }
                     put_u(c + 1);
                     arrive(kRdyU);
                     // ---- next chunk: P on A1, then -Cb^T of chunk c + 2 into the freed buffer -----
@@ -586,8 +622,12 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         if (failed) {
             *abort_flag = 1;
             if (lane == 0) atomicExch(prm.err, kDevTimeout);
-        } else if (prm.ST) {
-            float* st = prm.ST + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R;
+        } else if (prm.G > 1 || prm.ST) {
+            // S_T, else the segment's end-state slot [blockIdx.x][d_k][width]
+            float* st = prm.G == 1 ? prm.ST + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R
+                                   : (mtile ? prm.seg_m : prm.seg_state) +
+                                         (static_cast<int64_t>(bh * prm.G + g) * kDK + j) * (mtile ? kDK : prm.dv) +
+                                         j0 + 16 * R;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4)
                 *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
@@ -637,14 +677,26 @@ bool make_row_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int
 }  // namespace
 
 int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
-                 int* err) {
+                 int* err, const SegArgs& seg) {
     const int64_t total = a.cu ? a.total : a.B * a.T;
     const int64_t slots = chunks * a.H;
     if (slots * 128 >= (1ll << 31) || chunks >= (1ll << 31)) return GDR2_ERR_SHAPE;
-    CUtensorMap mv, mw, mo;
+    const bool segmented = seg.G > 1;
+    if (segmented && (a.cu || c0 != 0 || seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L * kC >= a.T ||
+                      !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r))
+        return GDR2_ERR_ARG;
+    CUtensorMap mv, mw, mo, mo32, mr;
     if (!make_row_map(&mv, a.v, total, a.H, a.dv, false) || !make_row_map(&mw, a.w, total, a.H, a.dv, false) ||
         !make_row_map(&mo, a.o, total, a.H, a.dv, a.out_dtype != GDR2_BF16))
         return GDR2_ERR_CUDA;
+    if (segmented) {
+        if (!make_row_map(&mo32, seg.o32, a.B * seg.Tr, a.H, a.dv, true) ||
+            !make_row_map(&mr, seg.r, a.B * seg.Tr, a.H, kDK, true))
+            return GDR2_ERR_CUDA;
+    } else {
+        mo32 = mo;   // not read
+        mr = mo;
+    }
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -655,9 +707,13 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c
     StateParams prm{s, a.S0, a.o, a.ST, err, a.cu, static_cast<int>(a.T), static_cast<int>(a.H),
                     static_cast<int>(a.dv), static_cast<int>(total),
                     a.cu ? 0 : cpiece, a.cu ? 0 : c0, static_cast<int>(chunks),
-                    a.out_dtype == GDR2_BF16 ? 1 : 0};
-    const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
-    state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, prm);
+                    a.out_dtype == GDR2_BF16 ? 1 : 0,
+                    segmented ? seg.G : 1, segmented ? seg.L : cpiece, segmented ? static_cast<int>(seg.Tr) : 0,
+                    seg.seg_state, seg.seg_m, seg.o32, seg.r};
+    // value tiles, then (segmented) the d_k / 64 transfer tiles of each (sequence, segment, head)
+    const int ytiles = static_cast<int>(a.dv / kDVT) + (segmented ? kDK / kDVT : 0);
+    const dim3 grid(static_cast<unsigned>(a.B * (segmented ? seg.G : 1) * a.H), static_cast<unsigned>(ytiles));
+    state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, mo32, mr, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 

@@ -169,6 +169,39 @@ int gdr2_forward_noalloc(const void* q, const void* k, const void* v,
                          int in_dtype, int out_dtype, cudaStream_t stream);
 
 /*
+ * gdr2_forward_segmented -- gdr2_forward with an explicit number of sequence
+ * segments for the chunk-parallel scan.
+ *
+ * The state update is affine in the state, so a run of chunks (a segment) maps
+ * its start state S to M S + N and adds S^T r_t to each of its outputs o_t
+ * (the page's "efficient implementation" section: chunkwise algorithm; the
+ * segment form follows from the same recurrence).  With G segments per
+ * sequence, the state pass runs every segment at once -- segment 0 from S0, the
+ * others from a zero state and, for M and r, from the identity -- then chains
+ * the segments' maps (G - 1 products of 128 x 128 by 128 x dv per head) and
+ * adds each later segment's start-state term to its o rows.  It shortens the
+ * chunk-to-chunk chain G-fold at the cost of (1 + 2/(dv/64)) times the state
+ * work and an fp32 scratch of (T - L*64) x H x (dk + dv) x 4 bytes per sequence
+ * (L = chunks per segment).  gdr2_forward chooses G itself: the most segments,
+ * each of at least 16 chunks, whose work still fits one wave of the GPU's SMs
+ * (with 148 SMs and dk = dv = 128: 2 for B*H = 16 heads at T = 65536, and 1
+ * whenever B*H >= 25).
+ *
+ *   segments : 0 = the library's choice (as gdr2_forward); n >= 1 = n segments
+ *              (capped at the number of 64-token chunks and rounded so that
+ *              none is empty; 1 = the plain sequential pass).
+ *
+ * Arguments, layouts, results and error codes as gdr2_forward, plus
+ * GDR2_ERR_ARG for segments < 0 and GDR2_ERR_UNSUPPORTED for segments > 1 on
+ * inputs that the chunked path does not take (fp32 inputs, d_k != 128).
+ */
+int gdr2_forward_segmented(const void* q, const void* k, const void* v,
+                           const void* b, const void* w, const void* log_decay,
+                           const float* S0, void* o, float* S_T,
+                           int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                           int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream);
+
+/*
  * gdr2_decode_step -- one autoregressive step for every (batch, head), the
  * state updated in place (same equation, one token):
  *

@@ -38,10 +38,11 @@ def bf16_output_bar(ref, base_tol) -> float:
     return base_tol + float(np.abs(ref).max()) * 2.0 ** -9 / max(rms, 1e-30)
 
 
-def run_gpu(x, S0=None, device="cuda", out_dtype=torch.float32):
+def run_gpu(x, S0=None, device="cuda", out_dtype=torch.float32, segments=None):
     d = x.to(device)
     S0d = None if S0 is None else S0.to(device)
-    o, ST = gdr2.forward(*d.tensors(), S0d if S0 is not None else d.S0, out_dtype=out_dtype)
+    o, ST = gdr2.forward(*d.tensors(), S0d if S0 is not None else d.S0, out_dtype=out_dtype,
+                         segments=segments)
     torch.cuda.synchronize()
     assert gdr2.gdr2_device_status() == 0
     return o.float().cpu().numpy(), ST.cpu().numpy()
@@ -51,12 +52,13 @@ def run_oracle(x, S0=None):
     return oracle.forward(*x.tensors(), S0 if S0 is not None else x.S0)
 
 
-def compare(x, label="", tol=None, out_dtype=torch.float32):
+def compare(x, label="", tol=None, out_dtype=torch.float32, segments=None, ref=None):
     """Run both sides on the prefill inputs x; return (err_o, err_S).  With a
-    bf16 o the bar on o grows by exactly the output rounding term."""
+    bf16 o the bar on o grows by exactly the output rounding term.  `segments`
+    is passed to gdr2.forward; `ref` = (o, S_T) of the oracle if already known."""
     tol = tol if tol is not None else tol_for(x.q.dtype)
-    go, gS = run_gpu(x, out_dtype=out_dtype)
-    ro, rS = run_oracle(x)
+    go, gS = run_gpu(x, out_dtype=out_dtype, segments=segments)
+    ro, rS = ref if ref is not None else run_oracle(x)
     eo, eS = err_over_rms(go, ro), err_over_rms(gS, rS)
     tol_o = tol if out_dtype == torch.float32 else bf16_output_bar(ro, tol)
     assert eo <= tol_o and eS <= tol, (

@@ -127,3 +127,16 @@ def test_varlen_rejects_bad_args():
     assert L.gdr2_forward_varlen(*varlen_args(dk=48)) == SHAPE
     assert L.gdr2_forward_varlen(*varlen_args(N=-1)) == ARG
     assert L.gdr2_forward_varlen(*varlen_args(total=1 << 31)) == SHAPE
+
+
+def test_segmented_rejects_bad_args():
+    L = _lib.lib()
+
+    def seg(n, **kw):   # gdr2_forward's arguments with `segments` before the stream
+        return L.gdr2_forward_segmented(*(fwd_args(**kw)[:-1] + [n, None]))
+
+    assert seg(-1) == ARG
+    assert seg(2, dk=16) == SHAPE
+    assert seg(3, B=-1) == ARG
+    assert seg(0, o=None) == ARG
+    assert seg(2, o=ctypes.c_void_p(BASE)) == ALIAS

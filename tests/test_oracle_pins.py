@@ -81,3 +81,31 @@ def test_bad_shapes_raise():
         oracle.forward(q, k[:, :2], v, b, w, g, S0)
     with pytest.raises(ValueError):
         oracle.forward(q, k, v, b, w, g, S0[..., :3])
+
+
+def test_segment_transfer_decomposition():
+    """The algebra behind the chunk-parallel scan of the GPU prefill: for a
+    segment of tokens, the run from S_start equals the run from zero plus the
+    start state pushed through the segment's transfer, where the transfer M and
+    the readout responses r_t come from the run that starts at the identity with
+    no writes (w = 0):  S_end = M S_start + N  and  o_t = o_t^0 + S_start^T r_t.
+    Chaining two segments this way must reproduce the unsplit run."""
+    rng = np.random.default_rng(21)
+    B, T, H, dk, dv, T1 = 2, 23, 2, 6, 5, 9
+    q, k, v, b, w, g, S0 = pins.rand_problem(rng, B=B, T=T, H=H, dk=dk, dv=dv, b_hi=2.0)
+    g = 0.05 * g   # slow decay: the start state stays visible through the segment
+    o_ref, S_ref = _c(q, k, v, b, w, g, S0)
+    eye = np.broadcast_to(np.eye(dk), (B, H, dk, dk)).copy()
+    zeros_k = np.zeros((B, T - T1, H, dk))
+    sl = slice(T1, None)
+    # segment 0 from S0, segment 1 from zero and from the identity
+    o0, S1 = _c(q[:, :T1], k[:, :T1], v[:, :T1], b[:, :T1], w[:, :T1], g[:, :T1], S0)
+    oz, N = _c(q[:, sl], k[:, sl], v[:, sl], b[:, sl], w[:, sl], g[:, sl], None)
+    r, M = _c(q[:, sl], k[:, sl], zeros_k, b[:, sl], zeros_k, g[:, sl], eye)
+    S_end = np.einsum("bhij,bhjd->bhid", M, S1) + N
+    o1 = oz + np.einsum("bthj,bhjd->bthd", r, S1)
+    assert pins.rel_err(S_end, S_ref) < 1e-12
+    assert pins.rel_err(np.concatenate([o0, o1], axis=1), o_ref) < 1e-12
+    # a plausible slip -- the transposed transfer -- breaks it
+    S_bad = np.einsum("bhji,bhjd->bhid", M, S1) + N
+    assert pins.rel_err(S_bad, S_ref) > 1e-3
