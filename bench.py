@@ -17,6 +17,8 @@ line carries:
 * e2e: the same prefill through the public API from pinned host buffers, the
   host->device copies of the step's inputs and the device->host copies of o
   and S_T inside the timed region;
+* long_context: the long-context workload (B=1, H=16, T=65536) through the
+  chunk-parallel scan over sequence segments, beside the sequential state pass;
 * cpu_baseline: the fp64 CPU oracle (as it stands) on a bounded sample of the
   same workload on the host cores;
 * clocks: nvidia-smi samples taken during the timed region.
@@ -292,6 +294,45 @@ def bench_decode(gdr2, steps=1024, pool=16, seed=5):
             "launches": steps, "input_pool": pool}
 
 
+def bench_long(gdr2, hbm_gbs, steps=10, warmup=3):
+    """The long-context workload (B=1, H=16, T=65536): gdr2_forward with the
+    library's segment count for the chunk-parallel scan, and the sequential state
+    pass (segments=1) for comparison; CUDA events around `steps` calls each."""
+    from gated_delta_rule_166_b300.inputs import WORKLOADS, make_workload
+
+    name = "long_T65536"
+    cfg = WORKLOADS[name]
+    B, T, H, dk, dv = cfg["B"], cfg["T"], cfg["H"], cfg["dk"], cfg["dv"]
+    x = make_workload(name).to("cuda")
+    o = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def timed(segments):
+        for _ in range(warmup):
+            gdr2.forward(*x.tensors(), x.S0, o=o, S_T=ST, segments=segments)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            gdr2.forward(*x.tensors(), x.S0, o=o, S_T=ST, segments=segments)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms_auto, ms_seq = timed(None), timed(1)
+    if gdr2.gdr2_device_status() != 0:
+        raise RuntimeError("device-side failure during the long-context prefill")
+    nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=x.S0 is not None, st=True)
+    achieved = nbytes / (ms_auto / 1e3) / 1e9
+    return {"workload": f"{name}: B={B} H={H} T={T} d_k=d_v={dk}, bf16 inputs, fp32 S0, state and o",
+            "ms_per_call": ms_auto, "tokens_per_s": B * T / (ms_auto / 1e3),
+            "ms_per_call_sequential": ms_seq, "speedup_vs_sequential": ms_seq / ms_auto,
+            "segments": "library choice (gdr2_forward)", "steps": steps, "warmup": warmup,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes}}
+
+
 def bench_e2e(gdr2, x_host, steps, warmup):
     """Pinned host inputs -> device -> gdr2_forward -> o and S_T back to host."""
     B, T, H, dk = x_host.q.shape
@@ -374,8 +415,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
-                    help="profiling aid: run just one kernel's leg (no JSON line for decode-only)")
+    ap.add_argument("--no-long", action="store_true", help="skip the long-context prefill leg")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long"], default="all",
+                    help="profiling aid: run just one leg (decode and long print only that leg)")
     ap.add_argument("--decode-steps", type=int, default=1024)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -441,6 +483,11 @@ def main():
         if rank == 0:
             print(json.dumps({"decode": dec}))
         return
+    if args.only == "long":
+        lc = bench_long(gdr2, hbm_gbs, steps=min(args.steps, 10), warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"long_context": lc}))
+        return
 
     with ClockSampler(local) as clk:
         ms, per_launch, launches = bench_prefill(gdr2, x, args.steps, args.warmup, world)
@@ -470,7 +517,7 @@ def main():
            "gpu_launches": launches}
 
     if args.only == "prefill":
-        args.no_e2e = args.no_decode = args.no_cpu_baseline = True
+        args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = True
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
@@ -484,6 +531,8 @@ def main():
                            "traffic": traffic_record("decode_B256_H16_d128")}
         out["decode"] = dec
         out["gpu_launches"] = launches  # timed prefill region only; decode launches in out["decode"]
+    if not args.no_long:
+        out["long_context"] = bench_long(gdr2, hbm_gbs)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x_host)
     if rank == 0:

@@ -114,13 +114,16 @@ __device__ __forceinline__ uint32_t vw_off(int t, int n) {
            (static_cast<uint32_t>(n & 7) << 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
-             const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_o32,
-             const __grid_constant__ CUtensorMap tm_r, const StateParams prm) {
-    // segment, tile kind and output routing (uniform over the CTA)
+// One CTA of the state pass; kTransfer: a transfer tile (identity start, U = 0).
+// The two kinds are separate instantiations so that value tiles carry no test of
+// the tile kind on their chain.
+template <bool kTransfer>
+__device__ __forceinline__ void state_cta(const CUtensorMap& tm_v, const CUtensorMap& tm_w, const CUtensorMap& tm_o,
+                                          const CUtensorMap& tm_o32, const CUtensorMap& tm_r,
+                                          const StateParams& prm) {
+    constexpr bool mtile = kTransfer;
+    // segment and output routing (uniform over the CTA)
     const int ntv = prm.dv / kDVT;
-    const bool mtile = static_cast<int>(blockIdx.y) >= ntv;
     const int h = static_cast<int>(blockIdx.x) % prm.H;
     const int sg = static_cast<int>(blockIdx.x) / prm.H;
     const int seq = sg / prm.G, g = sg % prm.G;
@@ -639,6 +642,16 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
         tc_fence_after();
         tmem_dealloc<kTmCols>(tmem);
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+             const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_o32,
+             const __grid_constant__ CUtensorMap tm_r, const StateParams prm) {
+    if (static_cast<int>(blockIdx.y) >= prm.dv / kDVT)
+        state_cta<true>(tm_v, tm_w, tm_o, tm_o32, tm_r, prm);
+    else
+        state_cta<false>(tm_v, tm_w, tm_o, tm_o32, tm_r, prm);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
