@@ -330,7 +330,9 @@ def bench_long(gdr2, hbm_gbs, steps=10, warmup=3):
             "ms_per_call_sequential": ms_seq, "speedup_vs_sequential": ms_seq / ms_auto,
             "segments": "library choice (gdr2_forward)", "steps": steps, "warmup": warmup,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes}}
+                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes,
+                         "traffic": traffic_record("prefill_" + name),
+                         "kernel": "gdr2 prefill: prep_kernel + state_kernel + scan_kernel + correct_kernel"}}
 
 
 def bench_e2e(gdr2, x_host, steps, warmup):
