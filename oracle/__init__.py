@@ -139,3 +139,46 @@ def forward_np(q, k, v, b, w, g, S0=None):
         S = A @ S + kt[..., :, None] * (w[:, t] * v[:, t])[..., None, :]
         o[:, t] = np.einsum("bhij,bhi->bhj", S, qt)
     return o, S
+
+
+def backward(q, k, v, b, w, g, S0, do, dST=None):
+    """Gradients of the recurrence, fp64, by reverse-mode automatic
+    differentiation of the plain sequential loop (PyTorch CPU autograd).
+
+    The scalar being differentiated is ``L = sum_t <o_t, do_t> + <S_T, dST>``:
+    ``do`` [B, T, H, dv] is the gradient arriving at o, ``dST`` [B, H, dk, dv]
+    (or None = zero) the one arriving at the final state.  The loop is the
+    update equation of the "Gated DeltaNet-2: Decoupling Erase and Write in
+    Linear Attention" page (section "Gated Delta Rule-2 update equation"),
+    written out per token,
+        X = diag(exp g_t) S,  S = X - k_t ((b_t * k_t)^T X) + k_t (w_t * v_t)^T,
+        o_t = S^T q_t,
+    with S0 = None taken as a zero initial state (its gradient is still
+    returned).  Returns float64 arrays (dq, dk, dv, db, dw, dg, dS0), where dg
+    is the gradient with respect to log_decay."""
+    import torch
+
+    q, k, v, b, w, g, S0, do, dST = (_f64(t) for t in (q, k, v, b, w, g, S0, do, dST))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if S0 is None:
+        S0 = np.zeros((B, H, dk, dv))
+    leaves = [torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v, b, w, g, S0)]
+    tq, tk, tv, tb, tw, tg, tS0 = leaves
+    S = tS0
+    outs = []
+    for t in range(T):
+        kt = tk[:, t]                                              # [B, H, dk]
+        X = torch.exp(tg[:, t])[..., :, None] * S                  # D_t S_{t-1}
+        erase_read = torch.einsum("bhi,bhij->bhj", tb[:, t] * kt, X)
+        write = tw[:, t] * tv[:, t]
+        S = X + kt[..., :, None] * (write - erase_read)[..., None, :]
+        outs.append(torch.einsum("bhij,bhi->bhj", S, tq[:, t]))
+    loss = torch.zeros((), dtype=torch.float64)
+    if T > 0:
+        o = torch.stack(outs, dim=1)
+        loss = loss + (o * torch.from_numpy(do)).sum()
+    if dST is not None:
+        loss = loss + (S * torch.from_numpy(dST)).sum()
+    grads = torch.autograd.grad(loss, leaves, allow_unused=True)
+    return tuple(np.zeros(leaf.shape) if gr is None else gr.numpy() for gr, leaf in zip(grads, leaves))
