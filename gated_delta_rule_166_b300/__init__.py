@@ -9,6 +9,9 @@ synthetic input generators used by the tests and the bench.
 from ._lib import (  # noqa: F401
     GDR2Error,
     GDR2LibraryError,
+    GatedDeltaRule2,
+    gdr2_apply,
+    gdr2_backward,
     gdr2_decode_step,
     gdr2_device_status,
     gdr2_forward,
@@ -21,3 +24,4 @@ forward = gdr2_forward
 forward_varlen = gdr2_forward_varlen
 forward_noalloc = gdr2_forward_noalloc
 decode_step = gdr2_decode_step
+backward = gdr2_backward

@@ -50,6 +50,8 @@ def lib():
         L.gdr2_forward_segmented.restype = ci
         L.gdr2_forward_varlen.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward_varlen.restype = ci
+        L.gdr2_backward.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
+        L.gdr2_backward.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
         L.gdr2_decode_step.restype = ci
         L.gdr2_device_status.argtypes = [vp]
@@ -197,6 +199,70 @@ def gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, o=None
     if st != 0:
         raise GDR2Error(st, "gdr2_forward_varlen")
     return o, S_T
+
+
+def gdr2_backward(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bool = True, stream=None):
+    """Gradients of gdr2_forward.  Forward inputs as for gdr2_forward (q, k, b,
+    log_decay: [B, T, H, dk]; v, w: [B, T, H, dv]; all fp32 or all bf16; S0 fp32
+    [B, H, dk, dv] or None); d_o: [B, T, H, dv] gradient at o; d_S_T: [B, H, dk,
+    dv] gradient at S_T or None.  Returns fp32 tensors (dq, dk, dv, db, dw,
+    dlog_decay, dS0), dS0 None when ``want_dS0`` is False."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q and v must be [B, T, H, d]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_backward runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (B, T, H, d), dtype, dev)
+    _check_tokens("d_o", d_o, (B, T, H, dv), torch.float32, dev)
+    for name, t in (("S0", S0), ("d_S_T", d_S_T)):
+        if t is not None:
+            _check_tokens(name, t, (B, H, dk, dv), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    gq, gk, gb, gg = (torch.empty((B, T, H, dk), **f32) for _ in range(4))
+    gv, gw = (torch.empty((B, T, H, dv), **f32) for _ in range(2))
+    gS0 = torch.empty((B, H, dk, dv), **f32) if want_dS0 else None
+    with torch.cuda.device(dev):
+        st = lib().gdr2_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
+                                 _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
+                                 _ptr(gg), _ptr(gS0), B, T, H, dk, dv, _DTYPES[dtype],
+                                 ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_backward")
+    return gq, gk, gv, gb, gw, gg, gS0
+
+
+class GatedDeltaRule2(torch.autograd.Function):
+    """(o, S_T) = gdr2_forward(q, k, v, b, w, log_decay, S0) as a differentiable
+    operation: the forward pass is gdr2_forward (fp32 o), the backward pass
+    gdr2_backward.  Gradients are fp32 and cast to each input's dtype."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, b, w, log_decay, S0=None):
+        o, S_T = gdr2_forward(q, k, v, b, w, log_decay, S0)
+        ctx.save_for_backward(q, k, v, b, w, log_decay, S0)
+        ctx.has_s0 = S0 is not None
+        return o, S_T
+
+    @staticmethod
+    def backward(ctx, d_o, d_S_T):
+        q, k, v, b, w, log_decay, S0 = ctx.saved_tensors
+        d_o = torch.zeros((*v.shape[:3], v.shape[-1]), dtype=torch.float32, device=q.device) if d_o is None \
+            else d_o.float().contiguous()
+        d_S_T = None if d_S_T is None else d_S_T.float().contiguous()
+        g = gdr2_backward(q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
+        cast = [g[i].to(t.dtype) for i, t in enumerate((q, k, v, b, w, log_decay))]
+        return (*cast, g[6] if ctx.has_s0 else None)
+
+
+def gdr2_apply(q, k, v, b, w, log_decay, S0=None):
+    """Differentiable prefill: ``(o, S_T)`` with gradients through gdr2_backward."""
+    return GatedDeltaRule2.apply(q, k, v, b, w, log_decay, S0)
 
 
 def gdr2_decode_step(q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.float32,

@@ -294,6 +294,60 @@ extern "C" int gdr2_forward_segmented(const void* q, const void* k, const void* 
                         out_dtype, stream, /*noalloc=*/false, segments);
 }
 
+extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
+                             const void* b, const void* w, const void* log_decay,
+                             const float* S0, const float* d_o, const float* d_S_T,
+                             float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                             float* d_log_decay, float* d_S0,
+                             int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                             int in_dtype, cudaStream_t stream) {
+    if (B < 0 || T < 0 || H < 0) return GDR2_ERR_ARG;
+    if (!dtype_ok(in_dtype)) return GDR2_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
+    const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
+    int64_t rows = 0, bh = 0, nk = 0, nv = 0, ns = 0;
+    if (!mul_ok(B, T, &rows) || !mul_ok(rows, H, &rows) || !mul_ok(B, H, &bh) || !mul_ok(rows, dk, &nk) ||
+        !mul_ok(rows, dv, &nv) || !mul_ok(bh, dk * dv, &ns) || nk > INT64_MAX / 8 || ns > INT64_MAX / 8 ||
+        bh >= 0x7fffffffLL)
+        return GDR2_ERR_SHAPE;
+    const bool has_tokens = rows > 0;
+    if (has_tokens && (!q || !k || !v || !b || !w || !log_decay || !d_o || !d_q || !d_k || !d_v || !d_b ||
+                       !d_w || !d_log_decay))
+        return GDR2_ERR_ARG;
+    const void* all[] = {q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0};
+    for (const void* ptr : all)
+        if (ptr && !aligned16(ptr)) return GDR2_ERR_ALIGN;
+    // outputs must not overlap any input or each other
+    const size_t bk = (size_t)nk * esz, bv = (size_t)nv * esz, bs = (size_t)ns * 4;
+    const size_t fk = (size_t)nk * 4, fv = (size_t)nv * 4;
+    const void* ins[] = {q, k, b, log_decay, v, w, S0, d_o, d_S_T};
+    const size_t in_bytes[] = {bk, bk, bk, bk, bv, bv, bs, fv, bs};
+    const void* outs[] = {d_q, d_k, d_b, d_log_decay, d_v, d_w, d_S0};
+    const size_t out_bytes[] = {fk, fk, fk, fk, fv, fv, bs};
+    for (int i = 0; i < 7; ++i) {
+        for (int j = 0; j < 9; ++j)
+            if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return GDR2_ERR_ALIAS;
+        for (int j = i + 1; j < 7; ++j)
+            if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return GDR2_ERR_ALIAS;
+    }
+    int st = device_setup(nullptr);
+    if (st != GDR2_OK) return st;
+    if (bh == 0) return GDR2_OK;
+    if (!has_tokens) {   // no tokens: dS0 = dS_T (or zero)
+        if (!d_S0) return GDR2_OK;
+        const cudaError_t e = d_S_T ? cudaMemcpyAsync(d_S0, d_S_T, bs, cudaMemcpyDeviceToDevice, stream)
+                                    : cudaMemsetAsync(d_S0, 0, bs, stream);
+        return e == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+    }
+    BackwardArgs a{q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                   B, T, H, dk, dv, in_dtype};
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, backward_workspace_bytes(B, T, H, dk, dv), stream) != cudaSuccess) return GDR2_ERR_CUDA;
+    int rc = launch_backward(a, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
+    return rc;
+}
+
 extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,
                                 const void* b, const void* w, const void* log_decay,
                                 float* S, void* o,

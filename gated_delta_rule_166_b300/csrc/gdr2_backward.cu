@@ -1,0 +1,338 @@
+// Gradients of the Gated Delta Rule-2 recurrence (fp32, token-sequential).
+//
+// Method: reverse-mode differentiation of the update of the "Gated DeltaNet-2:
+// Decoupling Erase and Write in Linear Attention" page (section "Gated Delta
+// Rule-2 update equation"), written per token with X_t = D_t S_{t-1},
+// c_t = b_t * k_t, delta_t = w_t * v_t - X_t^T c_t:
+//     S_t = X_t + k_t delta_t^T,      o_t = S_t^T q_t.
+// With G the gradient arriving at S_t (from later tokens and dS_T) plus
+// q_t do_t^T from the readout, one step back is
+//     dq_t = S_t do_t,               ddelta = G^T k_t,
+//     dv_t = ddelta * w_t,           dw_t = ddelta * v_t,
+//     dc = -X_t ddelta,              db_t = dc * k_t,
+//     dk_t = G delta_t + dc * b_t,   dX = G - c_t ddelta^T,
+//     dlog_decay_t = rowsum(dX * X_t),   dS_{t-1} = D_t dX.
+// The d_v columns of S evolve independently, so one CTA owns a 32-column tile
+// of one (sequence, head): the tile of S, later of G, stays in registers (lane
+// l of warp w: key rows l, l+32, ...; columns 4w .. 4w+3).  Column sums are
+// warp shuffles; the row vectors (dq, dk, dc, dlog_decay) are summed over the
+// CTA's warps in shared memory and over the tiles by a second kernel.
+//
+// States in reverse order come from recomputation: a forward sweep stores the
+// tile at the start of every 8-token block (checkpoints in the workspace); the
+// backward sweep reloads a block's checkpoint, recomputes its 8 states with the
+// same arithmetic (so the same fp32 values), keeps X_t and delta_t in shared
+// memory and walks the block backwards.
+#include <mutex>
+
+#include "gdr2.h"
+#include "gdr2_internal.cuh"
+
+namespace gdr2 {
+namespace {
+
+constexpr int kNW = 8;            // warps per CTA
+constexpr int kCPW = 4;           // value columns per warp
+constexpr int kDVT = kNW * kCPW;  // value columns per CTA
+constexpr int kCK = 8;            // tokens per checkpoint block
+constexpr int kVec = 4;           // row vectors reduced over tiles: dq, G delta, dc, dlog_decay
+
+struct BwdParams {
+    const void *q, *k, *v, *b, *w, *g;
+    const float *S0, *dO, *dST;
+    float *dv, *dw, *dS0;
+    float* ckpt;   // [B*H][tiles][blocks][DK * 32]
+    float* part;   // [B*T][H][tiles][kVec][DK]
+    int64_t T;
+    int H, dv_dim, tiles;
+};
+
+template <int DK> constexpr size_t bwd_smem() {
+    return sizeof(float) * (static_cast<size_t>(kCK) * DK * kDVT     // X_t stash
+                            + 4 * kCK * DK                           // q, k, c, alpha
+                            + 5 * kCK * kDVT                         // u, v, w, do, delta
+                            + 2 * kNW * kVec * DK);                  // row-vector partials (two buffers)
+}
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kNW * 32, 1) bwd_kernel(const BwdParams p) {
+    constexpr int RPL = DK / 32;
+    extern __shared__ __align__(16) float sm[];
+    float* xs = sm;                                   // [kCK][kNW][RPL][kCPW][32]
+    float* sq = xs + kCK * DK * kDVT;                 // [kCK][DK]
+    float* sk = sq + kCK * DK;
+    float* sc = sk + kCK * DK;
+    float* sa = sc + kCK * DK;
+    float* su = sa + kCK * DK;                        // [kCK][kDVT]
+    float* sv = su + kCK * kDVT;
+    float* sw = sv + kCK * kDVT;
+    float* sdo = sw + kCK * kDVT;
+    float* sdl = sdo + kCK * kDVT;                    // delta_t
+    float* red = sdl + kCK * kDVT;                    // [2][kNW][kVec][DK]
+
+    const Tin* q = static_cast<const Tin*>(p.q);
+    const Tin* k = static_cast<const Tin*>(p.k);
+    const Tin* v = static_cast<const Tin*>(p.v);
+    const Tin* b = static_cast<const Tin*>(p.b);
+    const Tin* w = static_cast<const Tin*>(p.w);
+    const Tin* g = static_cast<const Tin*>(p.g);
+    const int64_t bh = blockIdx.x;
+    const int64_t seq = bh / p.H, h = bh % p.H;
+    const int tile = blockIdx.y, j0 = tile * kDVT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cw = warp * kCPW;                       // first column of this warp in the tile
+    const int64_t T = p.T, tok0 = seq * T;
+    const int64_t nblk = (T + kCK - 1) / kCK;
+    float* ck = p.ckpt + (bh * p.tiles + tile) * nblk * (DK * kDVT);
+
+    // one block's token inputs into shared memory
+    auto load_block = [&](int64_t t0, int n) {
+        for (int e = tid; e < kCK * DK; e += kNW * 32) {
+            const int tt = e / DK, i = e % DK;
+            float qv = 0.f, kv = 0.f, cv = 0.f, av = 1.f;
+            if (tt < n) {
+                const int64_t off = ((tok0 + t0 + tt) * p.H + h) * DK + i;
+                kv = to_f32(k[off]);
+                qv = to_f32(q[off]);
+                cv = to_f32(b[off]) * kv;
+                av = expf(to_f32(g[off]));
+            }
+            sq[e] = qv; sk[e] = kv; sc[e] = cv; sa[e] = av;
+        }
+        for (int e = tid; e < kCK * kDVT; e += kNW * 32) {
+            const int tt = e / kDVT, j = e % kDVT;
+            float vv = 0.f, wv = 0.f, dov = 0.f;
+            if (tt < n) {
+                const int64_t off = ((tok0 + t0 + tt) * p.H + h) * p.dv_dim + j0 + j;
+                vv = to_f32(v[off]);
+                wv = to_f32(w[off]);
+                dov = p.dO[off];
+            }
+            sv[e] = vv; sw[e] = wv; su[e] = wv * vv; sdo[e] = dov;
+        }
+    };
+    // one forward step of token tt of the staged block: X = alpha * S, delta = u - X^T c,
+    // S = X + k delta^T; X (optional) and delta are kept for the backward walk
+    auto fwd_step = [&](float (&S)[RPL][kCPW], int tt, bool keep) {
+#pragma unroll
+        for (int c = 0; c < kCPW; ++c) {
+            float x = 0.f;
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) {
+                const int i = lane + 32 * r;
+                const float X = sa[tt * DK + i] * S[r][c];
+                S[r][c] = X;
+                x = fmaf(sc[tt * DK + i], X, x);
+                if (keep) xs[(((tt * kNW + warp) * RPL + r) * kCPW + c) * 32 + lane] = X;
+            }
+#pragma unroll
+            for (int s = 16; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
+            const float delta = su[tt * kDVT + cw + c] - x;
+            if (keep && lane == c) sdl[tt * kDVT + cw + c] = delta;
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) S[r][c] = fmaf(sk[tt * DK + lane + 32 * r], delta, S[r][c]);
+        }
+    };
+    auto ck_ptr = [&](int64_t blk, int r, int c) {
+        return ck + blk * (DK * kDVT) + ((warp * RPL + r) * kCPW + c) * 32 + lane;
+    };
+
+    // ---- forward sweep: the tile at the start of every block ------------------------------
+    float S[RPL][kCPW];
+#pragma unroll
+    for (int r = 0; r < RPL; ++r)
+#pragma unroll
+        for (int c = 0; c < kCPW; ++c)
+            S[r][c] = p.S0 ? p.S0[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] : 0.f;
+    for (int64_t blk = 0; blk < nblk; ++blk) {
+#pragma unroll
+        for (int r = 0; r < RPL; ++r)
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) *ck_ptr(blk, r, c) = S[r][c];
+        if (blk + 1 == nblk) break;   // the last block is recomputed from its checkpoint
+        const int64_t t0 = blk * kCK;
+        __syncthreads();
+        load_block(t0, kCK);
+        __syncthreads();
+        for (int tt = 0; tt < kCK; ++tt) fwd_step(S, tt, false);
+    }
+
+    // ---- backward sweep ---------------------------------------------------------------------
+    float G[RPL][kCPW];
+#pragma unroll
+    for (int r = 0; r < RPL; ++r)
+#pragma unroll
+        for (int c = 0; c < kCPW; ++c)
+            G[r][c] = p.dST ? p.dST[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] : 0.f;
+    int buf = 0;
+    for (int64_t blk = nblk - 1; blk >= 0; --blk) {
+        const int64_t t0 = blk * kCK;
+        const int n = static_cast<int>(T - t0 < kCK ? T - t0 : kCK);
+        __syncthreads();
+        load_block(t0, n);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < RPL; ++r)
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) S[r][c] = *ck_ptr(blk, r, c);
+        for (int tt = 0; tt < n; ++tt) fwd_step(S, tt, true);
+        __syncwarp();
+        for (int tt = n - 1; tt >= 0; --tt) {
+            const int64_t row = tok0 + t0 + tt;
+            float X[RPL][kCPW], dl[kCPW], dov[kCPW];
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) {
+                dl[c] = sdl[tt * kDVT + cw + c];
+                dov[c] = sdo[tt * kDVT + cw + c];
+            }
+            float pq[RPL], pk[RPL], pc[RPL], pg[RPL];
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) {
+                const int i = lane + 32 * r;
+                const float qi = sq[tt * DK + i], ki = sk[tt * DK + i];
+                pq[r] = 0.f;
+                pk[r] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kCPW; ++c) {
+                    X[r][c] = xs[(((tt * kNW + warp) * RPL + r) * kCPW + c) * 32 + lane];
+                    const float St = fmaf(ki, dl[c], X[r][c]);          // S_t
+                    G[r][c] = fmaf(qi, dov[c], G[r][c]);                // + q_t do_t^T
+                    pq[r] = fmaf(St, dov[c], pq[r]);
+                    pk[r] = fmaf(G[r][c], dl[c], pk[r]);
+                }
+            }
+            float dd[kCPW];   // ddelta = G^T k
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) {
+                float a = 0.f;
+#pragma unroll
+                for (int r = 0; r < RPL; ++r) a = fmaf(G[r][c], sk[tt * DK + lane + 32 * r], a);
+#pragma unroll
+                for (int s = 16; s > 0; s >>= 1) a += __shfl_xor_sync(0xffffffffu, a, s);
+                dd[c] = a;
+            }
+            if (lane < kCPW) {
+                const int c = lane;
+                const int64_t off = (row * p.H + h) * p.dv_dim + j0 + cw + c;
+                p.dv[off] = dd[c] * sw[tt * kDVT + cw + c];
+                p.dw[off] = dd[c] * sv[tt * kDVT + cw + c];
+            }
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) {
+                const int i = lane + 32 * r;
+                const float ci = sc[tt * DK + i], ai = sa[tt * DK + i];
+                pc[r] = 0.f;
+                pg[r] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kCPW; ++c) {
+                    pc[r] = fmaf(-X[r][c], dd[c], pc[r]);
+                    const float dX = fmaf(-ci, dd[c], G[r][c]);
+                    pg[r] = fmaf(dX, X[r][c], pg[r]);
+                    G[r][c] = ai * dX;                                   // dS_{t-1}
+                }
+            }
+            // row vectors: this warp's column partials -> shared memory -> sum over warps
+            float* rb = red + buf * (kNW * kVec * DK);
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) {
+                const int i = lane + 32 * r;
+                rb[(warp * kVec + 0) * DK + i] = pq[r];
+                rb[(warp * kVec + 1) * DK + i] = pk[r];
+                rb[(warp * kVec + 2) * DK + i] = pc[r];
+                rb[(warp * kVec + 3) * DK + i] = pg[r];
+            }
+            __syncthreads();
+            float* dst = p.part + ((row * p.H + h) * p.tiles + tile) * (kVec * DK);
+            for (int e = tid; e < kVec * DK; e += kNW * 32) {
+                float s = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kNW; ++ww) s += rb[ww * kVec * DK + e];
+                dst[e] = s;
+            }
+            buf ^= 1;   // the other buffer takes the next token; this one is reread only after
+                        // the next token's barrier
+        }
+    }
+    if (p.dS0) {
+#pragma unroll
+        for (int r = 0; r < RPL; ++r)
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) p.dS0[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] = G[r][c];
+    }
+}
+
+// dq, dk, db, dlog_decay of one (token row, head) per DK threads: the tiles' row
+// vectors summed, then db = dc * k and dk = G delta + dc * b.
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* __restrict__ part, const Tin* __restrict__ k,
+                                                         const Tin* __restrict__ b, float* __restrict__ dq,
+                                                         float* __restrict__ dk, float* __restrict__ db,
+                                                         float* __restrict__ dg, int64_t items, int tiles) {
+    constexpr int kPer = 256 / DK;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kPer + threadIdx.x / DK;   // row * H + head
+    const int j = threadIdx.x % DK;
+    if (item >= items) return;
+    const float* src = part + item * tiles * (kVec * DK) + j;
+    float s[kVec] = {0.f, 0.f, 0.f, 0.f};
+    for (int t = 0; t < tiles; ++t)
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) s[e] += src[(t * kVec + e) * DK];
+    const int64_t off = item * DK + j;
+    const float kv = to_f32(k[off]), bv = to_f32(b[off]);
+    dq[off] = s[0];
+    db[off] = s[2] * kv;
+    dk[off] = fmaf(s[2], bv, s[1]);
+    dg[off] = s[3];
+}
+
+template <typename Tin, int DK>
+int run_backward(const BwdParams& p, int64_t B, const float* part, const void* k, const void* b, float* dq,
+                 float* dk, float* db, float* dg, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(bwd_kernel<Tin, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(bwd_smem<DK>()));
+    });
+    if (attr != cudaSuccess) return GDR2_ERR_CUDA;
+    const dim3 grid(static_cast<unsigned>(B * p.H), static_cast<unsigned>(p.tiles));
+    bwd_kernel<Tin, DK><<<grid, kNW * 32, bwd_smem<DK>(), stream>>>(p);
+    if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
+    const int64_t items = B * p.T * p.H;
+    constexpr int kPer = 256 / DK;
+    bwd_reduce_kernel<Tin, DK><<<static_cast<unsigned>((items + kPer - 1) / kPer), 256, 0, stream>>>(
+        part, static_cast<const Tin*>(k), static_cast<const Tin*>(b), dq, dk, db, dg, items, p.tiles);
+    return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv) {
+    const int64_t tiles = dv / kDVT, nblk = (T + kCK - 1) / kCK;
+    const size_t ck = static_cast<size_t>(B * H * tiles * nblk) * dk * kDVT * 4;
+    const size_t part = static_cast<size_t>(B * T * H * tiles) * kVec * dk * 4;
+    return (ck + 255) / 256 * 256 + part;
+}
+
+int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream) {
+    if (a.dv % kDVT != 0 || a.B * a.H >= (1ll << 31) || a.dv / kDVT > 65535) return GDR2_ERR_SHAPE;
+    const int64_t tiles = a.dv / kDVT, nblk = (a.T + kCK - 1) / kCK;
+    const size_t ckb = (static_cast<size_t>(a.B * a.H * tiles * nblk) * a.dk * kDVT * 4 + 255) / 256 * 256;
+    BwdParams p{a.q, a.k, a.v, a.b, a.w, a.g, a.S0, a.dO, a.dST, a.d_v, a.d_w, a.d_S0,
+                static_cast<float*>(ws), reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ckb),
+                a.T, static_cast<int>(a.H), static_cast<int>(a.dv), static_cast<int>(tiles)};
+    const bool bf = a.in_dtype == GDR2_BF16;
+    using bf16 = __nv_bfloat16;
+#define GDR2_BWD(DKV)                                                                                           \
+    return bf ? run_backward<bf16, DKV>(p, a.B, p.part, a.k, a.b, a.d_q, a.d_k, a.d_b, a.d_g, stream)          \
+              : run_backward<float, DKV>(p, a.B, p.part, a.k, a.b, a.d_q, a.d_k, a.d_b, a.d_g, stream)
+    switch (a.dk) {
+        case 32: GDR2_BWD(32);
+        case 64: GDR2_BWD(64);
+        case 128: GDR2_BWD(128);
+        default: return GDR2_ERR_SHAPE;
+    }
+#undef GDR2_BWD
+}
+
+}  // namespace gdr2

@@ -31,6 +31,17 @@ struct ForwardArgs {
     int out_dtype;       // GDR2_F32 / GDR2_BF16: o
 };
 
+struct BackwardArgs {
+    const void *q, *k, *v, *b, *w, *g;   // forward inputs (in_dtype)
+    const float* S0;                     // [B, H, dk, dv] or null (zero)
+    const float* dO;                     // [B, T, H, dv] gradient at o
+    const float* dST;                    // [B, H, dk, dv] gradient at S_T, or null (zero)
+    float *d_q, *d_k, *d_v, *d_b, *d_w, *d_g;   // fp32 gradients, layouts of the inputs
+    float* d_S0;                         // [B, H, dk, dv] or null (not stored)
+    int64_t B, T, H, dk, dv;
+    int in_dtype;
+};
+
 struct DecodeArgs {
     const void *q, *k, *v, *b, *w, *g;
     float* S;
@@ -44,6 +55,10 @@ struct DecodeArgs {
 // of the library's error word (bounded waits record failures there).
 int launch_recurrent(const ForwardArgs& a, cudaStream_t stream);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// Gradients (token-sequential fp32 kernels); the workspace holds state
+// checkpoints and the per-tile row-vector partials.
+size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
+int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream);
 
 // ---- two-kernel chunked prefill (bf16 inputs, d_k = 128) --------------------------
 // The preparation kernel writes, for every 64-token chunk of every (sequence,

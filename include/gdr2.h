@@ -202,6 +202,45 @@ int gdr2_forward_segmented(const void* q, const void* k, const void* v,
                            int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream);
 
 /*
+ * gdr2_backward -- gradients of gdr2_forward (the training half).
+ *
+ * Differentiates L = sum_t <o_t, d_o_t> + <S_T, d_S_T> with respect to every
+ * input of the update equation above (the page's "Gated Delta Rule-2 update
+ * equation" section): q, k, v, b, w, log_decay and S0.  With X_t = D_t S_{t-1},
+ * c_t = b_t (.) k_t, delta_t = w_t (.) v_t - X_t^T c_t and G the gradient at S_t
+ * (later tokens, d_S_T, and q_t d_o_t^T from the readout):
+ *     dq_t = S_t d_o_t,  ddelta = G^T k_t,  dv_t = ddelta (.) w_t,  dw_t = ddelta (.) v_t,
+ *     dc = -X_t ddelta,  db_t = dc (.) k_t,  dk_t = G delta_t + dc (.) b_t,
+ *     dX = G - c_t ddelta^T,  dlog_decay_t = rowsum(dX (.) X_t),  dS_{t-1} = D_t dX.
+ * The kernels run the recurrence token by token in fp32: a forward sweep keeps
+ * the state every 8 tokens, the backward sweep recomputes each 8-token block
+ * from its checkpoint and walks it in reverse.
+ *
+ *   q, k, b, log_decay : [B, T, H, dk]  (in_dtype), the forward's inputs
+ *   v, w               : [B, T, H, dv]  (in_dtype)
+ *   S0                 : [B, H, dk, dv] fp32, or NULL (zero initial state)
+ *   d_o                : [B, T, H, dv] fp32, gradient arriving at o
+ *   d_S_T              : [B, H, dk, dv] fp32, gradient arriving at S_T, or NULL (zero)
+ *   d_q, d_k, d_b, d_log_decay : [B, T, H, dk] fp32, written
+ *   d_v, d_w           : [B, T, H, dv] fp32, written
+ *   d_S0               : [B, H, dk, dv] fp32, written, or NULL (not stored)
+ *
+ * dk, dv in {32, 64, 128}.  Workspace (stream-ordered pool, released on the
+ * stream): B*H*ceil(T/8)*dk*dv*4 bytes of checkpoints plus
+ * B*T*H*(dv/32)*4*dk*4 bytes of per-tile partial sums.  Outputs may overlap
+ * no input and no other output (GDR2_ERR_ALIAS).  T = 0 gives d_S0 = d_S_T (or
+ * zeros).  The page has no equations for the backward pass; these follow from
+ * the update equation by the chain rule.
+ */
+int gdr2_backward(const void* q, const void* k, const void* v,
+                  const void* b, const void* w, const void* log_decay,
+                  const float* S0, const float* d_o, const float* d_S_T,
+                  float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                  float* d_log_decay, float* d_S0,
+                  int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                  int in_dtype, cudaStream_t stream);
+
+/*
  * gdr2_decode_step -- one autoregressive step for every (batch, head), the
  * state updated in place (same equation, one token):
  *

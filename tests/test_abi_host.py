@@ -140,3 +140,26 @@ def test_segmented_rejects_bad_args():
     assert seg(3, B=-1) == ARG
     assert seg(0, o=None) == ARG
     assert seg(2, o=ctypes.c_void_p(BASE)) == ALIAS
+
+
+def bwd_args(B=1, T=4, H=2, dk=64, dv=64, dtype=1, **over):
+    names = ["q", "k", "v", "b", "w", "g", "S0", "do", "dST",
+             "gq", "gk", "gv", "gb", "gw", "gg", "gS0"]
+    p = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in enumerate(names)}
+    p.update(over)
+    return [p[n] for n in names] + [B, T, H, dk, dv, dtype, None]
+
+
+def test_backward_rejects_bad_args():
+    L = _lib.lib()
+    call = lambda **kw: L.gdr2_backward(*bwd_args(**kw))  # noqa: E731
+    assert call(B=-1) == ARG
+    assert call(dk=48) == SHAPE
+    assert call(dv=16) == SHAPE
+    assert call(dtype=5) == UNSUP
+    for n in ("q", "do", "gq", "gv", "gg"):
+        assert call(**{n: None}) == ARG, n
+    assert call(gk=ctypes.c_void_p(BASE + 11 * GAP + 4)) == ALIGN
+    assert call(gq=ctypes.c_void_p(BASE)) == ALIAS                 # d_q over q
+    assert call(gb=ctypes.c_void_p(BASE + 9 * GAP)) == ALIAS       # d_b over d_q
+    assert call(gS0=ctypes.c_void_p(BASE + 6 * GAP)) == ALIAS      # d_S0 over S0
