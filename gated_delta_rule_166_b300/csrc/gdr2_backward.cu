@@ -19,10 +19,13 @@
 // CTA's warps in shared memory and over the tiles by a second kernel.
 //
 // States in reverse order come from recomputation: a forward sweep stores the
-// tile at the start of every 8-token block (checkpoints in the workspace); the
-// backward sweep reloads a block's checkpoint, recomputes its 8 states with the
+// tile at the start of every 4-token block (checkpoints in the workspace); the
+// backward sweep reloads a block's checkpoint, recomputes its 4 states with the
 // same arithmetic (so the same fp32 values), keeps X_t and delta_t in shared
-// memory and walks the block backwards.
+// memory and walks the block backwards.  Each block's token inputs are fetched
+// into registers while the previous block is computed.  Short blocks keep the
+// shared memory at two CTAs per SM: the sweeps are chains of dependent steps,
+// so the second CTA's warps hide latency.
 #include <mutex>
 
 #include "gdr2.h"
@@ -34,7 +37,7 @@ namespace {
 constexpr int kNW = 8;            // warps per CTA
 constexpr int kCPW = 4;           // value columns per warp
 constexpr int kDVT = kNW * kCPW;  // value columns per CTA
-constexpr int kCK = 8;            // tokens per checkpoint block
+constexpr int kCK = 4;            // tokens per checkpoint block
 constexpr int kVec = 4;           // row vectors reduced over tiles: dq, G delta, dc, dlog_decay
 
 struct BwdParams {
@@ -47,6 +50,8 @@ struct BwdParams {
     int H, dv_dim, tiles;
 };
 
+// Shared memory: the X_t stash of one block, its token inputs and two buffers of
+// row-vector partials -- 106.5 KB at d_k = 128, so two CTAs share an SM.
 template <int DK> constexpr size_t bwd_smem() {
     return sizeof(float) * (static_cast<size_t>(kCK) * DK * kDVT     // X_t stash
                             + 4 * kCK * DK                           // q, k, c, alpha
@@ -55,7 +60,7 @@ template <int DK> constexpr size_t bwd_smem() {
 }
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(kNW * 32, 1) bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
     constexpr int RPL = DK / 32;
     extern __shared__ __align__(16) float sm[];
     float* xs = sm;                                   // [kCK][kNW][RPL][kCPW][32]
@@ -85,30 +90,49 @@ __global__ void __launch_bounds__(kNW * 32, 1) bwd_kernel(const BwdParams p) {
     const int64_t nblk = (T + kCK - 1) / kCK;
     float* ck = p.ckpt + (bh * p.tiles + tile) * nblk * (DK * kDVT);
 
-    // one block's token inputs into shared memory
-    auto load_block = [&](int64_t t0, int n) {
-        for (int e = tid; e < kCK * DK; e += kNW * 32) {
-            const int tt = e / DK, i = e % DK;
-            float qv = 0.f, kv = 0.f, cv = 0.f, av = 1.f;
-            if (tt < n) {
+    // A block's token inputs: fetched into registers one block ahead (so the global
+    // loads overlap the current block's arithmetic), then stored to shared memory.
+    constexpr int NE = (kCK * DK + kNW * 32 - 1) / (kNW * 32);   // key-side elements per thread
+    static_assert(kCK * kDVT <= kNW * 32, "at most one value-side element per thread");
+    float fq[NE], fk[NE], fb[NE], fg[NE], fv, fw, fd;
+    auto fetch = [&](int64_t t0, int n) {
+#pragma unroll
+        for (int u = 0; u < NE; ++u) {
+            const int e = tid + u * kNW * 32, tt = e / DK, i = e % DK;
+            fq[u] = fk[u] = fb[u] = fg[u] = 0.f;
+            if (e < kCK * DK && tt < n) {
                 const int64_t off = ((tok0 + t0 + tt) * p.H + h) * DK + i;
-                kv = to_f32(k[off]);
-                qv = to_f32(q[off]);
-                cv = to_f32(b[off]) * kv;
-                av = expf(to_f32(g[off]));
+                fq[u] = to_f32(q[off]);
+                fk[u] = to_f32(k[off]);
+                fb[u] = to_f32(b[off]);
+                fg[u] = to_f32(g[off]);
             }
-            sq[e] = qv; sk[e] = kv; sc[e] = cv; sa[e] = av;
         }
-        for (int e = tid; e < kCK * kDVT; e += kNW * 32) {
-            const int tt = e / kDVT, j = e % kDVT;
-            float vv = 0.f, wv = 0.f, dov = 0.f;
-            if (tt < n) {
-                const int64_t off = ((tok0 + t0 + tt) * p.H + h) * p.dv_dim + j0 + j;
-                vv = to_f32(v[off]);
-                wv = to_f32(w[off]);
-                dov = p.dO[off];
+        const int tt = tid / kDVT, j = tid % kDVT;
+        fv = fw = fd = 0.f;
+        if (tid < kCK * kDVT && tt < n) {
+            const int64_t off = ((tok0 + t0 + tt) * p.H + h) * p.dv_dim + j0 + j;
+            fv = to_f32(v[off]);
+            fw = to_f32(w[off]);
+            fd = p.dO[off];
+        }
+    };
+    auto stash = [&]() {
+#pragma unroll
+        for (int u = 0; u < NE; ++u) {
+            const int e = tid + u * kNW * 32;
+            if (e < kCK * DK) {
+                sq[e] = fq[u];
+                sk[e] = fk[u];
+                sc[e] = fb[u] * fk[u];
+                sa[e] = expf(fg[u]);
             }
-            sv[e] = vv; sw[e] = wv; su[e] = wv * vv; sdo[e] = dov;
+        }
+        if (tid < kCK * kDVT) {
+            sv[tid] = fv;
+            sw[tid] = fw;
+            su[tid] = fw * fv;
+            sdo[tid] = fd;
         }
     };
     // one forward step of token tt of the staged block: X = alpha * S, delta = u - X^T c,
@@ -144,16 +168,17 @@ __global__ void __launch_bounds__(kNW * 32, 1) bwd_kernel(const BwdParams p) {
 #pragma unroll
         for (int c = 0; c < kCPW; ++c)
             S[r][c] = p.S0 ? p.S0[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] : 0.f;
+    if (nblk > 1) fetch(0, kCK);
     for (int64_t blk = 0; blk < nblk; ++blk) {
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
 #pragma unroll
             for (int c = 0; c < kCPW; ++c) *ck_ptr(blk, r, c) = S[r][c];
         if (blk + 1 == nblk) break;   // the last block is recomputed from its checkpoint
-        const int64_t t0 = blk * kCK;
         __syncthreads();
-        load_block(t0, kCK);
+        stash();
         __syncthreads();
+        if (blk + 2 < nblk) fetch((blk + 1) * kCK, kCK);   // blocks before the last are full
         for (int tt = 0; tt < kCK; ++tt) fwd_step(S, tt, false);
     }
 
@@ -165,12 +190,14 @@ __global__ void __launch_bounds__(kNW * 32, 1) bwd_kernel(const BwdParams p) {
         for (int c = 0; c < kCPW; ++c)
             G[r][c] = p.dST ? p.dST[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] : 0.f;
     int buf = 0;
+    if (nblk > 0) fetch((nblk - 1) * kCK, static_cast<int>(T - (nblk - 1) * kCK));
     for (int64_t blk = nblk - 1; blk >= 0; --blk) {
         const int64_t t0 = blk * kCK;
         const int n = static_cast<int>(T - t0 < kCK ? T - t0 : kCK);
         __syncthreads();
-        load_block(t0, n);
+        stash();
         __syncthreads();
+        if (blk > 0) fetch((blk - 1) * kCK, kCK);
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
 #pragma unroll
@@ -249,8 +276,8 @@ __global__ void __launch_bounds__(kNW * 32, 1) bwd_kernel(const BwdParams p) {
                 for (int ww = 0; ww < kNW; ++ww) s += rb[ww * kVec * DK + e];
                 dst[e] = s;
             }
-            buf ^= 1;   // the other buffer takes the next token; this one is reread only after
-                        // the next token's barrier
+            buf ^= 1;   // the other buffer takes the next token; this one is reread only
+                        // after the next token's barrier
         }
     }
     if (p.dS0) {

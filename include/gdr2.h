@@ -213,7 +213,7 @@ int gdr2_forward_segmented(const void* q, const void* k, const void* v,
  *     dc = -X_t ddelta,  db_t = dc (.) k_t,  dk_t = G delta_t + dc (.) b_t,
  *     dX = G - c_t ddelta^T,  dlog_decay_t = rowsum(dX (.) X_t),  dS_{t-1} = D_t dX.
  * The kernels run the recurrence token by token in fp32: a forward sweep keeps
- * the state every 8 tokens, the backward sweep recomputes each 8-token block
+ * the state every 4 tokens, the backward sweep recomputes each 4-token block
  * from its checkpoint and walks it in reverse.
  *
  *   q, k, b, log_decay : [B, T, H, dk]  (in_dtype), the forward's inputs
@@ -226,7 +226,7 @@ int gdr2_forward_segmented(const void* q, const void* k, const void* v,
  *   d_S0               : [B, H, dk, dv] fp32, written, or NULL (not stored)
  *
  * dk, dv in {32, 64, 128}.  Workspace (stream-ordered pool, released on the
- * stream): B*H*ceil(T/8)*dk*dv*4 bytes of checkpoints plus
+ * stream): B*H*ceil(T/4)*dk*dv*4 bytes of checkpoints plus
  * B*T*H*(dv/32)*4*dk*4 bytes of per-tile partial sums.  Outputs may overlap
  * no input and no other output (GDR2_ERR_ALIAS).  T = 0 gives d_S0 = d_S_T (or
  * zeros).  The page has no equations for the backward pass; these follow from
