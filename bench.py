@@ -19,6 +19,8 @@ line carries:
   and S_T inside the timed region;
 * long_context: the long-context workload (B=1, H=16, T=65536) through the
   chunk-parallel scan over sequence segments, beside the sequential state pass;
+* backward: gdr2_backward (all input gradients) over the same GDN-2 layer
+  workload;
 * cpu_baseline: the fp64 CPU oracle (as it stands) on a bounded sample of the
   same workload on the host cores;
 * clocks: nvidia-smi samples taken during the timed region.
@@ -335,6 +337,46 @@ def bench_long(gdr2, hbm_gbs, steps=10, warmup=3):
                          "kernel": "gdr2 prefill: prep_kernel + state_kernel + scan_kernel + correct_kernel"}}
 
 
+def backward_bytes(B, T, H, dk, dv, esz=2):
+    """Bytes a perfect backward pass must move: the six forward inputs and the
+    fp32 gradient at o read once, the six fp32 input gradients and dS0 written
+    once."""
+    tok = B * T * H * ((4 * dk + 2 * dv) * esz + dv * 4 + (4 * dk + 2 * dv) * 4)
+    return tok + B * H * dk * dv * 4
+
+
+def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3):
+    """gdr2_backward over the GDN-2 layer workload with a seeded fp32 gradient at o
+    (no gradient at S_T), CUDA events around `steps` calls."""
+    B, T, H, dk = x.q.shape
+    dv = x.v.shape[-1]
+    gen = torch.Generator().manual_seed(11)
+    d_o = torch.randn(B, T, H, dv, generator=gen).to("cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        gdr2.backward(*x.tensors(), x.S0, d_o, None)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        gdr2.backward(*x.tensors(), x.S0, d_o, None)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if gdr2.gdr2_device_status() != 0:
+        raise RuntimeError("device-side failure during the backward pass")
+    ms = a.elapsed_time(b) / steps
+    nbytes = backward_bytes(B, T, H, dk, dv)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"{WORKLOAD} backward: gradients of all six inputs and S0, fp32, from a seeded "
+                        f"fp32 gradient at o",
+            "ms_per_call": ms, "tokens_per_s": B * T / (ms / 1e3), "steps": steps, "warmup": warmup,
+            "launches_per_call": 2,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes,
+                         "traffic": traffic_record("backward_" + WORKLOAD),
+                         "kernel": "gdr2 backward: bwd_kernel + bwd_reduce_kernel per call"}}
+
+
 def bench_e2e(gdr2, x_host, steps, warmup):
     """Pinned host inputs -> device -> gdr2_forward -> o and S_T back to host."""
     B, T, H, dk = x_host.q.shape
@@ -418,7 +460,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long", action="store_true", help="skip the long-context prefill leg")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "long"], default="all",
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass leg")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward"], default="all",
                     help="profiling aid: run just one leg (decode and long print only that leg)")
     ap.add_argument("--decode-steps", type=int, default=1024)
     args = ap.parse_args()
@@ -485,6 +528,11 @@ def main():
         if rank == 0:
             print(json.dumps({"decode": dec}))
         return
+    if args.only == "backward":
+        bw = bench_backward(gdr2, hbm_gbs, x, steps=min(args.steps, 5), warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"backward": bw}))
+        return
     if args.only == "long":
         lc = bench_long(gdr2, hbm_gbs, steps=min(args.steps, 10), warmup=args.warmup)
         if rank == 0:
@@ -519,7 +567,7 @@ def main():
            "gpu_launches": launches}
 
     if args.only == "prefill":
-        args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = True
+        args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = args.no_backward = True
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
@@ -535,6 +583,8 @@ def main():
         out["gpu_launches"] = launches  # timed prefill region only; decode launches in out["decode"]
     if not args.no_long:
         out["long_context"] = bench_long(gdr2, hbm_gbs)
+    if not args.no_backward:
+        out["backward"] = bench_backward(gdr2, hbm_gbs, x)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x_host)
     if rank == 0:

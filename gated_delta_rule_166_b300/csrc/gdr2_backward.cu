@@ -137,24 +137,39 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
     };
     // one forward step of token tt of the staged block: X = alpha * S, delta = u - X^T c,
     // S = X + k delta^T; X (optional) and delta are kept for the backward walk
+    // (the columns' shuffle reductions run round by round together, so their latencies overlap)
+    // (the token's per-row values are read into registers first: the stash stores
+    // below could otherwise force them to be reread for every column)
     auto fwd_step = [&](float (&S)[RPL][kCPW], int tt, bool keep) {
+        float x[kCPW], ar[RPL], cr[RPL], kr[RPL];
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) {
+            const int i = tt * DK + lane + 32 * r;
+            ar[r] = sa[i];
+            cr[r] = sc[i];
+            kr[r] = sk[i];
+        }
 #pragma unroll
         for (int c = 0; c < kCPW; ++c) {
-            float x = 0.f;
+            x[c] = 0.f;
 #pragma unroll
             for (int r = 0; r < RPL; ++r) {
-                const int i = lane + 32 * r;
-                const float X = sa[tt * DK + i] * S[r][c];
+                const float X = ar[r] * S[r][c];
                 S[r][c] = X;
-                x = fmaf(sc[tt * DK + i], X, x);
+                x[c] = fmaf(cr[r], X, x[c]);
                 if (keep) xs[(((tt * kNW + warp) * RPL + r) * kCPW + c) * 32 + lane] = X;
             }
+        }
 #pragma unroll
-            for (int s = 16; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
-            const float delta = su[tt * kDVT + cw + c] - x;
+        for (int s = 16; s > 0; s >>= 1)
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) x[c] += __shfl_xor_sync(0xffffffffu, x[c], s);
+#pragma unroll
+        for (int c = 0; c < kCPW; ++c) {
+            const float delta = su[tt * kDVT + cw + c] - x[c];
             if (keep && lane == c) sdl[tt * kDVT + cw + c] = delta;
 #pragma unroll
-            for (int r = 0; r < RPL; ++r) S[r][c] = fmaf(sk[tt * DK + lane + 32 * r], delta, S[r][c]);
+            for (int r = 0; r < RPL; ++r) S[r][c] = fmaf(kr[r], delta, S[r][c]);
         }
     };
     auto ck_ptr = [&](int64_t blk, int r, int c) {
@@ -212,11 +227,12 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
                 dl[c] = sdl[tt * kDVT + cw + c];
                 dov[c] = sdo[tt * kDVT + cw + c];
             }
-            float pq[RPL], pk[RPL], pc[RPL], pg[RPL];
+            float pq[RPL], pk[RPL], pc[RPL], pg[RPL], kr[RPL];
 #pragma unroll
             for (int r = 0; r < RPL; ++r) {
                 const int i = lane + 32 * r;
                 const float qi = sq[tt * DK + i], ki = sk[tt * DK + i];
+                kr[r] = ki;
                 pq[r] = 0.f;
                 pk[r] = 0.f;
 #pragma unroll
@@ -231,13 +247,14 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
             float dd[kCPW];   // ddelta = G^T k
 #pragma unroll
             for (int c = 0; c < kCPW; ++c) {
-                float a = 0.f;
+                dd[c] = 0.f;
 #pragma unroll
-                for (int r = 0; r < RPL; ++r) a = fmaf(G[r][c], sk[tt * DK + lane + 32 * r], a);
-#pragma unroll
-                for (int s = 16; s > 0; s >>= 1) a += __shfl_xor_sync(0xffffffffu, a, s);
-                dd[c] = a;
+                for (int r = 0; r < RPL; ++r) dd[c] = fmaf(G[r][c], kr[r], dd[c]);
             }
+#pragma unroll
+            for (int s = 16; s > 0; s >>= 1)
+#pragma unroll
+                for (int c = 0; c < kCPW; ++c) dd[c] += __shfl_xor_sync(0xffffffffu, dd[c], s);
             if (lane < kCPW) {
                 const int c = lane;
                 const int64_t off = (row * p.H + h) * p.dv_dim + j0 + cw + c;
