@@ -137,11 +137,16 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
     };
     // one forward step of token tt of the staged block: X = alpha * S, delta = u - X^T c,
     // S = X + k delta^T; X (optional) and delta are kept for the backward walk
-    // (the columns' shuffle reductions run round by round together, so their latencies overlap)
-    // (the token's per-row values are read into registers first: the stash stores
-    // below could otherwise force them to be reread for every column)
-    auto fwd_step = [&](float (&S)[RPL][kCPW], int tt, bool keep) {
-        float x[kCPW], ar[RPL], cr[RPL], kr[RPL];
+    // Arithmetic runs on column pairs (packed f32x2 FMA / MUL, each lane rounded as its
+    // scalar counterpart): S2[r][p] holds columns 2p, 2p+1 of row r.  The columns'
+    // shuffle reductions run round by round together, so their latencies overlap, and
+    // the token's per-row values are read into registers first (the stash stores could
+    // otherwise force them to be reread for every column).
+    constexpr int NP = kCPW / 2;
+    auto dup = [](float a) { return make_float2(a, a); };
+    auto fwd_step = [&](float2 (&S2)[RPL][NP], int tt, bool keep) {
+        float2 x2[NP];
+        float ar[RPL], cr[RPL], kr[RPL];
 #pragma unroll
         for (int r = 0; r < RPL; ++r) {
             const int i = tt * DK + lane + 32 * r;
@@ -150,26 +155,29 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
             kr[r] = sk[i];
         }
 #pragma unroll
-        for (int c = 0; c < kCPW; ++c) {
-            x[c] = 0.f;
+        for (int pp = 0; pp < NP; ++pp) x2[pp] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int r = 0; r < RPL; ++r) {
-                const float X = ar[r] * S[r][c];
-                S[r][c] = X;
-                x[c] = fmaf(cr[r], X, x[c]);
-                if (keep) xs[(((tt * kNW + warp) * RPL + r) * kCPW + c) * 32 + lane] = X;
+        for (int r = 0; r < RPL; ++r)
+#pragma unroll
+            for (int pp = 0; pp < NP; ++pp) {
+                const float2 X = __fmul2_rn(dup(ar[r]), S2[r][pp]);
+                S2[r][pp] = X;
+                x2[pp] = __ffma2_rn(dup(cr[r]), X, x2[pp]);
+                if (keep) reinterpret_cast<float2*>(xs)[(((tt * kNW + warp) * RPL + r) * NP + pp) * 32 + lane] = X;
             }
-        }
 #pragma unroll
         for (int s = 16; s > 0; s >>= 1)
 #pragma unroll
-            for (int c = 0; c < kCPW; ++c) x[c] += __shfl_xor_sync(0xffffffffu, x[c], s);
+            for (int pp = 0; pp < NP; ++pp)
+                x2[pp] = __fadd2_rn(x2[pp], make_float2(__shfl_xor_sync(0xffffffffu, x2[pp].x, s),
+                                                        __shfl_xor_sync(0xffffffffu, x2[pp].y, s)));
 #pragma unroll
-        for (int c = 0; c < kCPW; ++c) {
-            const float delta = su[tt * kDVT + cw + c] - x[c];
-            if (keep && lane == c) sdl[tt * kDVT + cw + c] = delta;
+        for (int pp = 0; pp < NP; ++pp) {
+            const float2 u2 = *reinterpret_cast<const float2*>(su + tt * kDVT + cw + 2 * pp);
+            const float2 d2 = make_float2(u2.x - x2[pp].x, u2.y - x2[pp].y);
+            if (keep && (lane >> 1) == pp) sdl[tt * kDVT + cw + lane] = (lane & 1) ? d2.y : d2.x;
 #pragma unroll
-            for (int r = 0; r < RPL; ++r) S[r][c] = fmaf(kr[r], delta, S[r][c]);
+            for (int r = 0; r < RPL; ++r) S2[r][pp] = __ffma2_rn(dup(kr[r]), d2, S2[r][pp]);
         }
     };
     auto ck_ptr = [&](int64_t blk, int r, int c) {
@@ -177,33 +185,40 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
     };
 
     // ---- forward sweep: the tile at the start of every block ------------------------------
-    float S[RPL][kCPW];
+    float2 S2[RPL][NP];
 #pragma unroll
     for (int r = 0; r < RPL; ++r)
 #pragma unroll
-        for (int c = 0; c < kCPW; ++c)
-            S[r][c] = p.S0 ? p.S0[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] : 0.f;
+        for (int pp = 0; pp < NP; ++pp) {
+            const int64_t o = (bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + 2 * pp;
+            S2[r][pp] = p.S0 ? make_float2(p.S0[o], p.S0[o + 1]) : make_float2(0.f, 0.f);
+        }
     if (nblk > 1) fetch(0, kCK);
     for (int64_t blk = 0; blk < nblk; ++blk) {
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
 #pragma unroll
-            for (int c = 0; c < kCPW; ++c) *ck_ptr(blk, r, c) = S[r][c];
+            for (int pp = 0; pp < NP; ++pp) {
+                *ck_ptr(blk, r, 2 * pp) = S2[r][pp].x;
+                *ck_ptr(blk, r, 2 * pp + 1) = S2[r][pp].y;
+            }
         if (blk + 1 == nblk) break;   // the last block is recomputed from its checkpoint
         __syncthreads();
         stash();
         __syncthreads();
         if (blk + 2 < nblk) fetch((blk + 1) * kCK, kCK);   // blocks before the last are full
-        for (int tt = 0; tt < kCK; ++tt) fwd_step(S, tt, false);
+        for (int tt = 0; tt < kCK; ++tt) fwd_step(S2, tt, false);
     }
 
     // ---- backward sweep ---------------------------------------------------------------------
-    float G[RPL][kCPW];
+    float2 G2[RPL][NP];
 #pragma unroll
     for (int r = 0; r < RPL; ++r)
 #pragma unroll
-        for (int c = 0; c < kCPW; ++c)
-            G[r][c] = p.dST ? p.dST[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] : 0.f;
+        for (int pp = 0; pp < NP; ++pp) {
+            const int64_t o = (bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + 2 * pp;
+            G2[r][pp] = p.dST ? make_float2(p.dST[o], p.dST[o + 1]) : make_float2(0.f, 0.f);
+        }
     int buf = 0;
     if (nblk > 0) fetch((nblk - 1) * kCK, static_cast<int>(T - (nblk - 1) * kCK));
     for (int64_t blk = nblk - 1; blk >= 0; --blk) {
@@ -216,64 +231,77 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
 #pragma unroll
-            for (int c = 0; c < kCPW; ++c) S[r][c] = *ck_ptr(blk, r, c);
-        for (int tt = 0; tt < n; ++tt) fwd_step(S, tt, true);
+            for (int pp = 0; pp < NP; ++pp) S2[r][pp] = make_float2(*ck_ptr(blk, r, 2 * pp), *ck_ptr(blk, r, 2 * pp + 1));
+        for (int tt = 0; tt < n; ++tt) fwd_step(S2, tt, true);
         __syncwarp();
         for (int tt = n - 1; tt >= 0; --tt) {
             const int64_t row = tok0 + t0 + tt;
-            float X[RPL][kCPW], dl[kCPW], dov[kCPW];
+            float2 X2[RPL][NP], dl2[NP], do2[NP];
 #pragma unroll
-            for (int c = 0; c < kCPW; ++c) {
-                dl[c] = sdl[tt * kDVT + cw + c];
-                dov[c] = sdo[tt * kDVT + cw + c];
+            for (int pp = 0; pp < NP; ++pp) {
+                dl2[pp] = *reinterpret_cast<const float2*>(sdl + tt * kDVT + cw + 2 * pp);
+                do2[pp] = *reinterpret_cast<const float2*>(sdo + tt * kDVT + cw + 2 * pp);
             }
+            // per row: dq = S_t do and G delta over this warp's columns (two partial sums each)
             float pq[RPL], pk[RPL], pc[RPL], pg[RPL], kr[RPL];
 #pragma unroll
             for (int r = 0; r < RPL; ++r) {
-                const int i = lane + 32 * r;
-                const float qi = sq[tt * DK + i], ki = sk[tt * DK + i];
+                const int i = tt * DK + lane + 32 * r;
+                const float qi = sq[i], ki = sk[i];
                 kr[r] = ki;
-                pq[r] = 0.f;
-                pk[r] = 0.f;
+                float2 aq = make_float2(0.f, 0.f), ak = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < kCPW; ++c) {
-                    X[r][c] = xs[(((tt * kNW + warp) * RPL + r) * kCPW + c) * 32 + lane];
-                    const float St = fmaf(ki, dl[c], X[r][c]);          // S_t
-                    G[r][c] = fmaf(qi, dov[c], G[r][c]);                // + q_t do_t^T
-                    pq[r] = fmaf(St, dov[c], pq[r]);
-                    pk[r] = fmaf(G[r][c], dl[c], pk[r]);
+                for (int pp = 0; pp < NP; ++pp) {
+                    X2[r][pp] = reinterpret_cast<const float2*>(xs)[(((tt * kNW + warp) * RPL + r) * NP + pp) * 32 + lane];
+                    const float2 St = __ffma2_rn(dup(ki), dl2[pp], X2[r][pp]);       // S_t
+                    G2[r][pp] = __ffma2_rn(dup(qi), do2[pp], G2[r][pp]);             // + q_t do_t^T
+                    aq = __ffma2_rn(St, do2[pp], aq);
+                    ak = __ffma2_rn(G2[r][pp], dl2[pp], ak);
                 }
+                pq[r] = aq.x + aq.y;
+                pk[r] = ak.x + ak.y;
             }
-            float dd[kCPW];   // ddelta = G^T k
+            float2 dd2[NP];   // ddelta = G^T k
 #pragma unroll
-            for (int c = 0; c < kCPW; ++c) {
-                dd[c] = 0.f;
+            for (int pp = 0; pp < NP; ++pp) {
+                dd2[pp] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int r = 0; r < RPL; ++r) dd[c] = fmaf(G[r][c], kr[r], dd[c]);
+                for (int r = 0; r < RPL; ++r) dd2[pp] = __ffma2_rn(G2[r][pp], dup(kr[r]), dd2[pp]);
             }
 #pragma unroll
             for (int s = 16; s > 0; s >>= 1)
 #pragma unroll
-                for (int c = 0; c < kCPW; ++c) dd[c] += __shfl_xor_sync(0xffffffffu, dd[c], s);
+                for (int pp = 0; pp < NP; ++pp)
+                    dd2[pp] = __fadd2_rn(dd2[pp], make_float2(__shfl_xor_sync(0xffffffffu, dd2[pp].x, s),
+                                                              __shfl_xor_sync(0xffffffffu, dd2[pp].y, s)));
             if (lane < kCPW) {
                 const int c = lane;
+                float ddc = 0.f;   // column c of ddelta (compile-time indices only)
+#pragma unroll
+                for (int pp = 0; pp < NP; ++pp) {
+                    if (c == 2 * pp) ddc = dd2[pp].x;
+                    if (c == 2 * pp + 1) ddc = dd2[pp].y;
+                }
                 const int64_t off = (row * p.H + h) * p.dv_dim + j0 + cw + c;
-                p.dv[off] = dd[c] * sw[tt * kDVT + cw + c];
-                p.dw[off] = dd[c] * sv[tt * kDVT + cw + c];
+                p.dv[off] = ddc * sw[tt * kDVT + cw + c];
+                p.dw[off] = ddc * sv[tt * kDVT + cw + c];
             }
+            // per row: dc = -X ddelta, dlog_decay = rowsum(dX * X); G <- D_t dX
 #pragma unroll
             for (int r = 0; r < RPL; ++r) {
-                const int i = lane + 32 * r;
-                const float ci = sc[tt * DK + i], ai = sa[tt * DK + i];
-                pc[r] = 0.f;
-                pg[r] = 0.f;
+                const int i = tt * DK + lane + 32 * r;
+                const float ci = sc[i], ai = sa[i];
+                float2 ac = make_float2(0.f, 0.f), ag = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < kCPW; ++c) {
-                    pc[r] = fmaf(-X[r][c], dd[c], pc[r]);
-                    const float dX = fmaf(-ci, dd[c], G[r][c]);
-                    pg[r] = fmaf(dX, X[r][c], pg[r]);
-                    G[r][c] = ai * dX;                                   // dS_{t-1}
+                for (int pp = 0; pp < NP; ++pp) {
+                    const float2 nX = make_float2(-X2[r][pp].x, -X2[r][pp].y);
+                    ac = __ffma2_rn(nX, dd2[pp], ac);
+                    const float2 dX = __ffma2_rn(dup(-ci), dd2[pp], G2[r][pp]);
+                    ag = __ffma2_rn(dX, X2[r][pp], ag);
+                    G2[r][pp] = __fmul2_rn(dup(ai), dX);                              // dS_{t-1}
                 }
+                pc[r] = ac.x + ac.y;
+                pg[r] = ag.x + ag.y;
             }
             // row vectors: this warp's column partials -> shared memory -> sum over warps
             float* rb = red + buf * (kNW * kVec * DK);
@@ -301,7 +329,11 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
 #pragma unroll
-            for (int c = 0; c < kCPW; ++c) p.dS0[(bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + c] = G[r][c];
+            for (int pp = 0; pp < NP; ++pp) {
+                const int64_t o = (bh * DK + lane + 32 * r) * p.dv_dim + j0 + cw + 2 * pp;
+                p.dS0[o] = G2[r][pp].x;
+                p.dS0[o + 1] = G2[r][pp].y;
+            }
     }
 }
 
