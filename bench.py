@@ -345,9 +345,15 @@ def backward_bytes(B, T, H, dk, dv, esz=2):
     return tok + B * H * dk * dv * 4
 
 
-def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3):
-    """gdr2_backward over the GDN-2 layer workload with a seeded fp32 gradient at o
-    (no gradient at S_T), CUDA events around `steps` calls."""
+def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None):
+    """gdr2_backward over the GDN-2 layer workload (or its first `batch` sequences)
+    with a seeded fp32 gradient at o (no gradient at S_T), CUDA events around
+    `steps` calls."""
+    if batch is not None and batch < x.q.shape[0]:
+        from gated_delta_rule_166_b300.inputs import PrefillInputs
+
+        x = PrefillInputs(*(t[:batch].contiguous() for t in x.tensors()),
+                          None if x.S0 is None else x.S0[:batch].contiguous())
     B, T, H, dk = x.q.shape
     dv = x.v.shape[-1]
     gen = torch.Generator().manual_seed(11)
@@ -367,8 +373,8 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3):
     ms = a.elapsed_time(b) / steps
     nbytes = backward_bytes(B, T, H, dk, dv)
     achieved = nbytes / (ms / 1e3) / 1e9
-    return {"workload": f"{WORKLOAD} backward: gradients of all six inputs and S0, fp32, from a seeded "
-                        f"fp32 gradient at o",
+    return {"workload": f"{WORKLOAD} backward (B={B}): gradients of all six inputs and S0, fp32, from a "
+                        f"seeded fp32 gradient at o",
             "ms_per_call": ms, "tokens_per_s": B * T / (ms / 1e3), "steps": steps, "warmup": warmup,
             "launches_per_call": 2,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
@@ -461,6 +467,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long", action="store_true", help="skip the long-context prefill leg")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass leg")
+    ap.add_argument("--backward-batch", type=int, default=None,
+                    help="profiling aid: the backward leg on the first N sequences only")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward"], default="all",
                     help="profiling aid: run just one leg (decode and long print only that leg)")
     ap.add_argument("--decode-steps", type=int, default=1024)
@@ -529,7 +537,8 @@ def main():
             print(json.dumps({"decode": dec}))
         return
     if args.only == "backward":
-        bw = bench_backward(gdr2, hbm_gbs, x, steps=min(args.steps, 5), warmup=args.warmup)
+        bw = bench_backward(gdr2, hbm_gbs, x, steps=min(args.steps, 5), warmup=args.warmup,
+                            batch=args.backward_batch)
         if rank == 0:
             print(json.dumps({"backward": bw}))
         return
