@@ -102,3 +102,20 @@ def test_backward_empty_sequence():
     assert torch.equal(g[6], d_ST)
     assert all(t.numel() == 0 for t in g[:6])
     assert np.isfinite(g[6].cpu().numpy()).all()
+
+
+def test_autograd_function_bf16_inputs():
+    """gdr2_apply on bf16 inputs: the chunked tensor-core forward (fp32 o) and the
+    fp32 backward, gradients returned in bf16 -- bar 2e-2 plus one bf16 rounding."""
+    x = make_prefill_inputs(1, 300, 2, 128, 128, dtype=torch.bfloat16, seed=705,
+                            decay_regime="slow", s0_std=0.2)
+    d_o, d_ST = upstream(x, 7)
+    leaves = [t.cuda().requires_grad_(True) for t in (*x.tensors(), x.S0)]
+    o, S_T = gdr2.gdr2_apply(*leaves)
+    ((o * d_o.cuda()).sum() + (S_T * d_ST.cuda()).sum()).backward()
+    ref = oracle.backward(*x.tensors(), x.S0, d_o, d_ST)
+    for name, leaf, rf in zip(NAMES, leaves, ref):
+        assert leaf.grad.dtype == leaf.dtype
+        e = err_over_rms(leaf.grad.float().cpu().numpy(), rf)
+        bar = 2e-2 + float(np.abs(rf).max()) * 2.0 ** -8 / float(np.sqrt(np.mean(rf * rf)))
+        assert e <= bar, f"{name}: {e:.3e} (bar {bar:.3g})"
