@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     gdr2_decode_step,
     gdr2_device_status,
     gdr2_forward,
+    gdr2_forward_cached,
     gdr2_forward_noalloc,
     gdr2_forward_varlen,
     gdr2_version,
@@ -23,5 +24,6 @@ from ._lib import (  # noqa: F401
 forward = gdr2_forward
 forward_varlen = gdr2_forward_varlen
 forward_noalloc = gdr2_forward_noalloc
+forward_cached = gdr2_forward_cached
 decode_step = gdr2_decode_step
 backward = gdr2_backward

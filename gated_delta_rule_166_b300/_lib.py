@@ -50,6 +50,8 @@ def lib():
         L.gdr2_forward_segmented.restype = ci
         L.gdr2_forward_varlen.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward_varlen.restype = ci
+        L.gdr2_forward_cached.argtypes = [vp] * 10 + [i64] * 6 + [ci, ci, vp]
+        L.gdr2_forward_cached.restype = ci
         L.gdr2_backward.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
         L.gdr2_backward.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
@@ -117,7 +119,8 @@ def gdr2_forward_noalloc(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None,
                     stream)
 
 
-def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream, extra=()):
+def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state, stream, extra=(),
+             cache=None):
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q and v must be [B, T, H, d]")
     B, T, H, dk = q.shape
@@ -145,13 +148,31 @@ def _forward(entry, q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_stat
     elif S_T is not None:
         _check_tokens("S_T", S_T, (B, H, dk, dv), torch.float32, dev)
     with torch.cuda.device(dev):
+        cache_args = () if cache is None else (_ptr(cache[0]) if cache[0].numel() else None, cache[1])
         st = getattr(lib(), entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
-                                   _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv,
+                                   _ptr(S0), _ptr(o), _ptr(S_T), *cache_args, B, T, H, dk, dv,
                                    _DTYPES[dtype], _DTYPES[o.dtype], *extra,
                                    ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
         raise GDR2Error(st, entry)
     return o, S_T
+
+
+def gdr2_forward_cached(q, k, v, b, w, log_decay, S0=None, *, cache_chunks: int, o=None, S_T=None,
+                        out_dtype=torch.float32, return_state: bool = True, stream=None):
+    """gdr2_forward that also returns the state at the end of every segment of
+    ``cache_chunks`` 64-token chunks: ``(o, S_T, S_cache)`` with S_cache
+    [B, H, T // (cache_chunks * 64), dk, dv] fp32 (the states after tokens
+    cache_chunks * 64 - 1, 2 * cache_chunks * 64 - 1, ...)."""
+    if int(cache_chunks) < 1:
+        raise ValueError("cache_chunks must be >= 1")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    n_cache = T // (int(cache_chunks) * 64)
+    S_cache = torch.empty((B, H, n_cache, dk, dv), dtype=torch.float32, device=q.device)
+    o, S_T = _forward("gdr2_forward_cached", q, k, v, b, w, log_decay, S0, o, S_T, out_dtype, return_state,
+                      stream, cache=(S_cache, int(cache_chunks)))
+    return o, S_T, S_cache
 
 
 def gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, o=None, S_T=None,

@@ -121,8 +121,9 @@ namespace {
 int forward_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
                  const void* log_decay, const float* S0, void* o, float* S_T, const int32_t* cu,
                  int64_t N, int64_t T, int64_t total, int64_t H, int64_t dk, int64_t dv, int in_dtype,
-                 int out_dtype, cudaStream_t stream, bool noalloc = false, int64_t segments = 0) {
-    if (N < 0 || T < 0 || total < 0 || H < 0 || segments < 0) return GDR2_ERR_ARG;
+                 int out_dtype, cudaStream_t stream, bool noalloc = false, int64_t segments = 0,
+                 float* S_cache = nullptr, int64_t cache_chunks = 0) {
+    if (N < 0 || T < 0 || total < 0 || H < 0 || segments < 0 || cache_chunks < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
     const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
@@ -150,6 +151,22 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         if (has_tokens && overlaps(S_T, bs, tok_in[i], tok_bytes[i])) return GDR2_ERR_ALIAS;
     if (S_T && S0 && S_T != S0 && overlaps(S_T, bs, S0, bs)) return GDR2_ERR_ALIAS;
     if (overlaps(S_T, bs, cu, bc)) return GDR2_ERR_ALIAS;
+    // cached states: [N][H][T / (cache_chunks * 64)][dk][dv], fixed-length calls only
+    const int64_t n_cache = cache_chunks > 0 ? T / (cache_chunks * 64) : 0;
+    size_t bcache = 0;
+    if (cache_chunks > 0) {
+        if (cu || noalloc) return GDR2_ERR_ARG;
+        int64_t nc = 0;
+        if (!mul_ok(ns, n_cache, &nc) || nc > INT64_MAX / 4) return GDR2_ERR_SHAPE;
+        bcache = static_cast<size_t>(nc) * 4;
+        if (bcache > 0 && !S_cache) return GDR2_ERR_ARG;
+        if (S_cache && !aligned16(S_cache)) return GDR2_ERR_ALIGN;
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(S_cache, bcache, tok_in[i], tok_bytes[i])) return GDR2_ERR_ALIAS;
+        if (overlaps(S_cache, bcache, o, bo) || overlaps(S_cache, bcache, S0, bs) ||
+            overlaps(S_cache, bcache, S_T, bs))
+            return GDR2_ERR_ALIAS;
+    }
 
     int* err = nullptr;
     int st = device_setup(&err);
@@ -166,6 +183,11 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
 
     ForwardArgs a{q, k, v, b, w, log_decay, S0, o, S_T, N, T, H, dk, dv,
                   reinterpret_cast<const int*>(cu), total, in_dtype, out_dtype};
+    if (bcache > 0) {
+        a.S_cache = S_cache;
+        a.cache_chunks = cache_chunks;
+        segments = 1;   // cached states come from the sequential state pass
+    }
     if (noalloc && two_kernel_supports(a)) {
         // The same two kernels over chunk ranges whose operands fit the scratch; the
         // state between ranges is carried in S_T (or, when the caller wants no S_T,
@@ -346,6 +368,18 @@ extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
     int rc = launch_backward(a, ws, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
     return rc;
+}
+
+extern "C" int gdr2_forward_cached(const void* q, const void* k, const void* v,
+                                   const void* b, const void* w, const void* log_decay,
+                                   const float* S0, void* o, float* S_T, float* S_cache, int64_t cache_chunks,
+                                   int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                   int in_dtype, int out_dtype, cudaStream_t stream) {
+    int64_t total = 0;
+    if (B >= 0 && T >= 0 && !mul_ok(B, T, &total)) return GDR2_ERR_SHAPE;
+    if (cache_chunks < 1) return GDR2_ERR_ARG;
+    return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, nullptr, B, T, total, H, dk, dv, in_dtype,
+                        out_dtype, stream, /*noalloc=*/false, /*segments=*/1, S_cache, cache_chunks);
 }
 
 extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,

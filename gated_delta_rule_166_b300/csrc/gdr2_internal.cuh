@@ -29,6 +29,10 @@ struct ForwardArgs {
     int64_t total;             // token rows of the packed tensors (cu != null)
     int in_dtype;        // GDR2_F32 / GDR2_BF16: q, k, v, b, w, log_decay
     int out_dtype;       // GDR2_F32 / GDR2_BF16: o
+    // fixed-length calls only: the state after every cache_chunks 64-token chunks,
+    // [B][H][n_cache][dk][dv] with n_cache = T / (cache_chunks * 64); null: none
+    float* S_cache = nullptr;
+    int64_t cache_chunks = 0;
 };
 
 struct BackwardArgs {

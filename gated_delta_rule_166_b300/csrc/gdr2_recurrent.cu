@@ -30,7 +30,8 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                  const Tin* __restrict__ w, const Tin* __restrict__ g,
                  const float* __restrict__ S0, Tout* __restrict__ o,
                  float* __restrict__ ST, int64_t Tfix, int H, int dv,
-                 const int* __restrict__ cu, int64_t total) {
+                 const int* __restrict__ cu, int64_t total,
+                 float* __restrict__ cache, int64_t cache_every, int n_cache) {
     constexpr int RPL = DK / 32;          // key rows per lane
     constexpr int CPW = kDVT / kNW;       // value columns per warp
     __shared__ float sq[kTB][DK], sk[kTB][DK], sc[kTB][DK], sa[kTB][DK];
@@ -121,6 +122,15 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
             const int64_t off = ((tok0 + t0 + tt) * H + h) * dv + j0 + j;
             o[off] = from_f32<Tout>(so[tt][j]);
         }
+        // the state at a cache point (cache_every is a multiple of the 16-token round)
+        if (cache && (t0 + n) % cache_every == 0 && (t0 + n) / cache_every <= n_cache) {
+            const int64_t m = (t0 + n) / cache_every - 1;
+#pragma unroll
+            for (int r = 0; r < RPL; ++r)
+#pragma unroll
+                for (int c = 0; c < CPW; ++c)
+                    cache[((bh * n_cache + m) * DK + lane + 32 * r) * dv + j0 + jw + c] = S[r][c];
+        }
         __syncthreads();
     }
 
@@ -141,7 +151,8 @@ int launch_typed(const ForwardArgs& a, cudaStream_t stream) {
         kern<<<grid, block, 0, stream>>>(
             (const Tin*)a.q, (const Tin*)a.k, (const Tin*)a.v, (const Tin*)a.b,
             (const Tin*)a.w, (const Tin*)a.g, a.S0, (Tout*)a.o, a.ST, a.T, (int)a.H, (int)a.dv, a.cu,
-            a.total);
+            a.total, a.S_cache, a.cache_chunks * 64,
+            a.S_cache ? static_cast<int>(a.T / (a.cache_chunks * 64)) : 0);
     };
     switch (a.dk) {
         case 32: args(recurrent_kernel<Tin, Tout, 32>); break;

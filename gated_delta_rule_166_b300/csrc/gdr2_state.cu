@@ -106,6 +106,9 @@ struct StateParams {
     float* seg_m;
     float* o32;                     // [N * Tr][H][dv] fp32
     float* r;                       // [N * Tr][H][d_k] fp32
+    // the state after every cache_chunks chunks: [N][H][n_cache][d_k][dv] (null: not kept)
+    float* cache;
+    int cache_chunks, n_cache;
 };
 
 // Element (token t, column n) of a TMA-loaded bf16 [64][64] tile (128-byte rows, swizzled).
@@ -117,7 +120,7 @@ __device__ __forceinline__ uint32_t vw_off(int t, int n) {
 // One CTA of the state pass; kTransfer: a transfer tile (identity start, U = 0).
 // The two kinds are separate instantiations so that value tiles carry no test of
 // the tile kind on their chain.
-template <bool kTransfer>
+template <bool kTransfer, bool kCache>
 __device__ __forceinline__ void state_cta(const CUtensorMap& tm_v, const CUtensorMap& tm_w, const CUtensorMap& tm_o,
                                           const CUtensorMap& tm_o32, const CUtensorMap& tm_r,
                                           const StateParams& prm) {
@@ -615,6 +618,15 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_v, const CUtenso
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(gam, S[jj], __uint_as_float(a[jj]) + __uint_as_float(b[jj]));
                 put_st();
+                // the state at a cache point (the end of every cache_chunks chunks)
+                if (kCache && (c + 1) % prm.cache_chunks == 0 && (c + 1) / prm.cache_chunks <= prm.n_cache) {
+                    float* cs = prm.cache +
+                                ((static_cast<int64_t>(bh) * prm.n_cache + (c + 1) / prm.cache_chunks - 1) * kDK + j) * prm.dv +
+                                j0 + 16 * R;
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 4)
+                        *reinterpret_cast<float4*>(cs + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+                }
             }
             if (c + 1 < n) {
                 put_kb(kbr);
@@ -649,9 +661,17 @@ state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ C
              const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_o32,
              const __grid_constant__ CUtensorMap tm_r, const StateParams prm) {
     if (static_cast<int>(blockIdx.y) >= prm.dv / kDVT)
-        state_cta<true>(tm_v, tm_w, tm_o, tm_o32, tm_r, prm);
+        state_cta<true, false>(tm_v, tm_w, tm_o, tm_o32, tm_r, prm);
     else
-        state_cta<false>(tm_v, tm_w, tm_o, tm_o32, tm_r, prm);
+        state_cta<false, false>(tm_v, tm_w, tm_o, tm_o32, tm_r, prm);
+}
+
+// The sequential state pass that also keeps the state at every cache point: a kernel
+// of its own, so that the pass above is compiled without the extra stores.
+__global__ void __launch_bounds__(kThreads, 1)
+state_kernel_cached(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_o, const StateParams prm) {
+    state_cta<false, true>(tm_v, tm_w, tm_o, tm_o, tm_o, prm);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -695,6 +715,7 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c
     const int64_t slots = chunks * a.H;
     if (slots * 128 >= (1ll << 31) || chunks >= (1ll << 31)) return GDR2_ERR_SHAPE;
     const bool segmented = seg.G > 1;
+    if (a.S_cache && (segmented || a.cu || c0 != 0 || a.cache_chunks < 1)) return GDR2_ERR_ARG;
     if (segmented && (a.cu || c0 != 0 || seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L * kC >= a.T ||
                       !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r))
         return GDR2_ERR_ARG;
@@ -715,6 +736,9 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(kSmemAlloc));
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(state_kernel_cached, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     StateParams prm{s, a.S0, a.o, a.ST, err, a.cu, static_cast<int>(a.T), static_cast<int>(a.H),
@@ -722,11 +746,16 @@ int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c
                     a.cu ? 0 : cpiece, a.cu ? 0 : c0, static_cast<int>(chunks),
                     a.out_dtype == GDR2_BF16 ? 1 : 0,
                     segmented ? seg.G : 1, segmented ? seg.L : cpiece, segmented ? static_cast<int>(seg.Tr) : 0,
-                    seg.seg_state, seg.seg_m, seg.o32, seg.r};
+                    seg.seg_state, seg.seg_m, seg.o32, seg.r,
+                    a.S_cache, static_cast<int>(a.cache_chunks),
+                    a.S_cache ? static_cast<int>(a.T / (a.cache_chunks * kC)) : 0};
     // value tiles, then (segmented) the d_k / 64 transfer tiles of each (sequence, segment, head)
     const int ytiles = static_cast<int>(a.dv / kDVT) + (segmented ? kDK / kDVT : 0);
     const dim3 grid(static_cast<unsigned>(a.B * (segmented ? seg.G : 1) * a.H), static_cast<unsigned>(ytiles));
-    state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, mo32, mr, prm);
+    if (a.S_cache)
+        state_kernel_cached<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, prm);
+    else
+        state_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mv, mw, mo, mo32, mr, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 

@@ -202,6 +202,34 @@ int gdr2_forward_segmented(const void* q, const void* k, const void* v,
                            int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream);
 
 /*
+ * gdr2_forward_cached -- gdr2_forward that also keeps the state at segment ends.
+ *
+ * The "Memory Caching (MC)" page ("caching the memory" section) splits a
+ * sequence into segments and keeps each segment's final memory state as a
+ * cached memory, so that later tokens can read the past through the cached
+ * states as well as the online one.  This call provides those states for this
+ * recurrence: S_cache[b][h][m] = the state after token (m + 1) * cache_chunks * 64
+ * - 1 of sequence b, for m = 0 .. n_cache - 1 with n_cache = floor(T /
+ * (cache_chunks * 64)) (segments of cache_chunks 64-token chunks; a final
+ * partial segment is not cached -- its end state is S_T).  How the cached
+ * states are combined with the readout is the caller's; the library computes o
+ * and S_T exactly as gdr2_forward.
+ *
+ *   S_cache      : [B, H, n_cache, dk, dv] fp32, written (may be NULL when n_cache = 0)
+ *   cache_chunks : >= 1, segment length in 64-token chunks
+ *
+ * Other arguments, layouts and errors as gdr2_forward (fixed-length sequences;
+ * the state pass is the sequential one, without sequence segments).
+ * GDR2_ERR_ARG for cache_chunks < 1 or a NULL S_cache with n_cache > 0;
+ * S_cache may overlap no other argument (GDR2_ERR_ALIAS).
+ */
+int gdr2_forward_cached(const void* q, const void* k, const void* v,
+                        const void* b, const void* w, const void* log_decay,
+                        const float* S0, void* o, float* S_T, float* S_cache, int64_t cache_chunks,
+                        int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                        int in_dtype, int out_dtype, cudaStream_t stream);
+
+/*
  * gdr2_backward -- gradients of gdr2_forward (the training half).
  *
  * Differentiates L = sum_t <o_t, d_o_t> + <S_T, d_S_T> with respect to every

@@ -163,3 +163,18 @@ def test_backward_rejects_bad_args():
     assert call(gq=ctypes.c_void_p(BASE)) == ALIAS                 # d_q over q
     assert call(gb=ctypes.c_void_p(BASE + 9 * GAP)) == ALIAS       # d_b over d_q
     assert call(gS0=ctypes.c_void_p(BASE + 6 * GAP)) == ALIAS      # d_S0 over S0
+
+
+def test_cached_rejects_bad_args():
+    L = _lib.lib()
+
+    def cached(n, S_cache=ctypes.c_void_p(BASE + 12 * GAP), **kw):   # T = 128: two cache points at n = 1
+        a = fwd_args(T=128, **kw)
+        return L.gdr2_forward_cached(*(a[:9] + [S_cache, n] + a[9:]))
+
+    assert cached(0) == ARG
+    assert cached(-2) == ARG
+    assert cached(1, S_cache=None) == ARG                         # two states to keep, no buffer
+    assert cached(1, S_cache=ctypes.c_void_p(BASE + 12 * GAP + 4)) == ALIGN
+    assert cached(1, S_cache=ctypes.c_void_p(BASE + 7 * GAP)) == ALIAS   # over o
+    assert cached(1, dk=48) == SHAPE
