@@ -24,12 +24,14 @@
  * --------------------------------
  * - All tensor pointers are DEVICE pointers on the current CUDA device,
  *   row-major and contiguous, 16-byte aligned.  The caller owns every buffer
- *   and the library keeps no pointer after return.  The chunked bf16 prefill
- *   (gdr2_forward, gdr2_forward_varlen with bf16 inputs and d_k = 128) takes a
- *   workspace of 66,048 bytes per (64-token chunk, head) -- the per-chunk
- *   operands its two kernels exchange -- from the device's default
- *   stream-ordered memory pool (cudaMallocAsync on `stream`) and releases it
- *   on the same stream; no other call allocates device memory.
+ *   and the library keeps no pointer after return.  Workspaces come from the
+ *   device's default stream-ordered memory pool (cudaMallocAsync on `stream`)
+ *   and are released on the same stream: the chunked bf16 prefill (bf16
+ *   inputs, d_k = 128) takes 66,048 bytes per (64-token chunk, head) -- the
+ *   per-chunk operands its two kernels exchange -- plus, when it splits
+ *   sequences into segments, the segment scratch described at
+ *   gdr2_forward_segmented; gdr2_backward takes its checkpoints and partial
+ *   sums.  gdr2_forward_noalloc and gdr2_decode_step allocate nothing.
  * - in_dtype selects the element type of the six token inputs and out_dtype
  *   that of o: GDR2_F32 (float) or GDR2_BF16 (__nv_bfloat16).  States are
  *   always fp32.  All arithmetic is fp32 (bf16 only as tensor-core operands
