@@ -15,8 +15,9 @@ line carries:
 * decode: the in-place decode step (B=256, H=16, d=128, fp32 state of 268 MB)
   over 1024 consecutive steps, in HBM GB/s, with its own roofline;
 * e2e: the same prefill through the public API from pinned host buffers, the
-  host->device copies of the step's inputs and the device->host copies of o
-  and S_T inside the timed region;
+  host->device copies of every step's inputs and the device->host copies of o
+  and S_T inside the timed region (uploads, computation and downloads
+  pipelined on three streams);
 * long_context: the long-context workload (B=1, H=16, T=65536) through the
   chunk-parallel scan over sequence segments, beside the sequential state pass;
 * backward: gdr2_backward (all input gradients) over the same GDN-2 layer
@@ -384,36 +385,61 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None):
 
 
 def bench_e2e(gdr2, x_host, steps, warmup):
-    """Pinned host inputs -> device -> gdr2_forward -> o and S_T back to host."""
+    """Pinned host inputs -> device -> gdr2_forward -> o and S_T back to host, every
+    step.  Steps are pipelined the way a serving loop would run them: inputs and
+    outputs are double-buffered on the device, and the uploads, the computation and
+    the downloads run on three streams, so step i + 1's upload overlaps step i's
+    download (separate copy engines).  The timed region spans all copies of all
+    steps."""
     B, T, H, dk = x_host.q.shape
     dv = x_host.v.shape[-1]
     pinned = [t.pin_memory() for t in x_host.tensors()]
-    dev_in = [torch.empty_like(t, device="cuda") for t in pinned]
-    o_h = torch.empty((B, T, H, dv), dtype=torch.float32).pin_memory()
-    S_h = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
-    o_d = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
-    S_d = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
+    dev_in = [[torch.empty_like(t, device="cuda") for t in pinned] for _ in range(2)]
+    o_h = [torch.empty((B, T, H, dv), dtype=torch.float32).pin_memory() for _ in range(2)]
+    S_h = [torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory() for _ in range(2)]
+    o_d = [torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda") for _ in range(2)]
+    S_d = [torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda") for _ in range(2)]
+    up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    done_comp = [torch.cuda.Event() for _ in range(2)]   # step's inputs consumed, outputs written
+    done_up = [torch.cuda.Event() for _ in range(2)]
+    done_down = [torch.cuda.Event() for _ in range(2)]   # step's outputs read back
+    for e in done_comp + done_down:
+        e.record(torch.cuda.current_stream())
+    torch.cuda.synchronize()
 
-    def step():
-        for h, d in zip(pinned, dev_in):
-            d.copy_(h, non_blocking=True)
-        gdr2.forward(*dev_in, None, o=o_d, S_T=S_d)
-        o_h.copy_(o_d, non_blocking=True)
-        S_h.copy_(S_d, non_blocking=True)
+    def step(i):
+        k = i & 1
+        up.wait_event(done_comp[k])                      # step i - 2 no longer reads these inputs
+        with torch.cuda.stream(up):
+            for h, d in zip(pinned, dev_in[k]):
+                d.copy_(h, non_blocking=True)
+        done_up[k].record(up)
+        comp.wait_event(done_up[k])
+        comp.wait_event(done_down[k])                    # step i - 2's outputs have been read back
+        gdr2.forward(*dev_in[k], None, o=o_d[k], S_T=S_d[k], stream=comp)
+        done_comp[k].record(comp)
+        down.wait_event(done_comp[k])
+        with torch.cuda.stream(down):
+            o_h[k].copy_(o_d[k], non_blocking=True)
+            S_h[k].copy_(S_d[k], non_blocking=True)
+        done_down[k].record(down)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(up)
+    for i in range(steps):
+        step(warmup + i)
+    down.wait_stream(up)
+    down.wait_stream(comp)
+    b.record(down)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    if gdr2.gdr2_device_status() != 0:
+        raise RuntimeError("device-side failure during the end-to-end prefill")
     h2d = sum(t.numel() * t.element_size() for t in pinned)
-    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+    d2h = o_h[0].numel() * o_h[0].element_size() + S_h[0].numel() * S_h[0].element_size()
     return ms, h2d, d2h
 
 
