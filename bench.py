@@ -4,14 +4,15 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one gdr2_forward over the GDN-2 1.3B layer workload (B=4, H=16,
-T=4096, d_k=d_v=128, bf16 inputs, fp32 state, zero S0): 16,384 tokens per
-step.  The headline value is tokens/s with inputs resident in HBM (402 MB of
-inputs > the 126 MB L2, so no flush is needed between steps).  The same JSON
-line carries:
+T=4096, d_k=d_v=128, bf16 inputs and o, fp32 state, zero S0): 16,384 tokens
+per step.  The headline value is tokens/s with inputs resident in HBM (402 MB
+of inputs > the 126 MB L2, so no flush is needed between steps).  The same
+JSON line carries:
 
-* roofline: the prefill's algorithmic bytes per call / the call's mean
-  CUDA-event duration (both of its kernels: the chunk-parallel preparation
-  kernel and the state kernel), against the measured HBM copy bandwidth;
+* roofline: the prefill's algorithmic bytes per call (473.96 MB) / the call's
+  mean CUDA-event duration, against the measured HBM copy bandwidth, with the
+  mean, median, first and slowest call;
+* prefill_fp32_o: the same prefill writing o in fp32 (541.1 MB per call);
 * decode: the in-place decode step (B=256, H=16, d=128, fp32 state of 268 MB)
   over 1024 consecutive steps, in HBM GB/s, with its own roofline;
 * e2e: the same prefill through the public API from pinned host buffers, the
@@ -220,11 +221,11 @@ def max_over_ranks(x, world):
 
 
 # --------------------------------------------------------------------------
-def bench_prefill(gdr2, x, steps, warmup, world):
+def bench_prefill(gdr2, x, steps, warmup, world, out_dtype=torch.bfloat16):
     B, T, H, dk = x.q.shape
     dv = x.v.shape[-1]
     stream = torch.cuda.current_stream()
-    o = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    o = torch.empty((B, T, H, dv), dtype=out_dtype, device="cuda")
     ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
     for _ in range(warmup):
         gdr2.forward(*x.tensors(), x.S0, o=o, S_T=ST)
@@ -249,6 +250,12 @@ def bench_prefill(gdr2, x, steps, warmup, world):
         raise RuntimeError("device-side failure during the timed prefill")
     # each bf16 gdr2_forward launches two kernels: preparation, then the state pass
     return total_ms / steps, per_launch, 2 * steps
+
+
+def launch_stats(per_launch):
+    """Mean, median, first and slowest of the per-call CUDA-event durations (ms)."""
+    return {"mean_ms": sum(per_launch) / len(per_launch), "median_ms": statistics.median(per_launch),
+            "first_ms": per_launch[0], "max_ms": max(per_launch), "calls": len(per_launch)}
 
 
 def bench_decode(gdr2, steps=1024, pool=16, seed=5):
@@ -307,7 +314,7 @@ def bench_long(gdr2, hbm_gbs, steps=10, warmup=3):
     cfg = WORKLOADS[name]
     B, T, H, dk, dv = cfg["B"], cfg["T"], cfg["H"], cfg["dk"], cfg["dv"]
     x = make_workload(name).to("cuda")
-    o = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
     ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -326,9 +333,9 @@ def bench_long(gdr2, hbm_gbs, steps=10, warmup=3):
     ms_auto, ms_seq = timed(None), timed(1)
     if gdr2.gdr2_device_status() != 0:
         raise RuntimeError("device-side failure during the long-context prefill")
-    nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=x.S0 is not None, st=True)
+    nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=2, s0=x.S0 is not None, st=True)
     achieved = nbytes / (ms_auto / 1e3) / 1e9
-    return {"workload": f"{name}: B={B} H={H} T={T} d_k=d_v={dk}, bf16 inputs, fp32 S0, state and o",
+    return {"workload": f"{name}: B={B} H={H} T={T} d_k=d_v={dk}, bf16 inputs and o, fp32 S0 and state",
             "ms_per_call": ms_auto, "tokens_per_s": B * T / (ms_auto / 1e3),
             "ms_per_call_sequential": ms_seq, "speedup_vs_sequential": ms_seq / ms_auto,
             "segments": "library choice (gdr2_forward)", "steps": steps, "warmup": warmup,
@@ -395,9 +402,9 @@ def bench_e2e(gdr2, x_host, steps, warmup):
     dv = x_host.v.shape[-1]
     pinned = [t.pin_memory() for t in x_host.tensors()]
     dev_in = [[torch.empty_like(t, device="cuda") for t in pinned] for _ in range(2)]
-    o_h = [torch.empty((B, T, H, dv), dtype=torch.float32).pin_memory() for _ in range(2)]
+    o_h = [torch.empty((B, T, H, dv), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     S_h = [torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory() for _ in range(2)]
-    o_d = [torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda") for _ in range(2)]
+    o_d = [torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     S_d = [torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda") for _ in range(2)]
     up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     done_comp = [torch.cuda.Event() for _ in range(2)]   # step's inputs consumed, outputs written
@@ -505,8 +512,8 @@ def main():
 
     cfg = WORKLOADS[WORKLOAD]
     B, T, H, dk, dv = cfg["B"], cfg["T"], cfg["H"], cfg["dk"], cfg["dv"]
-    config = {"workload": f"{WORKLOAD}: B={B} H={H} T={T} d_k=d_v={dk}, bf16 inputs, "
-                          f"fp32 state and fp32 o, S0=0, chunk 64",
+    config = {"workload": f"{WORKLOAD}: B={B} H={H} T={T} d_k=d_v={dk}, bf16 inputs and o, "
+                          f"fp32 state, S0=0, chunk 64",
               "global_batch": B, "seq_len": T, "heads": H, "head_dim": dk,
               "l2": "inputs (402 MB) larger than L2 (126 MB); no flush"}
 
@@ -582,7 +589,7 @@ def main():
     value = aggregate_tokens_per_s(tokens, ms_max, world)
 
     kern_ms = sum(per_launch) / len(per_launch)
-    nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=False, st=True)
+    nbytes = prefill_bytes(B, T, H, dk, dv, esz=2, osz=2, s0=False, st=True)
     nflops = prefill_flops(B, T, H, dk, dv)
     achieved = nbytes / (kern_ms / 1e3) / 1e9
     traffic = traffic_record("prefill_" + WORKLOAD)
@@ -592,7 +599,8 @@ def main():
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": nbytes,
                 "tflops": nflops / (kern_ms / 1e3) / 1e12,
-                "tensor_frac_of_bf16_peak": nflops / (kern_ms / 1e3) / 1e12 / bf16_tflops}
+                "tensor_frac_of_bf16_peak": nflops / (kern_ms / 1e3) / 1e12 / bf16_tflops,
+                "per_call": launch_stats(per_launch)}
 
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -600,6 +608,15 @@ def main():
            "data": "synthetic (seeded; distributions of the GDN-2 layer workload)",
            "config": config, "roofline": roofline, "clocks": clocks,
            "gpu_launches": launches}
+
+    # the same prefill with fp32 o (541.1 MB per call): a secondary figure
+    ms32, pl32, _ = bench_prefill(gdr2, x, max(args.steps, 20), args.warmup, world, out_dtype=torch.float32)
+    b32 = prefill_bytes(B, T, H, dk, dv, esz=2, osz=4, s0=False, st=True)
+    k32 = sum(pl32) / len(pl32)
+    out["prefill_fp32_o"] = {"ms_per_call": ms32, "tokens_per_s": tokens / (ms32 / 1e3),
+                             "algorithmic_bytes_per_launch": b32,
+                             "roofline_frac": b32 / (k32 / 1e3) / 1e9 / hbm_gbs,
+                             "per_call": launch_stats(pl32)}
 
     if args.only == "prefill":
         args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = args.no_backward = True
@@ -611,9 +628,15 @@ def main():
                       "ms_per_step": e2e_ms}
     if not args.no_decode:
         dec = bench_decode(gdr2, steps=args.decode_steps)
+        dtraffic = traffic_record("decode_B256_H16_d128")
         dec["roofline"] = {"bound": "hbm", "achieved": dec["gbs"], "peak": hbm_gbs, "unit": "GB/s",
-                           "frac": dec["gbs"] / hbm_gbs,
-                           "traffic": traffic_record("decode_B256_H16_d128")}
+                           "frac": dec["gbs"] / hbm_gbs, "traffic": dtraffic}
+        if dtraffic:
+            # part of the in-place state is still in L2 from the previous step, so the
+            # DRAM bytes per step are below the algorithmic ones: both rates reported
+            dram_gbs = dtraffic / (dec["us_per_step"] / 1e6) / 1e9
+            dec["roofline"]["dram_gbs"] = dram_gbs
+            dec["roofline"]["dram_frac"] = dram_gbs / hbm_gbs
         out["decode"] = dec
         out["gpu_launches"] = launches  # timed prefill region only; decode launches in out["decode"]
     if not args.no_long:

@@ -18,7 +18,9 @@ from ._lib import (  # noqa: F401
     gdr2_forward_cached,
     gdr2_forward_noalloc,
     gdr2_forward_varlen,
+    gdr2_release_workspace,
     gdr2_version,
+    gdr2_workspace_stats,
 )
 
 forward = gdr2_forward

@@ -62,6 +62,10 @@ def lib():
         L.gdr2_status_string.restype = ctypes.c_char_p
         L.gdr2_version.argtypes = []
         L.gdr2_version.restype = ci
+        L.gdr2_workspace_stats.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
+        L.gdr2_workspace_stats.restype = ci
+        L.gdr2_release_workspace.argtypes = []
+        L.gdr2_release_workspace.restype = ci
         _lib = L
     return _lib
 
@@ -328,3 +332,20 @@ def gdr2_device_status(stream=None) -> int:
 
 def gdr2_version() -> int:
     return lib().gdr2_version()
+
+
+def gdr2_workspace_stats(reset: bool = False):
+    """(reserved, used_high) bytes of the library's workspace pool on the current
+    device; ``reset`` sets the high-water mark back to zero after reading it."""
+    r, u = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = lib().gdr2_workspace_stats(ctypes.byref(r), ctypes.byref(u), 1 if reset else 0)
+    if st != 0:
+        raise GDR2Error(st, "gdr2_workspace_stats")
+    return r.value, u.value
+
+
+def gdr2_release_workspace() -> None:
+    """Return the workspace pool's unused memory on the current device to the system."""
+    st = lib().gdr2_release_workspace()
+    if st != 0:
+        raise GDR2Error(st, "gdr2_release_workspace")

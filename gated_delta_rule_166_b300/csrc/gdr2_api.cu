@@ -60,6 +60,44 @@ int scratch_setup(void** out) {
     return GDR2_OK;
 }
 
+// Stream-ordered pool of the library's workspaces on each device.  Its release
+// threshold is unlimited: memory freed at the end of a call stays mapped for the
+// next one, so a call that follows a synchronisation does not pay to map its
+// workspace again (a pool that trims at every synchronisation made the first
+// call after one slower than the rest).  gdr2_release_workspace() trims it.
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+int workspace_pool(cudaMemPool_t* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR2_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) return GDR2_ERR_CUDA;
+        uint64_t keep = UINT64_MAX;
+        if (cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return GDR2_ERR_CUDA;
+        }
+        g_pool[dev] = p;
+    }
+    *out = g_pool[dev];
+    return GDR2_OK;
+}
+
+// Workspace of `bytes` from the library's pool, stream-ordered on `stream`.
+int ws_alloc(void** p, size_t bytes, cudaStream_t stream) {
+    cudaMemPool_t pool = nullptr;
+    const int st = workspace_pool(&pool);
+    if (st != GDR2_OK) return st;
+    return cudaMallocFromPoolAsync(p, bytes, pool, stream) == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
 int g_sm_count[kMaxDevices] = {};
 
 // Streaming multiprocessors of the current device (looked up once per device).
@@ -232,8 +270,8 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
             return GDR2_ERR_UNSUPPORTED;
         }
         // Workspace for the per-chunk operands (and the segments' maps and partial
-        // outputs), stream-ordered from the device's default memory pool and released
-        // on the same stream.
+        // outputs), stream-ordered from the library's pool and released on the same
+        // stream.
         const int64_t chunks = prep_chunk_bound(a);
         const size_t wsb = round256(prep_workspace_bytes(chunks, H, N));
         size_t nb_state = 0, nb_m = 0, nb_o32 = 0, nb_r = 0;
@@ -244,8 +282,7 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
             nb_r = round256(static_cast<size_t>(N * seg.Tr * H) * dk * 4);
         }
         void* ws = nullptr;
-        if (cudaMallocAsync(&ws, wsb + 2 * nb_state + nb_m + nb_o32 + nb_r, stream) != cudaSuccess)
-            return GDR2_ERR_CUDA;
+        if ((st = ws_alloc(&ws, wsb + 2 * nb_state + nb_m + nb_o32 + nb_r, stream)) != GDR2_OK) return st;
         const PrepSlots s = prep_carve(ws, chunks, H);
         if (seg.G > 1) {
             uint8_t* p = static_cast<uint8_t*>(ws) + wsb;
@@ -364,7 +401,7 @@ extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
     BackwardArgs a{q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                    B, T, H, dk, dv, in_dtype};
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, backward_workspace_bytes(B, T, H, dk, dv), stream) != cudaSuccess) return GDR2_ERR_CUDA;
+    if ((st = ws_alloc(&ws, backward_workspace_bytes(B, T, H, dk, dv), stream)) != GDR2_OK) return st;
     int rc = launch_backward(a, ws, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
     return rc;
@@ -428,6 +465,32 @@ extern "C" int gdr2_device_status(cudaStream_t stream) {
         return GDR2_ERR_TIMEOUT;
     }
     return GDR2_OK;
+}
+
+extern "C" int gdr2_workspace_stats(int64_t* reserved, int64_t* used_high, int reset) {
+    if (!reserved || !used_high) return GDR2_ERR_ARG;
+    cudaMemPool_t pool = nullptr;
+    const int st = workspace_pool(&pool);
+    if (st != GDR2_OK) return st;
+    uint64_t r = 0, u = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &r) != cudaSuccess ||
+        cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &u) != cudaSuccess)
+        return GDR2_ERR_CUDA;
+    *reserved = static_cast<int64_t>(r);
+    *used_high = static_cast<int64_t>(u);
+    if (reset) {
+        uint64_t zero = 0;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess) return GDR2_ERR_CUDA;
+    }
+    return GDR2_OK;
+}
+
+extern "C" int gdr2_release_workspace(void) {
+    cudaMemPool_t pool = nullptr;
+    const int st = workspace_pool(&pool);
+    if (st != GDR2_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GDR2_ERR_CUDA;
+    return cudaMemPoolTrimTo(pool, 0) == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 
 extern "C" const char* gdr2_status_string(int status) {

@@ -24,10 +24,13 @@
  * --------------------------------
  * - All tensor pointers are DEVICE pointers on the current CUDA device,
  *   row-major and contiguous, 16-byte aligned.  The caller owns every buffer
- *   and the library keeps no pointer after return.  Workspaces come from the
- *   device's default stream-ordered memory pool (cudaMallocAsync on `stream`)
- *   and are released on the same stream: the chunked bf16 prefill (bf16
- *   inputs, d_k = 128) takes 66,048 bytes per (64-token chunk, head) -- the
+ *   and the library keeps no pointer after return.  Workspaces come from a
+ *   stream-ordered memory pool that the library creates on each device it is
+ *   called on (allocated and released on `stream`); the pool keeps freed memory
+ *   reserved for later calls until gdr2_release_workspace() is called, so a call
+ *   after a synchronisation does not map its workspace again.  The chunked
+ *   bf16 prefill (bf16 inputs, d_k = 128) takes 66,048 bytes per (64-token
+ *   chunk, head) -- the
  *   per-chunk operands its two kernels exchange -- plus, when it splits
  *   sequences into segments, the segment scratch described at
  *   gdr2_forward_segmented; gdr2_backward takes its checkpoints and partial
@@ -145,7 +148,7 @@ int gdr2_forward_varlen(const void* q, const void* k, const void* v,
  * not allocate at call time: a serving runtime that reserves all device memory
  * when it starts and forbids allocations on its request path, or an embedding
  * host whose memory is managed by someone else and that may not draw from the
- * device's stream-ordered pool (which gdr2_forward uses for its workspace).
+ * library's stream-ordered workspace pool (which gdr2_forward uses).
  *
  * Same arguments, layouts, results and error codes as gdr2_forward.  For bf16
  * inputs with d_k = 128 the two prefill kernels run over ranges of chunks
@@ -255,7 +258,7 @@ int gdr2_forward_cached(const void* q, const void* k, const void* v,
  *   d_v, d_w           : [B, T, H, dv] fp32, written
  *   d_S0               : [B, H, dk, dv] fp32, written, or NULL (not stored)
  *
- * dk, dv in {32, 64, 128}.  Workspace (stream-ordered pool, released on the
+ * dk, dv in {32, 64, 128}.  Workspace (the library's pool, released on the
  * stream): B*H*ceil(T/4)*dk*dv*4 bytes of checkpoints plus
  * B*T*H*(dv/32)*4*dk*4 bytes of per-tile partial sums.  Outputs may overlap
  * no input and no other output (GDR2_ERR_ALIAS).  T = 0 gives d_S0 = d_S_T (or
@@ -297,6 +300,20 @@ int gdr2_decode_step(const void* q, const void* k, const void* v,
  * stream reports a CUDA error.  Reading clears the recorded failure.
  */
 int gdr2_device_status(cudaStream_t stream);
+
+/*
+ * gdr2_workspace_stats -- the library's workspace pool on the current device:
+ * *reserved = device memory it holds now, *used_high = the most of it in use at
+ * once since the pool was created or last reset (bytes).  reset != 0 sets the
+ * high-water mark back to zero after reading it.  GDR2_ERR_ARG for a NULL output.
+ */
+int gdr2_workspace_stats(int64_t* reserved, int64_t* used_high, int reset);
+
+/*
+ * gdr2_release_workspace -- synchronises the current device and returns the
+ * memory that the library's workspace pool holds but does not use to the system.
+ */
+int gdr2_release_workspace(void);
 
 /* Human-readable name of a gdr2_status value (static storage). */
 const char* gdr2_status_string(int status);
