@@ -595,7 +595,7 @@ def main():
     traffic = traffic_record("prefill_" + WORKLOAD)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "traffic": traffic,
-                "kernel": "gdr2 prefill: prep_kernel + state_kernel per call",
+                "kernel": "gdr2 prefill: prep2_kernel + chain_kernel per call",
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": nbytes,
                 "tflops": nflops / (kern_ms / 1e3) / 1e12,

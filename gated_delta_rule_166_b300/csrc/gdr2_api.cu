@@ -252,6 +252,24 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         }
         return GDR2_OK;
     }
+    if (two_kernel_supports(a) && segments == 0 && bcache == 0 &&
+        (cu || auto_segments(bh, dv, (T + 63) / 64) == 1)) {
+        // One pass over the chunks in affine form: prep2 writes each chunk's maps, the
+        // chain kernel carries the state; workspace (slots, then chunk_base of packed
+        // sequences) from the library's pool.
+        const int64_t chunks = prep_chunk_bound(a);
+        const size_t slot_bytes = round256(static_cast<size_t>(chunks) * static_cast<size_t>(H) * kSlot2Bytes);
+        void* ws = nullptr;
+        if ((st = ws_alloc(&ws, slot_bytes + (cu ? static_cast<size_t>(N + 1) * 4 : 0), stream)) != GDR2_OK)
+            return st;
+        uint8_t* slots = static_cast<uint8_t*>(ws);
+        int* cb = cu ? reinterpret_cast<int*>(slots + slot_bytes) : nullptr;
+        int rc = cu ? launch_chunk_base(a.cu, N, total, cb, stream) : GDR2_OK;
+        if (rc == GDR2_OK) rc = launch_prep2(a, slots, cb, chunks, stream, err);
+        if (rc == GDR2_OK) rc = launch_chain(a, slots, cb, stream, err);
+        if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
+        return rc;
+    }
     if (two_kernel_supports(a)) {
         // Segments of the chunk-parallel scan (fixed-length sequences only).
         const int64_t nch = (T + 63) / 64;

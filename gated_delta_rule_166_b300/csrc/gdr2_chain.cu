@@ -1,0 +1,524 @@
+// Chunked Gated Delta Rule-2 prefill in affine form, part 2 of 2: the
+// chunk-to-chunk state pass, one CTA per (sequence * head, 64-column d_v tile).
+//
+// Method ("Gated DeltaNet-2: Decoupling Erase and Write in Linear Attention"
+// page, "efficient implementation" section: chunkwise algorithm).  Each 64-token
+// chunk maps its start state S (d_k x d_v, fp32) to
+//     S' = diag(gamma) S + M' S + Y U,      O = P S + X U,      U = w * v
+// with M', Y, P, X and gamma = e^{G_C} written per (chunk, head) by the
+// preparation kernel (gdr2_prep2.cu, which derives them).  Only M' S and the
+// state update sit on the chunk-to-chunk chain: Y U and X U of the next chunk
+// are issued while the chain runs, P S after it.
+//
+// Products on tcgen05 (kind::f16, fp32 accumulators in TMEM): M', Y, P, X are
+// K-major fp16 A operands copied from the workspace slot unchanged; S^T (fp16)
+// and U^T (an fp16 pair u = u_hi + u_lo, 22 significant bits) are K-major B
+// operands written by the elementwise warps.  The fp32 state stays in registers
+// (16 entries per thread); only its fp16 image is an operand.
+//
+// Work split: 640 threads.  One thread of the last warpgroup issues the bulk
+// copies, the v/w TMA loads and all MMAs; a second one issues the TMA stores of
+// O.  Warp w < 16 owns TMEM lane quarter w % 4 (d_k rows of the state, token
+// rows of O) and 16 columns 16 (w / 4) .. of the d_v tile.  Warps signal the MMA
+// thread through mbarriers with one arrival per warp; every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "gdr2.h"
+#include "gdr2_internal.cuh"
+#include "gdr2_tc.cuh"
+
+namespace gdr2 {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = kPrepC;
+constexpr int kDK = kPrepDK;
+constexpr int kDVT = 64;
+constexpr int kSimt = 512;
+constexpr int kThreads = kSimt + 128;
+constexpr int kRegsSimt = 104, kRegsMma = 56;
+static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96, "register pool");
+
+// ---- shared memory (bytes from a 1024-aligned base) ------------------------------
+// two slot buffers, each the chunk's images copied unchanged: M' (32 KB), P (16 KB),
+// Y (16 KB), X (8 KB)
+constexpr uint32_t kSlotBuf = 73728;
+constexpr uint32_t kBM = kSlotM, kBY = kSlotY, kBP = kSlotP, kBX = kSlotX;   // offsets within a slot buffer
+constexpr uint32_t kSB = 2 * kSlotBuf;   // two S^T operands, fp16 K-major [64 rows][128 K] (16 KB each)
+constexpr uint32_t kUB = kSB + 32768;    // two [U_hi^T | U_lo^T] operands, fp16 K-major [64][64] x 2 (16 KB each)
+constexpr uint32_t kO = kUB + 32768;     // O tile for the TMA store (16 KB)
+constexpr uint32_t kMisc = kO + 16384;
+enum : uint32_t {
+    kBarSlot0 = 0, kBarSlot1,                          // slot copies
+    kSRdy, kURdy0, kURdy1, kORead0, kORead1, kOFull,   // elementwise warps -> issuing threads
+    kOFree,                                            // O tile stored
+    kDS0, kDS1, kDO0, kDO1,                            // MMA commits
+    kNumBars
+};
+constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
+constexpr uint32_t kAbort = kTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kMisc + 256;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+static_assert(kAbort + 4 <= kSmemBytes, "misc area");
+static_assert(kSmemAlloc <= 232448, "shared memory");
+constexpr uint32_t kSlotCopyBytes = kSlotGam;   // M', Y, P, X (gamma is read from global memory)
+static_assert(kSlotCopyBytes <= kSlotBuf && (kSlotCopyBytes & 15u) == 0, "slot copy");
+
+// ---- TMEM columns ------------------------------------------------------------------
+// Products that accumulate into one TMEM accumulator run one after another (each
+// waits for the previous one), so every product is split over two accumulators
+// (K steps alternating, or u_hi / u_lo) whose instructions interleave; the read-out
+// adds the two halves.  Per chunk buffer b: S' - gamma S in columns 128 b + [0, 128),
+// O (M = 64) in 256 + 128 b + [0, 128).
+constexpr uint32_t kTmDS = 0;
+constexpr uint32_t kTmDO = 256;
+constexpr int kTmCols = 512;
+
+struct ChainParams {
+    const uint8_t* slots;
+    const float* S0;
+    const __nv_bfloat16 *v, *w;
+    void* o;
+    float* ST;
+    int* err;
+    const int* cu;           // packed sequences: [N + 1] token offsets, or null
+    const int* chunk_base;   // packed sequences: [N + 1] first global chunk of each sequence
+    int T, H, dv, nch, total;
+    int out_bf16;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
+    const int bh = static_cast<int>(blockIdx.x);
+    const int h = bh % prm.H, seq = bh / prm.H;
+    const int j0 = static_cast<int>(blockIdx.y) * kDVT;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));
+    auto bar = [&](uint32_t i) { return base + kMisc + 8u * i; };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + kAbort);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;
+    // this sequence's token rows and its first global chunk (offsets clamped as in prep2)
+    int T, tok0;
+    int64_t chunk0;
+    if (prm.cu) {
+        const int a = min(max(prm.cu[seq], 0), prm.total);
+        const int e = min(max(prm.cu[seq + 1], a), prm.total);
+        tok0 = a;
+        T = e - a;
+        chunk0 = prm.chunk_base[seq];
+    } else {
+        T = prm.T;
+        tok0 = seq * T;
+        chunk0 = static_cast<int64_t>(seq) * prm.nch;
+    }
+    const int n = (T + kC - 1) / kC;
+    auto slot_of = [&](int c) {
+        return prm.slots + ((chunk0 + c) * prm.H + h) * static_cast<int64_t>(kSlot2Bytes);
+    };
+
+    if (tid == 0) {
+        for (uint32_t i = 0; i < kNumBars; ++i) {
+            // one arrival per warp; a barrier never runs more than one phase ahead of its
+            // waiter (U of chunk c arrives on kURdy0 + c % 2, two chunks ahead of its use)
+            const bool per_warp = i == kSRdy || i == kURdy0 || i == kURdy1 || i == kORead0 || i == kORead1 ||
+                                  i == kOFull;
+            mbar_init(bar(i), per_warp ? 16u : 1u);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_async_smem();
+    }
+    if (warp == 0) tmem_alloc<kTmCols>(base + kTmemSlot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= kSimt / 32) {
+        // ================= copies / MMAs / O stores ===================================
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
+        if (warp == kSimt / 32 && lane == 0) {
+            // Per chunk c (buffer b = c & 1): the chain products of c as soon as its S^T is
+            // written; then Y U and X U of chunk c + 1 (the first products in its
+            // accumulators); then, once chunk c's products are done, the copy of chunk
+            // c + 2's slot into buffer b.  Counters give each wait's parity.  Descriptors
+            // are formed once; a K step adds its byte offset / 16 to the start address
+            // field (every operand lies below 256 KB, so the field never carries).
+            uint32_t c_slot0 = 0, c_slot1 = 0, c_s = 0, c_u0 = 0, c_u1 = 0, c_do0 = 0, c_do1 = 0, c_or0 = 0, c_or1 = 0;
+            uint32_t iss_slot0 = 0, iss_slot1 = 0;   // copies issued per buffer (at most one in flight)
+            auto wait = [&](uint32_t b, uint32_t& cnt) {
+                const bool ok = mbar_wait_ab(bar(b), cnt & 1u, abort_flag);
+                ++cnt;
+                return ok;
+            };
+            auto load_slot = [&](int c) {
+                const uint32_t b = static_cast<uint32_t>(c & 1);
+                mbar_expect_tx(bar(kBarSlot0 + b), kSlotCopyBytes);
+                bulk_g2s(base + kSlotBuf * b, slot_of(c), kSlotCopyBytes, bar(kBarSlot0 + b));
+                if (b) ++iss_slot1; else ++iss_slot0;
+            };
+            // every operand is K-major: a K step of 16 elements is 32 bytes within a 128-byte
+            // row; M' (K = 128) has its two K blocks 16 KB apart, P and S^T 8 KB apart
+            const uint64_t dM0 = umma_desc2(base + kBM, 16u, 1024u), dP0 = umma_desc2(base + kBP, 16u, 1024u);
+            const uint64_t dY0 = umma_desc2(base + kBY, 16u, 1024u), dX0 = umma_desc2(base + kBX, 16u, 1024u);
+            const uint64_t dS0 = umma_desc2(base + kSB, 16u, 1024u), dU0 = umma_desc2(base + kUB, 16u, 1024u);
+            constexpr uint32_t idS = idesc_f16x(128, 64, 0, 0, 0), idO = idesc_f16x(64, 64, 0, 0, 0);
+            // Y U and X U of chunk c into accumulator buffer c & 1 (the first products
+            // there): [U_hi^T; U_lo^T] is one 128-row B operand, so each product writes
+            // u_hi terms to the first 64 columns of its accumulator pair and u_lo terms to
+            // the second
+            constexpr uint32_t idSU = idesc_f16x(128, 128, 0, 0, 0), idOU = idesc_f16x(64, 128, 0, 0, 0);
+            auto issue_u = [&](int c) {
+                const uint32_t b = static_cast<uint32_t>(c & 1);
+                const uint64_t dY = dY0 + (kSlotBuf >> 4) * b, dX = dX0 + (kSlotBuf >> 4) * b;
+                const uint64_t dU = dU0 + (16384u >> 4) * b;
+                const uint32_t tS = tmem + kTmDS + 128u * b, tO = tmem + kTmDO + 128u * b;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t acc = k > 0 ? 1u : 0u;
+                    mma_ss_f16(tS, dY + 2u * k, dU + 2u * k, idSU, acc);
+                    mma_ss_f16(tO, dX + 2u * k, dU + 2u * k, idOU, acc);
+                }
+            };
+            bool ok = true;   // an empty sequence issues nothing
+            if (n > 0) {
+                if (n > 2) bulk_prefetch_l2(slot_of(2), kSlotCopyBytes);
+                load_slot(0);
+                if (n > 1) load_slot(1);
+                ok = wait(kURdy0, c_u0) && wait(kBarSlot0, c_slot0);
+                if (ok) issue_u(0);
+            }
+#pragma unroll 1
+            for (int c = 0; c < n && ok; ++c) {
+                const uint32_t b = static_cast<uint32_t>(c & 1);
+                const uint64_t dM = dM0 + (kSlotBuf >> 4) * b, dP = dP0 + (kSlotBuf >> 4) * b;
+                const uint64_t dS = dS0 + (16384u >> 4) * b;
+                // the slot of chunk c + 3 into L2, so that its copy two chunks later hits L2
+                if (c + 3 < n) bulk_prefetch_l2(slot_of(c + 3), kSlotCopyBytes);
+                // ---- chain: S' - gamma S += M' S;  O += P S ------------------------------
+                if (!(ok = wait(kSRdy, c_s))) break;
+                tc_fence_after();
+                {
+                    // K steps 0-3 (key channels 0-63) into the first accumulator of each
+                    // pair, 4-7 into the second
+                    const uint32_t tS = tmem + kTmDS + 128u * b, tO = tmem + kTmDO + 128u * b;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        mma_ss_f16(tS, dM + 2u * k, dS + 2u * k, idS, 1u);
+                        mma_ss_f16(tS + 64u, dM + (16384u >> 4) + 2u * k, dS + (8192u >> 4) + 2u * k, idS, 1u);
+                    }
+                    mma_commit(bar(kDS0 + b));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        mma_ss_f16(tO, dP + 2u * k, dS + 2u * k, idO, 1u);
+                        mma_ss_f16(tO + 64u, dP + (8192u >> 4) + 2u * k, dS + (8192u >> 4) + 2u * k, idO, 1u);
+                    }
+                    mma_commit(bar(kDO0 + b));
+                }
+                if (c + 1 < n) {
+                    // ---- next chunk's Y U and X U (its accumulators were read out) --------
+                    if (c >= 1 && !(ok = b ? wait(kORead0, c_or0) : wait(kORead1, c_or1))) break;
+                    if (!(ok = b ? (wait(kURdy0, c_u0) && wait(kBarSlot0, c_slot0))
+                                 : (wait(kURdy1, c_u1) && wait(kBarSlot1, c_slot1))))
+                        break;
+                    issue_u(c + 1);
+                }
+                if (c + 2 < n) {
+                    // ---- chunk c's products done: its slot buffer takes chunk c + 2 --------
+                    if (!(ok = b ? wait(kDO1, c_do1) : wait(kDO0, c_do0))) break;
+                    load_slot(c + 2);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicExch(prm.err, kDevTimeout);
+            }
+            // copies still in flight land before the CTA exits (bounded waits; the last
+            // copy of each buffer completes the phase of parity (issued - 1) & 1)
+            if (iss_slot0 > c_slot0) mbar_wait(bar(kBarSlot0), (iss_slot0 - 1u) & 1u);
+            if (iss_slot1 > c_slot1) mbar_wait(bar(kBarSlot1), (iss_slot1 - 1u) & 1u);
+        } else if (warp == kSimt / 32 + 1 && lane == 0) {
+            // O tile stores: one per chunk that lies wholly inside the sequence
+            uint32_t ph_full = 0;
+            mbar_arrive(bar(kOFree));   // the tile starts free
+#pragma unroll 1
+            for (int c = 0; (c + 1) * kC <= T && c < n; ++c) {
+                if (!mbar_wait_ab(bar(kOFull), ph_full, abort_flag)) break;
+                ph_full ^= 1u;
+                const int row = tok0 + c * kC;
+                tma_store_4d(&tm_o, base + kO, j0, h, row, 0);
+                if (!prm.out_bf16) tma_store_4d(&tm_o, base + kO + 8192u, j0 + 32, h, row, 0);
+                bulk_commit();
+                bulk_wait_read();
+                mbar_arrive(bar(kOFree));
+            }
+            bulk_wait_all();
+        }
+        __syncwarp();
+    } else {
+        // ================= 16 elementwise / accumulator warps ====================
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSimt));
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int R = warp >> 2;                 // column block: d_v columns 16R .. 16R + 15 of the tile
+        const int j = 32 * quarter + lane;       // state row (key channel)
+        const bool obf16 = prm.out_bf16;
+        bool failed = false;
+        uint32_t c_ds0 = 0, c_ds1 = 0, c_do0 = 0, c_do1 = 0, c_of = 0;
+        auto wait = [&](uint32_t b, uint32_t& cnt) {
+            const bool ok = mbar_wait_ab(bar(b), cnt & 1u, abort_flag);
+            ++cnt;
+            tc_fence_after();
+            return ok;
+        };
+        auto arrive = [&](uint32_t b) {
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(b));
+        };
+        // S^T operand (fp16, K-major [64 rows n][128 K]): element (n = 16R + i, k = j); pairs
+        // (j, j ^ 1) go to one 4-byte word, even lanes write even rows, odd lanes odd rows
+        auto put_st = [&](uint32_t buf, const float (&S)[16]) {
+            const bool odd = lane & 1;
+            uint8_t* img = sgen + kSB + 16384u * buf;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float x = __shfl_xor_sync(0xffffffffu, odd ? S[2 * e] : S[2 * e + 1], 1);
+                const uint32_t w = odd ? pack_h2(x, S[2 * e + 1]) : pack_h2(S[2 * e], x);
+                const uint32_t row = static_cast<uint32_t>(16 * R + 2 * e + (odd ? 1 : 0));
+                *reinterpret_cast<uint32_t*>(img + k_off16(8192u, row, static_cast<uint32_t>(j & ~1))) = w;
+            }
+        };
+        // v, w of chunk c for d_v column un, tokens 8 ug .. 8 ug + 7 (raw bf16 bits; tokens past
+        // the sequence end read as 0), fetched a chunk before they are used.  The loaded
+        // values stay unpacked until put_u, so the loads overlap the rest of the chunk.
+        const int un = tid & 63, ug = tid >> 6;
+        struct VW {
+            uint32_t v[8], w[8];   // raw bf16 bits, zero-extended by the load itself
+        };
+        auto fetch_vw = [&](int c, VW& x) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = min(c * kC + 8 * ug + e, T - 1);   // rows past the end: masked in put_u
+                const int64_t off = (static_cast<int64_t>(tok0 + t) * prm.H + h) * prm.dv + j0 + un;
+                x.v[e] = __ldg(reinterpret_cast<const unsigned short*>(prm.v) + off);
+                x.w[e] = __ldg(reinterpret_cast<const unsigned short*>(prm.w) + off);
+            }
+        };
+        // U^T of chunk c (fp16 pair u = u_hi + u_lo) into buffer c & 1: row un, tokens 8 ug ..
+        auto put_u = [&](int c, const VW& x) {
+            const int tvalid = T - c * kC - 8 * ug;   // tokens past the sequence end give U = 0
+            uint4 hk, lk;
+            __half2* hh = reinterpret_cast<__half2*>(&hk);
+            __half2* lh = reinterpret_cast<__half2*>(&lk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float u0 = 2 * e < tvalid ? __uint_as_float(x.v[2 * e] << 16) * __uint_as_float(x.w[2 * e] << 16) : 0.f;
+                const float u1 = 2 * e + 1 < tvalid
+                                     ? __uint_as_float(x.v[2 * e + 1] << 16) * __uint_as_float(x.w[2 * e + 1] << 16)
+                                     : 0.f;
+                const __half2 h2 = __floats2half2_rn(u0, u1);
+                const float2 hf = __half22float2(h2);
+                hh[e] = h2;
+                lh[e] = __floats2half2_rn(u0 - hf.x, u1 - hf.y);
+            }
+            uint8_t* ub = sgen + kUB + 16384u * static_cast<uint32_t>(c & 1);
+            const uint32_t off = static_cast<uint32_t>(un) * 128u + ((static_cast<uint32_t>(ug) ^ (static_cast<uint32_t>(un) & 7u)) << 4);
+            *reinterpret_cast<uint4*>(ub + off) = hk;
+            *reinterpret_cast<uint4*>(ub + 8192u + off) = lk;
+        };
+
+        float S[16];
+        {
+            const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R : nullptr;
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4) {
+                const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[jj] = x.x; S[jj + 1] = x.y; S[jj + 2] = x.z; S[jj + 3] = x.w;
+            }
+        }
+        // gamma of the next chunk, read from its slot one chunk ahead
+        float gam_next = n > 0 ? __ldg(reinterpret_cast<const float*>(slot_of(0) + kSlotGam) + j) : 1.f;
+        VW vpre;   // v, w of chunk c + 2
+        if (n > 0) {
+            put_st(0, S);
+            arrive(kSRdy);
+            fetch_vw(0, vpre);
+            put_u(0, vpre);
+            arrive(kURdy0);
+            if (n > 1) {
+                fetch_vw(1, vpre);
+                put_u(1, vpre);
+                arrive(kURdy1);
+            }
+            if (n > 2) fetch_vw(2, vpre);
+        }
+#pragma unroll 1
+        for (int c = 0; c < n && !failed; ++c) {
+            const uint32_t b = static_cast<uint32_t>(c & 1);
+            const int tc = c * kC;
+            // ---- chain: S <- gamma S + (M' S + Y U); S^T operand of the next chunk ------------
+            const float gam = gam_next;
+            if (c + 1 < n) gam_next = __ldg(reinterpret_cast<const float*>(slot_of(c + 1) + kSlotGam) + j);
+            if (!(b ? wait(kDS1, c_ds1) : wait(kDS0, c_ds0))) { failed = true; break; }
+            {
+                float v[16];
+                tmem_ld16_pair(tmem + lane_base + kTmDS + 128u * b + static_cast<uint32_t>(16 * R), v);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(gam, S[jj], v[jj]);
+            }
+            if (c + 1 < n) {
+                // the other S^T buffer was read by chunk c - 1's products, which completed
+                // before that chunk's O was read out
+                put_st(b ^ 1u, S);
+                arrive(kSRdy);
+            }
+            if (c + 2 < n) {
+                // ---- U^T of chunk c + 2 into the buffer chunk c's products have read ----
+                put_u(c + 2, vpre);
+                arrive(kURdy0 + b);
+                if (c + 3 < n) fetch_vw(c + 3, vpre);
+            }
+            // ---- O -> global ----------------------------------------------------------------
+            if (!(b ? wait(kDO1, c_do1) : wait(kDO0, c_do0))) { failed = true; break; }
+            {
+                float v[16];
+                tmem_ld16_pair(tmem + lane_base + kTmDO + 128u * b + static_cast<uint32_t>(16 * R), v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kORead0 + b));   // the accumulator may take chunk c + 2
+                const int r = 16 * quarter + (lane & 15);          // M = 64: token row r at lane 32 (r / 16) + r % 16
+                const bool active = lane < 16;
+                if (tc + kC <= T) {
+                    if (!wait(kOFree, c_of)) { failed = true; break; }
+                    if (active) {
+                        if (obf16) {
+                            uint4 pk[2];
+                            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                            for (int jj = 0; jj < 16; jj += 2) {
+                                __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                                pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
+                            }
+#pragma unroll
+                            for (int q = 0; q < 2; ++q)
+                                *reinterpret_cast<uint4*>(sgen + kO + r * 128 + ((((2 * R + q) ^ (r & 7)) & 7) << 4)) = pk[q];
+                        } else {
+                            const uint32_t tb = kO + static_cast<uint32_t>(R >> 1) * 8192u + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<float4*>(sgen + tb + ((((4 * (R & 1) + q) ^ (r & 7)) & 7) << 4)) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        }
+                    }
+                    arrive(kOFull);
+                } else if (active && tc + r < T) {   // the sequence's last, partial chunk: row by row
+                    const int64_t off = ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                    if (obf16) {
+                        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
+                        uint4 pk[2];
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 2) {
+                            __nv_bfloat162 x2 = __floats2bfloat162_rn(v[jj], v[jj + 1]);
+                            pw[jj / 2] = *reinterpret_cast<uint32_t*>(&x2);
+                        }
+                        reinterpret_cast<uint4*>(op)[0] = pk[0];
+                        reinterpret_cast<uint4*>(op)[1] = pk[1];
+                    } else {
+                        float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 4)
+                            op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                    }
+                }
+            }
+        }
+        if (failed) {
+            *abort_flag = 1;
+            if (lane == 0) atomicExch(prm.err, kDevTimeout);
+        } else if (prm.ST) {
+            float* st = prm.ST + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R;
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<kTmCols>(tmem);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Packed [1, total, H, dv] token rows (bf16 or fp32) as a 4-D map (dv, H, total, 1);
+// box (128 bytes of d_v, 1, 64 tokens, 1) with the 128-byte swizzle.  Loads past
+// the tensor read zeros; stores past it are dropped.
+bool make_row_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int64_t dv, bool f32) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t esz = f32 ? 4 : 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(total), 1};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(dv) * esz, static_cast<cuuint64_t>(H * dv) * esz,
+                                   static_cast<cuuint64_t>(total * H * dv) * esz};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), 1, 64, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err) {
+    if (a.cu && !chunk_base) return GDR2_ERR_ARG;
+    const int64_t total = a.cu ? a.total : a.B * a.T;
+    CUtensorMap mo;
+    if (!make_row_map(&mo, a.o, total, a.H, a.dv, a.out_dtype != GDR2_BF16)) return GDR2_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemAlloc));
+    });
+    if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
+    ChainParams prm{slots, a.S0, static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
+                    a.o, a.ST, err, a.cu, chunk_base, static_cast<int>(a.T), static_cast<int>(a.H),
+                    static_cast<int>(a.dv), static_cast<int>((a.T + kC - 1) / kC), static_cast<int>(total),
+                    a.out_dtype == GDR2_BF16 ? 1 : 0};
+    const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
+    chain_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mo, prm);
+    return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
+}  // namespace gdr2

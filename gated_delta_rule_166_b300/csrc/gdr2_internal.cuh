@@ -121,4 +121,24 @@ int launch_scan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream);
 int launch_correct(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream, int* err);
 bool two_kernel_supports(const ForwardArgs& a);
 
+// ---- two-kernel chunked prefill in affine form (fixed-length bf16, d_k = 128) ----
+// prep2 writes, for every (chunk, head), the maps of the chunk's state update
+//     S' = diag(gamma) S + M' S + Y U,      O = P S + X U      (U = w * v)
+// as fp16 images that the chain kernel copies to shared memory unchanged:
+// K-major (rows = M index), 128-byte swizzle, 64-element K blocks.
+constexpr uint32_t kSlotM = 0;         // M' [d_k out (M)][d_k in (K)]: 2 K blocks x 128 rows x 128 B
+constexpr uint32_t kSlotY = 32768;     // Y  [d_k (M)][token (K)]:       1 K block x 128 rows x 128 B
+constexpr uint32_t kSlotP = 49152;     // P  [token (M)][d_k (K)]:       2 K blocks x 64 rows x 128 B
+constexpr uint32_t kSlotX = 65536;     // X  [token (M)][token (K)]:     1 K block x 64 rows x 128 B
+constexpr uint32_t kSlotGam = 73728;   // gamma = e^{G_C} [d_k] fp32
+constexpr size_t kSlot2Bytes = 74240;
+// Slot index = (global chunk) * H + head; chunk_base as for the first form.
+int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, int64_t chunks, cudaStream_t stream,
+                 int* err);
+// One CTA per (sequence * head, 64-column d_v tile): the chunk-to-chunk chain over the
+// slots of prep2, o and S_T.  Packed sequences pass the chunk_base that prep2 used.
+int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err);
+// chunk_base[s] (s = 0 .. N) of packed sequences, offsets clamped to [0, total].
+int launch_chunk_base(const int* cu, int64_t N, int64_t total, int* chunk_base, cudaStream_t stream);
+
 }  // namespace gdr2

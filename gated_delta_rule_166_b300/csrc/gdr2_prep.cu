@@ -602,6 +602,11 @@ bool two_kernel_supports(const ForwardArgs& a) {
            total < (1ll << 31) && a.B * a.H < (1ll << 31) && a.H <= 65535 && get_encode() != nullptr;
 }
 
+int launch_chunk_base(const int* cu, int64_t N, int64_t total, int* chunk_base, cudaStream_t stream) {
+    chunk_base_kernel<<<1, 1024, 0, stream>>>(cu, static_cast<int>(N), static_cast<int>(total), chunk_base);
+    return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
 int64_t prep_chunk_bound(const ForwardArgs& a) {
     if (!a.cu) return a.B * ((a.T + kC - 1) / kC);
     return (a.total + kC - 1) / kC + a.B;
@@ -646,11 +651,7 @@ int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0
                                         static_cast<int>(kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
-    if (a.cu) {
-        chunk_base_kernel<<<1, 1024, 0, stream>>>(a.cu, static_cast<int>(a.B), static_cast<int>(total),
-                                                  s.chunk_base);
-        if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
-    }
+    if (a.cu && launch_chunk_base(a.cu, a.B, total, s.chunk_base, stream) != GDR2_OK) return GDR2_ERR_CUDA;
     const int64_t nitems = chunks * a.H;
     if (nitems >= (1ll << 31)) return GDR2_ERR_SHAPE;
     int dev = 0, sms = 0;

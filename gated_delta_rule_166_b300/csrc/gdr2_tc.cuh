@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -240,6 +241,111 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
 }
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+}  // namespace tc
+}  // namespace gdr2
+
+// ---- helpers of the two-kernel prefill in affine form (prep2 / chain kernels) ----
+namespace gdr2 {
+namespace tc {
+
+// Shared-memory matrix descriptor with explicit leading / stride byte offsets,
+// 128-byte swizzle.  K-major operands: sbo = 1024 (8-row groups), lbo unused.
+// MN-major operands: lbo = byte stride between 64-element MN blocks, sbo = 1024
+// (8-row groups along K).
+__device__ __forceinline__ uint64_t umma_desc2(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16, fp32 accumulate; ab_bf16 selects bf16 (else
+// fp16) for both operands; a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t idesc_f16x(uint32_t M, uint32_t N, uint32_t ab_bf16, uint32_t a_mn,
+                                                  uint32_t b_mn) {
+    return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+           ((M >> 4) << 24);
+}
+// D (TMEM) [+]= A (shared memory) x B (shared memory), kind::f16; K = 16 per call.
+__device__ __forceinline__ void mma_ss_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 32 lanes x 32 bit, 32 consecutive columns per thread (no wait).
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+// 32 lanes x 32 bit, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+// Bulk copy of `bytes` (multiple of 16) from global memory to shared memory,
+// completing on the mbarrier `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+// Sum of two 16-column accumulator pieces `off` columns apart (32 lanes x 32 bit).
+__device__ __forceinline__ void tmem_ld16_sum(uint32_t taddr, uint32_t off, float (&v)[16]) {
+    uint32_t a[16], b[16];
+    tmem_ld16_nw(taddr, a);
+    tmem_ld16_nw(taddr + off, b);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]) + __uint_as_float(b[i]);
+}
+// Bulk copy of `bytes` (multiple of 16) from shared memory to global memory
+// (bulk-group completion: commit, then wait_group.read before reusing the source).
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+// Hint: bring `bytes` (multiple of 16) of global memory into L2 ahead of a later copy.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+// Two fp32 values as an fp16x2 word (round to nearest even); lo at the lower address.
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// Byte offset of element (k, m) of an MN-major 128B-swizzled fp16 image whose
+// 64-element MN blocks are `blk` bytes apart (rows of 128 B along K).
+__device__ __forceinline__ uint32_t mn_off(uint32_t blk, uint32_t k, uint32_t m) {
+    return (m >> 6) * blk + k * 128u + (((((m & 63u) >> 3) ^ (k & 7u))) << 4) + ((m & 7u) << 1);
+}
+// Byte offset of element (row, k) of a K-major 128B-swizzled fp16 image whose
+// 64-element K blocks are `kblk` bytes apart.
+__device__ __forceinline__ uint32_t k_off16(uint32_t kblk, uint32_t row, uint32_t k) {
+    return (k >> 6) * kblk + row * 128u + (((((k & 63u) >> 3) ^ (row & 7u))) << 4) + ((k & 7u) << 1);
 }
 
 }  // namespace tc
