@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     gdr2_forward_noalloc,
     gdr2_forward_varlen,
     gdr2_release_workspace,
+    gdr2_set_wait_limit,
     gdr2_version,
     gdr2_workspace_stats,
 )

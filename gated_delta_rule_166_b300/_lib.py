@@ -66,6 +66,8 @@ def lib():
         L.gdr2_workspace_stats.restype = ci
         L.gdr2_release_workspace.argtypes = []
         L.gdr2_release_workspace.restype = ci
+        L.gdr2_set_wait_limit.argtypes = [i64]
+        L.gdr2_set_wait_limit.restype = i64
         _lib = L
     return _lib
 
@@ -349,3 +351,9 @@ def gdr2_release_workspace() -> None:
     st = lib().gdr2_release_workspace()
     if st != 0:
         raise GDR2Error(st, "gdr2_release_workspace")
+
+
+def gdr2_set_wait_limit(cycles: int) -> int:
+    """Testing hook: the chain kernel's handshake waits give up after ``cycles`` SM
+    cycles (<= 0: the default of about 2 s).  Returns the previous limit (0 = default)."""
+    return lib().gdr2_set_wait_limit(int(cycles))

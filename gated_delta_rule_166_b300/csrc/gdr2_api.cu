@@ -503,6 +503,10 @@ extern "C" int gdr2_workspace_stats(int64_t* reserved, int64_t* used_high, int r
     return GDR2_OK;
 }
 
+extern "C" int64_t gdr2_set_wait_limit(int64_t cycles) {
+    return gdr2::set_chain_wait_limit(cycles > 0 ? cycles : 0);
+}
+
 extern "C" int gdr2_release_workspace(void) {
     cudaMemPool_t pool = nullptr;
     const int st = workspace_pool(&pool);

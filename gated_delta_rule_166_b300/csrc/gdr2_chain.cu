@@ -17,7 +17,8 @@
 // (16 entries per thread); only its fp16 image is an operand.
 //
 // Work split: 640 threads.  One thread of the last warpgroup issues the bulk
-// copies, the v/w TMA loads and all MMAs; a second one issues the TMA stores of
+// copies of the slots and all MMAs (v and w are plain loads of the elementwise
+// warps, one chunk ahead); a second one issues the TMA stores of
 // O.  Warp w < 16 owns TMEM lane quarter w % 4 (d_k rows of the state, token
 // rows of O) and 16 columns 16 (w / 4) .. of the d_v tile.  Warps signal the MMA
 // thread through mbarriers with one arrival per warp; every wait is bounded.
@@ -26,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gdr2.h"
@@ -59,6 +61,7 @@ enum : uint32_t {
     kSRdy, kURdy0, kURdy1, kORead0, kORead1, kOFull,   // elementwise warps -> issuing threads
     kOFree,                                            // O tile stored
     kDS0, kDS1, kDO0, kDO1,                            // MMA commits
+    kDrain,                                            // every product issued has completed
     kNumBars
 };
 constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
@@ -91,6 +94,7 @@ struct ChainParams {
     const int* chunk_base;   // packed sequences: [N + 1] first global chunk of each sequence
     int T, H, dv, nch, total;
     int out_bf16;
+    long long wait_cycles;   // limit of each handshake wait (copy drains keep the default)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -158,9 +162,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
             // field (every operand lies below 256 KB, so the field never carries).
             uint32_t c_slot0 = 0, c_slot1 = 0, c_s = 0, c_u0 = 0, c_u1 = 0, c_do0 = 0, c_do1 = 0, c_or0 = 0, c_or1 = 0;
             uint32_t iss_slot0 = 0, iss_slot1 = 0;   // copies issued per buffer (at most one in flight)
+            // a wait that gave up does not count the phase as seen, so that the copy drain
+            // below still waits for a copy whose completion was not observed
             auto wait = [&](uint32_t b, uint32_t& cnt) {
-                const bool ok = mbar_wait_ab(bar(b), cnt & 1u, abort_flag);
-                ++cnt;
+                const bool ok = mbar_wait_ab(bar(b), cnt & 1u, abort_flag, prm.wait_cycles);
+                if (ok) ++cnt;
                 return ok;
             };
             auto load_slot = [&](int c) {
@@ -194,12 +200,16 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                 }
             };
             bool ok = true;   // an empty sequence issues nothing
+            bool issued = false;
             if (n > 0) {
                 if (n > 2) bulk_prefetch_l2(slot_of(2), kSlotCopyBytes);
                 load_slot(0);
                 if (n > 1) load_slot(1);
                 ok = wait(kURdy0, c_u0) && wait(kBarSlot0, c_slot0);
-                if (ok) issue_u(0);
+                if (ok) {
+                    issue_u(0);
+                    issued = true;
+                }
             }
 #pragma unroll 1
             for (int c = 0; c < n && ok; ++c) {
@@ -250,13 +260,19 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
             // copy of each buffer completes the phase of parity (issued - 1) & 1)
             if (iss_slot0 > c_slot0) mbar_wait(bar(kBarSlot0), (iss_slot0 - 1u) & 1u);
             if (iss_slot1 > c_slot1) mbar_wait(bar(kBarSlot1), (iss_slot1 - 1u) & 1u);
+            // and every product issued completes before the TMEM is freed (after an abort
+            // some may still be running)
+            if (issued) {
+                mma_commit(bar(kDrain));
+                mbar_wait(bar(kDrain), 0u);
+            }
         } else if (warp == kSimt / 32 + 1 && lane == 0) {
             // O tile stores: one per chunk that lies wholly inside the sequence
             uint32_t ph_full = 0;
             mbar_arrive(bar(kOFree));   // the tile starts free
 #pragma unroll 1
             for (int c = 0; (c + 1) * kC <= T && c < n; ++c) {
-                if (!mbar_wait_ab(bar(kOFull), ph_full, abort_flag)) break;
+                if (!mbar_wait_ab(bar(kOFull), ph_full, abort_flag, prm.wait_cycles)) break;
                 ph_full ^= 1u;
                 const int row = tok0 + c * kC;
                 tma_store_4d(&tm_o, base + kO, j0, h, row, 0);
@@ -278,7 +294,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         bool failed = false;
         uint32_t c_ds0 = 0, c_ds1 = 0, c_do0 = 0, c_do1 = 0, c_of = 0;
         auto wait = [&](uint32_t b, uint32_t& cnt) {
-            const bool ok = mbar_wait_ab(bar(b), cnt & 1u, abort_flag);
+            const bool ok = mbar_wait_ab(bar(b), cnt & 1u, abort_flag, prm.wait_cycles);
             ++cnt;
             tc_fence_after();
             return ok;
@@ -500,6 +516,12 @@ bool make_row_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, int
 
 }  // namespace
 
+namespace {
+std::atomic<int64_t> g_wait_limit{0};
+}  // namespace
+
+int64_t set_chain_wait_limit(int64_t cycles) { return g_wait_limit.exchange(cycles); }
+
 int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err) {
     if (a.cu && !chunk_base) return GDR2_ERR_ARG;
     const int64_t total = a.cu ? a.total : a.B * a.T;
@@ -515,7 +537,9 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
     ChainParams prm{slots, a.S0, static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
                     a.o, a.ST, err, a.cu, chunk_base, static_cast<int>(a.T), static_cast<int>(a.H),
                     static_cast<int>(a.dv), static_cast<int>((a.T + kC - 1) / kC), static_cast<int>(total),
-                    a.out_dtype == GDR2_BF16 ? 1 : 0};
+                    a.out_dtype == GDR2_BF16 ? 1 : 0, 0};
+    const int64_t lim = g_wait_limit.load();
+    prm.wait_cycles = lim > 0 ? static_cast<long long>(lim) : kWaitCycles;
     const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
     chain_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mo, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;

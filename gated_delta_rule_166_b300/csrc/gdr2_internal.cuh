@@ -138,6 +138,9 @@ int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, in
 // One CTA per (sequence * head, 64-column d_v tile): the chunk-to-chunk chain over the
 // slots of prep2, o and S_T.  Packed sequences pass the chunk_base that prep2 used.
 int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err);
+// Limit of the chain kernel's handshake waits for later launches (0: the default);
+// returns the previous value.
+int64_t set_chain_wait_limit(int64_t cycles);
 // chunk_base[s] (s = 0 .. N) of packed sequences, offsets clamped to [0, total].
 int launch_chunk_base(const int* cu, int64_t N, int64_t total, int* chunk_base, cudaStream_t stream);
 

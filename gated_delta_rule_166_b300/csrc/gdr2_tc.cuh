@@ -61,13 +61,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 // Bounded wait that also gives up as soon as another thread of the CTA has
-// raised `abort`; a wait that times out raises it.
-__device__ __forceinline__ bool mbar_wait_ab(uint32_t bar, uint32_t parity, volatile int* abort) {
+// raised `abort`; a wait that times out (after `limit` cycles) raises it.
+__device__ __forceinline__ bool mbar_wait_ab(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             long long limit = kWaitCycles) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try(bar, parity)) {
         if (*abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             return false;
         }

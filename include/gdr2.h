@@ -315,6 +315,19 @@ int gdr2_workspace_stats(int64_t* reserved, int64_t* used_high, int reset);
  */
 int gdr2_release_workspace(void);
 
+/*
+ * gdr2_set_wait_limit -- testing hook.  Every handshake wait inside the prefill's
+ * chain kernel (between its elementwise warps and its copy / tensor-core
+ * thread) gives up after `cycles` SM clock cycles instead of about 4e9
+ * (about 2 s); cycles <= 0 restores that default.  A wait that gives up makes
+ * the kernel stop: it lets its own copies in flight land and its products
+ * complete (with the default limit), frees its tensor memory, records
+ * GDR2_ERR_TIMEOUT for gdr2_device_status and returns; o and S_T of that call
+ * are then incomplete.  Process-wide, read at each launch; not for concurrent
+ * use with other calls.  Returns the previous limit (0 = the default).
+ */
+int64_t gdr2_set_wait_limit(int64_t cycles);
+
 /* Human-readable name of a gdr2_status value (static storage). */
 const char* gdr2_status_string(int status);
 

@@ -36,6 +36,17 @@ def test_status_strings_and_version():
     assert _lib.gdr2_version() >= 100
 
 
+def test_wait_limit_hook_swaps_and_restores():
+    """The testing hook is host state only: it returns the previous limit and
+    non-positive values mean the default (reported as 0)."""
+    prev = _lib.gdr2_set_wait_limit(1234)
+    try:
+        assert _lib.gdr2_set_wait_limit(-5) == 1234
+        assert _lib.gdr2_set_wait_limit(0) == 0
+    finally:
+        _lib.gdr2_set_wait_limit(prev)
+
+
 # fake, never-dereferenced device addresses (16-byte aligned, far apart)
 BASE = 1 << 40
 GAP = 1 << 32
