@@ -111,6 +111,67 @@ def make_prefill_inputs(B: int, T: int, H: int, dk: int, dv: int, *,
     return PrefillInputs(cast(q), cast(k), cast(v), cast(b), cast(w), cast(g), S0)
 
 
+@dataclass
+class SparseInputs:
+    """One sparse-write problem: per (batch, token, head) the K selected slot
+    indices and the key-side values at those slots; value-side tensors as in the
+    dense case; the slot memory S0 [B, H, M, dv] (fp32)."""
+    idx: torch.Tensor   # [B, T, H, K] int32
+    q: torch.Tensor     # [B, T, H, K]
+    k: torch.Tensor     # [B, T, H, K]
+    v: torch.Tensor     # [B, T, H, dv]
+    b: torch.Tensor     # [B, T, H, K]
+    w: torch.Tensor     # [B, T, H, dv]
+    log_decay: torch.Tensor   # [B, T, H, K]
+    S0: torch.Tensor    # [B, H, M, dv] fp32
+
+    @property
+    def M(self) -> int:
+        return int(self.S0.shape[2])
+
+    def tensors(self):
+        return (self.idx, self.q, self.k, self.v, self.b, self.w, self.log_decay)
+
+    def to(self, device):
+        return SparseInputs(*(t.to(device, non_blocking=True) for t in self.tensors()),
+                            self.S0.to(device, non_blocking=True))
+
+
+def make_sparse_inputs(B: int, T: int, H: int, M: int, K: int, dv: int, *,
+                       dtype=torch.bfloat16, seed: int = 0, s0_std: float = 0.02,
+                       decay_regime: str = "fast", decay_shift: float = 2.0) -> SparseInputs:
+    """Draw one sparse gated-delta-write problem over a memory of M slots.
+
+    Slot selection (a stand-in for a product-key router's top-K, which needs
+    trained keys): per (batch, token, head) a uniform start r0 in [0, M) and K - 1
+    gaps uniform in [1, G] with G = max(1, (M - 1) // K); the slots are r0 plus
+    the running sums of the gaps, mod M.  The K slots of one token are therefore
+    distinct, and consecutive tokens share slots about K^2 / M times.
+
+    Values at the selected slots follow the dense distributions: q and k
+    L2-normalised over the K entries, b = sigmoid(N), log_decay = -softplus(N +
+    shift) (or the other regimes), and w, v as in the dense case.  The slot
+    memory S0 ~ N(0, s0_std^2) stands for a learned initial memory.  Draw order:
+    slot starts, gaps, q, k, v, b, w, log_decay, S0."""
+    if K > M:
+        raise ValueError("K must not exceed M")
+    gen = torch.Generator().manual_seed(int(seed))
+    r0 = torch.randint(0, max(M, 1), (B, T, H, 1), generator=gen)
+    G = max(1, (M - 1) // max(K, 1))
+    gaps = torch.randint(1, G + 1, (B, T, H, max(K - 1, 0)), generator=gen)
+    offs = torch.cat([torch.zeros(B, T, H, 1, dtype=torch.long), torch.cumsum(gaps, dim=-1)], dim=-1)[..., :K]
+    idx = ((r0 + offs) % max(M, 1)).to(torch.int32).contiguous()
+    q = _normalise_rows(torch.randn(B, T, H, K, generator=gen))
+    k = _normalise_rows(torch.randn(B, T, H, K, generator=gen))
+    v = torch.randn(B, T, H, dv, generator=gen)
+    b = torch.sigmoid(torch.randn(B, T, H, K, generator=gen))
+    w = torch.sigmoid(torch.randn(B, T, H, dv, generator=gen))
+    g = _decay(gen, (B, T, H, K), decay_regime, decay_shift)
+    S0 = torch.randn(B, H, M, dv, generator=gen) * s0_std
+    cast = lambda t: t.to(dtype).contiguous()
+    return SparseInputs(idx, cast(q), cast(k), cast(v), cast(b), cast(w), cast(g), S0.contiguous())
+
+
 def make_decode_state(B: int, H: int, dk: int, dv: int, *, seed: int,
                       std: float = 0.02) -> torch.Tensor:
     """fp32 decode state S ~ N(0, std^2), [B, H, dk, dv]."""
@@ -154,3 +215,15 @@ def make_workload(name: str, **overrides) -> PrefillInputs:
     cfg = dict(WORKLOADS[name])
     cfg.update(overrides)
     return make_prefill_inputs(**cfg)
+
+
+# Sparse gated delta write over a slot memory: 2048 slots per head, 32 selected
+# per token, d_v = 128, 16 heads, 4K tokens, batch 4 (memory 16x the dense
+# d_k = 128 state; per-token work 1/4 of the dense update's)
+SPARSE_WORKLOAD = dict(B=4, T=4096, H=16, M=2048, K=32, dv=128, dtype=torch.bfloat16, seed=6, s0_std=0.02)
+
+
+def make_sparse_workload(**overrides) -> SparseInputs:
+    cfg = dict(SPARSE_WORKLOAD)
+    cfg.update(overrides)
+    return make_sparse_inputs(**cfg)

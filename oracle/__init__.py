@@ -17,6 +17,12 @@ Write in Linear Attention" page (section "Gated Delta Rule-2 update equation")
 with the readout ``o_t = S_t^T q_t`` after the update.  Layouts: token tensors
 ``[B, T, H, d]``, states ``[B, H, d_k, d_v]``.
 
+A third function, :func:`sparse_write`, is the gated delta write restricted
+to selected slots of a larger slot memory (the "Sparse Delta Memory" review
+page, section "3. Method & Key Results", with the routing-slot recurrence of
+the Raven summary page, section "2.1 RSM framework"): a NumPy fp64 token loop
+that gathers, updates and scatters the selected rows.
+
 Every function is pinned by the ``-m "not gpu"`` tests (closed forms, brute
 force, hand-computed worked examples, reductions to KDA / Gated DeltaNet /
 (gated) linear attention, invariants); none is "parity unpinned".
@@ -182,3 +188,61 @@ def backward(q, k, v, b, w, g, S0, do, dST=None):
         loss = loss + (S * torch.from_numpy(dST)).sum()
     grads = torch.autograd.grad(loss, leaves, allow_unused=True)
     return tuple(np.zeros(leaf.shape) if gr is None else gr.numpy() for gr, leaf in zip(grads, leaves))
+
+
+def sparse_write(idx, q, k, v, b, w, g, S0):
+    """Gated delta write on selected slots of a slot memory, fp64.
+
+    The memory S [M, d_v] per (batch, head) holds M slots.  At token t a router
+    has selected the K slots ``idx[b, t, h, :]`` (distinct; an index outside
+    [0, M) selects nothing), and the key-side inputs q, k, b, log_decay carry
+    one value per selected slot.  Reading of the pages (the "Sparse Delta
+    Memory" review page performs the Gated DeltaNet-2 write only on the slots a
+    product-key memory selects; the routing-slot recurrence of the Raven page,
+    S_t = (1 - r_t) * S_{t-1} + r_t * (update), leaves unselected slots as they
+    are, with no decay):
+
+        R   = the selected rows,  Sd = diag(exp g_t) S_{t-1}[R]     (decay)
+        x   = (b_t * k_t)^T Sd                                       (erase read)
+        S_t[R] = Sd - k_t x + k_t (w_t * v_t)^T                      (erase, write)
+        S_t[other rows] = S_{t-1}[other rows]
+        o_t = S_t[R]^T q_t                                           (read the selected slots)
+
+    which is the dense update of the Gated DeltaNet-2 page with k, b, q
+    scattered to the selected slots (zero elsewhere) and log_decay scattered
+    with zero elsewhere.  Shapes: idx, q, k, b, g [B, T, H, K]; v, w [B, T, H,
+    dv]; S0 [B, H, M, dv].  Returns ``(o [B, T, H, dv], S_T [B, H, M, dv])``.
+    Vectorised over (batch, head); one Python step per token."""
+    if hasattr(idx, "detach"):
+        idx = idx.detach().cpu().numpy()
+    idx = np.asarray(idx, dtype=np.int64)
+    q, k, v, b, w, g, S0 = (_f64(t) for t in (q, k, v, b, w, g, S0))
+    B, T, H, K = idx.shape
+    dv = v.shape[-1]
+    M = S0.shape[2]
+    for name, t, d in (("q", q, K), ("k", k, K), ("b", b, K), ("log_decay", g, K),
+                       ("v", v, dv), ("w", w, dv)):
+        if t.shape != (B, T, H, d):
+            raise ValueError(f"{name} has shape {t.shape}, expected {(B, T, H, d)}")
+    if S0.shape != (B, H, M, dv):
+        raise ValueError(f"S0 has shape {S0.shape}, expected {(B, H, M, dv)}")
+    n = B * H
+    S = S0.reshape(n, M, dv).copy()
+    o = np.zeros((B, T, H, dv))
+    heads = np.arange(n)[:, None]
+    for t in range(T):
+        sel = idx[:, t].reshape(n, K)
+        valid = (sel >= 0) & (sel < M)
+        rows = np.where(valid, sel, 0)
+        kt = np.where(valid, k[:, t].reshape(n, K), 0.0)
+        bt = np.where(valid, b[:, t].reshape(n, K), 0.0)
+        qt = np.where(valid, q[:, t].reshape(n, K), 0.0)
+        gt = np.where(valid, g[:, t].reshape(n, K), 0.0)
+        Sd = np.exp(gt)[..., None] * S[heads, rows]                  # decay of the selected rows
+        x = np.einsum("nk,nkd->nd", bt * kt, Sd)                      # (b * k)^T Sd
+        u = (w[:, t] * v[:, t]).reshape(n, dv)
+        new = Sd + kt[..., None] * (u - x)[:, None, :]                # erase and write
+        hv, kv = np.nonzero(valid)
+        S[hv, sel[hv, kv]] = new[hv, kv]                              # scatter the selected rows
+        o[:, t] = np.einsum("nk,nkd->nd", qt, new).reshape(B, H, dv)  # read the selected slots
+    return o, S.reshape(B, H, M, dv)
