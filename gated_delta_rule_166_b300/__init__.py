@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     gdr2_forward_varlen,
     gdr2_release_workspace,
     gdr2_set_wait_limit,
+    gdr2_sparse_write,
     gdr2_version,
     gdr2_workspace_stats,
 )
@@ -30,3 +31,4 @@ forward_noalloc = gdr2_forward_noalloc
 forward_cached = gdr2_forward_cached
 decode_step = gdr2_decode_step
 backward = gdr2_backward
+sparse_write = gdr2_sparse_write

@@ -66,6 +66,8 @@ def lib():
         L.gdr2_workspace_stats.restype = ci
         L.gdr2_release_workspace.argtypes = []
         L.gdr2_release_workspace.restype = ci
+        L.gdr2_sparse_write.argtypes = [vp] * 9 + [i64] * 6 + [ci, ci, vp]
+        L.gdr2_sparse_write.restype = ci
         L.gdr2_set_wait_limit.argtypes = [i64]
         L.gdr2_set_wait_limit.restype = i64
         _lib = L
@@ -324,6 +326,45 @@ def gdr2_decode_step(q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.flo
                                     _DTYPES[o.dtype], ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
         raise GDR2Error(st, "gdr2_decode_step")
+    return o
+
+
+def gdr2_sparse_write(idx, q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.float32,
+                      stream=None):
+    """Gated delta write on the selected slots of a slot memory, S updated in
+    place.  idx: int32 [B, T, H, K] (distinct slots per token; outside [0, M):
+    nothing); q, k, b, log_decay: [B, T, H, K]; v, w: [B, T, H, dv]; S: [B, H,
+    M, dv] fp32.  Returns o [B, T, H, dv] in ``out_dtype`` (fp32 by default, or
+    bf16)."""
+    if idx.dim() != 4 or v.dim() != 4 or S.dim() != 4:
+        raise ValueError("idx and v must be [B, T, H, *], S [B, H, M, dv]")
+    B, T, H, K = idx.shape
+    dv = v.shape[-1]
+    M = S.shape[2]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_sparse_write runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    _check_tokens("idx", idx, (B, T, H, K), torch.int32, dev)
+    for name, t, d in (("q", q, K), ("k", k, K), ("b", b, K), ("log_decay", log_decay, K),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (B, T, H, d), dtype, dev)
+    _check_tokens("S", S, (B, H, M, dv), torch.float32, dev)
+    if o is None:
+        if out_dtype not in _DTYPES:
+            raise ValueError(f"unsupported out_dtype {out_dtype}")
+        o = torch.empty((B, T, H, dv), dtype=out_dtype, device=dev)
+    else:
+        if o.dtype not in _DTYPES:
+            raise ValueError(f"unsupported o dtype {o.dtype}")
+        _check_tokens("o", o, (B, T, H, dv), o.dtype, dev)
+    with torch.cuda.device(dev):
+        st = lib().gdr2_sparse_write(_ptr(idx), _ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
+                                     _ptr(S), _ptr(o), B, T, H, M, K, dv, _DTYPES[dtype], _DTYPES[o.dtype],
+                                     ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_sparse_write")
     return o
 
 

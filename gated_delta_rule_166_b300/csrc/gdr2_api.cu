@@ -469,6 +469,43 @@ extern "C" int gdr2_decode_step(const void* q, const void* k, const void* v,
     return launch_decode(a, stream);
 }
 
+extern "C" int gdr2_sparse_write(const int32_t* idx, const void* q, const void* k, const void* v,
+                                 const void* b, const void* w, const void* log_decay, float* S, void* o,
+                                 int64_t B, int64_t T, int64_t H, int64_t M, int64_t K, int64_t dv,
+                                 int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (B < 0 || T < 0 || H < 0 || M < 0 || K < 0) return GDR2_ERR_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
+    if (dv != 32 && dv != 64 && dv != 128) return GDR2_ERR_SHAPE;
+    if (K > kSparseMaxK || K > M) return GDR2_ERR_SHAPE;
+    int64_t bh = 0, rows = 0, nsel = 0, nval = 0, nmem = 0;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, T, &rows) || !mul_ok(rows, K, &nsel) || !mul_ok(rows, dv, &nval) ||
+        !mul_ok(bh, M, &nmem) || !mul_ok(nmem, dv, &nmem) || nmem > INT64_MAX / 4 || nval > INT64_MAX / 4 ||
+        nsel > INT64_MAX / 4 || bh > 0x7fffffffLL || T > 0x7fffffffLL || M > 0x7fffffffLL)
+        return GDR2_ERR_SHAPE;
+    const bool has_tokens = rows > 0;
+    if (has_tokens && (!v || !w || !o || (nsel > 0 && (!idx || !q || !k || !b || !log_decay || !S))))
+        return GDR2_ERR_ARG;
+    for (const void* p : {(const void*)idx, q, k, v, b, w, log_decay, (const void*)S, (const void*)o})
+        if (p && !aligned16(p)) return GDR2_ERR_ALIGN;
+    const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
+    const size_t osz = out_dtype == GDR2_F32 ? 4 : 2;
+    const size_t bsel = (size_t)nsel * esz, bval = (size_t)nval * esz, bmem = (size_t)nmem * 4;
+    const size_t bo = (size_t)nval * osz, bidx = (size_t)nsel * 4;
+    if (has_tokens) {
+        const void* ins[7] = {idx, q, k, b, log_decay, v, w};
+        const size_t nb[7] = {bidx, bsel, bsel, bsel, bsel, bval, bval};
+        for (int i = 0; i < 7; ++i)
+            if (overlaps(o, bo, ins[i], nb[i]) || overlaps(S, bmem, ins[i], nb[i])) return GDR2_ERR_ALIAS;
+        if (overlaps(o, bo, S, bmem)) return GDR2_ERR_ALIAS;
+    }
+
+    int st = device_setup(nullptr);
+    if (st != GDR2_OK) return st;
+    if (!has_tokens) return GDR2_OK;
+    SparseArgs a{idx, q, k, v, b, w, log_decay, S, o, B, T, H, M, K, dv, in_dtype, out_dtype};
+    return launch_sparse(a, stream);
+}
+
 extern "C" int gdr2_device_status(cudaStream_t stream) {
     int* err = nullptr;
     int st = device_setup(&err);

@@ -55,6 +55,19 @@ struct DecodeArgs {
     int out_dtype;
 };
 
+// Sparse gated delta write over a slot memory (gdr2_sparse.cu).
+constexpr int64_t kSparseMaxK = 64;   // selected slots per token
+struct SparseArgs {
+    const int* idx;
+    const void *q, *k, *v, *b, *w, *g;
+    float* S;
+    void* o;
+    int64_t B, T, H, M, K, dv;
+    int in_dtype;
+    int out_dtype;
+};
+int launch_sparse(const SparseArgs& a, cudaStream_t stream);
+
 // Launchers; each returns a gdr2_status value.  `err` is the device address
 // of the library's error word (bounded waits record failures there).
 int launch_recurrent(const ForwardArgs& a, cudaStream_t stream);

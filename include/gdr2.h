@@ -29,9 +29,9 @@
  *   called on (allocated and released on `stream`); the pool keeps freed memory
  *   reserved for later calls until gdr2_release_workspace() is called, so a call
  *   after a synchronisation does not map its workspace again.  The chunked
- *   bf16 prefill (bf16 inputs, d_k = 128) takes 66,048 bytes per (64-token
- *   chunk, head) -- the
- *   per-chunk operands its two kernels exchange -- plus, when it splits
+ *   bf16 prefill (bf16 inputs, d_k = 128) in one pass takes 74,240 bytes per
+ *   (64-token chunk, head) -- the maps of each chunk's state update that its
+ *   two kernels exchange (plus 4 bytes per packed sequence) -- or, when it splits
  *   sequences into segments, the segment scratch described at
  *   gdr2_forward_segmented; gdr2_backward takes its checkpoints and partial
  *   sums.  gdr2_forward_noalloc and gdr2_decode_step allocate nothing.
@@ -272,6 +272,40 @@ int gdr2_backward(const void* q, const void* k, const void* v,
                   float* d_log_decay, float* d_S0,
                   int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
                   int in_dtype, cudaStream_t stream);
+
+/*
+ * gdr2_sparse_write -- the gated delta write on selected slots of a slot
+ * memory ("Sparse Delta Memory" review page, section "3. Method & Key
+ * Results": the write is applied only to the slots a product-key memory
+ * selects; routing-slot recurrence of the Raven summary page, section "2.1
+ * RSM framework": unselected slots keep their contents).  Per (sequence, head)
+ * the memory S is M x dv; token t has selected the K slots R = idx[t] and
+ *
+ *     Sd = diag(exp log_decay_t) S[R],   x = (b_t (.) k_t)^T Sd,
+ *     S[R] <- Sd + k_t (w_t (.) v_t - x)^T,   o_t = S[R]^T q_t,
+ *
+ * the dense update with k, b, q scattered to the selected slots and the decay
+ * applied to those slots only.  Tokens run in order; the state is updated in
+ * place.
+ *
+ *   idx                : [B, T, H, K] int32 slot indices; the K slots of one
+ *                        token must be distinct (otherwise the result is
+ *                        unspecified, accesses stay in bounds); an index outside
+ *                        [0, M) selects nothing
+ *   q, k, b, log_decay : [B, T, H, K]  (in_dtype), values at the selected slots
+ *   v, w               : [B, T, H, dv] (in_dtype)
+ *   S                  : [B, H, M, dv] fp32, read (S0) and overwritten (S_T)
+ *   o                  : [B, T, H, dv] (out_dtype), written
+ *
+ * dv in {32, 64, 128}; 0 <= K <= min(M, 64) (GDR2_ERR_SHAPE otherwise).  o
+ * and S may overlap no input and not each other (GDR2_ERR_ALIAS).  K = 0 writes
+ * o = 0 and leaves S as it is; T = 0 does nothing.  Allocates nothing.
+ * Asynchronous on `stream`.
+ */
+int gdr2_sparse_write(const int32_t* idx, const void* q, const void* k, const void* v,
+                      const void* b, const void* w, const void* log_decay, float* S, void* o,
+                      int64_t B, int64_t T, int64_t H, int64_t M, int64_t K, int64_t dv,
+                      int in_dtype, int out_dtype, cudaStream_t stream);
 
 /*
  * gdr2_decode_step -- one autoregressive step for every (batch, head), the
