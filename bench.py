@@ -391,6 +391,43 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None):
                          "kernel": "gdr2 backward: bwd_kernel + bwd_reduce_kernel per call"}}
 
 
+def bench_sparse(gdr2, hbm_gbs, steps=10, warmup=3):
+    """gdr2_sparse_write over the slot-memory workload (B4 H16 T4096, 2048 slots,
+    32 selected per token, d_v 128, bf16 inputs and o): CUDA events around
+    `steps` calls, the memory updated in place call after call."""
+    from gated_delta_rule_166_b300.inputs import SPARSE_WORKLOAD, make_sparse_workload
+
+    cfg = SPARSE_WORKLOAD
+    B, T, H, M, K, dv = cfg["B"], cfg["T"], cfg["H"], cfg["M"], cfg["K"], cfg["dv"]
+    x = make_sparse_workload().to("cuda")
+    S = x.S0.clone()
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        gdr2.sparse_write(*x.tensors(), S, o=o)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        gdr2.sparse_write(*x.tensors(), S, o=o)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if gdr2.gdr2_device_status() != 0:
+        raise RuntimeError("device-side failure during the sparse write")
+    ms = a.elapsed_time(b) / steps
+    # idx (int32) and q, k, b, log_decay (bf16) per selected slot; v, w in and o out
+    # per value channel; the slot memory read and written once
+    nbytes = B * T * H * (K * (4 + 4 * 2) + dv * 3 * 2) + 2 * B * H * M * dv * 4
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"sparse gated delta write: B={B} H={H} T={T}, M={M} slots, K={K} selected per token, "
+                        f"d_v={dv}, bf16 inputs and o, fp32 slot memory",
+            "ms_per_call": ms, "tokens_per_s": B * T / (ms / 1e3), "steps": steps, "warmup": warmup,
+            "roofline": {"bound": "latency (token-sequential per column tile; memory tile in shared memory)",
+                         "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                         "algorithmic_bytes_per_launch": nbytes, "traffic": None,
+                         "kernel": "gdr2 sparse write: sparse_tile_kernel"}}
+
+
 def bench_e2e(gdr2, x_host, steps, warmup):
     """Pinned host inputs -> device -> gdr2_forward -> o and S_T back to host, every
     step.  Steps are pipelined the way a serving loop would run them: inputs and
@@ -502,7 +539,8 @@ def main():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass leg")
     ap.add_argument("--backward-batch", type=int, default=None,
                     help="profiling aid: the backward leg on the first N sequences only")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward"], default="all",
+    ap.add_argument("--no-sparse", action="store_true", help="skip the sparse-write leg")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward", "sparse"], default="all",
                     help="profiling aid: run just one leg (decode and long print only that leg)")
     ap.add_argument("--decode-steps", type=int, default=1024)
     args = ap.parse_args()
@@ -580,6 +618,11 @@ def main():
         if rank == 0:
             print(json.dumps({"long_context": lc}))
         return
+    if args.only == "sparse":
+        sp = bench_sparse(gdr2, hbm_gbs, steps=min(args.steps, 10), warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"sparse_write": sp}))
+        return
 
     with ClockSampler(local) as clk:
         ms, per_launch, launches = bench_prefill(gdr2, x, args.steps, args.warmup, world)
@@ -620,6 +663,7 @@ def main():
 
     if args.only == "prefill":
         args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = args.no_backward = True
+        args.no_sparse = True
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
@@ -643,6 +687,8 @@ def main():
         out["long_context"] = bench_long(gdr2, hbm_gbs)
     if not args.no_backward:
         out["backward"] = bench_backward(gdr2, hbm_gbs, x)
+    if not args.no_sparse:
+        out["sparse_write"] = bench_sparse(gdr2, hbm_gbs)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x_host)
     if rank == 0:

@@ -85,6 +85,14 @@ def test_sparse_nothing_selected():
     assert not np.any(o)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sparse_memory_beyond_shared_memory(dtype):
+    """60,000 slots: too many for a one-column tile in shared memory, so the
+    kernel that gathers from and scatters to global memory runs."""
+    x = make_sparse_inputs(1, 45, 2, 60000, 24, 32, dtype=dtype, seed=21, s0_std=0.3)
+    _check(x, TOL_F32 if dtype == torch.float32 else TOL_BF16)
+
+
 def test_sparse_full_workload():
     """2048 slots x 128 value columns per head, 32 slots per token, B4 H16
     T4096, bf16 inputs: the whole output and memory against the oracle."""
