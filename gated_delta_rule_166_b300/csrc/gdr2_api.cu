@@ -252,8 +252,16 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         }
         return GDR2_OK;
     }
-    if (two_kernel_supports(a) && segments == 0 && bcache == 0 &&
-        (cu || auto_segments(bh, dv, (T + 63) / 64) == 1)) {
+    // bf16 head sizes below the P-form kernels' (d_k < 128 or d_v = 32) run the
+    // affine-form kernels with zero-padded channels: TMA fills key channels past
+    // d_k with zeros (k = b = q = 0, log decay 0), so those state rows stay zero
+    // and add nothing; value columns past d_v are computed and never stored.
+    ForwardArgs full = a;
+    full.dk = kPrepDK;
+    full.dv = 128;
+    const bool padded = (dk < kPrepDK || dv < 64) && two_kernel_supports(full);
+    if ((two_kernel_supports(a) || padded) && segments == 0 && bcache == 0 &&
+        (cu || padded || auto_segments(bh, dv, (T + 63) / 64) == 1)) {
         // One pass over the chunks in affine form: prep2 writes each chunk's maps, the
         // chain kernel carries the state; workspace (slots, then chunk_base of packed
         // sequences) from the library's pool.

@@ -92,7 +92,7 @@ struct ChainParams {
     int* err;
     const int* cu;           // packed sequences: [N + 1] token offsets, or null
     const int* chunk_base;   // packed sequences: [N + 1] first global chunk of each sequence
-    int T, H, dv, nch, total;
+    int T, H, dk, dv, nch, total;   // dk, dv <= 128 / 64 per tile; channels past them are zero padding
     int out_bf16;
     long long wait_cycles;   // limit of each handshake wait (copy drains keep the default)
 };
@@ -276,7 +276,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                 ph_full ^= 1u;
                 const int row = tok0 + c * kC;
                 tma_store_4d(&tm_o, base + kO, j0, h, row, 0);
-                if (!prm.out_bf16) tma_store_4d(&tm_o, base + kO + 8192u, j0 + 32, h, row, 0);
+                if (!prm.out_bf16 && j0 + 32 < prm.dv) tma_store_4d(&tm_o, base + kO + 8192u, j0 + 32, h, row, 0);
                 bulk_commit();
                 bulk_wait_read();
                 mbar_arrive(bar(kOFree));
@@ -329,7 +329,9 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int t = min(c * kC + 8 * ug + e, T - 1);   // rows past the end: masked in put_u
-                const int64_t off = (static_cast<int64_t>(tok0 + t) * prm.H + h) * prm.dv + j0 + un;
+                // columns past d_v (a 32-column value dim in a 64-column tile) read column
+                // d_v - 1: they only feed state columns that are never stored
+                const int64_t off = (static_cast<int64_t>(tok0 + t) * prm.H + h) * prm.dv + min(j0 + un, prm.dv - 1);
                 x.v[e] = __ldg(reinterpret_cast<const unsigned short*>(prm.v) + off);
                 x.w[e] = __ldg(reinterpret_cast<const unsigned short*>(prm.w) + off);
             }
@@ -359,7 +361,9 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
 
         float S[16];
         {
-            const float* s0 = prm.S0 ? prm.S0 + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R : nullptr;
+            // state rows past d_k and columns past d_v are zero padding
+            const bool live = j < prm.dk && j0 + 16 * R < prm.dv;
+            const float* s0 = prm.S0 && live ? prm.S0 + (static_cast<int64_t>(bh) * prm.dk + j) * prm.dv + j0 + 16 * R : nullptr;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
                 const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -441,7 +445,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                         }
                     }
                     arrive(kOFull);
-                } else if (active && tc + r < T) {   // the sequence's last, partial chunk: row by row
+                } else if (active && tc + r < T && j0 + 16 * R < prm.dv) {   // the last, partial chunk: row by row
                     const int64_t off = ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
                     if (obf16) {
                         __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
@@ -466,8 +470,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         if (failed) {
             *abort_flag = 1;
             if (lane == 0) atomicExch(prm.err, kDevTimeout);
-        } else if (prm.ST) {
-            float* st = prm.ST + (static_cast<int64_t>(bh) * kDK + j) * prm.dv + j0 + 16 * R;
+        } else if (prm.ST && j < prm.dk && j0 + 16 * R < prm.dv) {
+            float* st = prm.ST + (static_cast<int64_t>(bh) * prm.dk + j) * prm.dv + j0 + 16 * R;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4)
                 *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
@@ -536,11 +540,12 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     ChainParams prm{slots, a.S0, static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
                     a.o, a.ST, err, a.cu, chunk_base, static_cast<int>(a.T), static_cast<int>(a.H),
-                    static_cast<int>(a.dv), static_cast<int>((a.T + kC - 1) / kC), static_cast<int>(total),
+                    static_cast<int>(a.dk), static_cast<int>(a.dv), static_cast<int>((a.T + kC - 1) / kC),
+                    static_cast<int>(total),
                     a.out_dtype == GDR2_BF16 ? 1 : 0, 0};
     const int64_t lim = g_wait_limit.load();
     prm.wait_cycles = lim > 0 ? static_cast<long long>(lim) : kWaitCycles;
-    const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.dv / kDVT));
+    const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>((a.dv + kDVT - 1) / kDVT));
     chain_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mo, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }

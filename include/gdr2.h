@@ -29,7 +29,7 @@
  *   called on (allocated and released on `stream`); the pool keeps freed memory
  *   reserved for later calls until gdr2_release_workspace() is called, so a call
  *   after a synchronisation does not map its workspace again.  The chunked
- *   bf16 prefill (bf16 inputs, d_k = 128) in one pass takes 74,240 bytes per
+ *   bf16 prefill in one pass takes 74,240 bytes per
  *   (64-token chunk, head) -- the maps of each chunk's state update that its
  *   two kernels exchange (plus 4 bytes per packed sequence) -- or, when it splits
  *   sequences into segments, the segment scratch described at
@@ -82,11 +82,13 @@ typedef enum {
  * Applies the update above for t = 0 .. T-1 to every (batch, head) pair,
  * starting from S0, writes every o_t and (optionally) the final state.
  * The page's "efficient implementation" section (WY form with decay
- * absorption, chunkwise algorithm) describes the method used for bf16 inputs
- * with d_k = 128: fixed 64-token chunks, a per-chunk UT/WY transform with the
- * cumulative channel decay folded into the rank-1 erase factors (computed for
- * all chunks in parallel), and an fp32 state carried across the chunks of a
- * sequence on chip.  Other inputs run a token-sequential fp32 kernel.
+ * absorption, chunkwise algorithm) describes the method used for bf16 inputs:
+ * fixed 64-token chunks, a per-chunk UT/WY transform with the cumulative
+ * channel decay folded into the rank-1 erase factors (computed for all chunks
+ * in parallel), and an fp32 state carried across the chunks of a sequence on
+ * chip.  Head sizes below 128 key channels or 64 value columns run the same
+ * kernels on zero-padded channels.  fp32 inputs run a token-sequential fp32
+ * kernel.
  *
  *   q, k, b, log_decay : [B, T, H, dk]  (in_dtype)
  *   v, w               : [B, T, H, dv]  (in_dtype)

@@ -4,6 +4,8 @@ inputs, fp32 state), for o and for S_T."""
 import pytest
 import torch
 
+import gated_delta_rule_166_b300 as gdr2
+
 from gated_delta_rule_166_b300.inputs import WORKLOADS, make_prefill_inputs, make_workload
 from gpu_util import compare
 
@@ -38,10 +40,32 @@ def test_fp32_head_dims(dk, dv, regime):
     compare(x, f"fp32 dk={dk} dv={dv} {regime}")
 
 
-@pytest.mark.parametrize("dk,dv", [(64, 64), (32, 128), (128, 32)])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (32, 128), (128, 32), (32, 32), (64, 32), (32, 64)])
 def test_bf16_small_head_dims(dk, dv):
     x = make_prefill_inputs(2, 130, 2, dk, dv, dtype=torch.bfloat16, seed=5 * dk + dv, s0_std=0.2)
     compare(x, f"bf16 dk={dk} dv={dv}")
+    compare(x, f"bf16 dk={dk} dv={dv} (bf16 o)", out_dtype=torch.bfloat16)
+
+
+def _kernel_names(fn):
+    """Names of the CUDA kernels that ``fn`` launches (torch profiler)."""
+    from torch.profiler import ProfilerActivity, profile
+
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    return {e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA}
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 32)])
+def test_bf16_small_head_dims_run_the_chunked_kernels(dk, dv):
+    """Small bf16 head sizes take the chunked tensor-core kernels (with zero-padded
+    channels), not the token-recurrent one."""
+    x = make_prefill_inputs(2, 200, 2, dk, dv, dtype=torch.bfloat16, seed=3, s0_std=0.2).to("cuda")
+    names = _kernel_names(lambda: gdr2.forward(*x.tensors(), x.S0))
+    assert any("prep2_kernel" in n for n in names), names
+    assert any("chain_kernel" in n for n in names), names
+    assert not any("recurrent" in n for n in names), names
 
 
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129])

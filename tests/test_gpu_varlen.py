@@ -26,6 +26,7 @@ def _packed(lengths, H, dk, dv, dtype, seed, **kw):
 
 @pytest.mark.parametrize("dtype,dk,dv,regime", [(torch.bfloat16, 128, 128, "mixed"),
                                                  (torch.bfloat16, 128, 64, "fast"),
+                                                 (torch.bfloat16, 32, 32, "mixed"),
                                                  (torch.float32, 64, 32, "slow")])
 def test_ragged_batch_matches_oracle_per_sequence(dtype, dk, dv, regime):
     lengths = [1, 63, 64, 65, 0, 200, 1000, 130]
