@@ -11,9 +11,9 @@
 // are issued while the chain runs, P S after it.
 //
 // Products on tcgen05 (kind::f16, fp32 accumulators in TMEM): M', Y, P, X are
-// K-major fp16 A operands copied from the workspace slot unchanged; S^T (fp16)
-// and U^T (an fp16 pair u = u_hi + u_lo, 22 significant bits) are K-major B
-// operands written by the elementwise warps.  The fp32 state stays in registers
+// K-major fp16 A operands copied from the workspace slot unchanged; S (fp16,
+// MN-major) and U^T (an fp16 pair u = u_hi + u_lo, 22 significant bits,
+// K-major) are the B operands written by the elementwise warps.  The fp32 state stays in registers
 // (16 entries per thread); only its fp16 image is an operand.
 //
 // Work split: 640 threads.  One thread of the last warpgroup issues the bulk
@@ -40,7 +40,6 @@ namespace {
 using namespace tc;
 
 constexpr int kC = kPrepC;
-constexpr int kDK = kPrepDK;
 constexpr int kDVT = 64;
 constexpr int kSimt = 512;
 constexpr int kThreads = kSimt + 128;
@@ -52,7 +51,7 @@ static_assert(kSimt * kRegsSimt + (kThreads - kSimt) * kRegsMma <= kThreads * 96
 // Y (16 KB), X (8 KB)
 constexpr uint32_t kSlotBuf = 73728;
 constexpr uint32_t kBM = kSlotM, kBY = kSlotY, kBP = kSlotP, kBX = kSlotX;   // offsets within a slot buffer
-constexpr uint32_t kSB = 2 * kSlotBuf;   // two S^T operands, fp16 K-major [64 rows][128 K] (16 KB each)
+constexpr uint32_t kSB = 2 * kSlotBuf;   // two S operands, fp16 MN-major [128 K rows][64] (16 KB each)
 constexpr uint32_t kUB = kSB + 32768;    // two [U_hi^T | U_lo^T] operands, fp16 K-major [64][64] x 2 (16 KB each)
 constexpr uint32_t kO = kUB + 32768;     // O tile for the TMA store (16 KB)
 constexpr uint32_t kMisc = kO + 16384;
@@ -175,12 +174,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                 bulk_g2s(base + kSlotBuf * b, slot_of(c), kSlotCopyBytes, bar(kBarSlot0 + b));
                 if (b) ++iss_slot1; else ++iss_slot0;
             };
-            // every operand is K-major: a K step of 16 elements is 32 bytes within a 128-byte
-            // row; M' (K = 128) has its two K blocks 16 KB apart, P and S^T 8 KB apart
+            // A operands and U^T are K-major: a K step of 16 elements is 32 bytes within a
+            // 128-byte row; M' (K = 128) has its two K blocks 16 KB apart, P 8 KB apart.  The
+            // state S is MN-major (one 64-column block): a K step is 16 rows = 2048 bytes
             const uint64_t dM0 = umma_desc2(base + kBM, 16u, 1024u), dP0 = umma_desc2(base + kBP, 16u, 1024u);
             const uint64_t dY0 = umma_desc2(base + kBY, 16u, 1024u), dX0 = umma_desc2(base + kBX, 16u, 1024u);
-            const uint64_t dS0 = umma_desc2(base + kSB, 16u, 1024u), dU0 = umma_desc2(base + kUB, 16u, 1024u);
-            constexpr uint32_t idS = idesc_f16x(128, 64, 0, 0, 0), idO = idesc_f16x(64, 64, 0, 0, 0);
+            const uint64_t dS0 = umma_desc2(base + kSB, 16384u, 1024u), dU0 = umma_desc2(base + kUB, 16u, 1024u);
+            constexpr uint32_t idS = idesc_f16x(128, 64, 0, 0, 1), idO = idesc_f16x(64, 64, 0, 0, 1);
             // Y U and X U of chunk c into accumulator buffer c & 1 (the first products
             // there): [U_hi^T; U_lo^T] is one 128-row B operand, so each product writes
             // u_hi terms to the first 64 columns of its accumulator pair and u_lo terms to
@@ -202,7 +202,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
             bool ok = true;   // an empty sequence issues nothing
             bool issued = false;
             if (n > 0) {
-                if (n > 2) bulk_prefetch_l2(slot_of(2), kSlotCopyBytes);
                 load_slot(0);
                 if (n > 1) load_slot(1);
                 ok = wait(kURdy0, c_u0) && wait(kBarSlot0, c_slot0);
@@ -216,8 +215,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                 const uint32_t b = static_cast<uint32_t>(c & 1);
                 const uint64_t dM = dM0 + (kSlotBuf >> 4) * b, dP = dP0 + (kSlotBuf >> 4) * b;
                 const uint64_t dS = dS0 + (16384u >> 4) * b;
-                // the slot of chunk c + 3 into L2, so that its copy two chunks later hits L2
-                if (c + 3 < n) bulk_prefetch_l2(slot_of(c + 3), kSlotCopyBytes);
                 // ---- chain: S' - gamma S += M' S;  O += P S ------------------------------
                 if (!(ok = wait(kSRdy, c_s))) break;
                 tc_fence_after();
@@ -227,14 +224,14 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                     const uint32_t tS = tmem + kTmDS + 128u * b, tO = tmem + kTmDO + 128u * b;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        mma_ss_f16(tS, dM + 2u * k, dS + 2u * k, idS, 1u);
-                        mma_ss_f16(tS + 64u, dM + (16384u >> 4) + 2u * k, dS + (8192u >> 4) + 2u * k, idS, 1u);
+                        mma_ss_f16(tS, dM + 2u * k, dS + 128u * k, idS, 1u);
+                        mma_ss_f16(tS + 64u, dM + (16384u >> 4) + 2u * k, dS + 512u + 128u * k, idS, 1u);
                     }
                     mma_commit(bar(kDS0 + b));
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        mma_ss_f16(tO, dP + 2u * k, dS + 2u * k, idO, 1u);
-                        mma_ss_f16(tO + 64u, dP + (8192u >> 4) + 2u * k, dS + (8192u >> 4) + 2u * k, idO, 1u);
+                        mma_ss_f16(tO, dP + 2u * k, dS + 128u * k, idO, 1u);
+                        mma_ss_f16(tO + 64u, dP + (8192u >> 4) + 2u * k, dS + 512u + 128u * k, idO, 1u);
                     }
                     mma_commit(bar(kDO0 + b));
                 }
@@ -305,18 +302,17 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(b));
         };
-        // S^T operand (fp16, K-major [64 rows n][128 K]): element (n = 16R + i, k = j); pairs
-        // (j, j ^ 1) go to one 4-byte word, even lanes write even rows, odd lanes odd rows
+        // S operand (fp16, MN-major: 128 K rows j of 64 n-values, 128-byte swizzle): the
+        // thread's 16 columns n = 16R .. 16R + 15 of row j are two 16-byte pieces
         auto put_st = [&](uint32_t buf, const float (&S)[16]) {
-            const bool odd = lane & 1;
-            uint8_t* img = sgen + kSB + 16384u * buf;
+            uint8_t* img = sgen + kSB + 16384u * buf + static_cast<uint32_t>(j) * 128u;
+            uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float x = __shfl_xor_sync(0xffffffffu, odd ? S[2 * e] : S[2 * e + 1], 1);
-                const uint32_t w = odd ? pack_h2(x, S[2 * e + 1]) : pack_h2(S[2 * e], x);
-                const uint32_t row = static_cast<uint32_t>(16 * R + 2 * e + (odd ? 1 : 0));
-                *reinterpret_cast<uint32_t*>(img + k_off16(8192u, row, static_cast<uint32_t>(j & ~1))) = w;
-            }
+            for (int e = 0; e < 8; ++e) w[e] = pack_h2(S[2 * e], S[2 * e + 1]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                *reinterpret_cast<uint4*>(img + ((static_cast<uint32_t>((2 * R + q) ^ (j & 7))) << 4)) =
+                    make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         };
         // v, w of chunk c for d_v column un, tokens 8 ug .. 8 ug + 7 (raw bf16 bits; tokens past
         // the sequence end read as 0), fetched a chunk before they are used.  The loaded
@@ -325,15 +321,32 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         struct VW {
             uint32_t v[8], w[8];   // raw bf16 bits, zero-extended by the load itself
         };
+        // Consecutive tokens are H * d_v elements apart: one base address per chunk, and
+        // rows past the sequence end (masked in put_u) read the last row instead.  Columns
+        // past d_v (a 32-column value dim in a 64-column tile) read column d_v - 1: they
+        // only feed state columns that are never stored.
+        const int64_t row_stride = static_cast<int64_t>(prm.H) * prm.dv;
+        const unsigned short* const vcol = reinterpret_cast<const unsigned short*>(prm.v) +
+                                           static_cast<int64_t>(tok0) * row_stride + static_cast<int64_t>(h) * prm.dv +
+                                           min(j0 + un, prm.dv - 1);
+        const unsigned short* const wcol = reinterpret_cast<const unsigned short*>(prm.w) + (vcol - reinterpret_cast<const unsigned short*>(prm.v));
         auto fetch_vw = [&](int c, VW& x) {
+            const int t0 = c * kC + 8 * ug;
+            if (t0 + 7 < T) {
+                const unsigned short* pv = vcol + static_cast<int64_t>(t0) * row_stride;
+                const unsigned short* pw = wcol + static_cast<int64_t>(t0) * row_stride;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = min(c * kC + 8 * ug + e, T - 1);   // rows past the end: masked in put_u
-                // columns past d_v (a 32-column value dim in a 64-column tile) read column
-                // d_v - 1: they only feed state columns that are never stored
-                const int64_t off = (static_cast<int64_t>(tok0 + t) * prm.H + h) * prm.dv + min(j0 + un, prm.dv - 1);
-                x.v[e] = __ldg(reinterpret_cast<const unsigned short*>(prm.v) + off);
-                x.w[e] = __ldg(reinterpret_cast<const unsigned short*>(prm.w) + off);
+                for (int e = 0; e < 8; ++e) {
+                    x.v[e] = __ldg(pv + e * row_stride);
+                    x.w[e] = __ldg(pw + e * row_stride);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t t = min(t0 + e, T - 1);
+                    x.v[e] = __ldg(vcol + t * row_stride);
+                    x.w[e] = __ldg(wcol + t * row_stride);
+                }
             }
         };
         // U^T of chunk c (fp16 pair u = u_hi + u_lo) into buffer c & 1: row un, tokens 8 ug ..
