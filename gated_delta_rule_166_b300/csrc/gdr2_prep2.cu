@@ -75,10 +75,13 @@ constexpr uint32_t kAG = 147456;   // constant stripe matrix, bf16 K-major 128 r
 constexpr uint32_t kCB = 163840;   // Cb fp16 MN-major image [2][64 tokens][64 channels]
 constexpr uint32_t kKB = 180224;   // Kb, same layout
 constexpr uint32_t kQB = 196608;   // Qb, same layout
-constexpr uint32_t kTab = 212992;  // per-channel tables, [row][128] fp32
-enum : uint32_t { kTSh = 0, kTSf = 4, kTEm = 8, kTEc = 12, kTEg = 16, kTGam = 22, kTRows = 23 };
-constexpr uint32_t kMisc = kTab + kTRows * 512;
-enum : uint32_t { kBarRaw = 0, kOpsRdy, kGDone, kProdDone, kWDone, kDDone, kNumBars };
+// per-channel decay tables, [row][128] fp32, two buffers (items alternate): e^{G_m(s)},
+// e^{G_C - G_m(s)}, e^{G_m(R) - G_m(s)} (R > s, row R (R - 1) / 2 + s) and e^{G_C}
+constexpr uint32_t kTab = 212992;
+enum : uint32_t { kTEm = 0, kTEc = 4, kTEg = 8, kTGam = 14, kTRows = 16 };
+constexpr uint32_t kTabBuf = kTRows * 512;
+constexpr uint32_t kMisc = kTab + 2 * kTabBuf;
+enum : uint32_t { kBarRaw = 0, kOpsRdy, kTabRdy, kGDone, kProdDone, kWDone, kDDone, kPDrain, kNumBars };
 constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
 constexpr uint32_t kSmemBytes = kMisc + 128;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -87,11 +90,13 @@ static_assert(kSmemAlloc <= 232448, "shared memory");
 static_assert(kSlot2Bytes <= 4 * kKGStride, "slot staging in the K-group area");
 
 // ---- TMEM columns ---------------------------------------------------------------
+// The next item's d offsets land in kTmA while this item's map products (D1, D2)
+// are still in use, so those stay clear of columns 0-127.
 constexpr uint32_t kTmA = 0;      // d offsets, then the A operand [Ct; Qt] (tf32), 128 columns
 constexpr uint32_t kTmP = 128;    // intra-chunk products [Ct; Qt] x [G3|G1|G2|G0]^T, 160 columns
-constexpr uint32_t kTmW = 288;    // W^T, 64 columns
-constexpr uint32_t kTmD1 = 288;   // [Y | Kb^T W], 192 columns (after W^T is read out)
-constexpr uint32_t kTmD2 = 0;     // [X | A_qk W] (M = 64), 192 columns (after the products are read out)
+constexpr uint32_t kTmW = 320;    // W^T, 64 columns
+constexpr uint32_t kTmD1 = 320;   // [Y | Kb^T W], 192 columns (after W^T is read out)
+constexpr uint32_t kTmD2 = 128;   // [X | A_qk W] (M = 64), 192 columns (after the products are read out)
 constexpr int kTmCols = 512;
 
 constexpr float kMinLogDecay = -10.f;
@@ -101,6 +106,21 @@ static_assert(kSlotM == 0 && kSlotY == 32768 && kSlotP == 49152 && kSlotX == 655
               "slot layout");
 
 __device__ __forceinline__ void simt_sync() { team_sync<kSimt>(); }
+// the table team: warps 17-19 (named barrier 2)
+constexpr int kTeam = 96;
+__device__ __forceinline__ void team2_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kTeam) : "memory"); }
+__device__ __forceinline__ bool team2_all(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 2, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "n"(kTeam)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ bool simt_any(bool p) { return team_any<kSimt>(p); }
 // first row of K-group R within the merged [G3 | G1 | G2 | G0] operand
 __device__ __forceinline__ uint32_t group_row(int R) {
@@ -241,6 +261,103 @@ prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 atomicExch(prm.err, kDevTimeout);
                 if (loads > 0) mbar_wait(bar(kBarRaw), static_cast<uint32_t>((loads - 1) & 1));
             }
+        } else if (warp > kSimt / 32) {
+            // ---- table team (warps 17-19): per item, once its raw tiles are in, the
+            // floored log decays (tokens past the sequence end: 0), the decay tables into
+            // buffer (item & 1), and the d-offset product into kTmA once the previous
+            // item's intra-chunk products have read that region; then kTabRdy.  The
+            // elementwise warps meanwhile finish the previous item.
+            const int pt = tid - (kSimt + 32);
+            bool ok = true, issued = false;
+            uint32_t ph = 0;
+            Item cur = first;
+#pragma unroll 1
+            for (int it = it0, k = 0; it < prm.nitems; ph ^= 1u, ++k) {
+                const int nvalid = min(cur.T - cur.tp, kC);
+                if (!(ok = team2_all(mbar_wait(bar(kBarRaw), ph)))) break;
+                const __nv_bfloat162 lo2 = __float2bfloat162_rn(kMinLogDecay);
+#pragma unroll 1
+                for (uint32_t ui = static_cast<uint32_t>(pt); ui < 1024u; ui += kTeam) {   // 16-byte units
+                    const int r = static_cast<int>((ui >> 3) & 63u);
+                    uint4 x = *reinterpret_cast<const uint4*>(sgen + kRawG + 16u * ui);
+                    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) p2[e] = __hmax2(p2[e], lo2);
+                    if (r >= nvalid) x = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sgen + kRawG + 16u * ui) = x;
+                }
+                fence_async_smem();   // the floored tile is the B operand of the d-offset product
+                team2_sync();
+                float* const tb = F + ((kTab + kTabBuf * ph) >> 2);
+                if (pt < kDK / 2) {
+                    // channels j, j + 1 (one 32-bit word of the MN-major tile per token); the
+                    // swizzled offset of token 8 q + e is e * 128 + ((c8 ^ e) << 4) + q * 1024
+                    const uint32_t j = 2u * static_cast<uint32_t>(pt);
+                    const uint8_t* const gt = sgen + kRawG + (j >> 6) * 8192u + ((j & 7u) << 1);
+                    const uint32_t c8 = (j & 63u) >> 3;
+                    float gm0[4], gm1[4], run0 = 0.f, run1 = 0.f;
+#pragma unroll
+                    for (int sx = 0; sx < 4; ++sx) {
+                        float a0 = 0.f, a1 = 0.f, h0 = 0.f, h1 = 0.f;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                                    gt + static_cast<uint32_t>(e) * 128u + ((c8 ^ static_cast<uint32_t>(e)) << 4) +
+                                    static_cast<uint32_t>(2 * sx + q) * 1024u);
+                                a0 += __uint_as_float(w << 16);
+                                a1 += __uint_as_float(w & 0xFFFF0000u);
+                            }
+                            if (q == 0) { h0 = a0; h1 = a1; }
+                        }
+                        gm0[sx] = run0 + h0;   // G at the stripe's middle token 16 s + 7
+                        gm1[sx] = run1 + h1;
+                        run0 += a0;
+                        run1 += a1;
+                    }
+                    auto put = [&](uint32_t c, const float (&gm)[4], float gC) {
+#pragma unroll
+                        for (int sx = 0; sx < 4; ++sx) {
+                            tb[(kTEm + sx) * 128 + c] = __expf(gm[sx]);         // e^{G_m(s)}        (<= 1)
+                            tb[(kTEc + sx) * 128 + c] = __expf(gC - gm[sx]);    // e^{G_C - G_m(s)}  (<= 1)
+#pragma unroll
+                            for (int R = sx + 1; R < 4; ++R) tb[(kTEg + R * (R - 1) / 2 + sx) * 128 + c] = __expf(gm[R] - gm[sx]);
+                        }
+                        tb[kTGam * 128 + c] = __expf(gC);
+                    };
+                    put(j, gm0, run0);
+                    put(j + 1u, gm1, run1);
+                }
+                team2_sync();
+                bool ok0 = true;
+                if (pt == 0) {
+                    // the previous item's intra-chunk products have read kTmA
+                    ok0 = k == 0 || mbar_wait(bar(kProdDone), ph ^ 1u);
+                    if (ok0) {
+                        tc_fence_after();
+                        // d offsets: [A_G] (128 x 64, K-major bf16) x floored log decays (MN-major)
+                        const uint64_t dAG = umma_desc2(base + kAG, 16u, 1024u), dG = umma_desc2(base + kRawG, 8192u, 1024u);
+#pragma unroll
+                        for (int sx = 0; sx < 4; ++sx)
+                            mma_ss_f16(tmem + kTmA, dAG + 2u * sx, dG + 128u * sx, idesc_f16x(128, 128, 1, 0, 1),
+                                       sx > 0 ? 1u : 0u);
+                        mma_commit(bar(kGDone));
+                        issued = true;
+                        mbar_arrive(bar(kTabRdy));   // tables (ordered by the team barrier) and floor done
+                    }
+                }
+                if (!(ok = team2_all(ok0))) break;
+                Item nx;
+                it = next_item(it, nx);
+                cur = nx;
+            }
+            if (!ok && pt == 0) atomicExch(prm.err, kDevTimeout);
+            if (pt == 0 && issued) {
+                // a d-offset product still in flight completes before the TMEM is freed
+                mma_commit(bar(kPDrain));
+                mbar_wait(bar(kPDrain), 0u);
+            }
         }
         __syncwarp();
     } else {
@@ -270,73 +387,16 @@ prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
         };
 
-        float* const tab = F + (kTab >> 2);
-
         uint32_t ph = 0;
         Item cur = first;
 #pragma unroll 1
         for (int it = it0; it < prm.nitems && !failed; ph ^= 1u) {
             const int nvalid = min(cur.T - cur.tp, kC);   // tokens of this chunk inside the sequence
             uint8_t* const slot = prm.slots + static_cast<int64_t>(it) * kSlot2Bytes;
-            if (!wait_done(kBarRaw, ph)) { failed = true; break; }
-            // ---- floored log decays (tokens past the sequence end: 0) -----------------------
-            {
-                const __nv_bfloat162 lo2 = __float2bfloat162_rn(kMinLogDecay);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t ui = static_cast<uint32_t>(tid + h * kSimt);   // 16-byte unit of the g tile
-                    const int r = static_cast<int>((ui >> 3) & 63u);
-                    uint4 x = *reinterpret_cast<const uint4*>(sgen + kRawG + 16u * ui);
-                    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&x);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) p2[e] = __hmax2(p2[e], lo2);
-                    if (r >= nvalid) x = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(sgen + kRawG + 16u * ui) = x;
-                }
-            }
-            operands_done();   // the floored tile is the B operand of the d-offset product
-            if (tid == 0) {
-                // d offsets: [A_G] (128 x 64, K-major bf16) x floored log decays (MN-major)
-                const uint64_t dAG = umma_desc2(base + kAG, 16u, 1024u), dG = umma_desc2(base + kRawG, 8192u, 1024u);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_ss_f16(tmem + kTmA, dAG + 2u * s, dG + 128u * s, idesc_f16x(128, 128, 1, 0, 1), s > 0 ? 1u : 0u);
-                mma_commit(bar(kGDone));
-            }
-            // ---- per-channel sums over half stripes and stripes -----------------------------
-            {
-                const int j = tid & 127, s = tid >> 7;
-                float sh = 0.f, sf = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint32_t t = static_cast<uint32_t>(16 * s + e);
-                    const uint32_t off = static_cast<uint32_t>(j >> 6) * 8192u + t * 128u +
-                                         (((((static_cast<uint32_t>(j) & 63u) >> 3) ^ (t & 7u))) << 4) +
-                                         ((static_cast<uint32_t>(j) & 7u) << 1);
-                    const float gv = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(sgen + kRawG + off)) << 16);
-                    sf += gv;
-                    if (e == 7) sh = sf;
-                }
-                tab[(kTSh + s) * 128 + j] = sh;
-                tab[(kTSf + s) * 128 + j] = sf;
-            }
-            simt_sync();
-            {
-                const int j = tid & 127, s = tid >> 7;
-                float gm[4], run = 0.f;
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    gm[x] = run + tab[(kTSh + x) * 128 + j];
-                    run += tab[(kTSf + x) * 128 + j];
-                }
-                const float gC = run;
-                tab[(kTEm + s) * 128 + j] = __expf(gm[s]);          // e^{G_m(s)}        (<= 1)
-                tab[(kTEc + s) * 128 + j] = __expf(gC - gm[s]);     // e^{G_C - G_m(s)}  (<= 1)
-#pragma unroll
-                for (int R = 1; R < 4; ++R)
-                    if (R > s) tab[(kTEg + R * (R - 1) / 2 + s) * 128 + j] = __expf(gm[R] - gm[s]);
-                if (s == 0) tab[kTGam * 128 + j] = __expf(gC);
-            }
+            float* const tab = F + ((kTab + kTabBuf * ph) >> 2);   // this item's decay tables
+            // the table team has floored the log decays, written the tables and issued the
+            // d-offset product (the raw tiles are in)
+            if (!wait_done(kTabRdy, ph)) { failed = true; break; }
             if (tid == 0) bulk_wait_read();   // the previous item's slot copy has left the K-group area
             simt_sync();
             // ---- pass 1, one token row per thread: [Ct; Qt] -> TMEM, K-groups, Cb, Kb, Qb ----
@@ -616,6 +676,10 @@ prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (col < 64) put_row(kSlotY, 0u, j, col, v, false);
                     else put_row(kSlotM, 16384u, j, col - 64u, v, true);
                 }
+                // M' and Y leave while X and P are staged
+                fence_async_smem();
+                simt_sync();
+                if (tid == 0) bulk_s2g(slot, base + kKG, kSlotP);
                 // D2 (M = 64): row r at lanes 32 (r / 16) + r % 16
                 const uint32_t r = static_cast<uint32_t>(16 * quarter + (lane & 15));
                 const bool active = lane < 16;
@@ -650,7 +714,7 @@ prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_before();
             simt_sync();   // D2, the Qb image and the staged slot are complete
             if (tid == 0) {
-                bulk_s2g(slot, base + kKG, static_cast<uint32_t>(kSlot2Bytes));
+                bulk_s2g(slot + kSlotP, base + kKG + kSlotP, static_cast<uint32_t>(kSlot2Bytes) - kSlotP);
                 bulk_commit();
             }
             Item nx;
