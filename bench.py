@@ -342,7 +342,7 @@ def bench_long(gdr2, hbm_gbs, steps=10, warmup=3):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes,
                          "traffic": traffic_record("prefill_" + name),
-                         "kernel": "gdr2 prefill: prep_kernel + state_kernel + scan_kernel + correct_kernel"}}
+                         "kernel": "gdr2 prefill: prep2_kernel + chain_kernel (segments) + scan_kernel + correct_kernel"}}
 
 
 def backward_bytes(B, T, H, dk, dv, esz=2):

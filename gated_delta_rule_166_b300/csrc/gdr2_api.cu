@@ -278,6 +278,42 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
         return rc;
     }
+    if (two_kernel_supports(a) && !cu && bcache == 0 && segments != 1) {
+        // Few long fixed-length sequences: segments of the chunk-parallel scan in affine
+        // form (prep2 over every chunk, the chain kernel over segments with value and
+        // transfer tiles, then the scan and the correction).
+        const int64_t nch = (T + 63) / 64;
+        int64_t G = segments > 0 ? (segments < nch ? segments : nch) : auto_segments(bh, dv, nch);
+        int64_t L = (nch + G - 1) / G;
+        L += L & 1;              // even: 128-row tiles of the correction stay in one segment
+        G = (nch + L - 1) / L;   // no empty segment
+        if (G > 1) {
+            SegArgs seg;
+            seg.G = static_cast<int>(G);
+            seg.L = static_cast<int>(L);
+            seg.Tr = T - L * 64;
+            const int64_t chunks = N * nch;
+            const size_t slot_bytes = round256(static_cast<size_t>(chunks) * static_cast<size_t>(H) * kSlot2Bytes);
+            const size_t nb_state = round256(static_cast<size_t>(N * G * H) * dk * dv * 4);   // also sT
+            const size_t nb_m = round256(static_cast<size_t>(N * G * H) * dk * dk * 4);
+            const size_t nb_o32 = round256(static_cast<size_t>(N * seg.Tr * H) * dv * 4);
+            const size_t nb_r = round256(static_cast<size_t>(N * seg.Tr * H) * dk * 4);
+            void* ws = nullptr;
+            if ((st = ws_alloc(&ws, slot_bytes + 2 * nb_state + nb_m + nb_o32 + nb_r, stream)) != GDR2_OK) return st;
+            uint8_t* p = static_cast<uint8_t*>(ws) + slot_bytes;
+            seg.seg_state = reinterpret_cast<float*>(p);
+            seg.sT = reinterpret_cast<float*>(p + nb_state);
+            seg.seg_m = reinterpret_cast<float*>(p + 2 * nb_state);
+            seg.o32 = reinterpret_cast<float*>(p + 2 * nb_state + nb_m);
+            seg.r = reinterpret_cast<float*>(p + 2 * nb_state + nb_m + nb_o32);
+            int rc = launch_prep2(a, static_cast<uint8_t*>(ws), nullptr, chunks, stream, err);
+            if (rc == GDR2_OK) rc = launch_chain(a, static_cast<const uint8_t*>(ws), nullptr, stream, err, seg);
+            if (rc == GDR2_OK) rc = launch_scan(a, seg, stream);
+            if (rc == GDR2_OK) rc = launch_correct(a, seg, stream, err);
+            if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
+            return rc;
+        }
+    }
     if (two_kernel_supports(a)) {
         // Segments of the chunk-parallel scan (fixed-length sequences only).
         const int64_t nch = (T + 63) / 64;

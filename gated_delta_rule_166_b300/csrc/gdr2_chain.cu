@@ -94,13 +94,29 @@ struct ChainParams {
     int T, H, dk, dv, nch, total;   // dk, dv <= 128 / 64 per tile; channels past them are zero padding
     int out_bf16;
     long long wait_cycles;   // limit of each handshake wait (copy drains keep the default)
+    // Segments (fixed-length sequences, G > 1): blockIdx.x = (sequence * G + g) * H + head
+    // runs chunks g L .. g L + L - 1.  Value tiles of segment 0 start from S0 and write o;
+    // those of later segments start from zero and write fp32 rows to o32.  Transfer tiles
+    // (blockIdx.y >= the value tiles, segments g >= 1) start from identity columns j0 ..
+    // of d_k with U = 0: their O rows are r_t = M_t^T q_t (M_t the map from the segment
+    // start to token t), written to r.  End states go to seg_state [sequence][head][g]
+    // [d_k][dv] (value) or seg_m [sequence][head][g][d_k][d_k] (transfer).
+    int G, L, Tr;            // G = 1: one pass, L = the chunks of a sequence
+    float *seg_state, *seg_m, *o32, *r;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
-    const int bh = static_cast<int>(blockIdx.x);
-    const int h = bh % prm.H, seq = bh / prm.H;
-    const int j0 = static_cast<int>(blockIdx.y) * kDVT;
+// One CTA; kTransfer: a transfer tile (identity start, U = 0), a separate
+// instantiation so that value tiles carry no test of the tile kind on their chain.
+template <bool kTransfer>
+__device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtensorMap& tm_o32, const CUtensorMap& tm_r,
+                                          const ChainParams& prm) {
+    const int ntv = (prm.dv + kDVT - 1) / kDVT;
+    const int h = static_cast<int>(blockIdx.x) % prm.H;
+    const int sg = static_cast<int>(blockIdx.x) / prm.H;
+    const int seq = sg / prm.G, g = sg - seq * prm.G;
+    if (kTransfer && g == 0) return;   // segment 0 starts from S0 itself: no transfer map
+    const int bh = seq * prm.H + h;
+    const int j0 = (kTransfer ? static_cast<int>(blockIdx.y) - ntv : static_cast<int>(blockIdx.y)) * kDVT;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -122,11 +138,19 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         T = e - a;
         chunk0 = prm.chunk_base[seq];
     } else {
-        T = prm.T;
-        tok0 = seq * T;
-        chunk0 = static_cast<int64_t>(seq) * prm.nch;
+        // chunks g L .. of the sequence: tokens counted from the segment's start
+        T = prm.T - g * prm.L * kC;
+        tok0 = seq * prm.T + g * prm.L * kC;
+        chunk0 = static_cast<int64_t>(seq) * prm.nch + static_cast<int64_t>(g) * prm.L;
     }
-    const int n = (T + kC - 1) / kC;
+    const int n = min((T + kC - 1) / kC, prm.L);
+    // o rows: the caller's o (one pass, or segment 0), else fp32 scratch rows
+    const bool to_o = prm.G == 1 || (!kTransfer && g == 0);
+    const CUtensorMap* const om = to_o ? &tm_o : (kTransfer ? &tm_r : &tm_o32);
+    const bool obf16 = to_o && prm.out_bf16;
+    const int ow = kTransfer ? kPrepDK : prm.dv;   // width of an output row
+    const int orow0 = to_o ? tok0 : seq * prm.Tr + (g - 1) * prm.L * kC;
+    void* const obase = to_o ? prm.o : (kTransfer ? static_cast<void*>(prm.r) : static_cast<void*>(prm.o32));
     auto slot_of = [&](int c) {
         return prm.slots + ((chunk0 + c) * prm.H + h) * static_cast<int64_t>(kSlot2Bytes);
     };
@@ -271,9 +295,9 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
             for (int c = 0; (c + 1) * kC <= T && c < n; ++c) {
                 if (!mbar_wait_ab(bar(kOFull), ph_full, abort_flag, prm.wait_cycles)) break;
                 ph_full ^= 1u;
-                const int row = tok0 + c * kC;
-                tma_store_4d(&tm_o, base + kO, j0, h, row, 0);
-                if (!prm.out_bf16 && j0 + 32 < prm.dv) tma_store_4d(&tm_o, base + kO + 8192u, j0 + 32, h, row, 0);
+                const int row = orow0 + c * kC;
+                tma_store_4d(om, base + kO, j0, h, row, 0);
+                if (!obf16 && j0 + 32 < ow) tma_store_4d(om, base + kO + 8192u, j0 + 32, h, row, 0);
                 bulk_commit();
                 bulk_wait_read();
                 mbar_arrive(bar(kOFree));
@@ -287,7 +311,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int R = warp >> 2;                 // column block: d_v columns 16R .. 16R + 15 of the tile
         const int j = 32 * quarter + lane;       // state row (key channel)
-        const bool obf16 = prm.out_bf16;
         bool failed = false;
         uint32_t c_ds0 = 0, c_ds1 = 0, c_do0 = 0, c_do1 = 0, c_of = 0;
         auto wait = [&](uint32_t b, uint32_t& cnt) {
@@ -331,6 +354,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                                            min(j0 + un, prm.dv - 1);
         const unsigned short* const wcol = reinterpret_cast<const unsigned short*>(prm.w) + (vcol - reinterpret_cast<const unsigned short*>(prm.v));
         auto fetch_vw = [&](int c, VW& x) {
+            if (kTransfer) return;   // U = 0
             const int t0 = c * kC + 8 * ug;
             if (t0 + 7 < T) {
                 const unsigned short* pv = vcol + static_cast<int64_t>(t0) * row_stride;
@@ -351,6 +375,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         };
         // U^T of chunk c (fp16 pair u = u_hi + u_lo) into buffer c & 1: row un, tokens 8 ug ..
         auto put_u = [&](int c, const VW& x) {
+            if (kTransfer) {   // U = 0
+                uint8_t* ub = sgen + kUB + 16384u * static_cast<uint32_t>(c & 1);
+                const uint32_t off = static_cast<uint32_t>(un) * 128u + ((static_cast<uint32_t>(ug) ^ (static_cast<uint32_t>(un) & 7u)) << 4);
+                *reinterpret_cast<uint4*>(ub + off) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(ub + 8192u + off) = make_uint4(0u, 0u, 0u, 0u);
+                return;
+            }
             const int tvalid = T - c * kC - 8 * ug;   // tokens past the sequence end give U = 0
             uint4 hk, lk;
             __half2* hh = reinterpret_cast<__half2*>(&hk);
@@ -373,9 +404,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         };
 
         float S[16];
-        {
-            // state rows past d_k and columns past d_v are zero padding
-            const bool live = j < prm.dk && j0 + 16 * R < prm.dv;
+        if (kTransfer) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) S[jj] = j == j0 + 16 * R + jj ? 1.f : 0.f;   // identity columns
+        } else {
+            // state rows past d_k and columns past d_v are zero padding; segments after the
+            // first start from zero
+            const bool live = j < prm.dk && j0 + 16 * R < prm.dv && g == 0;
             const float* s0 = prm.S0 && live ? prm.S0 + (static_cast<int64_t>(bh) * prm.dk + j) * prm.dv + j0 + 16 * R : nullptr;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
@@ -458,10 +493,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                         }
                     }
                     arrive(kOFull);
-                } else if (active && tc + r < T && j0 + 16 * R < prm.dv) {   // the last, partial chunk: row by row
-                    const int64_t off = ((static_cast<int64_t>(tok0) + tc + r) * prm.H + h) * prm.dv + j0 + 16 * R;
+                } else if (active && tc + r < T && j0 + 16 * R < ow) {   // the last, partial chunk: row by row
+                    const int64_t off = ((static_cast<int64_t>(orow0) + tc + r) * prm.H + h) * ow + j0 + 16 * R;
                     if (obf16) {
-                        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(prm.o) + off;
+                        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(obase) + off;
                         uint4 pk[2];
                         uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
@@ -472,7 +507,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
                         reinterpret_cast<uint4*>(op)[0] = pk[0];
                         reinterpret_cast<uint4*>(op)[1] = pk[1];
                     } else {
-                        float4* op = reinterpret_cast<float4*>(static_cast<float*>(prm.o) + off);
+                        float4* op = reinterpret_cast<float4*>(static_cast<float*>(obase) + off);
 #pragma unroll
                         for (int jj = 0; jj < 16; jj += 4)
                             op[jj / 4] = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
@@ -483,6 +518,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         if (failed) {
             *abort_flag = 1;
             if (lane == 0) atomicExch(prm.err, kDevTimeout);
+        } else if (prm.G > 1) {
+            // the segment's end state (d_k = 128 on this path)
+            float* st = (kTransfer ? prm.seg_m : prm.seg_state) +
+                        (static_cast<int64_t>(bh * prm.G + g) * kPrepDK + j) * ow + j0 + 16 * R;
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(st + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
         } else if (prm.ST && j < prm.dk && j0 + 16 * R < prm.dv) {
             float* st = prm.ST + (static_cast<int64_t>(bh) * prm.dk + j) * prm.dv + j0 + 16 * R;
 #pragma unroll
@@ -496,6 +538,15 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChainParams prm) {
         tc_fence_after();
         tmem_dealloc<kTmCols>(tmem);
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+chain_kernel(const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_o32,
+             const __grid_constant__ CUtensorMap tm_r, const ChainParams prm) {
+    if (static_cast<int>(blockIdx.y) >= (prm.dv + kDVT - 1) / kDVT)
+        chain_cta<true>(tm_o, tm_o32, tm_r, prm);
+    else
+        chain_cta<false>(tm_o, tm_o32, tm_r, prm);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -539,11 +590,25 @@ std::atomic<int64_t> g_wait_limit{0};
 
 int64_t set_chain_wait_limit(int64_t cycles) { return g_wait_limit.exchange(cycles); }
 
-int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err) {
+int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err,
+                 const SegArgs& seg) {
     if (a.cu && !chunk_base) return GDR2_ERR_ARG;
+    const bool segmented = seg.G > 1;
+    const int64_t nch = (a.T + kC - 1) / kC;
+    if (segmented && (a.cu || a.dk != kPrepDK || seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L >= nch ||
+                      !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r))
+        return GDR2_ERR_ARG;
     const int64_t total = a.cu ? a.total : a.B * a.T;
-    CUtensorMap mo;
+    CUtensorMap mo, mo32, mr;
     if (!make_row_map(&mo, a.o, total, a.H, a.dv, a.out_dtype != GDR2_BF16)) return GDR2_ERR_CUDA;
+    if (segmented) {
+        if (!make_row_map(&mo32, seg.o32, a.B * seg.Tr, a.H, a.dv, true) ||
+            !make_row_map(&mr, seg.r, a.B * seg.Tr, a.H, kPrepDK, true))
+            return GDR2_ERR_CUDA;
+    } else {
+        mo32 = mo;   // not read
+        mr = mo;
+    }
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -553,13 +618,19 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     ChainParams prm{slots, a.S0, static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
                     a.o, a.ST, err, a.cu, chunk_base, static_cast<int>(a.T), static_cast<int>(a.H),
-                    static_cast<int>(a.dk), static_cast<int>(a.dv), static_cast<int>((a.T + kC - 1) / kC),
+                    static_cast<int>(a.dk), static_cast<int>(a.dv), static_cast<int>(nch),
                     static_cast<int>(total),
-                    a.out_dtype == GDR2_BF16 ? 1 : 0, 0};
+                    a.out_dtype == GDR2_BF16 ? 1 : 0, 0,
+                    segmented ? seg.G : 1,
+                    segmented ? seg.L : (a.cu ? 0x7fffffff : static_cast<int>(nch)),
+                    segmented ? static_cast<int>(seg.Tr) : 0,
+                    seg.seg_state, seg.seg_m, seg.o32, seg.r};
     const int64_t lim = g_wait_limit.load();
     prm.wait_cycles = lim > 0 ? static_cast<long long>(lim) : kWaitCycles;
-    const dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>((a.dv + kDVT - 1) / kDVT));
-    chain_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mo, prm);
+    const int ntv = static_cast<int>((a.dv + kDVT - 1) / kDVT);
+    const dim3 grid(static_cast<unsigned>(a.B * (segmented ? seg.G : 1) * a.H),
+                    static_cast<unsigned>(ntv + (segmented ? kPrepDK / kDVT : 0)));
+    chain_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mo, mo32, mr, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 

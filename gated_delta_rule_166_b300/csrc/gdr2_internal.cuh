@@ -150,7 +150,11 @@ int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, in
                  int* err);
 // One CTA per (sequence * head, 64-column d_v tile): the chunk-to-chunk chain over the
 // slots of prep2, o and S_T.  Packed sequences pass the chunk_base that prep2 used.
-int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err);
+// With seg.G > 1 (fixed-length, d_k = 128) the chain runs over segments as the
+// segmented state pass does (value and transfer tiles, then launch_scan and
+// launch_correct).
+int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err,
+                 const SegArgs& seg = SegArgs{});
 // Limit of the chain kernel's handshake waits for later launches (0: the default);
 // returns the previous value.
 int64_t set_chain_wait_limit(int64_t cycles);
