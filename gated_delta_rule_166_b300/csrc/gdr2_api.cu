@@ -1,4 +1,5 @@
 // C ABI of libgdr2: host-side validation, dispatch, and the device error word.
+#include <algorithm>
 #include <mutex>
 
 #include "gdr2.h"
@@ -224,47 +225,82 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
     if (bcache > 0) {
         a.S_cache = S_cache;
         a.cache_chunks = cache_chunks;
-        segments = 1;   // cached states come from the sequential state pass
     }
-    if (noalloc && two_kernel_supports(a)) {
-        // The same two kernels over chunk ranges whose operands fit the scratch; the
-        // state between ranges is carried in S_T (or, when the caller wants no S_T,
-        // in the scratch).
-        void* scratch = nullptr;
-        if ((st = scratch_setup(&scratch)) != GDR2_OK) return st;
-        const int64_t nch = (T + 63) / 64;
-        const size_t carry = S_T ? 0 : (static_cast<size_t>(ns) * 4 + 255) / 256 * 256;
-        int64_t cpiece = 0;
-        while (cpiece < nch && carry + prep_workspace_bytes(N * (cpiece + 1), H, N) <= kNoAllocScratchBytes)
-            ++cpiece;
-        if (cpiece == 0) return GDR2_ERR_SCRATCH;
-        float* state = S_T ? S_T : reinterpret_cast<float*>(scratch);
-        const PrepSlots s = prep_carve(static_cast<uint8_t*>(scratch) + carry, N * cpiece, H);
-        for (int64_t c0 = 0; c0 < nch; c0 += cpiece) {
-            const int64_t cp = nch - c0 < cpiece ? nch - c0 : cpiece;
-            ForwardArgs ap = a;
-            ap.S0 = c0 == 0 ? S0 : state;
-            ap.ST = state;
-            int rc = launch_prep(ap, s, N * cp, static_cast<int>(c0), static_cast<int>(cp), stream, err);
-            if (rc == GDR2_OK)
-                rc = launch_state(ap, s, N * cp, static_cast<int>(c0), static_cast<int>(cp), stream, err);
-            if (rc != GDR2_OK) return rc;
-        }
-        return GDR2_OK;
-    }
-    // bf16 head sizes below the P-form kernels' (d_k < 128 or d_v = 32) run the
-    // affine-form kernels with zero-padded channels: TMA fills key channels past
-    // d_k with zeros (k = b = q = 0, log decay 0), so those state rows stay zero
-    // and add nothing; value columns past d_v are computed and never stored.
+    // bf16 inputs run the affine-form kernels.  Head sizes below d_k = 128 or d_v =
+    // 64 run them with zero-padded channels: TMA fills key channels past d_k with
+    // zeros (k = b = q = 0, log decay 0), so those state rows stay zero and add
+    // nothing; value columns past d_v are computed and never stored.
     ForwardArgs full = a;
     full.dk = kPrepDK;
     full.dv = 128;
-    const bool padded = (dk < kPrepDK || dv < 64) && two_kernel_supports(full);
-    if ((two_kernel_supports(a) || padded) && segments == 0 && bcache == 0 &&
-        (cu || padded || auto_segments(bh, dv, (T + 63) / 64) == 1)) {
-        // One pass over the chunks in affine form: prep2 writes each chunk's maps, the
-        // chain kernel carries the state; workspace (slots, then chunk_base of packed
-        // sequences) from the library's pool.
+    const bool exact = two_kernel_supports(a);
+    const bool padded = !exact && two_kernel_supports(full);
+    if (exact || padded) {
+        const int64_t nch = (T + 63) / 64;
+        if (noalloc) {
+            // chunk ranges whose slots fit the fixed scratch; the state between ranges is
+            // carried in S_T (or, when the caller wants no S_T, in the scratch)
+            void* scratch = nullptr;
+            if ((st = scratch_setup(&scratch)) != GDR2_OK) return st;
+            const size_t carry = S_T ? 0 : (static_cast<size_t>(ns) * 4 + 255) / 256 * 256;
+            const size_t per_chunk = static_cast<size_t>(N) * static_cast<size_t>(H) * kSlot2Bytes;
+            const int64_t cpiece = carry < kNoAllocScratchBytes
+                                       ? std::min<int64_t>(nch, static_cast<int64_t>((kNoAllocScratchBytes - carry) / per_chunk))
+                                       : 0;
+            if (cpiece == 0) return GDR2_ERR_SCRATCH;
+            float* state = S_T ? S_T : reinterpret_cast<float*>(scratch);
+            uint8_t* slots = static_cast<uint8_t*>(scratch) + carry;
+            for (int64_t c0 = 0; c0 < nch; c0 += cpiece) {
+                const int64_t cp = nch - c0 < cpiece ? nch - c0 : cpiece;
+                ForwardArgs ap = a;
+                ap.S0 = c0 == 0 ? S0 : state;
+                ap.ST = state;
+                int rc = launch_prep2(ap, slots, nullptr, N * cp, stream, err, static_cast<int>(c0), static_cast<int>(cp));
+                if (rc == GDR2_OK)
+                    rc = launch_chain(ap, slots, nullptr, stream, err, SegArgs{}, static_cast<int>(c0), static_cast<int>(cp));
+                if (rc != GDR2_OK) return rc;
+            }
+            return GDR2_OK;
+        }
+        if (segments > 1 && (cu || padded)) return GDR2_ERR_UNSUPPORTED;
+        if (exact && !cu && bcache == 0 && segments != 1) {
+            // Few long fixed-length sequences: segments of the chunk-parallel scan (prep2
+            // over every chunk, the chain kernel over segments with value and transfer
+            // tiles, then the scan and the correction).
+            int64_t G = segments > 0 ? (segments < nch ? segments : nch) : auto_segments(bh, dv, nch);
+            int64_t L = (nch + G - 1) / G;
+            L += L & 1;              // even: 128-row tiles of the correction stay in one segment
+            G = (nch + L - 1) / L;   // no empty segment
+            if (G > 1) {
+                SegArgs seg;
+                seg.G = static_cast<int>(G);
+                seg.L = static_cast<int>(L);
+                seg.Tr = T - L * 64;
+                const int64_t chunks = N * nch;
+                const size_t slot_bytes = round256(static_cast<size_t>(chunks) * static_cast<size_t>(H) * kSlot2Bytes);
+                const size_t nb_state = round256(static_cast<size_t>(N * G * H) * dk * dv * 4);   // also sT
+                const size_t nb_m = round256(static_cast<size_t>(N * G * H) * dk * dk * 4);
+                const size_t nb_o32 = round256(static_cast<size_t>(N * seg.Tr * H) * dv * 4);
+                const size_t nb_r = round256(static_cast<size_t>(N * seg.Tr * H) * dk * 4);
+                void* ws = nullptr;
+                if ((st = ws_alloc(&ws, slot_bytes + 2 * nb_state + nb_m + nb_o32 + nb_r, stream)) != GDR2_OK) return st;
+                uint8_t* p = static_cast<uint8_t*>(ws) + slot_bytes;
+                seg.seg_state = reinterpret_cast<float*>(p);
+                seg.sT = reinterpret_cast<float*>(p + nb_state);
+                seg.seg_m = reinterpret_cast<float*>(p + 2 * nb_state);
+                seg.o32 = reinterpret_cast<float*>(p + 2 * nb_state + nb_m);
+                seg.r = reinterpret_cast<float*>(p + 2 * nb_state + nb_m + nb_o32);
+                int rc = launch_prep2(a, static_cast<uint8_t*>(ws), nullptr, chunks, stream, err);
+                if (rc == GDR2_OK) rc = launch_chain(a, static_cast<const uint8_t*>(ws), nullptr, stream, err, seg);
+                if (rc == GDR2_OK) rc = launch_scan(a, seg, stream);
+                if (rc == GDR2_OK) rc = launch_correct(a, seg, stream, err);
+                if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
+                return rc;
+            }
+        }
+        // One pass over the chunks: prep2 writes each chunk's maps, the chain kernel
+        // carries the state (and keeps the cached states); workspace (slots, then
+        // chunk_base of packed sequences) from the library's pool.
         const int64_t chunks = prep_chunk_bound(a);
         const size_t slot_bytes = round256(static_cast<size_t>(chunks) * static_cast<size_t>(H) * kSlot2Bytes);
         void* ws = nullptr;
@@ -275,92 +311,6 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
         int rc = cu ? launch_chunk_base(a.cu, N, total, cb, stream) : GDR2_OK;
         if (rc == GDR2_OK) rc = launch_prep2(a, slots, cb, chunks, stream, err);
         if (rc == GDR2_OK) rc = launch_chain(a, slots, cb, stream, err);
-        if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
-        return rc;
-    }
-    if (two_kernel_supports(a) && !cu && bcache == 0 && segments != 1) {
-        // Few long fixed-length sequences: segments of the chunk-parallel scan in affine
-        // form (prep2 over every chunk, the chain kernel over segments with value and
-        // transfer tiles, then the scan and the correction).
-        const int64_t nch = (T + 63) / 64;
-        int64_t G = segments > 0 ? (segments < nch ? segments : nch) : auto_segments(bh, dv, nch);
-        int64_t L = (nch + G - 1) / G;
-        L += L & 1;              // even: 128-row tiles of the correction stay in one segment
-        G = (nch + L - 1) / L;   // no empty segment
-        if (G > 1) {
-            SegArgs seg;
-            seg.G = static_cast<int>(G);
-            seg.L = static_cast<int>(L);
-            seg.Tr = T - L * 64;
-            const int64_t chunks = N * nch;
-            const size_t slot_bytes = round256(static_cast<size_t>(chunks) * static_cast<size_t>(H) * kSlot2Bytes);
-            const size_t nb_state = round256(static_cast<size_t>(N * G * H) * dk * dv * 4);   // also sT
-            const size_t nb_m = round256(static_cast<size_t>(N * G * H) * dk * dk * 4);
-            const size_t nb_o32 = round256(static_cast<size_t>(N * seg.Tr * H) * dv * 4);
-            const size_t nb_r = round256(static_cast<size_t>(N * seg.Tr * H) * dk * 4);
-            void* ws = nullptr;
-            if ((st = ws_alloc(&ws, slot_bytes + 2 * nb_state + nb_m + nb_o32 + nb_r, stream)) != GDR2_OK) return st;
-            uint8_t* p = static_cast<uint8_t*>(ws) + slot_bytes;
-            seg.seg_state = reinterpret_cast<float*>(p);
-            seg.sT = reinterpret_cast<float*>(p + nb_state);
-            seg.seg_m = reinterpret_cast<float*>(p + 2 * nb_state);
-            seg.o32 = reinterpret_cast<float*>(p + 2 * nb_state + nb_m);
-            seg.r = reinterpret_cast<float*>(p + 2 * nb_state + nb_m + nb_o32);
-            int rc = launch_prep2(a, static_cast<uint8_t*>(ws), nullptr, chunks, stream, err);
-            if (rc == GDR2_OK) rc = launch_chain(a, static_cast<const uint8_t*>(ws), nullptr, stream, err, seg);
-            if (rc == GDR2_OK) rc = launch_scan(a, seg, stream);
-            if (rc == GDR2_OK) rc = launch_correct(a, seg, stream, err);
-            if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
-            return rc;
-        }
-    }
-    if (two_kernel_supports(a)) {
-        // Segments of the chunk-parallel scan (fixed-length sequences only).
-        const int64_t nch = (T + 63) / 64;
-        SegArgs seg;
-        if (!cu) {
-            int64_t G = segments > 0 ? (segments < nch ? segments : nch) : auto_segments(bh, dv, nch);
-            int64_t L = (nch + G - 1) / G;
-            L += L & 1;              // even: 128-row tiles of the correction stay in one segment
-            G = (nch + L - 1) / L;   // no empty segment
-            if (G > 1) {
-                seg.G = static_cast<int>(G);
-                seg.L = static_cast<int>(L);
-                seg.Tr = T - L * 64;
-            }
-        } else if (segments > 1) {
-            return GDR2_ERR_UNSUPPORTED;
-        }
-        // Workspace for the per-chunk operands (and the segments' maps and partial
-        // outputs), stream-ordered from the library's pool and released on the same
-        // stream.
-        const int64_t chunks = prep_chunk_bound(a);
-        const size_t wsb = round256(prep_workspace_bytes(chunks, H, N));
-        size_t nb_state = 0, nb_m = 0, nb_o32 = 0, nb_r = 0;
-        if (seg.G > 1) {
-            nb_state = round256(static_cast<size_t>(N * seg.G * H) * dk * dv * 4);   // also sT
-            nb_m = round256(static_cast<size_t>(N * seg.G * H) * dk * dk * 4);
-            nb_o32 = round256(static_cast<size_t>(N * seg.Tr * H) * dv * 4);
-            nb_r = round256(static_cast<size_t>(N * seg.Tr * H) * dk * 4);
-        }
-        void* ws = nullptr;
-        if ((st = ws_alloc(&ws, wsb + 2 * nb_state + nb_m + nb_o32 + nb_r, stream)) != GDR2_OK) return st;
-        const PrepSlots s = prep_carve(ws, chunks, H);
-        if (seg.G > 1) {
-            uint8_t* p = static_cast<uint8_t*>(ws) + wsb;
-            seg.seg_state = reinterpret_cast<float*>(p);
-            seg.sT = reinterpret_cast<float*>(p + nb_state);
-            seg.seg_m = reinterpret_cast<float*>(p + 2 * nb_state);
-            seg.o32 = reinterpret_cast<float*>(p + 2 * nb_state + nb_m);
-            seg.r = reinterpret_cast<float*>(p + 2 * nb_state + nb_m + nb_o32);
-        }
-        const int cpiece = static_cast<int>(nch);
-        int rc = launch_prep(a, s, chunks, 0, cpiece, stream, err);
-        if (rc == GDR2_OK) rc = launch_state(a, s, chunks, 0, cpiece, stream, err, seg);
-        if (seg.G > 1) {
-            if (rc == GDR2_OK) rc = launch_scan(a, seg, stream);
-            if (rc == GDR2_OK) rc = launch_correct(a, seg, stream, err);
-        }
         if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
         return rc;
     }

@@ -103,6 +103,12 @@ struct ChainParams {
     // [d_k][dv] (value) or seg_m [sequence][head][g][d_k][d_k] (transfer).
     int G, L, Tr;            // G = 1: one pass, L = the chunks of a sequence
     float *seg_state, *seg_m, *o32, *r;
+    // fixed-length: this launch covers chunks c0 .. c0 + nch - 1 of every sequence (its
+    // slots numbered from 0 per sequence); S0 is the state before chunk c0
+    int c0;
+    // the state after every cache_chunks chunks: [N][H][n_cache][d_k][dv] (null: not kept)
+    float* cache;
+    int cache_chunks, n_cache;
 };
 
 // One CTA; kTransfer: a transfer tile (identity start, U = 0), a separate
@@ -138,9 +144,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
         T = e - a;
         chunk0 = prm.chunk_base[seq];
     } else {
-        // chunks g L .. of the sequence: tokens counted from the segment's start
-        T = prm.T - g * prm.L * kC;
-        tok0 = seq * prm.T + g * prm.L * kC;
+        // chunks c0 + g L .. of the sequence: tokens counted from the first of them
+        T = prm.T - (prm.c0 + g * prm.L) * kC;
+        tok0 = seq * prm.T + (prm.c0 + g * prm.L) * kC;
         chunk0 = static_cast<int64_t>(seq) * prm.nch + static_cast<int64_t>(g) * prm.L;
     }
     const int n = min((T + kC - 1) / kC, prm.L);
@@ -448,6 +454,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(gam, S[jj], v[jj]);
             }
+            if (!kTransfer && prm.cache) {
+                // the state after chunk cc of the sequence, every cache_chunks chunks
+                const int cc = prm.c0 + c;
+                const int ci = (cc + 1) / prm.cache_chunks - 1;
+                if ((cc + 1) % prm.cache_chunks == 0 && ci < prm.n_cache && j < prm.dk && j0 + 16 * R < prm.dv) {
+                    float* cp = prm.cache + ((static_cast<int64_t>(bh) * prm.n_cache + ci) * prm.dk + j) * prm.dv + j0 + 16 * R;
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 4)
+                        *reinterpret_cast<float4*>(cp + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+                }
+            }
             if (c + 1 < n) {
                 // the other S^T buffer was read by chunk c - 1's products, which completed
                 // before that chunk's O was read out
@@ -591,10 +608,11 @@ std::atomic<int64_t> g_wait_limit{0};
 int64_t set_chain_wait_limit(int64_t cycles) { return g_wait_limit.exchange(cycles); }
 
 int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err,
-                 const SegArgs& seg) {
+                 const SegArgs& seg, int c0, int cpiece) {
     if (a.cu && !chunk_base) return GDR2_ERR_ARG;
     const bool segmented = seg.G > 1;
-    const int64_t nch = (a.T + kC - 1) / kC;
+    const int64_t nch = cpiece > 0 ? cpiece : (a.T + kC - 1) / kC;   // chunks per sequence in this launch
+    if ((segmented || a.cu) && (c0 != 0 || cpiece > 0)) return GDR2_ERR_ARG;
     if (segmented && (a.cu || a.dk != kPrepDK || seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L >= nch ||
                       !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r))
         return GDR2_ERR_ARG;
@@ -624,7 +642,9 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
                     segmented ? seg.G : 1,
                     segmented ? seg.L : (a.cu ? 0x7fffffff : static_cast<int>(nch)),
                     segmented ? static_cast<int>(seg.Tr) : 0,
-                    seg.seg_state, seg.seg_m, seg.o32, seg.r};
+                    seg.seg_state, seg.seg_m, seg.o32, seg.r, c0, a.S_cache,
+                    a.S_cache ? static_cast<int>(a.cache_chunks) : 1,
+                    a.S_cache ? static_cast<int>(a.T / (a.cache_chunks * kC)) : 0};
     const int64_t lim = g_wait_limit.load();
     prm.wait_cycles = lim > 0 ? static_cast<long long>(lim) : kWaitCycles;
     const int ntv = static_cast<int>((a.dv + kDVT - 1) / kDVT);

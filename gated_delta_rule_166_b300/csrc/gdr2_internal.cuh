@@ -77,43 +77,32 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
 int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream);
 
-// ---- two-kernel chunked prefill (bf16 inputs, d_k = 128) --------------------------
-// The preparation kernel writes, for every 64-token chunk of every (sequence,
-// head), the state-independent operands of that chunk into one workspace slot;
-// the state kernel then carries the state across the chunks of each sequence.
-// Slot index = (global chunk) * H + head, where a sequence's chunks are
-// numbered consecutively from chunk_base[sequence].
+// ---- chunked prefill in affine form (bf16 inputs) -----------------------------------
+// prep2 writes, for every 64-token chunk of every (sequence, head), the maps of the
+// chunk's state update
+//     S' = diag(gamma) S + M' S + Y U,      O = P S + X U      (U = w * v)
+// into one workspace slot, as fp16 images that the chain kernel copies to shared
+// memory unchanged: K-major (rows = M index), 128-byte swizzle, 64-element K blocks.
+// The chain kernel then carries the state across the chunks of each sequence.
+// Slot index = (global chunk) * H + head, where a sequence's chunks are numbered
+// consecutively from chunk_base[sequence] (packed sequences) or from sequence *
+// chunks per sequence.
 constexpr int kPrepC = 64;     // chunk length
-constexpr int kPrepDK = 128;   // key channels
-// The fp16 arrays are laid out for 16-byte loads whose 32 lanes read 512
-// contiguous bytes in the state kernel: 8 consecutive tokens (-Cb, Kb) or 8
-// consecutive key channels (Qb) per 16-byte group.
-struct PrepSlots {
-    uint16_t* a0;      // [slots][4][128][16]  [T; A_qk T] as fp16 in 16-column blocks:
-                       // [col / 16][row][col % 16] (rows 0..63 T, 64..127 A_qk T)
-    uint16_t* cbt;     // [slots][8][128][8]  -Cb: [token / 8][key channel][token % 8], fp16
-    uint16_t* kbt;     // [slots][8][128][8]  Kb, same layout
-    uint16_t* qb;      // [slots][16][64][8]  Qb: [channel / 8][token][channel % 8], fp16
-    float* gam;        // [slots][128]        e^{G_C} per key channel
-    int* chunk_base;   // [N + 1] first global chunk of each packed sequence (null: fixed length)
-};
-constexpr size_t kSlotBytes = 4 * 64 * 128 * 2 + 128 * 4;
+constexpr int kPrepDK = 128;   // key channels (smaller d_k: zero-padded channels)
+constexpr uint32_t kSlotM = 0;         // M' [d_k out (M)][d_k in (K)]: 2 K blocks x 128 rows x 128 B
+constexpr uint32_t kSlotY = 32768;     // Y  [d_k (M)][token (K)]:       1 K block x 128 rows x 128 B
+constexpr uint32_t kSlotP = 49152;     // P  [token (M)][d_k (K)]:       2 K blocks x 64 rows x 128 B
+constexpr uint32_t kSlotX = 65536;     // X  [token (M)][token (K)]:     1 K block x 64 rows x 128 B
+constexpr uint32_t kSlotGam = 73728;   // gamma = e^{G_C} [d_k] fp32
+constexpr size_t kSlot2Bytes = 74240;
 // Global chunks of a call: exact for fixed-length sequences, an upper bound
 // (ceil(total / 64) + N) for packed ones.
 int64_t prep_chunk_bound(const ForwardArgs& a);
-// Workspace bytes for `chunks` global chunks and N sequences; carve() lays the
-// arrays out in `ws` (256-byte aligned).
-size_t prep_workspace_bytes(int64_t chunks, int64_t H, int64_t N);
-PrepSlots prep_carve(void* ws, int64_t chunks, int64_t H);
-// Fixed-length calls may run chunks [c0, c0 + cpiece) of every sequence (the
-// slots then hold only those chunks, `chunks` = N * cpiece); the state kernel
-// starts from a.S0 and leaves the state after the range in a.ST.  Packed calls
-// ignore c0 and cpiece.
-int launch_prep(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
-                int* err);
-// Chunk-parallel scan over segments of the sequences (fixed-length calls with
-// c0 = 0): G segments of L chunks per sequence, L even (the last may be shorter,
-// none is empty).  The state kernel then runs every segment at once: value tiles from S0
+// bf16 inputs, d_k = 128, d_v in {64, 128} (the unpadded shapes; others run padded)
+bool two_kernel_supports(const ForwardArgs& a);
+// Chunk-parallel scan over segments of the sequences (fixed-length calls): G
+// segments of L chunks per sequence, L even (the last may be shorter, none is
+// empty).  The chain kernel runs every segment at once: value tiles from S0
 // (segment 0) or zero, transfer tiles from the identity with U = 0; launch_scan
 // chains the segments' affine maps S -> M S + N and launch_correct adds each later
 // segment's start-state term S_start^T r_t to its o rows.  G = 1: no segments.
@@ -126,35 +115,25 @@ struct SegArgs {
     float* r = nullptr;          // [B * Tr][H][d_k] r_t = M_t^T q_t of segments g >= 1
     float* sT = nullptr;         // [B][H][G][dv][d_k] S_start(g)^T (g >= 1)
 };
-int launch_state(const ForwardArgs& a, const PrepSlots& s, int64_t chunks, int c0, int cpiece, cudaStream_t stream,
-                 int* err, const SegArgs& seg = SegArgs{});
 // S_start of every segment and the final state (into a.ST when non-null); then o of
 // segments g >= 1 = o32 + S_start^T r in the output dtype.
 int launch_scan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream);
 int launch_correct(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream, int* err);
-bool two_kernel_supports(const ForwardArgs& a);
-
-// ---- two-kernel chunked prefill in affine form (fixed-length bf16, d_k = 128) ----
-// prep2 writes, for every (chunk, head), the maps of the chunk's state update
-//     S' = diag(gamma) S + M' S + Y U,      O = P S + X U      (U = w * v)
-// as fp16 images that the chain kernel copies to shared memory unchanged:
-// K-major (rows = M index), 128-byte swizzle, 64-element K blocks.
-constexpr uint32_t kSlotM = 0;         // M' [d_k out (M)][d_k in (K)]: 2 K blocks x 128 rows x 128 B
-constexpr uint32_t kSlotY = 32768;     // Y  [d_k (M)][token (K)]:       1 K block x 128 rows x 128 B
-constexpr uint32_t kSlotP = 49152;     // P  [token (M)][d_k (K)]:       2 K blocks x 64 rows x 128 B
-constexpr uint32_t kSlotX = 65536;     // X  [token (M)][token (K)]:     1 K block x 64 rows x 128 B
-constexpr uint32_t kSlotGam = 73728;   // gamma = e^{G_C} [d_k] fp32
-constexpr size_t kSlot2Bytes = 74240;
-// Slot index = (global chunk) * H + head; chunk_base as for the first form.
+// Fixed-length calls may prepare chunks [c0, c0 + cpiece) of every sequence only
+// (cpiece > 0; `chunks` = N * cpiece, slots numbered from 0 per sequence).
 int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, int64_t chunks, cudaStream_t stream,
-                 int* err);
+                 int* err, int c0 = 0, int cpiece = 0);
 // One CTA per (sequence * head, 64-column d_v tile): the chunk-to-chunk chain over the
 // slots of prep2, o and S_T.  Packed sequences pass the chunk_base that prep2 used.
 // With seg.G > 1 (fixed-length, d_k = 128) the chain runs over segments as the
 // segmented state pass does (value and transfer tiles, then launch_scan and
 // launch_correct).
+// Fixed-length calls may run chunks [c0, c0 + cpiece) of every sequence (cpiece > 0;
+// the slots then hold only those chunks, numbered from 0 per sequence): S0 is the
+// state before chunk c0, and S_T receives the state after the range.  a.S_cache
+// (fixed-length, one pass) keeps the state after every a.cache_chunks chunks.
 int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_base, cudaStream_t stream, int* err,
-                 const SegArgs& seg = SegArgs{});
+                 const SegArgs& seg = SegArgs{}, int c0 = 0, int cpiece = 0);
 // Limit of the chain kernel's handshake waits for later launches (0: the default);
 // returns the previous value.
 int64_t set_chain_wait_limit(int64_t cycles);

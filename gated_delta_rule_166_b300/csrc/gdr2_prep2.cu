@@ -138,6 +138,7 @@ struct Prep2Params {
     int N, T, H, total;
     int nitems;           // global chunk bound x H; item = slot index
     int* err;
+    int c0, cpiece;       // fixed-length: chunks c0 .. c0 + cpiece - 1 of every sequence
 };
 
 struct Item {
@@ -160,11 +161,10 @@ __device__ __forceinline__ bool locate(const Prep2Params& prm, int it, Item& x) 
         x.T = e - a;
         x.tp = (gc - cb[lo]) * kC;
     } else {
-        const int nch = (prm.T + kC - 1) / kC;
-        const int seq = gc / nch;
+        const int seq = gc / prm.cpiece;
         x.tok0 = seq * prm.T;
         x.T = prm.T;
-        x.tp = (gc - seq * nch) * kC;
+        x.tp = (prm.c0 + gc - seq * prm.cpiece) * kC;
     }
     return true;
 }
@@ -762,10 +762,60 @@ bool make_token_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// First global chunk of each packed sequence: cb[s] = sum_{s' < s} ceil(len_s' / 64),
+// with the same offset clamping the kernels use.  One CTA.
+__global__ void chunk_base_kernel(const int* cu, int N, int total, int* cb) {
+    __shared__ int part[1024];
+    const int tid = threadIdx.x;
+    const int per = (N + blockDim.x - 1) / blockDim.x;
+    const int s0 = tid * per, s1 = min(N, s0 + per);
+    auto nch = [&](int s) {
+        const int a = min(max(cu[s], 0), total);
+        const int e = min(max(cu[s + 1], a), total);
+        return (e - a + kC - 1) / kC;
+    };
+    int sum = 0;
+    for (int s = s0; s < s1; ++s) sum += nch(s);
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {   // exclusive scan of the partial sums
+        int run = 0;
+        for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
+            const int x = part[i];
+            part[i] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    int run = part[tid];
+    for (int s = s0; s < s1; ++s) {
+        cb[s] = run;
+        run += nch(s);
+    }
+    if (s1 == N && s0 < s1) cb[N] = run;
+    if (N == 0 && tid == 0) cb[0] = 0;
+}
+
 }  // namespace
 
+bool two_kernel_supports(const ForwardArgs& a) {
+    const int64_t total = a.cu ? a.total : a.B * a.T;
+    return a.in_dtype == GDR2_BF16 && a.dk == kDK && (a.dv == 64 || a.dv == 128) && total > 0 &&
+           total < (1ll << 31) && a.B * a.H < (1ll << 31) && a.H <= 65535 && get_encode() != nullptr;
+}
+
+int launch_chunk_base(const int* cu, int64_t N, int64_t total, int* chunk_base, cudaStream_t stream) {
+    chunk_base_kernel<<<1, 1024, 0, stream>>>(cu, static_cast<int>(N), static_cast<int>(total), chunk_base);
+    return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
+int64_t prep_chunk_bound(const ForwardArgs& a) {
+    if (!a.cu) return a.B * ((a.T + kC - 1) / kC);
+    return (a.total + kC - 1) / kC + a.B;
+}
+
 int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, int64_t chunks, cudaStream_t stream,
-                 int* err) {
+                 int* err, int c0, int cpiece) {
     const int64_t total = a.cu ? a.total : a.B * a.T;
     if (chunks <= 0) return GDR2_OK;
     const int64_t nitems = chunks * a.H;
@@ -785,8 +835,10 @@ int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, in
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return GDR2_ERR_CUDA;
+    const int nch = static_cast<int>((a.T + kC - 1) / kC);
+    if (!a.cu && (c0 < 0 || cpiece < 0 || c0 + cpiece > nch)) return GDR2_ERR_ARG;
     Prep2Params prm{slots, chunk_base, a.cu, static_cast<int>(a.B), static_cast<int>(a.T), static_cast<int>(a.H),
-                    static_cast<int>(total), static_cast<int>(nitems), err};
+                    static_cast<int>(total), static_cast<int>(nitems), err, c0, cpiece > 0 ? cpiece : nch};
     const unsigned grid = static_cast<unsigned>(nitems < sms ? nitems : sms);
     prep2_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;

@@ -153,13 +153,14 @@ int gdr2_forward_varlen(const void* q, const void* k, const void* v,
  * library's stream-ordered workspace pool (which gdr2_forward uses).
  *
  * Same arguments, layouts, results and error codes as gdr2_forward.  For bf16
- * inputs with d_k = 128 the two prefill kernels run over ranges of chunks
- * whose per-chunk operands fit a fixed 64 MiB device array inside the library
- * (file-scope memory that every GPU which loads the library holds until the
- * process exits): a range covers min(all, floor(scratch / (B*H*66,048 B)))
- * chunks of every sequence, and the state is carried between ranges in S_T (in
- * the scratch when S_T is NULL).  B*H above about 1000 (fewer when S_T is NULL)
- * returns GDR2_ERR_SCRATCH before anything is enqueued.  Other inputs run the
+ * inputs the two prefill kernels run over ranges of chunks whose per-chunk
+ * maps fit a fixed 64 MiB device array inside the library (file-scope memory
+ * that every GPU which loads the library holds until the process exits): a
+ * range covers min(all, floor(scratch / (B*H*74,240 B))) chunks of every
+ * sequence, and the state is carried between ranges in S_T (in the scratch
+ * when S_T is NULL).  The results are bit for bit those of gdr2_forward_segmented
+ * with one segment.  B*H above about 900 (fewer when S_T is NULL) returns
+ * GDR2_ERR_SCRATCH before anything is enqueued.  fp32 inputs run the
  * token-sequential kernel, which needs no scratch.
  *
  * Every call shares the one array per device: two calls that overlap on the
@@ -220,7 +221,8 @@ int gdr2_forward_segmented(const void* q, const void* k, const void* v,
  * (cache_chunks * 64)) (segments of cache_chunks 64-token chunks; a final
  * partial segment is not cached -- its end state is S_T).  How the cached
  * states are combined with the readout is the caller's; the library computes o
- * and S_T exactly as gdr2_forward.
+ * and S_T as gdr2_forward_segmented with one segment does, bit for bit (the
+ * chain kernel writes the cached states as it passes them).
  *
  *   S_cache      : [B, H, n_cache, dk, dv] fp32, written (may be NULL when n_cache = 0)
  *   cache_chunks : >= 1, segment length in 64-token chunks
