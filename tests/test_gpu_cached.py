@@ -59,3 +59,18 @@ def test_cached_states_fp32_token_kernel_and_short_sequence():
     _, _, C = gdr2.forward_cached(*y.tensors(), y.S0, cache_chunks=2)
     torch.cuda.synchronize()
     assert C.shape[2] == 0 and gdr2.gdr2_device_status() == 0
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 32), (32, 128)])
+def test_cached_states_small_head_dims(dk, dv):
+    """Small bf16 head sizes (zero-padded channels in the chunked kernels)."""
+    x = make_prefill_inputs(1, 700, 2, dk, dv, dtype=torch.bfloat16, seed=880 + dk + dv, s0_std=0.4)
+    d = x.to("cuda")
+    o, S_T, S_cache = gdr2.forward_cached(*d.tensors(), d.S0, cache_chunks=2)
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    n = 700 // 128
+    ref = oracle_segment_states(x, 128, n)
+    assert err_over_rms(S_cache.cpu().numpy(), ref) <= tol_for(torch.bfloat16)
+    o1, S1 = gdr2.forward(*d.tensors(), d.S0, segments=1)
+    assert torch.equal(o, o1) and torch.equal(S_T, S1)

@@ -81,14 +81,17 @@ def _noalloc_twice(x, return_state=True):
     return outs
 
 
-@pytest.mark.parametrize("case", ["layer_with_S0", "ragged_many_heads"])
+@pytest.mark.parametrize("case", ["layer_with_S0", "ragged_many_heads", "small_head_dims"])
 def test_noalloc_matches_oracle_and_forward_on_two_calls(case):
     if case == "layer_with_S0":
-        # B*H = 64: ranges of 12 chunks, the state carried in S_T across 6 ranges
+        # B*H = 64: ranges of 14 chunks, the state carried in S_T across 5 ranges
         xh = make_workload("gdn2_layer_T4096", s0_std=0.02)
-    else:
-        # B*H = 128: ranges of 6 chunks over 16 chunks, the last one partial
+    elif case == "ragged_many_heads":
+        # B*H = 128: ranges of 7 chunks over 16 chunks, the last one partial
         xh = make_prefill_inputs(8, 1000, 16, 128, 128, seed=11, decay_regime="slow", s0_std=0.3)
+    else:
+        # d_k = 64, d_v = 32 (zero-padded channels); B*H = 480: ranges of 1 chunk
+        xh = make_prefill_inputs(30, 300, 16, 64, 32, seed=12, s0_std=0.3)
     x = xh.to("cuda")
     # the same kernels over the whole sequence at once (one sequential state pass)
     ref_o, ref_S = gdr2.forward(*x.tensors(), x.S0, segments=1)
