@@ -353,10 +353,11 @@ def backward_bytes(B, T, H, dk, dv, esz=2):
     return tok + B * H * dk * dv * 4
 
 
-def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None):
-    """gdr2_backward over the GDN-2 layer workload (or its first `batch` sequences)
+def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None, chunked=True):
+    """The gradients over the GDN-2 layer workload (or its first `batch` sequences)
     with a seeded fp32 gradient at o (no gradient at S_T), CUDA events around
-    `steps` calls."""
+    `steps` calls: gdr2_backward_chunked (chunkwise WY form on tensor cores) or,
+    with chunked=False, the exact token-sequential gdr2_backward."""
     if batch is not None and batch < x.q.shape[0]:
         from gated_delta_rule_166_b300.inputs import PrefillInputs
 
@@ -367,13 +368,14 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None):
     gen = torch.Generator().manual_seed(11)
     d_o = torch.randn(B, T, H, dv, generator=gen).to("cuda")
     stream = torch.cuda.current_stream()
+    fn = gdr2.backward_chunked if chunked else gdr2.backward
     for _ in range(warmup):
-        gdr2.backward(*x.tensors(), x.S0, d_o, None)
+        fn(*x.tensors(), x.S0, d_o, None)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(steps):
-        gdr2.backward(*x.tensors(), x.S0, d_o, None)
+        fn(*x.tensors(), x.S0, d_o, None)
     b.record(stream)
     torch.cuda.synchronize()
     if gdr2.gdr2_device_status() != 0:
@@ -381,14 +383,18 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None):
     ms = a.elapsed_time(b) / steps
     nbytes = backward_bytes(B, T, H, dk, dv)
     achieved = nbytes / (ms / 1e3) / 1e9
+    kind = "chunked" if chunked else "exact"
+    kernels = ("gdr2_backward_chunked: prep2_kernel (maps and backward records) + chain_kernel (start "
+               "states) + rchain_kernel + cgrad_kernel per call" if chunked else
+               "gdr2_backward: bwd_kernel + bwd_reduce_kernel per call")
     return {"workload": f"{WORKLOAD} backward (B={B}): gradients of all six inputs and S0, fp32, from a "
                         f"seeded fp32 gradient at o",
-            "ms_per_call": ms, "tokens_per_s": B * T / (ms / 1e3), "steps": steps, "warmup": warmup,
-            "launches_per_call": 2,
+            "path": kind, "ms_per_call": ms, "tokens_per_s": B * T / (ms / 1e3), "steps": steps,
+            "warmup": warmup, "launches_per_call": 4 if chunked else 2,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes,
-                         "traffic": traffic_record("backward_" + WORKLOAD),
-                         "kernel": "gdr2 backward: bwd_kernel + bwd_reduce_kernel per call"}}
+                         "traffic": traffic_record(("backward_chunked_" if chunked else "backward_") + WORKLOAD),
+                         "kernel": kernels}}
 
 
 def bench_sparse(gdr2, hbm_gbs, steps=10, warmup=3):
@@ -610,8 +616,10 @@ def main():
     if args.only == "backward":
         bw = bench_backward(gdr2, hbm_gbs, x, steps=min(args.steps, 5), warmup=args.warmup,
                             batch=args.backward_batch)
+        bx = bench_backward(gdr2, hbm_gbs, x, steps=min(args.steps, 5), warmup=args.warmup,
+                            batch=args.backward_batch, chunked=False)
         if rank == 0:
-            print(json.dumps({"backward": bw}))
+            print(json.dumps({"backward": bw, "backward_exact": bx}))
         return
     if args.only == "long":
         lc = bench_long(gdr2, hbm_gbs, steps=min(args.steps, 10), warmup=args.warmup)
@@ -687,6 +695,7 @@ def main():
         out["long_context"] = bench_long(gdr2, hbm_gbs)
     if not args.no_backward:
         out["backward"] = bench_backward(gdr2, hbm_gbs, x)
+        out["backward_exact"] = bench_backward(gdr2, hbm_gbs, x, chunked=False)
     if not args.no_sparse:
         out["sparse_write"] = bench_sparse(gdr2, hbm_gbs)
     if rank == 0 and not args.no_cpu_baseline:

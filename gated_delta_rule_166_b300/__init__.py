@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     GatedDeltaRule2,
     gdr2_apply,
     gdr2_backward,
+    gdr2_backward_chunked,
     gdr2_decode_step,
     gdr2_device_status,
     gdr2_forward,
@@ -31,4 +32,5 @@ forward_noalloc = gdr2_forward_noalloc
 forward_cached = gdr2_forward_cached
 decode_step = gdr2_decode_step
 backward = gdr2_backward
+backward_chunked = gdr2_backward_chunked
 sparse_write = gdr2_sparse_write

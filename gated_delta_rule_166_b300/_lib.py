@@ -54,6 +54,8 @@ def lib():
         L.gdr2_forward_cached.restype = ci
         L.gdr2_backward.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
         L.gdr2_backward.restype = ci
+        L.gdr2_backward_chunked.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
+        L.gdr2_backward_chunked.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
         L.gdr2_decode_step.restype = ci
         L.gdr2_device_status.argtypes = [vp]
@@ -236,13 +238,24 @@ def gdr2_backward(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bo
     [B, H, dk, dv] or None); d_o: [B, T, H, dv] gradient at o; d_S_T: [B, H, dk,
     dv] gradient at S_T or None.  Returns fp32 tensors (dq, dk, dv, db, dw,
     dlog_decay, dS0), dS0 None when ``want_dS0`` is False."""
+    return _backward("gdr2_backward", q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream)
+
+
+def gdr2_backward_chunked(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bool = True,
+                          stream=None):
+    """gdr2_backward through the chunkwise WY form on tensor cores: bf16 inputs
+    with dk = dv = 128, the same arguments and outputs."""
+    return _backward("gdr2_backward_chunked", q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream)
+
+
+def _backward(fn, q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream):
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q and v must be [B, T, H, d]")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dtype, dev = q.dtype, q.device
     if dev.type != "cuda":
-        raise ValueError("gdr2_backward runs on CUDA tensors only")
+        raise ValueError(f"{fn} runs on CUDA tensors only")
     if dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
@@ -257,12 +270,12 @@ def gdr2_backward(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bo
     gv, gw = (torch.empty((B, T, H, dv), **f32) for _ in range(2))
     gS0 = torch.empty((B, H, dk, dv), **f32) if want_dS0 else None
     with torch.cuda.device(dev):
-        st = lib().gdr2_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
-                                 _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
-                                 _ptr(gg), _ptr(gS0), B, T, H, dk, dv, _DTYPES[dtype],
-                                 ctypes.c_void_p(_stream_handle(stream)))
+        st = getattr(lib(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
+                                _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
+                                _ptr(gg), _ptr(gS0), B, T, H, dk, dv, _DTYPES[dtype],
+                                ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
-        raise GDR2Error(st, "gdr2_backward")
+        raise GDR2Error(st, fn)
     return gq, gk, gv, gb, gw, gg, gS0
 
 

@@ -365,13 +365,14 @@ extern "C" int gdr2_forward_segmented(const void* q, const void* k, const void* 
                         out_dtype, stream, /*noalloc=*/false, segments);
 }
 
-extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
-                             const void* b, const void* w, const void* log_decay,
-                             const float* S0, const float* d_o, const float* d_S_T,
-                             float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
-                             float* d_log_decay, float* d_S0,
-                             int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
-                             int in_dtype, cudaStream_t stream) {
+namespace {
+
+// Shared by the token-sequential and the chunked backward: the same arguments,
+// checks and empty-sequence behaviour.
+int backward_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
+                  const void* log_decay, const float* S0, const float* d_o, const float* d_S_T, float* d_q,
+                  float* d_k, float* d_v, float* d_b, float* d_w, float* d_log_decay, float* d_S0, int64_t B,
+                  int64_t T, int64_t H, int64_t dk, int64_t dv, int in_dtype, cudaStream_t stream, bool chunked) {
     if (B < 0 || T < 0 || H < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
@@ -401,7 +402,9 @@ extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
         for (int j = i + 1; j < 7; ++j)
             if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return GDR2_ERR_ALIAS;
     }
-    int st = device_setup(nullptr);
+    if (chunked && (in_dtype != GDR2_BF16 || dk != kPrepDK || dv != 128)) return GDR2_ERR_UNSUPPORTED;
+    int* err = nullptr;
+    int st = device_setup(&err);
     if (st != GDR2_OK) return st;
     if (bh == 0) return GDR2_OK;
     if (!has_tokens) {   // no tokens: dS0 = dS_T (or zero)
@@ -413,11 +416,37 @@ extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
     BackwardArgs a{q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                    B, T, H, dk, dv, in_dtype};
     void* ws = nullptr;
-    if ((st = ws_alloc(&ws, backward_workspace_bytes(B, T, H, dk, dv), stream)) != GDR2_OK) return st;
-    int rc = launch_backward(a, ws, stream);
+    const size_t wsb = chunked ? backward_chunked_workspace_bytes(B, T, H) : backward_workspace_bytes(B, T, H, dk, dv);
+    if ((st = ws_alloc(&ws, wsb, stream)) != GDR2_OK) return st;
+    int rc = chunked ? launch_backward_chunked(a, ws, stream, err) : launch_backward(a, ws, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
     return rc;
 }
+
+}  // namespace
+
+extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
+                             const void* b, const void* w, const void* log_decay,
+                             const float* S0, const float* d_o, const float* d_S_T,
+                             float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                             float* d_log_decay, float* d_S0,
+                             int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                             int in_dtype, cudaStream_t stream) {
+    return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                         B, T, H, dk, dv, in_dtype, stream, false);
+}
+
+extern "C" int gdr2_backward_chunked(const void* q, const void* k, const void* v,
+                                     const void* b, const void* w, const void* log_decay,
+                                     const float* S0, const float* d_o, const float* d_S_T,
+                                     float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                     float* d_log_decay, float* d_S0,
+                                     int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                     int in_dtype, cudaStream_t stream) {
+    return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                         B, T, H, dk, dv, in_dtype, stream, true);
+}
+
 
 extern "C" int gdr2_forward_cached(const void* q, const void* k, const void* v,
                                    const void* b, const void* w, const void* log_decay,

@@ -76,6 +76,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // checkpoints and the per-tile row-vector partials.
 size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
 int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream);
+// Chunked gradients (bf16 inputs, d_k = d_v = 128, T > 0): the forward's prep2 (with
+// backward records) and chain kernels keep every chunk's maps and start state, the
+// reverse chain carries dS across the chunks, one CTA per (chunk, head) forms the
+// token gradients (gdr2_bwd_chunk.cu).
+size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H);
+int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err);
 
 // ---- chunked prefill in affine form (bf16 inputs) -----------------------------------
 // prep2 writes, for every 64-token chunk of every (sequence, head), the maps of the
@@ -95,6 +101,12 @@ constexpr uint32_t kSlotP = 49152;     // P  [token (M)][d_k (K)]:       2 K blo
 constexpr uint32_t kSlotX = 65536;     // X  [token (M)][token (K)]:     1 K block x 64 rows x 128 B
 constexpr uint32_t kSlotGam = 73728;   // gamma = e^{G_C} [d_k] fp32
 constexpr size_t kSlot2Bytes = 74240;
+// Backward record of a (chunk, head) item, written by prep2 in its backward mode:
+// the fp16 images of W^T [d_k (rows)][token], A_qk [token][token], T [token][token]
+// (K-major, one 64-element K block) and Cb, Kb [token][d_k] (two K blocks), with
+// Cb = (b k) e^{G}, Kb = k e^{G_C - G}, T = (I + A_kk)^-1 and W = T Cb.
+constexpr uint32_t kWyWt = 0, kWyAq = 16384, kWyT = 24576, kWyCb = 32768, kWyKb = 49152;
+constexpr uint32_t kWyBytes = 65536;
 // Global chunks of a call: exact for fixed-length sequences, an upper bound
 // (ceil(total / 64) + N) for packed ones.
 int64_t prep_chunk_bound(const ForwardArgs& a);
@@ -121,8 +133,9 @@ int launch_scan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream);
 int launch_correct(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream, int* err);
 // Fixed-length calls may prepare chunks [c0, c0 + cpiece) of every sequence only
 // (cpiece > 0; `chunks` = N * cpiece, slots numbered from 0 per sequence).
+// wy (non-null): also the backward record of every item, [chunks * H][kWyBytes].
 int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, int64_t chunks, cudaStream_t stream,
-                 int* err, int c0 = 0, int cpiece = 0);
+                 int* err, int c0 = 0, int cpiece = 0, uint8_t* wy = nullptr);
 // One CTA per (sequence * head, 64-column d_v tile): the chunk-to-chunk chain over the
 // slots of prep2, o and S_T.  Packed sequences pass the chunk_base that prep2 used.
 // With seg.G > 1 (fixed-length, d_k = 128) the chain runs over segments as the

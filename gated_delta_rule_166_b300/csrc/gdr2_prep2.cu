@@ -88,6 +88,10 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kTmemSlot + 4 <= kSmemBytes, "misc area");
 static_assert(kSmemAlloc <= 232448, "shared memory");
 static_assert(kSlot2Bytes <= 4 * kKGStride, "slot staging in the K-group area");
+// the backward record copies [W^T | A_qk | T] from the K-group area and [Cb | Kb] as they lie
+static_assert(kB1 + 8192u + kWyWt == kKG + 8192u && kAq == kB1 + 8192u + (kWyAq - kWyWt) &&
+                  kTo == kB1 + 8192u + (kWyT - kWyWt) && kKB == kCB + (kWyKb - kWyCb),
+              "backward record layout");
 
 // ---- TMEM columns ---------------------------------------------------------------
 // The next item's d offsets land in kTmA while this item's map products (D1, D2)
@@ -139,6 +143,7 @@ struct Prep2Params {
     int nitems;           // global chunk bound x H; item = slot index
     int* err;
     int c0, cpiece;       // fixed-length: chunks c0 .. c0 + cpiece - 1 of every sequence
+    uint8_t* wy;          // backward records [items][kWyBytes], or null (prep2_kernel<true> only)
 };
 
 struct Item {
@@ -169,6 +174,9 @@ __device__ __forceinline__ bool locate(const Prep2Params& prm, int it, Item& x) 
     return true;
 }
 
+// kWY: also write each item's W^T, A_qk, T, Cb and Kb images to its backward record
+// (the operands of the chunk gradients, gdr2_bwd_chunk.cu).
+template <bool kWY>
 __global__ void __launch_bounds__(kThreads, 1)
 prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_g,
@@ -653,11 +661,22 @@ prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     mma_ss_f16(tmem + kTmD2, dAq + 2u * s, dB1 + 2u * s, idesc_f16x(64, 192, 0, 0, 0), s > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(kDDone));
+                if (kWY) {
+                    // backward record: [W^T | A_qk | T] (contiguous in the K-group area) and [Cb | Kb]
+                    uint8_t* const rec = prm.wy + static_cast<int64_t>(it) * kWyBytes;
+                    bulk_s2g(rec + kWyWt, base + kB1 + 8192u, kWyCb - kWyWt);
+                    bulk_s2g(rec + kWyCb, base + kCB, kWyBytes - kWyCb);
+                    bulk_commit();
+                }
             }
             // ---- slot images: Y, M' = -Kb^T W (rows d_k), X, P = Qb - A_qk W (rows tokens) ----
             // K-major fp16 images staged in the K-group area (its operands are consumed),
             // then one bulk copy to the workspace slot
             if (!wait_done(kDDone, ph)) { failed = true; break; }
+            if (kWY) {
+                if (tid == 0) bulk_wait_read();   // the record copy has read the K-group area
+                simt_sync();
+            }
             uint8_t* const stage = sgen + kKG;
             {
                 auto put_row = [&](uint32_t img, uint32_t kblk, uint32_t row, uint32_t k0, const float (&v)[16], bool neg) {
@@ -815,7 +834,7 @@ int64_t prep_chunk_bound(const ForwardArgs& a) {
 }
 
 int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, int64_t chunks, cudaStream_t stream,
-                 int* err, int c0, int cpiece) {
+                 int* err, int c0, int cpiece, uint8_t* wy) {
     const int64_t total = a.cu ? a.total : a.B * a.T;
     if (chunks <= 0) return GDR2_OK;
     const int64_t nitems = chunks * a.H;
@@ -827,8 +846,11 @@ int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, in
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prep2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(prep2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(kSmemAlloc));
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(prep2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     int dev = 0, sms = 0;
@@ -838,9 +860,12 @@ int launch_prep2(const ForwardArgs& a, uint8_t* slots, const int* chunk_base, in
     const int nch = static_cast<int>((a.T + kC - 1) / kC);
     if (!a.cu && (c0 < 0 || cpiece < 0 || c0 + cpiece > nch)) return GDR2_ERR_ARG;
     Prep2Params prm{slots, chunk_base, a.cu, static_cast<int>(a.B), static_cast<int>(a.T), static_cast<int>(a.H),
-                    static_cast<int>(total), static_cast<int>(nitems), err, c0, cpiece > 0 ? cpiece : nch};
+                    static_cast<int>(total), static_cast<int>(nitems), err, c0, cpiece > 0 ? cpiece : nch, wy};
     const unsigned grid = static_cast<unsigned>(nitems < sms ? nitems : sms);
-    prep2_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
+    if (wy)
+        prep2_kernel<true><<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
+    else
+        prep2_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mb, mg, prm);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 

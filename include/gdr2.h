@@ -278,6 +278,40 @@ int gdr2_backward(const void* q, const void* k, const void* v,
                   int in_dtype, cudaStream_t stream);
 
 /*
+ * gdr2_backward_chunked -- the gradients of gdr2_backward (same arguments, same
+ * outputs) through the chunkwise WY form on tensor cores, for bf16 inputs with
+ * dk = dv = 128 (GDR2_ERR_UNSUPPORTED otherwise).  Per 64-token chunk, with
+ * start state S, the gradient dS' at its end state and dO at its outputs
+ * (Cb = c e^G, Qb = q e^G, Kb = k e^{G_C - G}, Kh = k e^{-G}, u = w (.) v,
+ * A_kk = strict_tril(Cb Kh^T), A_qk = tril(Qb Kh^T), T = (I + A_kk)^-1,
+ * W = T Cb, E = T u - W S):
+ *     dE = A_qk^T dO + Kb dS',   dA_qk = tril(dO E^T),   dKb = E dS'^T,
+ *     dW = -dE S^T,   du = T^T dE,   dT = dE u^T + dW Cb^T,
+ *     dA_kk = strict_tril(-T^T dT T^T),   dCb = T^T dW + dA_kk Kh,
+ *     dQb = dO S^T + dA_qk Kh,   dKh = dA_kk^T Cb + dA_qk^T Qb,
+ * then through the exponential factors and the prefix sums of log_decay; dS'
+ * runs from chunk to chunk as dS = diag(e^{G_C}) dS' + Qb^T dO - W^T dE.  The
+ * products take fp16 operands (tf32 for the decay-weighted ones) with fp32
+ * accumulation, like the chunked forward, where gdr2_backward keeps fp32
+ * throughout (max|err| / RMS within 1e-4).  Against exact gradients the chunked
+ * ones stay within 2e-2 (max|err| / RMS) except db and dlog_decay under fast
+ * decays (about e^-2 per token in every channel): those two are differences of
+ * chunk terms 30 to 60 times their size, and reach about 7e-2 there.  Per-token
+ * log decays below -10 count as -10, as in the chunked forward.  Workspace (the library's pool, released on the stream): per
+ * (chunk, head) 139,776 bytes (the forward's maps and backward record) plus
+ * 128 KB of start state and end-state gradient, plus B*T*H*dv*2 bytes of o
+ * that the recomputed forward writes.  The page gives no backward equations;
+ * these follow from its chunkwise form by the chain rule.
+ */
+int gdr2_backward_chunked(const void* q, const void* k, const void* v,
+                          const void* b, const void* w, const void* log_decay,
+                          const float* S0, const float* d_o, const float* d_S_T,
+                          float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                          float* d_log_decay, float* d_S0,
+                          int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                          int in_dtype, cudaStream_t stream);
+
+/*
  * gdr2_sparse_write -- the gated delta write on selected slots of a slot
  * memory ("Sparse Delta Memory" review page, section "3. Method & Key
  * Results": the write is applied only to the slots a product-key memory
