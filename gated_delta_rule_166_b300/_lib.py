@@ -282,13 +282,16 @@ def _backward(fn, q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream):
 class GatedDeltaRule2(torch.autograd.Function):
     """(o, S_T) = gdr2_forward(q, k, v, b, w, log_decay, S0) as a differentiable
     operation: the forward pass is gdr2_forward (fp32 o), the backward pass
-    gdr2_backward.  Gradients are fp32 and cast to each input's dtype."""
+    gdr2_backward, or gdr2_backward_chunked when ``chunked`` is set and the inputs
+    are bf16 with dk = dv = 128.  Gradients are fp32 and cast to each input's
+    dtype."""
 
     @staticmethod
-    def forward(ctx, q, k, v, b, w, log_decay, S0=None):
+    def forward(ctx, q, k, v, b, w, log_decay, S0=None, chunked=False):
         o, S_T = gdr2_forward(q, k, v, b, w, log_decay, S0)
         ctx.save_for_backward(q, k, v, b, w, log_decay, S0)
         ctx.has_s0 = S0 is not None
+        ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16 and q.shape[-1] == 128 and v.shape[-1] == 128
         return o, S_T
 
     @staticmethod
@@ -297,14 +300,17 @@ class GatedDeltaRule2(torch.autograd.Function):
         d_o = torch.zeros((*v.shape[:3], v.shape[-1]), dtype=torch.float32, device=q.device) if d_o is None \
             else d_o.float().contiguous()
         d_S_T = None if d_S_T is None else d_S_T.float().contiguous()
-        g = gdr2_backward(q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
+        fn = gdr2_backward_chunked if ctx.chunked else gdr2_backward
+        g = fn(q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
         cast = [g[i].to(t.dtype) for i, t in enumerate((q, k, v, b, w, log_decay))]
-        return (*cast, g[6] if ctx.has_s0 else None)
+        return (*cast, g[6] if ctx.has_s0 else None, None)
 
 
-def gdr2_apply(q, k, v, b, w, log_decay, S0=None):
-    """Differentiable prefill: ``(o, S_T)`` with gradients through gdr2_backward."""
-    return GatedDeltaRule2.apply(q, k, v, b, w, log_decay, S0)
+def gdr2_apply(q, k, v, b, w, log_decay, S0=None, *, chunked_backward: bool = False):
+    """Differentiable prefill: ``(o, S_T)`` with gradients through gdr2_backward
+    (exact fp32), or through gdr2_backward_chunked (tensor cores; bf16 inputs with
+    dk = dv = 128, else the exact path) when ``chunked_backward`` is set."""
+    return GatedDeltaRule2.apply(q, k, v, b, w, log_decay, S0, chunked_backward)
 
 
 def gdr2_decode_step(q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.float32,

@@ -34,7 +34,10 @@
 //     products dA_kk Kh, dA_qk Kh and dKh on tf32 with the stripe-referenced factors of
 //     the forward (e^{G_r - G_i} = e^{G_r - G_m} e^{G_m - G_i}, m the middle token of a
 //     16-token stripe; factors across stripes are <= 1), the per-channel factors held
-//     in TMEM as the A operand (lane = key channel).
+//     in TMEM as the A operand (lane = key channel).  dG adds each token pair's product
+//     through dq q (or dc c) and subtracts it through Y1 k; it multiplies those terms by
+//     the group factors exactly as the MMAs saw them (rounded to tf32), so that a pair
+//     within a stripe enters both sides as the same product and cancels.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -762,13 +765,16 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             const float dc = eg * c0[jj] + ed * x1[jj];
             const float dq = eg * qb[jj] + ed * x2[jj];
             const float z1 = kb[jj] * ec;
+            // dG's pair terms take the C- and Q-group factors as rounded for Y1, so that
+            // a pair within a stripe enters dG_r and dG_i as the same product
+            const float cgr = tf32r(bv * kv * ed), qgr = tf32r(qv * ed);
             if (r < nvalid) {
                 const int64_t gi = gidx(r, a);
                 prm.dq[gi] = dq;
                 prm.db[gi] = dc * kv;
             }
             dkp[jj] = z1 + dc * bv;
-            dgp[jj] = dc * (bv * kv) + dq * qv - z1 * kv;
+            dgp[jj] = (eg * c0[jj]) * (bv * kv) + x1[jj] * cgr + (eg * qb[jj]) * qv + x2[jj] * qgr - z1 * kv;
             zk = fmaf(z1, kv, zk);
         }
         scr[cb * 128 + a] = zk;
@@ -823,9 +829,10 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             const int r = 16 * cb + jj;
             const float gr = Gt[r * 128 + a];
             const float kv = bf(raw[8192 + r * 128 + a]);
-            const float y1 = y[jj] * __expf(gM - gr);
+            const float fi = __expf(gM - gr);
+            const float y1 = y[jj] * fi;
             dkp[jj] += y1;
-            dgp[jj] -= y1 * kv;
+            dgp[jj] -= y[jj] * tf32r(kv * fi);   // the K-group factor as rounded for X
             if (r < nvalid) prm.dk[gidx(r, a)] = dkp[jj];
         }
         if (cb == 3) {
