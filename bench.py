@@ -393,7 +393,8 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None, chunked=True
             "warmup": warmup, "launches_per_call": 4 if chunked else 2,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes,
-                         "traffic": traffic_record(("backward_chunked_" if chunked else "backward_") + WORKLOAD),
+                         "traffic": (traffic_record(("backward_chunked_" if chunked else "backward_") + WORKLOAD)
+                                     if batch is None else None),   # the records cover the full workload
                          "kernel": kernels}}
 
 
