@@ -26,7 +26,9 @@
 //     the last chunk to the first on tcgen05 (M'^T and P^T are the forward slot's fp16
 //     images read through MN-major descriptors; dO is an fp16 pair hi + lo), keeps the
 //     gradient at every chunk's end state and writes dS0.
-//   cgrad_kernel: one CTA per (chunk, head) forms all token gradients of the chunk:
+//   cgrad_kernel: one CTA per (chunk, head) forms all token gradients of the chunk
+//     (the record holds W^T, A_qk, T and Kb; with dA_kk in the one-product form below
+//     the gradient needs no Cb):
 //     eleven fp16 products (fp32 accumulators in TMEM), dA_kk in its one-product form
 //     (T^T dW = -du S^T and T Cb = W give -T^T dT T^T = -du (T u)^T + du S^T W^T
 //     = -du E^T, one rounding where the three-product form rounds dT and dT T^T too),
@@ -331,8 +333,8 @@ namespace cgr {
 constexpr int kThreads = 512;
 // ---- shared memory (bytes from a 1024-aligned base); fp16 images are 128-byte
 // swizzled rows of 64 elements ("[rows][cols]": rows written by one thread each) ----
-constexpr uint32_t kWt = 0, kAq = 16384, kT = 24576, kCb = 32768, kKb = 49152;   // the backward record
-static_assert(kWt == kWyWt && kAq == kWyAq && kT == kWyT && kCb == kWyCb && kKb == kWyKb, "record layout");
+constexpr uint32_t kWt = 0, kAq = 16384, kT = 24576, kKb = 32768;   // the backward record (48 KB)
+static_assert(kWt == kWyWt && kAq == kWyAq && kT == kWyT && kKb == kWyKb, "record layout");
 constexpr uint32_t kdWt = kWt;            // dW^T [d_k][token] (after W^T is consumed)
 constexpr uint32_t kScr = kAq;            // cross-warp sums, 2 x [4][128] fp32 (after A_qk)
 constexpr uint32_t kdEtL = kKb;           // low half of dE^T (after Kb), then
@@ -347,6 +349,10 @@ constexpr uint32_t kEt = 163840;          // E^T [d_v][token]
 constexpr uint32_t kdEt = 180224;         // dE^T [d_v][token]
 constexpr uint32_t kAkk = kEt, kAkkT = kdEt;   // dA_kk [r][i], [i][r] tf32 (after E^T, dE^T)
 constexpr uint32_t kAqk = 196608, kAqkT = 212992;   // dA_qk [r][i], [i][r] tf32
+// Per-warp 2 KB transpose buffers for the token-gradient stores: during the third
+// phase's read-out (where dO and u were), and from the fourth phase on (where T and
+// du^T were)
+constexpr uint32_t kXpA = kdO, kXpB = kT;
 // Low halves x - fp16(x) of the pairs dS', dO and u (read by the first products only),
 // in regions whose own contents are written after those products complete
 constexpr uint32_t kdSL = kAqk, kdOL = kdEt, kUL = kEt;
@@ -357,6 +363,7 @@ constexpr uint32_t kGsum = kMisc + 64;    // rowsum(dS' * S) [d_k] fp32
 constexpr uint32_t kSmemBytes = kGsum + 512;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kTmemSlot + 4 <= kGsum && kSmemAlloc <= 232448, "shared memory");
+static_assert(kXpA + 16 * 2048 <= kEt && kXpB + 16 * 2048 <= kS && kXpB >= kScr + 8192, "transpose buffers");
 // ---- TMEM columns (M = 128 accumulators: lane = row; M = 64: row r at lane 32 (r / 16) + r % 16) ----
 constexpr uint32_t kTmEa = 0, kTmEb = 64;                              // u^T T^T, S^T W^T
 constexpr uint32_t kTmAqk = 128, kTmKb = 192, kTmdE = 256, kTmQb = 320;   // dO E^T, dS' E^T, dE^T, S dO^T
@@ -395,6 +402,25 @@ __device__ __forceinline__ void put16(uint8_t* img, uint32_t kblk, uint32_t row,
     for (int e = 0; e < 8; ++e) w[e] = pack_h2(v[2 * e], v[2 * e + 1]);
     *reinterpret_cast<uint4*>(img + k_off16(kblk, row, k0)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(img + k_off16(kblk, row, k0 + 8u)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Lane l of a warp holds one key / value channel (a0 + l) at 16 tokens r0 .. r0 + 15;
+// the warp writes them to its 2 KB buffer and reads them back as 4 channels of one
+// token, so that each global store moves 16 bytes (8 lanes: one token's 32 channels)
+// instead of 4.  Rows at or past `nvalid` are not stored.
+__device__ __forceinline__ void store_tokens(float* buf, const float (&v)[16], float* out, int64_t row0, int H,
+                                             int h, int a0, int r0, int nvalid, int lane) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) buf[t * 32 + lane] = v[t];
+    __syncwarp();
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+        const int t = 4 * s4 + (lane >> 3), c4 = 4 * (lane & 7);
+        const float4 x = *reinterpret_cast<const float4*>(buf + t * 32 + c4);
+        if (r0 + t < nvalid)
+            *reinterpret_cast<float4*>(out + ((row0 + r0 + t) * H + h) * 128 + a0 + c4) = x;
+    }
+    __syncwarp();
 }
 
 // 16 values as an fp16 pair x = hi + lo (about 22 significant bits) in two images
@@ -635,14 +661,15 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
         for (int jj = 0; jj < 16; ++jj) v[jj] = -v[jj];
         put16(sgen + kdWt, 0u, static_cast<uint32_t>(a), 16u * cb, v);
         tmem_ld16(tmem + lane_base + kTmdu + 16u * cb, v);
+        {
+            float* xb = reinterpret_cast<float*>(sgen + kXpA) + warp * 512;
+            float t[16];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int r = 16 * cb + jj;
-            if (r < nvalid) {
-                const int64_t gi = gidx(r, a);
-                prm.dv[gi] = v[jj] * bf(wb[jj]);
-                prm.dw[gi] = v[jj] * bf(vb[jj]);
-            }
+            for (int jj = 0; jj < 16; ++jj) t[jj] = v[jj] * bf(wb[jj]);
+            store_tokens(xb, t, prm.dv, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) t[jj] = v[jj] * bf(vb[jj]);
+            store_tokens(xb, t, prm.dw, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
         }
         put16(sgen + kdUt, 0u, static_cast<uint32_t>(a), 16u * cb, v);
     }
@@ -749,35 +776,45 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
     const float gC = Gt[63 * 128 + a], gM = Gt[(16 * cb + 7) * 128 + a];
     float dkp[16], dgp[16];
     {
-        float x1[16], x2[16], kb[16], qb[16], c0[16];
-        tmem_ld16(tmem + lane_base + kTmX1 + 16u * cb, x1);
-        tmem_ld16(tmem + lane_base + kTmX2 + 16u * cb, x2);
-        tmem_ld16(tmem + lane_base + kTmKb + 16u * cb, kb);
-        tmem_ld16(tmem + lane_base + kTmQb + 16u * cb, qb);
-        tmem_ld16(tmem + lane_base + kTmCb0 + 16u * cb, c0);
+        // two halves of 8 tokens, so that the accumulators read out stay few in registers
         float zk = 0.f;
+        float dqv[16], dbv[16];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
+        for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t col = 16u * cb + 8u * hf;
+        uint32_t x1[8], x2[8], kb[8], qb[8], c0[8];
+        tmem_ld8_nw(tmem + lane_base + kTmX1 + col, x1);
+        tmem_ld8_nw(tmem + lane_base + kTmX2 + col, x2);
+        tmem_ld8_nw(tmem + lane_base + kTmKb + col, kb);
+        tmem_ld8_nw(tmem + lane_base + kTmQb + col, qb);
+        tmem_ld8_nw(tmem + lane_base + kTmCb0 + col, c0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j8 = 0; j8 < 8; ++j8) {
+            const int jj = 8 * hf + j8;
             const int r = 16 * cb + jj;
             const float gr = Gt[r * 128 + a];
             const float eg = __expf(gr), ed = __expf(gr - gM), ec = __expf(gC - gr);
             const float qv = bf(raw[r * 128 + a]), kv = bf(raw[8192 + r * 128 + a]), bv = bf(raw[16384 + r * 128 + a]);
-            const float dc = eg * c0[jj] + ed * x1[jj];
-            const float dq = eg * qb[jj] + ed * x2[jj];
-            const float z1 = kb[jj] * ec;
+            const float x1v = __uint_as_float(x1[j8]), x2v = __uint_as_float(x2[j8]);
+            const float c0v = __uint_as_float(c0[j8]), qbv = __uint_as_float(qb[j8]);
+            const float dc = eg * c0v + ed * x1v;
+            const float dq = eg * qbv + ed * x2v;
+            const float z1 = __uint_as_float(kb[j8]) * ec;
             // dG's pair terms take the C- and Q-group factors as rounded for Y1, so that
             // a pair within a stripe enters dG_r and dG_i as the same product
             const float cgr = tf32r(bv * kv * ed), qgr = tf32r(qv * ed);
-            if (r < nvalid) {
-                const int64_t gi = gidx(r, a);
-                prm.dq[gi] = dq;
-                prm.db[gi] = dc * kv;
-            }
+            dqv[jj] = dq;
+            dbv[jj] = dc * kv;
             dkp[jj] = z1 + dc * bv;
-            dgp[jj] = (eg * c0[jj]) * (bv * kv) + x1[jj] * cgr + (eg * qb[jj]) * qv + x2[jj] * qgr - z1 * kv;
+            dgp[jj] = (eg * c0v) * (bv * kv) + x1v * cgr + (eg * qbv) * qv + x2v * qgr - z1 * kv;
             zk = fmaf(z1, kv, zk);
         }
+        }
         scr[cb * 128 + a] = zk;
+        float* xb = reinterpret_cast<float*>(sgen + kXpB) + warp * 512;
+        store_tokens(xb, dqv, prm.dq, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+        store_tokens(xb, dbv, prm.db, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -833,8 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             const float y1 = y[jj] * fi;
             dkp[jj] += y1;
             dgp[jj] -= y[jj] * tf32r(kv * fi);   // the K-group factor as rounded for X
-            if (r < nvalid) prm.dk[gidx(r, a)] = dkp[jj];
         }
+        float* xb = reinterpret_cast<float*>(sgen + kXpB) + warp * 512;
+        store_tokens(xb, dkp, prm.dk, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
         if (cb == 3) {
             // G_C's own terms land on the chunk's last token row
             float zk = 0.f;
@@ -851,9 +889,9 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 #pragma unroll
         for (int jj = 15; jj >= 0; --jj) {
             run += dgp[jj];
-            const int r = 16 * cb + jj;
-            if (r < nvalid) prm.dg[gidx(r, a)] = run;
+            dgp[jj] = run;
         }
+        store_tokens(xb, dgp, prm.dg, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
     }
     if (!ok && tid == 0) atomicExch(prm.err, kDevTimeout);
     if (tid == 0) {

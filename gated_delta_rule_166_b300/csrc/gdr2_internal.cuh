@@ -103,10 +103,10 @@ constexpr uint32_t kSlotGam = 73728;   // gamma = e^{G_C} [d_k] fp32
 constexpr size_t kSlot2Bytes = 74240;
 // Backward record of a (chunk, head) item, written by prep2 in its backward mode:
 // the fp16 images of W^T [d_k (rows)][token], A_qk [token][token], T [token][token]
-// (K-major, one 64-element K block) and Cb, Kb [token][d_k] (two K blocks), with
-// Cb = (b k) e^{G}, Kb = k e^{G_C - G}, T = (I + A_kk)^-1 and W = T Cb.
-constexpr uint32_t kWyWt = 0, kWyAq = 16384, kWyT = 24576, kWyCb = 32768, kWyKb = 49152;
-constexpr uint32_t kWyBytes = 65536;
+// (K-major, one 64-element K block) and Kb [token][d_k] (two K blocks), with
+// Kb = k e^{G_C - G}, T = (I + A_kk)^-1 and W = T (b k) e^{G}.
+constexpr uint32_t kWyWt = 0, kWyAq = 16384, kWyT = 24576, kWyKb = 32768;
+constexpr uint32_t kWyBytes = 49152;
 // Global chunks of a call: exact for fixed-length sequences, an upper bound
 // (ceil(total / 64) + N) for packed ones.
 int64_t prep_chunk_bound(const ForwardArgs& a);

@@ -88,9 +88,9 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kTmemSlot + 4 <= kSmemBytes, "misc area");
 static_assert(kSmemAlloc <= 232448, "shared memory");
 static_assert(kSlot2Bytes <= 4 * kKGStride, "slot staging in the K-group area");
-// the backward record copies [W^T | A_qk | T] from the K-group area and [Cb | Kb] as they lie
+// the backward record copies [W^T | A_qk | T] from the K-group area as it lies, then Kb
 static_assert(kB1 + 8192u + kWyWt == kKG + 8192u && kAq == kB1 + 8192u + (kWyAq - kWyWt) &&
-                  kTo == kB1 + 8192u + (kWyT - kWyWt) && kKB == kCB + (kWyKb - kWyCb),
+                  kTo == kB1 + 8192u + (kWyT - kWyWt) && kWyKb - kWyWt == 32768u && kWyBytes - kWyKb == 16384u,
               "backward record layout");
 
 // ---- TMEM columns ---------------------------------------------------------------
@@ -174,7 +174,7 @@ __device__ __forceinline__ bool locate(const Prep2Params& prm, int it, Item& x) 
     return true;
 }
 
-// kWY: also write each item's W^T, A_qk, T, Cb and Kb images to its backward record
+// kWY: also write each item's W^T, A_qk, T and Kb images to its backward record
 // (the operands of the chunk gradients, gdr2_bwd_chunk.cu).
 template <bool kWY>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -662,10 +662,10 @@ prep2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 mma_commit(bar(kDDone));
                 if (kWY) {
-                    // backward record: [W^T | A_qk | T] (contiguous in the K-group area) and [Cb | Kb]
+                    // backward record: [W^T | A_qk | T] (contiguous in the K-group area) and Kb
                     uint8_t* const rec = prm.wy + static_cast<int64_t>(it) * kWyBytes;
-                    bulk_s2g(rec + kWyWt, base + kB1 + 8192u, kWyCb - kWyWt);
-                    bulk_s2g(rec + kWyCb, base + kCB, kWyBytes - kWyCb);
+                    bulk_s2g(rec + kWyWt, base + kB1 + 8192u, kWyKb - kWyWt);
+                    bulk_s2g(rec + kWyKb, base + kKB, kWyBytes - kWyKb);
                     bulk_commit();
                 }
             }

@@ -280,6 +280,12 @@ __device__ __forceinline__ void mma_ss_f16(uint32_t d_tmem, uint64_t a, uint64_t
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// 32 lanes x 32 bit, 8 consecutive columns per thread (no wait).
+__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 // 32 lanes x 32 bit, 32 consecutive columns per thread (no wait).
 __device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

@@ -298,7 +298,7 @@ int gdr2_backward(const void* q, const void* k, const void* v,
  * decays (about e^-2 per token in every channel): those two are differences of
  * chunk terms 30 to 60 times their size, and reach about 7e-2 there.  Per-token
  * log decays below -10 count as -10, as in the chunked forward.  Workspace (the library's pool, released on the stream): per
- * (chunk, head) 139,776 bytes (the forward's maps and backward record) plus
+ * (chunk, head) 123,392 bytes (the forward's maps and backward record) plus
  * 128 KB of start state and end-state gradient, plus B*T*H*dv*2 bytes of o
  * that the recomputed forward writes.  The page gives no backward equations;
  * these follow from its chunkwise form by the chain rule.
