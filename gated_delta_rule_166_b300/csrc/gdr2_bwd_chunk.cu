@@ -339,6 +339,7 @@ constexpr uint32_t kdWt = kWt;            // dW^T [d_k][token] (after W^T is con
 constexpr uint32_t kScr = kAq;            // cross-warp sums, 2 x [4][128] fp32 (after A_qk)
 constexpr uint32_t kdEtL = kKb;           // low half of dE^T (after Kb), then
 constexpr uint32_t kdUt = kKb;            // du^T [d_v][token]
+constexpr uint32_t kEtL = kKb + 16384;    // low half of E^T (the record ends at kKb + 16 KB)
 constexpr uint32_t kS = 65536;            // S [d_k][d_v], two 64-column blocks 16 KB apart
 constexpr uint32_t kdS = 98304;           // dS' [d_k][d_v]
 constexpr uint32_t kRaw = kS;             // bf16 [token][128] tiles q, k, b, log decay (after S, dS')
@@ -354,8 +355,9 @@ constexpr uint32_t kAqk = 196608, kAqkT = 212992;   // dA_qk [r][i], [i][r] tf32
 // du^T were)
 constexpr uint32_t kXpA = kdO, kXpB = kT;
 // Low halves x - fp16(x) of the pairs dS', dO and u (read by the first products only),
-// in regions whose own contents are written after those products complete
-constexpr uint32_t kdSL = kAqk, kdOL = kdEt, kUL = kEt;
+// in regions whose own contents are written after those products complete; du's low
+// half where dE^T was (read by the fourth phase, before dA_kk^T is written there)
+constexpr uint32_t kdSL = kAqk, kdOL = kdEt, kUL = kEt, kdUtL = kdEt;
 constexpr uint32_t kMisc = 229376;
 enum : uint32_t { kBarLd = 0, kBarMma, kBarDrain, kNumBars };
 constexpr uint32_t kTmemSlot = kMisc + 8 * kNumBars;
@@ -364,6 +366,7 @@ constexpr uint32_t kSmemBytes = kGsum + 512;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kTmemSlot + 4 <= kGsum && kSmemAlloc <= 232448, "shared memory");
 static_assert(kXpA + 16 * 2048 <= kEt && kXpB + 16 * 2048 <= kS && kXpB >= kScr + 8192, "transpose buffers");
+static_assert(kEtL + 16384 <= kS && kEtL >= kKb + 16384, "low half of E^T");
 // ---- TMEM columns (M = 128 accumulators: lane = row; M = 64: row r at lane 32 (r / 16) + r % 16) ----
 constexpr uint32_t kTmEa = 0, kTmEb = 64;                              // u^T T^T, S^T W^T
 constexpr uint32_t kTmAqk = 128, kTmKb = 192, kTmdE = 256, kTmQb = 320;   // dO E^T, dS' E^T, dE^T, S dO^T
@@ -568,14 +571,26 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
         tmem_ld16(tmem + lane_base + kTmEb + 16u * cb, eb);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) ea[jj] -= eb[jj];
-        put16(sgen + kEt, 0u, static_cast<uint32_t>(a), 16u * cb, ea);
+        put16_pair(sgen + kEt, sgen + kEtL, 0u, static_cast<uint32_t>(a), 16u * cb, ea);
     }
     operands_done();
 
     // ---- 2. dA_qk = dO E^T, dKb^T = dS' E^T, dE^T = dO^T A_qk + dS'^T Kb^T, dQb0^T = S dO^T ------
     if (tid == 0) {
-        // dO, dS' as hi + lo pairs: each product with them runs once per half
+        // dO, dS' and E as hi + lo pairs: each product runs once per half of dO / dS',
+        // plus once with E's low half and the high half of dO / dS'
         const uint64_t dEm = umma_desc2(base + kEt, 8192u, 1024u), dSk0 = umma_desc2(base + kS, 16u, 1024u);
+        {
+            const uint64_t dELm = umma_desc2(base + kEtL, 8192u, 1024u);
+            const uint64_t dOk = umma_desc2(base + kdO, 16u, 1024u), dSk = umma_desc2(base + kdS, 16u, 1024u);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = kk < 4 ? 2u * kk : (8192u >> 4) + 2u * (kk - 4);
+                const uint32_t ks = kk < 4 ? 2u * kk : (16384u >> 4) + 2u * (kk - 4);
+                mma_ss_f16(tmem + kTmAqk, dOk + ko, dELm + 128u * kk, idesc_f16x(64, 64, 0, 0, 1), kk > 0);
+                mma_ss_f16(tmem + kTmKb, dSk + ks, dELm + 128u * kk, idesc_f16x(128, 64, 0, 0, 1), kk > 0);
+            }
+        }
         const uint64_t dKk = umma_desc2(base + kKb, 16u, 1024u), dAm = umma_desc2(base + kAq, 8192u, 1024u);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -588,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
                 const uint32_t ko = kk < 4 ? 2u * kk : (8192u >> 4) + 2u * (kk - 4);
                 const uint32_t ks = kk < 4 ? 2u * kk : (16384u >> 4) + 2u * (kk - 4);
                 const uint32_t acc = half > 0 || kk > 0;
-                mma_ss_f16(tmem + kTmAqk, dOk + ko, dEm + 128u * kk, idesc_f16x(64, 64, 0, 0, 1), acc);
-                mma_ss_f16(tmem + kTmKb, dSk + ks, dEm + 128u * kk, idesc_f16x(128, 64, 0, 0, 1), acc);
+                mma_ss_f16(tmem + kTmAqk, dOk + ko, dEm + 128u * kk, idesc_f16x(64, 64, 0, 0, 1), 1u);
+                mma_ss_f16(tmem + kTmKb, dSk + ks, dEm + 128u * kk, idesc_f16x(128, 64, 0, 0, 1), 1u);
                 mma_ss_f16(tmem + kTmQb, dSk0 + ks, dOk + ko, idesc_f16x(128, 64, 0, 0, 0), acc);
             }
 #pragma unroll
@@ -671,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             for (int jj = 0; jj < 16; ++jj) t[jj] = v[jj] * bf(vb[jj]);
             store_tokens(xb, t, prm.dw, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
         }
-        put16(sgen + kdUt, 0u, static_cast<uint32_t>(a), 16u * cb, v);
+        put16_pair(sgen + kdUt, sgen + kdUtL, 0u, static_cast<uint32_t>(a), 16u * cb, v);
     }
     // raw q, k, b, log decay rows of the chunk -> [4][64][128] bf16 (S and dS' are consumed);
     // rows past the sequence end read as zero
@@ -692,10 +707,16 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 
     // ---- 4. du E^T (dA_kk = -du E^T below the diagonal) and (T^T dW)^T = dW^T T -------------------
     if (tid == 0) {
+        // du and E as hi + lo pairs: du_hi E_hi + du_hi E_lo + du_lo E_hi
         const uint64_t dUm = umma_desc2(base + kdUt, 8192u, 1024u), dEm = umma_desc2(base + kEt, 8192u, 1024u);
+        const uint64_t dULm = umma_desc2(base + kdUtL, 8192u, 1024u), dELm = umma_desc2(base + kEtL, 8192u, 1024u);
         const uint64_t dWk = umma_desc2(base + kdWt, 16u, 1024u), dTm = umma_desc2(base + kT, 8192u, 1024u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss_f16(tmem + kTmAkk, dUm + 128u * kk, dEm + 128u * kk, idesc_f16x(64, 64, 0, 1, 1), kk > 0);
+        for (int kk = 0; kk < 8; ++kk) {
+            mma_ss_f16(tmem + kTmAkk, dUm + 128u * kk, dEm + 128u * kk, idesc_f16x(64, 64, 0, 1, 1), kk > 0);
+            mma_ss_f16(tmem + kTmAkk, dUm + 128u * kk, dELm + 128u * kk, idesc_f16x(64, 64, 0, 1, 1), 1u);
+            mma_ss_f16(tmem + kTmAkk, dULm + 128u * kk, dEm + 128u * kk, idesc_f16x(64, 64, 0, 1, 1), 1u);
+        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_ss_f16(tmem + kTmCb0, dWk + 2u * kk, dTm + 128u * kk, idesc_f16x(128, 64, 0, 0, 1), kk > 0);
         mma_commit(bar(kBarMma));

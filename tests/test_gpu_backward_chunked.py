@@ -93,18 +93,14 @@ def test_chunked_backward_agrees_with_exact_backward_on_ragged_batch():
         assert e <= TOL, f"{name}: {e:.3e}"
 
 
-# Fast decays (about e^-2 per token in every key channel): dlog_decay is a suffix sum
-# of dG = dc c + dq q - (Z1 + Y1) k, whose terms are some 30-60 times larger than dG
-# and cancel in pairs: token pair (r, i) adds a product to dq_r q_r (through the
-# K-group factor k_i e^{G_m(R) - G_i}) and subtracts it from Y1_i k_i (through the
-# Q-group factor q_r e^{G_r - G_m(s)}).  The kernel rounds both sides alike for pairs
-# within a stripe, but a pair across a stripe boundary meets two independently
-# rounded tf32 factors (2^-11 each): about 2^-11 x (30-60) x sqrt(64 tokens) per
-# suffix sum, some 0.1 of RMS(dlog_decay).  db = dc k has its own cancellation
-# (dc = -X_t du_t, the decayed state against a nearly orthogonal du) carried by the
-# fp16 rounding of du and E: 2^-11 x sqrt(128) x (30-60), again about 0.1.  That is
-# the bar for these two; the other gradients keep 2e-2, and gdr2_backward is exact
-# to 1e-4 throughout.
+# Fast decays (about e^-2 per token in every key channel): db and dlog_decay are
+# heavy-tailed there, max|ref| / RMS(ref) of 40-55 against about 10 for dq at the GDN-2
+# layer workload, and they are formed from chunk terms several times their size (dc
+# from the decayed state against a nearly orthogonal du; dG from token pairs that
+# cancel in its suffix sums).  The chunked path's element accuracy, about 1e-3 relative
+# at those largest elements (fp16 operands, measured), is therefore 4-5e-2 of RMS: the
+# bar for these two is 0.1.  The other gradients keep 2e-2, and gdr2_backward is
+# exact to 1e-4 throughout.
 FAST_BAR = {"db": 1e-1, "dlog_decay": 1e-1}
 
 
