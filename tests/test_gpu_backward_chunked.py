@@ -136,3 +136,12 @@ def test_autograd_function_with_chunked_backward():
         e = err_over_rms(leaf.grad.float().cpu().numpy(), rf)
         bar = TOL + float(np.abs(rf).max()) * 2.0 ** -8 / float(np.sqrt(np.mean(rf * rf)))
         assert e <= bar, f"{name}: {e:.3e} (bar {bar:.3g})"
+
+
+@pytest.mark.parametrize("gates,decay", [("tied", "channel"), ("tied", "scalar")])
+def test_chunked_backward_degenerate_gates(gates, decay):
+    """KDA (b = w = one scalar per token and head) and Gated DeltaNet (plus one
+    scalar decay per token and head) through the general chunked gradients."""
+    x = make_prefill_inputs(2, 200, 2, 128, 128, dtype=torch.bfloat16, seed=990, gates=gates, decay=decay,
+                            decay_regime="slow", s0_std=0.2)
+    check(x, *upstream(x, 50), f"{gates} gates, {decay} decay")
