@@ -299,9 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
                 for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(gam, S[jj], v[jj]);
             }
             if (k + 1 < n) {
-                keep(c - 1, S);
                 put_st(b ^ 1u, S);
                 arrive(kSRdy);
+                keep(c - 1, S);   // after the next chunk's operand is released
             }
             if (k + 2 < n) {
                 put_do(k + 2, xpre);

@@ -454,8 +454,15 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(gam, S[jj], v[jj]);
             }
+            if (c + 1 < n) {
+                // the other S^T buffer was read by chunk c - 1's products, which completed
+                // before that chunk's O was read out
+                put_st(b ^ 1u, S);
+                arrive(kSRdy);
+            }
             if (!kTransfer && prm.cache) {
-                // the state after chunk cc of the sequence, every cache_chunks chunks
+                // the state after chunk cc of the sequence, every cache_chunks chunks (stored
+                // after the next chunk's operand is released: off the chain's critical path)
                 const int cc = prm.c0 + c;
                 const int ci = (cc + 1) / prm.cache_chunks - 1;
                 if ((cc + 1) % prm.cache_chunks == 0 && ci < prm.n_cache && j < prm.dk && j0 + 16 * R < prm.dv) {
@@ -464,12 +471,6 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
                     for (int jj = 0; jj < 16; jj += 4)
                         *reinterpret_cast<float4*>(cp + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
                 }
-            }
-            if (c + 1 < n) {
-                // the other S^T buffer was read by chunk c - 1's products, which completed
-                // before that chunk's O was read out
-                put_st(b ^ 1u, S);
-                arrive(kSRdy);
             }
             if (c + 2 < n) {
                 // ---- U^T of chunk c + 2 into the buffer chunk c's products have read ----
