@@ -145,3 +145,26 @@ def test_chunked_backward_degenerate_gates(gates, decay):
     x = make_prefill_inputs(2, 200, 2, 128, 128, dtype=torch.bfloat16, seed=990, gates=gates, decay=decay,
                             decay_regime="slow", s0_std=0.2)
     check(x, *upstream(x, 50), f"{gates} gates, {decay} decay")
+
+
+def test_chunked_backward_full_workload_sampled():
+    """The bench's call: the GDN-2 layer workload (B4 H16 T4096, fast decays) with the
+    bench's seeded gradient at o, in one launch configuration; two (sequence, head)
+    pairs are checked against the oracle, which computes each independently."""
+    from gated_delta_rule_166_b300.inputs import PrefillInputs, make_workload
+
+    x = make_workload("gdn2_layer_T4096")
+    gen = torch.Generator().manual_seed(11)
+    d_o = torch.randn(4, 4096, 16, 128, generator=gen)
+    d = x.to("cuda")
+    got = gdr2.backward_chunked(*d.tensors(), d.S0, d_o.cuda(), None)
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    for bb, hh in ((0, 0), (3, 15)):
+        xs = PrefillInputs(*(t[bb:bb + 1, :, hh:hh + 1].contiguous() for t in x.tensors()),
+                           None if x.S0 is None else x.S0[bb:bb + 1, hh:hh + 1].contiguous())
+        ref = oracle.backward(*xs.tensors(), xs.S0, d_o[bb:bb + 1, :, hh:hh + 1].contiguous(), None)
+        errs = {name: err_over_rms(g[bb:bb + 1, :, hh:hh + 1].cpu().numpy(), r)
+                for name, g, r in zip(NAMES[:6], got[:6], ref[:6])}
+        bad = {k: v for k, v in errs.items() if not v <= FAST_BAR.get(k, TOL)}
+        assert not bad, f"(b{bb}, h{hh}): " + ", ".join(f"{k}={v:.3e}" for k, v in errs.items())
