@@ -26,20 +26,23 @@
 //     the last chunk to the first on tcgen05 (M'^T and P^T are the forward slot's fp16
 //     images read through MN-major descriptors; dO is an fp16 pair hi + lo), keeps the
 //     gradient at every chunk's end state and writes dS0.
-//   cgrad_kernel: one CTA per (chunk, head) forms all token gradients of the chunk
-//     (the record holds W^T, A_qk, T and Kb; with dA_kk in the one-product form below
-//     the gradient needs no Cb):
-//     eleven fp16 products (fp32 accumulators in TMEM), dA_kk in its one-product form
-//     (T^T dW = -du S^T and T Cb = W give -T^T dT T^T = -du (T u)^T + du S^T W^T
-//     = -du E^T, one rounding where the three-product form rounds dT and dT T^T too),
-//     then the decay-weighted
-//     products dA_kk Kh, dA_qk Kh and dKh on tf32 with the stripe-referenced factors of
-//     the forward (e^{G_r - G_i} = e^{G_r - G_m} e^{G_m - G_i}, m the middle token of a
-//     16-token stripe; factors across stripes are <= 1), the per-channel factors held
-//     in TMEM as the A operand (lane = key channel).  dG adds each token pair's product
-//     through dq q (or dc c) and subtracts it through Y1 k; it multiplies those terms by
-//     the group factors exactly as the MMAs saw them (rounded to tf32), so that a pair
-//     within a stripe enters both sides as the same product and cancels.
+//   cgrad_kernel: one CTA per (chunk, head) forms all token gradients of the chunk from
+//     its backward record (W^T, A_qk, T and Kb), S, dS' and dO:
+//     - eleven fp16 products with fp32 accumulators in TMEM: E; then dA_qk, dKb, dE and
+//       dO S^T; then dW and du; then du E^T and dW^T T.  dA_kk takes its one-product
+//       form: T^T dW = -du S^T and T Cb = W give -T^T dT T^T = -du (T u)^T + du S^T W^T
+//       = -du E^T, one rounding where the three-product form also rounds dT and dT T^T,
+//       and no Cb.  dS', dO, u, dE, du and E enter as fp16 pairs hi + lo (a product
+//       runs once per half);
+//     - the decay-weighted products dA_kk Kh, dA_qk Kh and dKh on tf32 with the
+//       stripe-referenced factors of the forward (e^{G_r - G_i} = e^{G_r - G_m}
+//       e^{G_m - G_i}, m the middle token of a 16-token stripe; factors across stripes
+//       are <= 1), the per-channel factors held in TMEM as the A operand (lane = key
+//       channel);
+//     - dG adds each token pair's product through dq q (or dc c) and subtracts it
+//       through Y1 k; it multiplies those terms by the group factors exactly as the
+//       MMAs saw them (rounded to tf32), so that a pair within a stripe enters both
+//       sides as the same product and cancels.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -295,9 +295,11 @@ int gdr2_backward(const void* q, const void* k, const void* v,
  * accumulation, like the chunked forward, where gdr2_backward keeps fp32
  * throughout (max|err| / RMS within 1e-4).  Against exact gradients the chunked
  * ones stay within 2e-2 (max|err| / RMS) except db and dlog_decay under fast
- * decays (about e^-2 per token in every channel): those two are differences of
- * chunk terms 30 to 60 times their size, and reach about 7e-2 there.  Per-token
- * log decays below -10 count as -10, as in the chunked forward.  Workspace (the library's pool, released on the stream): per
+ * decays (about e^-2 per token in every channel): there both are heavy-tailed
+ * (max / RMS of 40-55) and formed from chunk terms several times their size, so
+ * an element accuracy near 1e-3 relative reaches 2-5e-2 of RMS (measured at
+ * B4 H16 T4096).  Per-token log decays below -10 count as -10, as in the chunked
+ * forward.  Workspace (the library's pool, released on the stream): per
  * (chunk, head) 123,392 bytes (the forward's maps and backward record) plus
  * 128 KB of start state and end-state gradient, plus B*T*H*dv*2 bytes of o
  * that the recomputed forward writes.  The page gives no backward equations;
