@@ -10,9 +10,12 @@ from ._lib import (  # noqa: F401
     GDR2Error,
     GDR2LibraryError,
     GatedDeltaRule2,
+    GatedDeltaRule2Varlen,
     gdr2_apply,
+    gdr2_apply_varlen,
     gdr2_backward,
     gdr2_backward_chunked,
+    gdr2_backward_varlen,
     gdr2_decode_step,
     gdr2_device_status,
     gdr2_forward,
@@ -33,4 +36,6 @@ forward_cached = gdr2_forward_cached
 decode_step = gdr2_decode_step
 backward = gdr2_backward
 backward_chunked = gdr2_backward_chunked
+backward_varlen = gdr2_backward_varlen
+apply_varlen = gdr2_apply_varlen
 sparse_write = gdr2_sparse_write

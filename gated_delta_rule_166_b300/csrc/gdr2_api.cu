@@ -367,18 +367,20 @@ extern "C" int gdr2_forward_segmented(const void* q, const void* k, const void* 
 
 namespace {
 
-// Shared by the token-sequential and the chunked backward: the same arguments,
-// checks and empty-sequence behaviour.
+// Shared by the token-sequential and the chunked backward, fixed-length or packed
+// (cu: device offsets [B + 1] of B sequences over `total` token rows; T unused):
+// the same arguments, checks and empty-sequence behaviour.
 int backward_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
                   const void* log_decay, const float* S0, const float* d_o, const float* d_S_T, float* d_q,
                   float* d_k, float* d_v, float* d_b, float* d_w, float* d_log_decay, float* d_S0, int64_t B,
-                  int64_t T, int64_t H, int64_t dk, int64_t dv, int in_dtype, cudaStream_t stream, bool chunked) {
-    if (B < 0 || T < 0 || H < 0) return GDR2_ERR_ARG;
+                  int64_t T, int64_t H, int64_t dk, int64_t dv, int in_dtype, cudaStream_t stream, bool chunked,
+                  const int32_t* cu = nullptr, int64_t total = 0) {
+    if (B < 0 || T < 0 || H < 0 || total < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
     const size_t esz = in_dtype == GDR2_F32 ? 4 : 2;
-    int64_t rows = 0, bh = 0, nk = 0, nv = 0, ns = 0;
-    if (!mul_ok(B, T, &rows) || !mul_ok(rows, H, &rows) || !mul_ok(B, H, &bh) || !mul_ok(rows, dk, &nk) ||
+    int64_t rows = cu ? total : 0, bh = 0, nk = 0, nv = 0, ns = 0;
+    if ((!cu && !mul_ok(B, T, &rows)) || !mul_ok(rows, H, &rows) || !mul_ok(B, H, &bh) || !mul_ok(rows, dk, &nk) ||
         !mul_ok(rows, dv, &nv) || !mul_ok(bh, dk * dv, &ns) || nk > INT64_MAX / 8 || ns > INT64_MAX / 8 ||
         bh >= 0x7fffffffLL)
         return GDR2_ERR_SHAPE;
@@ -389,6 +391,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
     const void* all[] = {q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0};
     for (const void* ptr : all)
         if (ptr && !aligned16(ptr)) return GDR2_ERR_ALIGN;
+    if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u)) return GDR2_ERR_ALIGN;
     // outputs must not overlap any input or each other
     const size_t bk = (size_t)nk * esz, bv = (size_t)nv * esz, bs = (size_t)ns * 4;
     const size_t fk = (size_t)nk * 4, fv = (size_t)nv * 4;
@@ -396,13 +399,15 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
     const size_t in_bytes[] = {bk, bk, bk, bk, bv, bv, bs, fv, bs};
     const void* outs[] = {d_q, d_k, d_b, d_log_decay, d_v, d_w, d_S0};
     const size_t out_bytes[] = {fk, fk, fk, fk, fv, fv, bs};
+    const size_t bc = cu ? static_cast<size_t>(B + 1) * 4 : 0;
     for (int i = 0; i < 7; ++i) {
         for (int j = 0; j < 9; ++j)
             if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return GDR2_ERR_ALIAS;
         for (int j = i + 1; j < 7; ++j)
             if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return GDR2_ERR_ALIAS;
+        if (overlaps(outs[i], out_bytes[i], cu, bc)) return GDR2_ERR_ALIAS;
     }
-    if (chunked && (in_dtype != GDR2_BF16 || dk != kPrepDK || dv != 128)) return GDR2_ERR_UNSUPPORTED;
+    if (chunked && (cu || in_dtype != GDR2_BF16 || dk != kPrepDK || dv != 128)) return GDR2_ERR_UNSUPPORTED;
     int* err = nullptr;
     int st = device_setup(&err);
     if (st != GDR2_OK) return st;
@@ -414,9 +419,10 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
         return e == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
     }
     BackwardArgs a{q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
-                   B, T, H, dk, dv, in_dtype};
+                   B, cu ? 0 : T, H, dk, dv, in_dtype, reinterpret_cast<const int*>(cu), cu ? total : 0};
     void* ws = nullptr;
-    const size_t wsb = chunked ? backward_chunked_workspace_bytes(B, T, H) : backward_workspace_bytes(B, T, H, dk, dv);
+    const size_t wsb = chunked ? backward_chunked_workspace_bytes(B, T, H)
+                               : backward_workspace_bytes(B, a.T, H, dk, dv, cu != nullptr, a.total);
     if ((st = ws_alloc(&ws, wsb, stream)) != GDR2_OK) return st;
     int rc = chunked ? launch_backward_chunked(a, ws, stream, err) : launch_backward(a, ws, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
@@ -434,6 +440,20 @@ extern "C" int gdr2_backward(const void* q, const void* k, const void* v,
                              int in_dtype, cudaStream_t stream) {
     return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                          B, T, H, dk, dv, in_dtype, stream, false);
+}
+
+extern "C" int gdr2_backward_varlen(const void* q, const void* k, const void* v,
+                                    const void* b, const void* w, const void* log_decay,
+                                    const float* S0, const float* d_o, const float* d_S_T,
+                                    float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                    float* d_log_decay, float* d_S0, const int32_t* cu_seqlens,
+                                    int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                    int in_dtype, cudaStream_t stream) {
+    if (N > 0 && !cu_seqlens) return GDR2_ERR_ARG;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
+    if (N < 0 || total_T < 0) return GDR2_ERR_ARG;
+    return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                         N, 0, H, dk, dv, in_dtype, stream, false, N > 0 ? cu_seqlens : nullptr, total_T);
 }
 
 extern "C" int gdr2_backward_chunked(const void* q, const void* k, const void* v,

@@ -44,10 +44,14 @@ struct BwdParams {
     const void *q, *k, *v, *b, *w, *g;
     const float *S0, *dO, *dST;
     float *dv, *dw, *dS0;
-    float* ckpt;   // [B*H][tiles][blocks][DK * 32]
-    float* part;   // [B*T][H][tiles][kVec][DK]
+    float* ckpt;   // [B*H][tiles][blocks][DK * 32]; packed: [H][tiles][blk_stride][DK * 32]
+    float* part;   // [token rows][H][tiles][kVec][DK]
     int64_t T;
     int H, dv_dim, tiles;
+    // packed sequences (cu != null): sequence n owns rows cu[n] .. cu[n+1] - 1 of the
+    // `total` token rows; its checkpoint blocks start at floor(cu[n] / kCK) + n
+    const int* cu;
+    int64_t total, blk_stride;
 };
 
 // Shared memory: the X_t stash of one block, its token inputs and two buffers of
@@ -86,9 +90,24 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
     const int tile = blockIdx.y, j0 = tile * kDVT;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cw = warp * kCPW;                       // first column of this warp in the tile
-    const int64_t T = p.T, tok0 = seq * T;
+    int64_t T, tok0, ck_blk0;   // this sequence's rows and its first checkpoint block
+    if (p.cu) {
+        // offsets clamped into [0, total], the end to at least the start.  With
+        // a <= e: floor(a / kCK) + ceil((e - a) / kCK) <= floor(e / kCK) + 1, so the
+        // blocks of sequence n end at or before the first block of sequence n + 1 and
+        // below floor(total / kCK) + N + 1 <= blk_stride, whatever the offsets are
+        const int64_t a = min(max(static_cast<int64_t>(p.cu[seq]), static_cast<int64_t>(0)), p.total);
+        const int64_t e = min(max(static_cast<int64_t>(p.cu[seq + 1]), a), p.total);
+        T = e - a;
+        tok0 = a;
+        ck_blk0 = (h * p.tiles + tile) * p.blk_stride + a / kCK + seq;
+    } else {
+        T = p.T;
+        tok0 = seq * T;
+        ck_blk0 = (bh * p.tiles + tile) * ((T + kCK - 1) / kCK);
+    }
     const int64_t nblk = (T + kCK - 1) / kCK;
-    float* ck = p.ckpt + (bh * p.tiles + tile) * nblk * (DK * kDVT);
+    float* ck = p.ckpt + ck_blk0 * (DK * kDVT);
 
     // A block's token inputs: fetched into registers one block ahead (so the global
     // loads overlap the current block's arithmetic), then stored to shared memory.
@@ -337,17 +356,37 @@ __global__ void __launch_bounds__(kNW * 32, 2) bwd_kernel(const BwdParams p) {
     }
 }
 
+// Packed sequences: whether token row `row` belongs to a sequence (offsets clamped
+// as in bwd_kernel).  Valid offsets are non-decreasing, so the owner is the last
+// sequence whose start is at or before the row; rows before the first start, after
+// the last end or in no sequence are not written.  Malformed offsets only change
+// which rows are written.
+__device__ __forceinline__ bool row_in_sequence(const int* cu, int N, int64_t total, int64_t row) {
+    auto start = [&](int n) { return min(max(static_cast<int64_t>(cu[n]), static_cast<int64_t>(0)), total); };
+    if (N <= 0 || row < start(0)) return false;
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start(mid) <= row) lo = mid; else hi = mid;
+    }
+    const int64_t a = start(lo);
+    const int64_t e = min(max(static_cast<int64_t>(cu[lo + 1]), a), total);
+    return row >= a && row < e;
+}
+
 // dq, dk, db, dlog_decay of one (token row, head) per DK threads: the tiles' row
 // vectors summed, then db = dc * k and dk = G delta + dc * b.
 template <typename Tin, int DK>
 __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* __restrict__ part, const Tin* __restrict__ k,
                                                          const Tin* __restrict__ b, float* __restrict__ dq,
                                                          float* __restrict__ dk, float* __restrict__ db,
-                                                         float* __restrict__ dg, int64_t items, int tiles) {
+                                                         float* __restrict__ dg, int64_t items, int tiles,
+                                                         const int* __restrict__ cu, int N, int64_t total, int H) {
     constexpr int kPer = 256 / DK;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * kPer + threadIdx.x / DK;   // row * H + head
     const int j = threadIdx.x % DK;
     if (item >= items) return;
+    if (cu && !row_in_sequence(cu, N, total, item / H)) return;
     const float* src = part + item * tiles * (kVec * DK) + j;
     float s[kVec] = {0.f, 0.f, 0.f, 0.f};
     for (int t = 0; t < tiles; ++t)
@@ -362,8 +401,8 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* __restrict
 }
 
 template <typename Tin, int DK>
-int run_backward(const BwdParams& p, int64_t B, const float* part, const void* k, const void* b, float* dq,
-                 float* dk, float* db, float* dg, cudaStream_t stream) {
+int run_backward(const BwdParams& p, int64_t B, int64_t rows, const float* part, const void* k, const void* b,
+                 float* dq, float* dk, float* db, float* dg, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
@@ -374,34 +413,47 @@ int run_backward(const BwdParams& p, int64_t B, const float* part, const void* k
     const dim3 grid(static_cast<unsigned>(B * p.H), static_cast<unsigned>(p.tiles));
     bwd_kernel<Tin, DK><<<grid, kNW * 32, bwd_smem<DK>(), stream>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
-    const int64_t items = B * p.T * p.H;
+    const int64_t items = rows * p.H;
     constexpr int kPer = 256 / DK;
     bwd_reduce_kernel<Tin, DK><<<static_cast<unsigned>((items + kPer - 1) / kPer), 256, 0, stream>>>(
-        part, static_cast<const Tin*>(k), static_cast<const Tin*>(b), dq, dk, db, dg, items, p.tiles);
+        part, static_cast<const Tin*>(k), static_cast<const Tin*>(b), dq, dk, db, dg, items, p.tiles, p.cu,
+        static_cast<int>(B), p.total, p.H);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 
 }  // namespace
 
-size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv) {
-    const int64_t tiles = dv / kDVT, nblk = (T + kCK - 1) / kCK;
-    const size_t ck = static_cast<size_t>(B * H * tiles * nblk) * dk * kDVT * 4;
-    const size_t part = static_cast<size_t>(B * T * H * tiles) * kVec * dk * 4;
+namespace {
+// checkpoint blocks per (sequence * head, tile), or per (head, tile) over all packed
+// sequences (see bwd_kernel for why blocks from floor(start / kCK) + n fit)
+int64_t ckpt_blocks(int64_t N, int64_t T, int64_t H, int64_t tiles, bool packed, int64_t total) {
+    return packed ? H * tiles * (total / kCK + N + 2) : N * H * tiles * ((T + kCK - 1) / kCK);
+}
+}  // namespace
+
+size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv, bool packed,
+                                int64_t total) {
+    const int64_t tiles = dv / kDVT, rows = packed ? total : B * T;
+    const size_t ck = static_cast<size_t>(ckpt_blocks(B, T, H, tiles, packed, total)) * dk * kDVT * 4;
+    const size_t part = static_cast<size_t>(rows * H * tiles) * kVec * dk * 4;
     return (ck + 255) / 256 * 256 + part;
 }
 
 int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream) {
     if (a.dv % kDVT != 0 || a.B * a.H >= (1ll << 31) || a.dv / kDVT > 65535) return GDR2_ERR_SHAPE;
-    const int64_t tiles = a.dv / kDVT, nblk = (a.T + kCK - 1) / kCK;
-    const size_t ckb = (static_cast<size_t>(a.B * a.H * tiles * nblk) * a.dk * kDVT * 4 + 255) / 256 * 256;
+    const bool packed = a.cu != nullptr;
+    const int64_t tiles = a.dv / kDVT, rows = packed ? a.total : a.B * a.T;
+    const size_t ckb =
+        (static_cast<size_t>(ckpt_blocks(a.B, a.T, a.H, tiles, packed, a.total)) * a.dk * kDVT * 4 + 255) / 256 * 256;
     BwdParams p{a.q, a.k, a.v, a.b, a.w, a.g, a.S0, a.dO, a.dST, a.d_v, a.d_w, a.d_S0,
                 static_cast<float*>(ws), reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ckb),
-                a.T, static_cast<int>(a.H), static_cast<int>(a.dv), static_cast<int>(tiles)};
+                packed ? 0 : a.T, static_cast<int>(a.H), static_cast<int>(a.dv), static_cast<int>(tiles),
+                a.cu, packed ? a.total : 0, packed ? a.total / kCK + a.B + 2 : 0};
     const bool bf = a.in_dtype == GDR2_BF16;
     using bf16 = __nv_bfloat16;
 #define GDR2_BWD(DKV)                                                                                           \
-    return bf ? run_backward<bf16, DKV>(p, a.B, p.part, a.k, a.b, a.d_q, a.d_k, a.d_b, a.d_g, stream)          \
-              : run_backward<float, DKV>(p, a.B, p.part, a.k, a.b, a.d_q, a.d_k, a.d_b, a.d_g, stream)
+    return bf ? run_backward<bf16, DKV>(p, a.B, rows, p.part, a.k, a.b, a.d_q, a.d_k, a.d_b, a.d_g, stream)    \
+              : run_backward<float, DKV>(p, a.B, rows, p.part, a.k, a.b, a.d_q, a.d_k, a.d_b, a.d_g, stream)
     switch (a.dk) {
         case 32: GDR2_BWD(32);
         case 64: GDR2_BWD(64);

@@ -42,8 +42,10 @@ struct BackwardArgs {
     const float* dST;                    // [B, H, dk, dv] gradient at S_T, or null (zero)
     float *d_q, *d_k, *d_v, *d_b, *d_w, *d_g;   // fp32 gradients, layouts of the inputs
     float* d_S0;                         // [B, H, dk, dv] or null (not stored)
-    int64_t B, T, H, dk, dv;
+    int64_t B, T, H, dk, dv;   // B sequences; T their common length when cu is null
     int in_dtype;
+    const int* cu = nullptr;   // packed sequences: start offsets [B + 1] on the device, or null
+    int64_t total = 0;         // token rows of the packed tensors (cu != null)
 };
 
 struct DecodeArgs {
@@ -74,7 +76,8 @@ int launch_recurrent(const ForwardArgs& a, cudaStream_t stream);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Gradients (token-sequential fp32 kernels); the workspace holds state
 // checkpoints and the per-tile row-vector partials.
-size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
+size_t backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv, bool packed = false,
+                                int64_t total = 0);
 int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream);
 // Chunked gradients (bf16 inputs, d_k = d_v = 128, T > 0): the forward's prep2 (with
 // backward records) and chain kernels keep every chunk's maps and start state, the

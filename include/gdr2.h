@@ -278,6 +278,42 @@ int gdr2_backward(const void* q, const void* k, const void* v,
                   int in_dtype, cudaStream_t stream);
 
 /*
+ * gdr2_backward_varlen -- gdr2_backward over N packed sequences of different
+ * lengths: the gradients of gdr2_forward_varlen.  Sequence n owns token rows
+ * [cu_seqlens[n], cu_seqlens[n+1]) and its own S0[n], d_S_T[n] and d_S0[n];
+ * each sequence is an independent recurrence, so its gradients are those of
+ * gdr2_backward on that sequence alone, with the same fp32 arithmetic.
+ *
+ *   q, k, b, log_decay : [total_T, H, dk]  (in_dtype), the forward's inputs
+ *   v, w               : [total_T, H, dv]  (in_dtype)
+ *   S0                 : [N, H, dk, dv] fp32, or NULL (zero initial states)
+ *   d_o                : [total_T, H, dv] fp32, gradient arriving at o
+ *   d_S_T              : [N, H, dk, dv] fp32, or NULL (zero)
+ *   d_q, d_k, d_b, d_log_decay : [total_T, H, dk] fp32, written for every row
+ *                        that belongs to a sequence (other rows are left as they are)
+ *   d_v, d_w           : [total_T, H, dv] fp32, likewise
+ *   d_S0               : [N, H, dk, dv] fp32, written, or NULL (not stored)
+ *   cu_seqlens         : [N + 1] int32 DEVICE offsets, as for gdr2_forward_varlen
+ *                        (non-decreasing, from 0 to total_T; clamped on the device,
+ *                        so malformed offsets give empty, truncated or unspecified
+ *                        sequences, never out-of-range accesses)
+ *
+ * dk, dv in {32, 64, 128}.  Workspace (the library's pool, released on the
+ * stream): H*(dv/32)*(total_T/4 + N + 2)*dk*32*4 bytes of checkpoints plus
+ * total_T*H*(dv/32)*4*dk*4 bytes of per-tile partial sums.  An empty sequence
+ * gives d_S0[n] = d_S_T[n] (or zeros).  Errors and aliasing rules are those of
+ * gdr2_backward; no output may overlap cu_seqlens, and a null cu_seqlens with
+ * N > 0 is GDR2_ERR_ARG.
+ */
+int gdr2_backward_varlen(const void* q, const void* k, const void* v,
+                         const void* b, const void* w, const void* log_decay,
+                         const float* S0, const float* d_o, const float* d_S_T,
+                         float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                         float* d_log_decay, float* d_S0, const int32_t* cu_seqlens,
+                         int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                         int in_dtype, cudaStream_t stream);
+
+/*
  * gdr2_backward_chunked -- the gradients of gdr2_backward (same arguments, same
  * outputs) through the chunkwise WY form on tensor cores, for bf16 inputs with
  * dk = dv = 128 (GDR2_ERR_UNSUPPORTED otherwise).  Per 64-token chunk, with

@@ -176,6 +176,30 @@ def test_backward_rejects_bad_args():
     assert call(gS0=ctypes.c_void_p(BASE + 6 * GAP)) == ALIAS      # d_S0 over S0
 
 
+def bwd_varlen_args(N=3, total=10, H=2, dk=64, dv=64, dtype=1, **over):
+    names = ["q", "k", "v", "b", "w", "g", "S0", "do", "dST",
+             "gq", "gk", "gv", "gb", "gw", "gg", "gS0", "cu"]
+    p = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in enumerate(names)}
+    p.update(over)
+    return [p[n] for n in names] + [N, total, H, dk, dv, dtype, None]
+
+
+def test_backward_varlen_rejects_bad_args():
+    L = _lib.lib()
+    call = lambda **kw: L.gdr2_backward_varlen(*bwd_varlen_args(**kw))  # noqa: E731
+    assert call(cu=None) == ARG
+    assert call(N=-1) == ARG
+    assert call(total=-5) == ARG
+    assert call(total=1 << 31) == SHAPE
+    assert call(dk=48) == SHAPE
+    assert call(dtype=5) == UNSUP
+    assert call(gq=None) == ARG
+    assert call(cu=ctypes.c_void_p(BASE + 16 * GAP + 2)) == ALIGN
+    assert call(gg=ctypes.c_void_p(BASE + 16 * GAP)) == ALIAS      # d_log_decay over cu_seqlens
+    assert call(gS0=ctypes.c_void_p(BASE + 16 * GAP)) == ALIAS     # d_S0 over cu_seqlens
+    assert call(gv=ctypes.c_void_p(BASE + 2 * GAP)) == ALIAS       # d_v over v
+
+
 def test_cached_rejects_bad_args():
     L = _lib.lib()
 
