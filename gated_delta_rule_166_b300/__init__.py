@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     gdr2_apply_varlen,
     gdr2_backward,
     gdr2_backward_chunked,
+    gdr2_backward_chunked_varlen,
     gdr2_backward_varlen,
     gdr2_decode_step,
     gdr2_device_status,
@@ -37,5 +38,6 @@ decode_step = gdr2_decode_step
 backward = gdr2_backward
 backward_chunked = gdr2_backward_chunked
 backward_varlen = gdr2_backward_varlen
+backward_chunked_varlen = gdr2_backward_chunked_varlen
 apply_varlen = gdr2_apply_varlen
 sparse_write = gdr2_sparse_write

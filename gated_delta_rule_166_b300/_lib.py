@@ -56,6 +56,8 @@ def lib():
         L.gdr2_backward.restype = ci
         L.gdr2_backward_varlen.argtypes = [vp] * 17 + [i64] * 5 + [ci, vp]
         L.gdr2_backward_varlen.restype = ci
+        L.gdr2_backward_chunked_varlen.argtypes = [vp] * 17 + [i64] * 5 + [ci, vp]
+        L.gdr2_backward_chunked_varlen.restype = ci
         L.gdr2_backward_chunked.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
         L.gdr2_backward_chunked.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
@@ -289,13 +291,26 @@ def gdr2_backward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T=No
     d_o: [total_T, H, dv] fp32; d_S_T: [N, H, dk, dv] fp32 or None.  Returns fp32
     (dq, dk, dv, db, dw, dlog_decay, dS0), dS0 None when ``want_dS0`` is False.
     Rows that belong to no sequence are returned as zeros."""
+    return _backward_varlen("gdr2_backward_varlen", q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T,
+                            want_dS0, stream)
+
+
+def gdr2_backward_chunked_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T=None, *,
+                                 want_dS0: bool = True, stream=None):
+    """gdr2_backward_varlen through the chunkwise WY form on tensor cores: bf16
+    inputs with dk = dv = 128, the same arguments and outputs."""
+    return _backward_varlen("gdr2_backward_chunked_varlen", q, k, v, b, w, log_decay, cu_seqlens, S0, d_o,
+                            d_S_T, want_dS0, stream)
+
+
+def _backward_varlen(fn, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0, stream):
     if q.dim() != 3 or v.dim() != 3:
         raise ValueError("q and v must be [total_T, H, d]")
     total, H, dk = q.shape
     dv = v.shape[-1]
     dtype, dev = q.dtype, q.device
     if dev.type != "cuda":
-        raise ValueError("gdr2_backward_varlen runs on CUDA tensors only")
+        raise ValueError(f"{fn} runs on CUDA tensors only")
     if dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
@@ -314,12 +329,12 @@ def gdr2_backward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T=No
     gv, gw = (torch.zeros((total, H, dv), **f32) for _ in range(2))
     gS0 = torch.empty((N, H, dk, dv), **f32) if want_dS0 else None
     with torch.cuda.device(dev):
-        st = lib().gdr2_backward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
-                                        _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
-                                        _ptr(gg), _ptr(gS0), _ptr(cu_seqlens), N, total, H, dk, dv,
-                                        _DTYPES[dtype], ctypes.c_void_p(_stream_handle(stream)))
+        st = getattr(lib(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
+                                _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
+                                _ptr(gg), _ptr(gS0), _ptr(cu_seqlens), N, total, H, dk, dv,
+                                _DTYPES[dtype], ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
-        raise GDR2Error(st, "gdr2_backward_varlen")
+        raise GDR2Error(st, fn)
     return gq, gk, gv, gb, gw, gg, gS0
 
 
@@ -360,14 +375,17 @@ def gdr2_apply(q, k, v, b, w, log_decay, S0=None, *, chunked_backward: bool = Fa
 class GatedDeltaRule2Varlen(torch.autograd.Function):
     """(o, S_T) = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0) as
     a differentiable operation over packed sequences: the forward pass is
-    gdr2_forward_varlen (fp32 o), the backward pass gdr2_backward_varlen.
-    Gradients are fp32 and cast to each input's dtype; cu_seqlens gets none."""
+    gdr2_forward_varlen (fp32 o), the backward pass gdr2_backward_varlen, or
+    gdr2_backward_chunked_varlen when ``chunked`` is set and the inputs are bf16
+    with dk = dv = 128.  Gradients are fp32 and cast to each input's dtype;
+    cu_seqlens gets none."""
 
     @staticmethod
-    def forward(ctx, q, k, v, b, w, log_decay, cu_seqlens, S0=None):
+    def forward(ctx, q, k, v, b, w, log_decay, cu_seqlens, S0=None, chunked=False):
         o, S_T = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0)
         ctx.save_for_backward(q, k, v, b, w, log_decay, cu_seqlens, S0)
         ctx.has_s0 = S0 is not None
+        ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16 and q.shape[-1] == 128 and v.shape[-1] == 128
         return o, S_T
 
     @staticmethod
@@ -376,15 +394,18 @@ class GatedDeltaRule2Varlen(torch.autograd.Function):
         d_o = torch.zeros(v.shape, dtype=torch.float32, device=q.device) if d_o is None \
             else d_o.float().contiguous()
         d_S_T = None if d_S_T is None else d_S_T.float().contiguous()
-        g = gdr2_backward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
+        fn = gdr2_backward_chunked_varlen if ctx.chunked else gdr2_backward_varlen
+        g = fn(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
         cast = [g[i].to(t.dtype) for i, t in enumerate((q, k, v, b, w, log_decay))]
-        return (*cast, None, g[6] if ctx.has_s0 else None)
+        return (*cast, None, g[6] if ctx.has_s0 else None, None)
 
 
-def gdr2_apply_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None):
+def gdr2_apply_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, chunked_backward: bool = False):
     """Differentiable prefill over packed sequences: ``(o, S_T)`` of
-    gdr2_forward_varlen with gradients through gdr2_backward_varlen (exact fp32)."""
-    return GatedDeltaRule2Varlen.apply(q, k, v, b, w, log_decay, cu_seqlens, S0)
+    gdr2_forward_varlen with gradients through gdr2_backward_varlen (exact fp32),
+    or through gdr2_backward_chunked_varlen (tensor cores; bf16 inputs with dk =
+    dv = 128, else the exact path) when ``chunked_backward`` is set."""
+    return GatedDeltaRule2Varlen.apply(q, k, v, b, w, log_decay, cu_seqlens, S0, chunked_backward)
 
 
 def gdr2_decode_step(q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.float32,

@@ -407,7 +407,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
             if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return GDR2_ERR_ALIAS;
         if (overlaps(outs[i], out_bytes[i], cu, bc)) return GDR2_ERR_ALIAS;
     }
-    if (chunked && (cu || in_dtype != GDR2_BF16 || dk != kPrepDK || dv != 128)) return GDR2_ERR_UNSUPPORTED;
+    if (chunked && (in_dtype != GDR2_BF16 || dk != kPrepDK || dv != 128)) return GDR2_ERR_UNSUPPORTED;
     int* err = nullptr;
     int st = device_setup(&err);
     if (st != GDR2_OK) return st;
@@ -421,7 +421,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
     BackwardArgs a{q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                    B, cu ? 0 : T, H, dk, dv, in_dtype, reinterpret_cast<const int*>(cu), cu ? total : 0};
     void* ws = nullptr;
-    const size_t wsb = chunked ? backward_chunked_workspace_bytes(B, T, H)
+    const size_t wsb = chunked ? backward_chunked_workspace_bytes(B, a.T, H, cu != nullptr, a.total)
                                : backward_workspace_bytes(B, a.T, H, dk, dv, cu != nullptr, a.total);
     if ((st = ws_alloc(&ws, wsb, stream)) != GDR2_OK) return st;
     int rc = chunked ? launch_backward_chunked(a, ws, stream, err) : launch_backward(a, ws, stream);
@@ -454,6 +454,20 @@ extern "C" int gdr2_backward_varlen(const void* q, const void* k, const void* v,
     if (N < 0 || total_T < 0) return GDR2_ERR_ARG;
     return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                          N, 0, H, dk, dv, in_dtype, stream, false, N > 0 ? cu_seqlens : nullptr, total_T);
+}
+
+extern "C" int gdr2_backward_chunked_varlen(const void* q, const void* k, const void* v,
+                                            const void* b, const void* w, const void* log_decay,
+                                            const float* S0, const float* d_o, const float* d_S_T,
+                                            float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                            float* d_log_decay, float* d_S0, const int32_t* cu_seqlens,
+                                            int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                            int in_dtype, cudaStream_t stream) {
+    if (N > 0 && !cu_seqlens) return GDR2_ERR_ARG;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
+    if (N < 0 || total_T < 0) return GDR2_ERR_ARG;
+    return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                         N, 0, H, dk, dv, in_dtype, stream, true, N > 0 ? cu_seqlens : nullptr, total_T);
 }
 
 extern "C" int gdr2_backward_chunked(const void* q, const void* k, const void* v,

@@ -84,20 +84,42 @@ constexpr int kTmCols = 256;   // per buffer b: 128 b + [0, 64) and + [64, 128),
 struct Params {
     const uint8_t* slots;
     const float* dST;   // [B H][d_k][d_v] or null (zero)
-    const float* dO;    // [B T][H][d_v]
-    float* dsn;         // [B H][nch][d_k][d_v]: gradient at each chunk's end state
+    const float* dO;    // [token rows][H][d_v]
+    float* dsn;         // [global chunk][H][d_k][d_v]: gradient at each chunk's end state
     float* dS0;         // [B H][d_k][d_v] or null
     int* err;
     int T, H, nch;
     long long wait_cycles;
+    // packed sequences: token offsets [B + 1] and first global chunk of each sequence
+    // (T and nch unused), or null
+    const int* cu;
+    const int* chunk_base;
+    int total;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
     const int bh = static_cast<int>(blockIdx.x);
     const int h = bh % prm.H, seq = bh / prm.H;
     const int j0 = static_cast<int>(blockIdx.y) * kDVT;
-    const int n = prm.nch, T = prm.T;
-    const int64_t tok0 = static_cast<int64_t>(seq) * T;
+    // this sequence's token rows and its first global chunk (packed offsets clamped as
+    // in the forward kernels)
+    int n, T;
+    int64_t tok0, chunk0;
+    if (prm.cu) {
+        const int a = min(max(prm.cu[seq], 0), prm.total);
+        const int e = min(max(prm.cu[seq + 1], a), prm.total);
+        // only the chunks this sequence was given (see chunk_base_kernel)
+        T = static_cast<int>(min(static_cast<int64_t>(e - a),
+                                     static_cast<int64_t>(prm.chunk_base[seq + 1] - prm.chunk_base[seq]) * kC));
+        n = (T + kC - 1) / kC;
+        tok0 = a;
+        chunk0 = prm.chunk_base[seq];
+    } else {
+        T = prm.T;
+        n = prm.nch;
+        tok0 = static_cast<int64_t>(seq) * T;
+        chunk0 = static_cast<int64_t>(seq) * n;
+    }
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -107,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + kAbort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quarter = warp & 3;
     auto slot_of = [&](int c) {
-        return prm.slots + (static_cast<int64_t>(seq * n + c) * prm.H + h) * static_cast<int64_t>(kSlot2Bytes);
+        return prm.slots + ((chunk0 + c) * prm.H + h) * static_cast<int64_t>(kSlot2Bytes);
     };
 
     if (tid == 0) {
@@ -225,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
                 *reinterpret_cast<uint4*>(img + ((static_cast<uint32_t>((2 * R + q) ^ (j & 7))) << 4)) =
                     make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         };
-        float* const dsn_row = prm.dsn + (static_cast<int64_t>(bh) * n * kPrepDK + j) * 128 + j0 + 16 * R;
+        float* const dsn_row = prm.dsn + ((chunk0 * prm.H + h) * kPrepDK + j) * 128 + j0 + 16 * R;
         auto keep = [&](int c, const float (&S)[16]) {
-            float* p = dsn_row + static_cast<int64_t>(c) * kPrepDK * 128;
+            float* p = dsn_row + static_cast<int64_t>(c) * prm.H * kPrepDK * 128;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4)
                 *reinterpret_cast<float4*>(p + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
@@ -384,14 +406,20 @@ constexpr int kTmCols = 512;
 
 struct Params {
     const uint8_t* wy;          // backward records [items][kWyBytes]
-    const float* Sc;            // state after chunk c (c < n_cache): [B H][n_cache][d_k][d_v]
+    const float* Sc;            // state after chunk c (c < n_cache): [B H][n_cache][d_k][d_v];
+                                // packed: after every global chunk, [global chunk][H][d_k][d_v]
     const float* S0;            // [B H][d_k][d_v] or null
-    const float* dsn;           // [B H][nch][d_k][d_v]
-    const float* dO;            // [B T][H][d_v]
+    const float* dsn;           // [global chunk][H][d_k][d_v]
+    const float* dO;            // [token rows][H][d_v]
     const __nv_bfloat16 *q, *k, *b, *g, *v, *w;
     float *dq, *dk, *db, *dg, *dv, *dw;
     int T, H, nch, n_cache;
     int* err;
+    // packed sequences: token offsets [N + 1] and first global chunk of each sequence
+    // (T, nch and n_cache unused), or null; the grid may hold items past the last chunk
+    const int* cu;
+    const int* chunk_base;
+    int N, total;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -457,11 +485,32 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
     const int a = 32 * quarter + lane;   // M = 128 accumulator row (key channel or d_v column)
 
     const int it = static_cast<int>(blockIdx.x);
-    const int gc = it / prm.H, h = it - gc * prm.H;
-    const int seq = gc / prm.nch, c = gc - seq * prm.nch;
+    const int gc = it / prm.H, h = it - gc * prm.H;   // global chunk, head
+    int seq, c, nvalid;
+    int64_t row0;   // first token row of the chunk
+    if (prm.cu) {
+        // packed sequences: the last sequence whose first global chunk is at or before gc
+        // (offsets clamped as in the forward kernels); items past the last chunk exit
+        const int* cbs = prm.chunk_base;
+        if (gc >= cbs[prm.N]) return;
+        int lo = 0, hi = prm.N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cbs[mid] <= gc) lo = mid; else hi = mid;
+        }
+        seq = lo;
+        c = gc - cbs[lo];
+        const int a = min(max(prm.cu[seq], 0), prm.total);
+        const int e = min(max(prm.cu[seq + 1], a), prm.total);
+        nvalid = min(e - a - c * kC, kC);
+        row0 = static_cast<int64_t>(a) + static_cast<int64_t>(c) * kC;
+    } else {
+        seq = gc / prm.nch;
+        c = gc - seq * prm.nch;
+        nvalid = min(prm.T - c * kC, kC);
+        row0 = static_cast<int64_t>(seq) * prm.T + static_cast<int64_t>(c) * kC;
+    }
     const int bh = seq * prm.H + h;
-    const int nvalid = min(prm.T - c * kC, kC);
-    const int64_t row0 = static_cast<int64_t>(seq) * prm.T + static_cast<int64_t>(c) * kC;   // first token row
     auto gidx = [&](int r, int ch) { return ((row0 + r) * prm.H + h) * 128 + ch; };
 
     if (tid == 0) {
@@ -493,9 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 
     // ---- S, dS' -> fp16 images [d_k][d_v]; rowsum(dS' * S) ----------------------------------
     {
-        const float* Sp = c == 0 ? (prm.S0 ? prm.S0 + static_cast<int64_t>(bh) * 16384 : nullptr)
-                                 : prm.Sc + (static_cast<int64_t>(bh) * prm.n_cache + (c - 1)) * 16384;
-        const float* dSp = prm.dsn + (static_cast<int64_t>(bh) * prm.nch + c) * 16384;
+        const float* Sp = c == 0  ? (prm.S0 ? prm.S0 + static_cast<int64_t>(bh) * 16384 : nullptr)
+                          : prm.cu ? prm.Sc + (static_cast<int64_t>(it) - prm.H) * 16384   // global chunk gc - 1
+                                   : prm.Sc + (static_cast<int64_t>(bh) * prm.n_cache + (c - 1)) * 16384;
+        const float* dSp = prm.dsn + static_cast<int64_t>(it) * 16384;   // global chunk gc, head h
         const int r = tid >> 2, e0 = 32 * (tid & 3);
         float part = 0.f;
 #pragma unroll
@@ -934,42 +984,70 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 
 }  // namespace
 
-size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H) {
-    const int64_t nch = (T + kC - 1) / kC, n_cache = T / kC;
-    const size_t items = static_cast<size_t>(B * nch * H);
+namespace {
+// Chunks of the call (packed sequences: an upper bound, every sequence adding at most
+// one partial chunk) and the workspace regions, in order: forward slots, backward
+// records, start states (the chain's cached states), end-state gradients, the
+// recomputed forward's o, and (packed) the first global chunk of each sequence.
+struct ChunkedLayout {
+    int64_t chunks, n_cache;
+    size_t slots, wy, sc, dsn, o, cb, total;
+};
+ChunkedLayout chunked_layout(int64_t B, int64_t T, int64_t H, bool packed, int64_t total_rows) {
     auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
-    return r256(items * kSlot2Bytes) + r256(items * kWyBytes) +
-           r256(static_cast<size_t>(B * H * n_cache) * 16384 * 4) + r256(static_cast<size_t>(B * H * nch) * 16384 * 4) +
-           r256(static_cast<size_t>(B * T * H) * 128 * 2);
+    ChunkedLayout l{};
+    const int64_t rows = packed ? total_rows : B * T;
+    l.chunks = packed ? (total_rows + kC - 1) / kC + B : B * ((T + kC - 1) / kC);
+    l.n_cache = packed ? 0 : T / kC;
+    const size_t items = static_cast<size_t>(l.chunks * H);
+    l.slots = r256(items * kSlot2Bytes);
+    l.wy = r256(items * kWyBytes);
+    l.sc = r256((packed ? items : static_cast<size_t>(B * H * l.n_cache)) * 16384 * 4);
+    l.dsn = r256(items * 16384 * 4);
+    l.o = r256(static_cast<size_t>(rows * H) * 128 * 2);
+    l.cb = packed ? r256(static_cast<size_t>(B + 1) * 4) : 0;
+    l.total = l.slots + l.wy + l.sc + l.dsn + l.o + l.cb;
+    return l;
+}
+}  // namespace
+
+size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed, int64_t total) {
+    return chunked_layout(B, T, H, packed, total).total;
 }
 
 int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err) {
-    if (a.in_dtype != GDR2_BF16 || a.dk != kPrepDK || a.dv != 128 || a.T <= 0) return GDR2_ERR_UNSUPPORTED;
-    const int64_t nch = (a.T + kC - 1) / kC, n_cache = a.T / kC;
-    const int64_t chunks = a.B * nch, items = chunks * a.H;
-    if (items >= (1ll << 31) || a.B * a.H >= 65536ll * 32768ll) return GDR2_ERR_SHAPE;
-    auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+    const bool packed = a.cu != nullptr;
+    if (a.in_dtype != GDR2_BF16 || a.dk != kPrepDK || a.dv != 128 || (packed ? a.total <= 0 : a.T <= 0))
+        return GDR2_ERR_UNSUPPORTED;
+    const ChunkedLayout l = chunked_layout(a.B, a.T, a.H, packed, a.total);
+    const int64_t chunks = l.chunks, items = chunks * a.H, n_cache = l.n_cache;
+    const int64_t nch = packed ? 0 : (a.T + kC - 1) / kC;
+    if (items >= (1ll << 31) || a.B * a.H >= 65536ll * 32768ll || (packed && a.total >= (1ll << 31)))
+        return GDR2_ERR_SHAPE;
     uint8_t* p = static_cast<uint8_t*>(ws);
     uint8_t* slots = p;
-    p += r256(static_cast<size_t>(items) * kSlot2Bytes);
+    p += l.slots;
     uint8_t* wy = p;
-    p += r256(static_cast<size_t>(items) * kWyBytes);
+    p += l.wy;
     float* Sc = reinterpret_cast<float*>(p);
-    p += r256(static_cast<size_t>(a.B * a.H * n_cache) * 16384 * 4);
+    p += l.sc;
     float* dsn = reinterpret_cast<float*>(p);
-    p += r256(static_cast<size_t>(a.B * a.H * nch) * 16384 * 4);
+    p += l.dsn;
     void* o_scratch = p;
+    p += l.o;
+    int* cb = packed ? reinterpret_cast<int*>(p) : nullptr;
 
     // forward: every chunk's maps and backward record, and its start state (the chain's
     // cached state after each chunk)
-    ForwardArgs f{a.q, a.k, a.v, a.b, a.w, a.g, a.S0, o_scratch, nullptr, a.B, a.T, a.H, a.dk, a.dv,
-                  nullptr, a.B * a.T, GDR2_BF16, GDR2_BF16};
-    if (n_cache > 0) {
+    ForwardArgs f{a.q, a.k, a.v, a.b, a.w, a.g, a.S0, o_scratch, nullptr, a.B, packed ? 0 : a.T, a.H, a.dk, a.dv,
+                  a.cu, packed ? a.total : a.B * a.T, GDR2_BF16, GDR2_BF16};
+    if (packed || n_cache > 0) {
         f.S_cache = Sc;
         f.cache_chunks = 1;
     }
-    int rc = launch_prep2(f, slots, nullptr, chunks, stream, err, 0, 0, wy);
-    if (rc == GDR2_OK) rc = launch_chain(f, slots, nullptr, stream, err);
+    int rc = packed ? launch_chunk_base(a.cu, a.B, a.total, cb, stream) : GDR2_OK;
+    if (rc == GDR2_OK) rc = launch_prep2(f, slots, cb, chunks, stream, err, 0, 0, wy);
+    if (rc == GDR2_OK) rc = launch_chain(f, slots, cb, stream, err);
     if (rc != GDR2_OK) return rc;
 
     static std::once_flag attr_once;
@@ -983,7 +1061,7 @@ int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     rch::Params rp{slots, a.dST, a.dO, dsn, a.d_S0, err, static_cast<int>(a.T), static_cast<int>(a.H),
-                   static_cast<int>(nch), kWaitCycles};
+                   static_cast<int>(nch), kWaitCycles, a.cu, cb, static_cast<int>(packed ? a.total : 0)};
     rch::rchain_kernel<<<dim3(static_cast<unsigned>(a.B * a.H), 2), rch::kThreads, rch::kSmemAlloc, stream>>>(rp);
     if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
     cgr::Params gp{wy, Sc, a.S0, dsn, a.dO,
@@ -991,7 +1069,8 @@ int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream
                    static_cast<const __nv_bfloat16*>(a.b), static_cast<const __nv_bfloat16*>(a.g),
                    static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
                    a.d_q, a.d_k, a.d_b, a.d_g, a.d_v, a.d_w,
-                   static_cast<int>(a.T), static_cast<int>(a.H), static_cast<int>(nch), static_cast<int>(n_cache), err};
+                   static_cast<int>(a.T), static_cast<int>(a.H), static_cast<int>(nch), static_cast<int>(n_cache), err,
+                   a.cu, cb, static_cast<int>(a.B), static_cast<int>(packed ? a.total : 0)};
     cgr::cgrad_kernel<<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }

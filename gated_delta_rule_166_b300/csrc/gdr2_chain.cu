@@ -106,7 +106,8 @@ struct ChainParams {
     // fixed-length: this launch covers chunks c0 .. c0 + nch - 1 of every sequence (its
     // slots numbered from 0 per sequence); S0 is the state before chunk c0
     int c0;
-    // the state after every cache_chunks chunks: [N][H][n_cache][d_k][dv] (null: not kept)
+    // the state after every cache_chunks chunks: [N][H][n_cache][d_k][dv] (null: not kept);
+    // packed sequences (cache_chunks = 1): after every chunk, [global chunk][H][d_k][dv]
     float* cache;
     int cache_chunks, n_cache;
 };
@@ -141,8 +142,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
         const int a = min(max(prm.cu[seq], 0), prm.total);
         const int e = min(max(prm.cu[seq + 1], a), prm.total);
         tok0 = a;
-        T = e - a;
         chunk0 = prm.chunk_base[seq];
+        // only the chunks this sequence was given slots for (fewer than its length only
+        // for overlapping malformed offsets, see chunk_base_kernel)
+        T = static_cast<int>(min(static_cast<int64_t>(e - a),
+                                     static_cast<int64_t>(prm.chunk_base[seq + 1] - prm.chunk_base[seq]) * kC));
     } else {
         // chunks c0 + g L .. of the sequence: tokens counted from the first of them
         T = prm.T - (prm.c0 + g * prm.L) * kC;
@@ -463,13 +467,22 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
             if (!kTransfer && prm.cache) {
                 // the state after chunk cc of the sequence, every cache_chunks chunks (stored
                 // after the next chunk's operand is released: off the chain's critical path)
-                const int cc = prm.c0 + c;
-                const int ci = (cc + 1) / prm.cache_chunks - 1;
-                if ((cc + 1) % prm.cache_chunks == 0 && ci < prm.n_cache && j < prm.dk && j0 + 16 * R < prm.dv) {
-                    float* cp = prm.cache + ((static_cast<int64_t>(bh) * prm.n_cache + ci) * prm.dk + j) * prm.dv + j0 + 16 * R;
+                if (prm.cu) {
+                    if (j < prm.dk && j0 + 16 * R < prm.dv) {
+                        float* cp = prm.cache + (((chunk0 + c) * prm.H + h) * prm.dk + j) * prm.dv + j0 + 16 * R;
 #pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4)
-                        *reinterpret_cast<float4*>(cp + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+                        for (int jj = 0; jj < 16; jj += 4)
+                            *reinterpret_cast<float4*>(cp + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+                    }
+                } else {
+                    const int cc = prm.c0 + c;
+                    const int ci = (cc + 1) / prm.cache_chunks - 1;
+                    if ((cc + 1) % prm.cache_chunks == 0 && ci < prm.n_cache && j < prm.dk && j0 + 16 * R < prm.dv) {
+                        float* cp = prm.cache + ((static_cast<int64_t>(bh) * prm.n_cache + ci) * prm.dk + j) * prm.dv + j0 + 16 * R;
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 4)
+                            *reinterpret_cast<float4*>(cp + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+                    }
                 }
             }
             if (c + 2 < n) {
@@ -614,6 +627,7 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
     const bool segmented = seg.G > 1;
     const int64_t nch = cpiece > 0 ? cpiece : (a.T + kC - 1) / kC;   // chunks per sequence in this launch
     if ((segmented || a.cu) && (c0 != 0 || cpiece > 0)) return GDR2_ERR_ARG;
+    if (a.cu && a.S_cache && a.cache_chunks != 1) return GDR2_ERR_ARG;   // packed: every chunk's state
     if (segmented && (a.cu || a.dk != kPrepDK || seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L >= nch ||
                       !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r))
         return GDR2_ERR_ARG;

@@ -83,7 +83,7 @@ int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream);
 // backward records) and chain kernels keep every chunk's maps and start state, the
 // reverse chain carries dS across the chunks, one CTA per (chunk, head) forms the
 // token gradients (gdr2_bwd_chunk.cu).
-size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H);
+size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed = false, int64_t total = 0);
 int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err);
 
 // ---- chunked prefill in affine form (bf16 inputs) -----------------------------------

@@ -782,36 +782,41 @@ bool make_token_map(CUtensorMap* m, const void* ptr, int64_t total, int64_t H, i
 }
 
 // First global chunk of each packed sequence: cb[s] = sum_{s' < s} ceil(len_s' / 64),
-// with the same offset clamping the kernels use.  One CTA.
+// with the same offset clamping the kernels use, capped at the workspace's chunk bound
+// ceil(total / 64) + N.  Valid offsets never reach the cap (each sequence adds at most
+// one partial chunk); overlapping malformed ones can, and then the sequences past the
+// cap get fewer chunks (cb[s + 1] - cb[s]) than their length, so that no kernel indexes
+// a chunk beyond the workspace.  One CTA.
 __global__ void chunk_base_kernel(const int* cu, int N, int total, int* cb) {
-    __shared__ int part[1024];
+    __shared__ long long part[1024];
     const int tid = threadIdx.x;
     const int per = (N + blockDim.x - 1) / blockDim.x;
     const int s0 = tid * per, s1 = min(N, s0 + per);
+    const long long cap = min(static_cast<long long>((total + kC - 1) / kC) + N, 0x7fffffffLL);
     auto nch = [&](int s) {
         const int a = min(max(cu[s], 0), total);
         const int e = min(max(cu[s + 1], a), total);
-        return (e - a + kC - 1) / kC;
+        return static_cast<long long>((e - a + kC - 1) / kC);
     };
-    int sum = 0;
+    long long sum = 0;
     for (int s = s0; s < s1; ++s) sum += nch(s);
     part[tid] = sum;
     __syncthreads();
     if (tid == 0) {   // exclusive scan of the partial sums
-        int run = 0;
+        long long run = 0;
         for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
-            const int x = part[i];
+            const long long x = part[i];
             part[i] = run;
             run += x;
         }
     }
     __syncthreads();
-    int run = part[tid];
+    long long run = part[tid];
     for (int s = s0; s < s1; ++s) {
-        cb[s] = run;
+        cb[s] = static_cast<int>(min(run, cap));
         run += nch(s);
     }
-    if (s1 == N && s0 < s1) cb[N] = run;
+    if (s1 == N && s0 < s1) cb[N] = static_cast<int>(min(run, cap));
     if (N == 0 && tid == 0) cb[0] = 0;
 }
 

@@ -350,6 +350,25 @@ int gdr2_backward_chunked(const void* q, const void* k, const void* v,
                           int in_dtype, cudaStream_t stream);
 
 /*
+ * gdr2_backward_chunked_varlen -- gdr2_backward_chunked over N packed sequences:
+ * the gradients of gdr2_forward_varlen through the chunkwise WY form on tensor
+ * cores, for bf16 inputs with dk = dv = 128 (GDR2_ERR_UNSUPPORTED otherwise).
+ * Arguments, layouts and row ownership are those of gdr2_backward_varlen; the
+ * precision is that of gdr2_backward_chunked, sequence by sequence.  Workspace
+ * (the library's pool, released on the stream): per (chunk, head) 123,392
+ * bytes plus 128 KB of start state and end-state gradient, counting
+ * ceil(total_T / 64) + N chunks (each sequence adds at most one partial chunk),
+ * plus total_T*H*dv*2 bytes of o that the recomputed forward writes.
+ */
+int gdr2_backward_chunked_varlen(const void* q, const void* k, const void* v,
+                                 const void* b, const void* w, const void* log_decay,
+                                 const float* S0, const float* d_o, const float* d_S_T,
+                                 float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                 float* d_log_decay, float* d_S0, const int32_t* cu_seqlens,
+                                 int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                 int in_dtype, cudaStream_t stream);
+
+/*
  * gdr2_sparse_write -- the gated delta write on selected slots of a slot
  * memory ("Sparse Delta Memory" review page, section "3. Method & Key
  * Results": the write is applied only to the slots a product-key memory

@@ -200,6 +200,19 @@ def test_backward_varlen_rejects_bad_args():
     assert call(gv=ctypes.c_void_p(BASE + 2 * GAP)) == ALIAS       # d_v over v
 
 
+def test_backward_chunked_varlen_rejects_bad_args():
+    L = _lib.lib()
+    call = lambda **kw: L.gdr2_backward_chunked_varlen(*bwd_varlen_args(**kw))  # noqa: E731
+    assert call(cu=None) == ARG
+    assert call(N=-1) == ARG
+    assert call(total=1 << 31) == SHAPE
+    assert call(dk=48) == SHAPE
+    assert call(dtype=0, dk=128, dv=128) == UNSUP            # fp32 inputs
+    assert call(dk=64, dv=128) == UNSUP                      # head sizes other than 128
+    assert call(cu=ctypes.c_void_p(BASE + 16 * GAP + 2), dk=128, dv=128) == ALIGN
+    assert call(gq=ctypes.c_void_p(BASE + 16 * GAP), dk=128, dv=128) == ALIAS   # d_q over cu_seqlens
+
+
 def test_cached_rejects_bad_args():
     L = _lib.lib()
 

@@ -1,9 +1,10 @@
-"""gdr2_backward_varlen (and the differentiable gdr2_apply_varlen) on the GPU:
-the gradients of every sequence of a packed ragged batch match the fp64
-gradient oracle run on that sequence alone, at the fp32 bar of the exact
-backward (max|err| / RMS(ref) <= 1e-4, fp32 or bf16 inputs); an equal-length
-batch reproduces gdr2_backward bit for bit; rows that belong to no sequence are
-not written; malformed offsets stay in bounds."""
+"""gdr2_backward_varlen, gdr2_backward_chunked_varlen and the differentiable
+gdr2_apply_varlen on the GPU: the gradients of every sequence of a packed
+ragged batch match the fp64 gradient oracle run on that sequence alone -- at
+the fp32 bar of the exact backward (max|err| / RMS(ref) <= 1e-4, fp32 or bf16
+inputs), and at the bf16 bar (2e-2) for the tensor-core path; an equal-length
+batch reproduces gdr2_backward (gdr2_backward_chunked) bit for bit; rows that
+belong to no sequence are not written; malformed offsets stay in bounds."""
 import ctypes
 
 import numpy as np
@@ -154,3 +155,121 @@ def test_autograd_varlen_matches_oracle():
             ro, rS = oracle.forward(*s.tensors(), S0[i:i + 1])
             assert err_over_rms(o[a:e].detach().cpu().numpy(), ro[0]) <= TOL
             assert err_over_rms(S_T[i:i + 1].detach().cpu().numpy(), rS) <= TOL
+
+
+# ---- gdr2_backward_chunked_varlen: the chunkwise WY form on tensor cores -----------------
+# fp16 operands (tf32 for the decay-weighted products) with fp32 accumulation, as in
+# gdr2_backward_chunked, so the bar is the bf16 one on every gradient; the regimes
+# here are those where gdr2_backward_chunked meets 2e-2 on all of them.
+TOL_CHUNKED = 2e-2
+
+
+def _check_sequence_chunked(got, s, i, a, e, S0, d_o, d_ST, label):
+    L = e - a
+    gS0 = got[6].cpu().numpy()
+    if L == 0:
+        assert np.array_equal(gS0[i], d_ST[i].numpy()), f"{label}: empty sequence {i}"
+        return
+    ref = oracle.backward(*s.tensors(), S0[i:i + 1], d_o[a:e].unsqueeze(0), d_ST[i:i + 1])
+    errs = {n: err_over_rms(g[a:e].cpu().numpy(), r[0]) for n, g, r in zip(NAMES, got[:6], ref[:6])}
+    errs["dS0"] = err_over_rms(gS0[i:i + 1], ref[6])
+    bad = {k: v for k, v in errs.items() if not v <= TOL_CHUNKED}
+    assert not bad, f"{label}, sequence {i} (T={L}): " + ", ".join(f"{k}={v:.3e}" for k, v in errs.items())
+
+
+@pytest.mark.parametrize("regime,seed", [("slow", 870), ("mixed", 871)])
+def test_chunked_ragged_batch_matches_oracle_per_sequence(regime, seed):
+    """Ragged against the 64-token chunks: a single token, an empty sequence, exact
+    multiples and partial last chunks, so global chunks of different sequences sit
+    side by side in every workspace region."""
+    lengths = [1, 64, 0, 65, 130, 7, 257]
+    H = 2
+    seqs, toks, S0, cu, d_o, d_ST = _packed(lengths, H, 128, 128, torch.bfloat16, seed=seed, decay_regime=regime)
+    got = gdr2.backward_chunked_varlen(*[t.cuda() for t in toks], cu.cuda(), S0.cuda(), d_o.cuda(), d_ST.cuda())
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    for i, s in enumerate(seqs):
+        _check_sequence_chunked(got, s, i, int(cu[i]), int(cu[i + 1]), S0, d_o, d_ST, f"chunked {regime}")
+
+
+def test_chunked_equal_lengths_reproduce_fixed_length_backward():
+    """The same kernels and arithmetic per chunk: equal lengths give
+    gdr2_backward_chunked's gradients bit for bit (T = 150 leaves a partial chunk)."""
+    B, T, H = 3, 150, 2
+    x = make_prefill_inputs(B, T, H, 128, 128, dtype=torch.bfloat16, seed=880, s0_std=0.3,
+                            decay_regime="slow").to("cuda")
+    gen = torch.Generator().manual_seed(881)
+    d_o = torch.randn(B, T, H, 128, generator=gen).cuda()
+    d_ST = torch.randn(B, H, 128, 128, generator=gen).cuda()
+    ref = gdr2.backward_chunked(*x.tensors(), x.S0, d_o, d_ST)
+    cu = torch.arange(0, (B + 1) * T, T, dtype=torch.int32, device="cuda")
+    packed = [t.reshape(B * T, H, -1) for t in x.tensors()]
+    got = gdr2.backward_chunked_varlen(*packed, cu, x.S0, d_o.reshape(B * T, H, -1), d_ST)
+    torch.cuda.synchronize()
+    for n, g, r in zip(NAMES + ("dS0",), got, ref):
+        assert torch.equal(g.reshape(r.shape), r), n
+
+
+def test_chunked_varlen_without_initial_state_or_final_gradient_and_unsupported_shapes():
+    lengths = [100, 28]
+    H = 2
+    seqs, toks, _, cu, d_o, _ = _packed(lengths, H, 128, 128, torch.bfloat16, seed=890, decay_regime="slow")
+    d = [t.cuda() for t in toks]
+    got = gdr2.backward_chunked_varlen(*d, cu.cuda(), None, d_o.cuda(), None)
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    zeros = torch.zeros(len(lengths), H, 128, 128)
+    for i, s in enumerate(seqs):
+        _check_sequence_chunked(got, s, i, int(cu[i]), int(cu[i + 1]), zeros, d_o, zeros, "S0 = 0, dS_T = 0")
+    with pytest.raises(gdr2.GDR2Error):   # fp32 inputs: the exact path only
+        gdr2.backward_chunked_varlen(*[t.float() for t in d], cu.cuda(), None, d_o.cuda(), None)
+
+
+def test_autograd_varlen_chunked_backward():
+    """gdr2_apply_varlen(chunked_backward=True) on bf16 inputs: gradients through
+    the tensor-core path, returned in bf16 (bar 2e-2 plus one bf16 rounding)."""
+    lengths = [90, 0, 200]
+    H = 2
+    seqs, toks, S0, cu, d_o, d_ST = _packed(lengths, H, 128, 128, torch.bfloat16, seed=895, decay_regime="slow")
+    leaves = [t.cuda().requires_grad_(True) for t in toks] + [S0.cuda().requires_grad_(True)]
+    o, S_T = gdr2.gdr2_apply_varlen(*leaves[:6], cu.cuda(), leaves[6], chunked_backward=True)
+    ((o * d_o.cuda()).sum() + (S_T * d_ST.cuda()).sum()).backward()
+    for i, s in enumerate(seqs):
+        a, e = int(cu[i]), int(cu[i + 1])
+        if e == a:
+            assert torch.equal(leaves[6].grad[i].cpu(), d_ST[i])
+            continue
+        ref = oracle.backward(*s.tensors(), S0[i:i + 1], d_o[a:e].unsqueeze(0), d_ST[i:i + 1])
+        for name, leaf, rf in zip(NAMES + ("dS0",), leaves, ref):
+            g = leaf.grad[i:i + 1] if name == "dS0" else leaf.grad[a:e].unsqueeze(0)
+            assert g.dtype == leaf.dtype
+            bar = TOL_CHUNKED + float(np.abs(rf).max()) * 2.0 ** -8 / float(np.sqrt(np.mean(rf * rf)))
+            err = err_over_rms(g.float().cpu().numpy(), rf)
+            assert err <= bar, f"sequence {i} {name}: {err:.3e} (bar {bar:.3g})"
+
+
+def test_chunked_overlapping_offsets_stay_within_the_workspace():
+    """Offsets [0, 640, 0, 640, 0, 640] claim 30 chunks where the workspace holds 15
+    (see the forward's test of the same offsets): sequence 0 keeps its 10 chunks,
+    sequence 2 gets its first 5 and sequence 4 none.  dS0 of each follows from the
+    chunks it was given: the full sequence, the first 320 tokens with dS_T at their
+    end, and dS_T itself."""
+    H, total = 2, 640
+    x = make_prefill_inputs(1, total, H, 128, 128, dtype=torch.bfloat16, seed=896, s0_std=0.3,
+                            decay_regime="slow")
+    gen = torch.Generator().manual_seed(897)
+    S0 = torch.randn(5, H, 128, 128, generator=gen) * 0.3
+    d_o = torch.randn(total, H, 128, generator=gen)
+    d_ST = torch.randn(5, H, 128, 128, generator=gen)
+    cu = torch.tensor([0, 640, 0, 640, 0, 640], dtype=torch.int32)
+    toks = [t[0].contiguous().cuda() for t in x.tensors()]
+    got = gdr2.backward_chunked_varlen(*toks, cu.cuda(), S0.cuda(), d_o.cuda(), d_ST.cuda())
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    dS0 = got[6].cpu()
+    for i in (1, 3, 4):
+        assert torch.equal(dS0[i], d_ST[i]), i
+    for i, L in ((0, 640), (2, 320)):
+        ref = oracle.backward(*(t[:, :L] for t in x.tensors()), S0[i:i + 1], d_o[:L].unsqueeze(0), d_ST[i:i + 1])
+        err = err_over_rms(dS0[i:i + 1].numpy(), ref[6])
+        assert err <= TOL_CHUNKED, f"sequence {i}: dS0 {err:.3e}"

@@ -75,3 +75,29 @@ def test_malformed_offsets_are_clamped():
     ro, rS = oracle.forward(*(t[:, :50] for t in x.tensors()), S0[0:1])
     assert err_over_rms(o[:30].float().cpu().numpy(), ro[0, :30]) <= TOL_BF16
     assert err_over_rms(ST[0:1].cpu().numpy(), rS) <= TOL_BF16
+
+
+def test_overlapping_offsets_stay_within_the_workspace():
+    """Offsets [0, 640, 0, 640, 0, 640] over 640 rows: sequences 0, 2 and 4 each
+    claim all 10 chunks, 30 in all, where the workspace holds ceil(640 / 64) + 5 =
+    15.  The chunk offsets are capped there: sequence 0 keeps its 10 chunks (its o
+    rows past the overlap and its S_T match the oracle), sequence 2 gets 5 (its S_T
+    is the state after its first 320 tokens), sequence 4 none (S_T = S0), and the
+    call stays inside its workspace."""
+    H, total = 2, 640
+    x = make_prefill_inputs(1, total, H, 128, 128, dtype=torch.bfloat16, seed=24, s0_std=0.3,
+                            decay_regime="slow")
+    S0 = torch.randn(5, H, 128, 128) * 0.3
+    cu = torch.tensor([0, 640, 0, 640, 0, 640], dtype=torch.int32)
+    toks = [t[0].cuda() for t in x.tensors()]
+    o, ST = gdr2.forward_varlen(*toks, cu.cuda(), S0.cuda())
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    ST = ST.cpu()
+    for i in (1, 3, 4):
+        assert torch.equal(ST[i], S0[i]), i
+    ro, rS = oracle.forward(*x.tensors(), S0[0:1])
+    assert err_over_rms(o[320:].float().cpu().numpy(), ro[0, 320:]) <= TOL_BF16
+    assert err_over_rms(ST[0:1].numpy(), rS) <= TOL_BF16
+    _, rS2 = oracle.forward(*(t[:, :320] for t in x.tensors()), S0[2:3])
+    assert err_over_rms(ST[2:3].numpy(), rS2) <= TOL_BF16
