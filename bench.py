@@ -47,6 +47,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "GDR-2 fwd tokens/sec at H16 d128 T4K (1×B300); % of roofline; decode GB/s"
@@ -398,6 +399,63 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None, chunked=True
                          "kernel": kernels}}
 
 
+def packed_offsets(total, n, seed=12):
+    """cu_seqlens of `n` ragged sequences covering `total` token rows: n - 1 seeded
+    cut points, distinct and uniform over the rows (lengths not multiples of 64)."""
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, total), size=n - 1, replace=False))
+    return torch.tensor(np.concatenate([[0], cuts, [total]]), dtype=torch.int32)
+
+
+def bench_packed(gdr2, hbm_gbs, x, steps=20, warmup=3, nseq=8):
+    """The GDN-2 layer workload's 16,384 token rows as `nseq` packed sequences of
+    seeded ragged lengths (the serving and packed-training layout): CUDA events
+    around gdr2_forward_varlen (bf16 o, per-sequence S_T) and around
+    gdr2_backward_chunked_varlen (seeded fp32 gradient at o)."""
+    B, T, H, dk = x.q.shape
+    dv = x.v.shape[-1]
+    total = B * T
+    toks = [t.reshape(total, H, -1) for t in x.tensors()]
+    cu = packed_offsets(total, nseq).to("cuda")
+    o = torch.empty((total, H, dv), dtype=torch.bfloat16, device="cuda")
+    S_T = torch.empty((nseq, H, dk, dv), dtype=torch.float32, device="cuda")
+    gen = torch.Generator().manual_seed(13)
+    d_o = torch.randn(total, H, dv, generator=gen).to("cuda")
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if gdr2.gdr2_device_status() != 0:
+            raise RuntimeError("device-side failure in the packed-sequence leg")
+        return a.elapsed_time(b) / n
+
+    fwd_ms = timed(lambda: gdr2.forward_varlen(*toks, cu, None, o=o, S_T=S_T), steps)
+    bwd_steps = max(1, min(steps, 5))
+    bwd_ms = timed(lambda: gdr2.backward_chunked_varlen(*toks, cu, None, d_o, None), bwd_steps)
+    fbytes = total * H * ((4 * dk + 2 * dv) * 2 + dv * 2) + nseq * H * dk * dv * 4
+    bbytes = total * H * ((4 * dk + 2 * dv) * 2 + dv * 4 + (4 * dk + 2 * dv) * 4) + nseq * H * dk * dv * 4
+    lengths = (cu[1:] - cu[:-1]).tolist()
+    return {"workload": f"{WORKLOAD} rows as {nseq} packed sequences of lengths {lengths} (H={H}, "
+                        f"d_k=d_v={dk}, bf16 inputs, S0=0)",
+            "forward": {"ms_per_call": fwd_ms, "tokens_per_s": total / (fwd_ms / 1e3), "steps": steps,
+                        "warmup": warmup, "algorithmic_bytes_per_launch": fbytes,
+                        "roofline_frac": fbytes / (fwd_ms / 1e3) / 1e9 / hbm_gbs,
+                        "kernel": "gdr2_forward_varlen: chunk_base_kernel + prep2_kernel + chain_kernel"},
+            "backward_chunked": {"ms_per_call": bwd_ms, "tokens_per_s": total / (bwd_ms / 1e3),
+                                 "steps": bwd_steps, "warmup": warmup, "algorithmic_bytes_per_launch": bbytes,
+                                 "roofline_frac": bbytes / (bwd_ms / 1e3) / 1e9 / hbm_gbs,
+                                 "kernel": "gdr2_backward_chunked_varlen: chunk_base_kernel + prep2_kernel + "
+                                           "chain_kernel + rchain_kernel + cgrad_kernel"}}
+
+
 def bench_sparse(gdr2, hbm_gbs, steps=10, warmup=3):
     """gdr2_sparse_write over the slot-memory workload (B4 H16 T4096, 2048 slots,
     32 selected per token, d_v 128, bf16 inputs and o): CUDA events around
@@ -547,7 +605,9 @@ def main():
     ap.add_argument("--backward-batch", type=int, default=None,
                     help="profiling aid: the backward leg on the first N sequences only")
     ap.add_argument("--no-sparse", action="store_true", help="skip the sparse-write leg")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward", "sparse"], default="all",
+    ap.add_argument("--no-packed", action="store_true", help="skip the packed-sequence leg")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward", "sparse", "packed"],
+                    default="all",
                     help="profiling aid: run just one leg (decode and long print only that leg)")
     ap.add_argument("--decode-steps", type=int, default=1024)
     args = ap.parse_args()
@@ -632,6 +692,11 @@ def main():
         if rank == 0:
             print(json.dumps({"sparse_write": sp}))
         return
+    if args.only == "packed":
+        pk = bench_packed(gdr2, hbm_gbs, x, steps=min(args.steps, 20), warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"packed": pk}))
+        return
 
     with ClockSampler(local) as clk:
         ms, per_launch, launches = bench_prefill(gdr2, x, args.steps, args.warmup, world)
@@ -672,7 +737,7 @@ def main():
 
     if args.only == "prefill":
         args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = args.no_backward = True
-        args.no_sparse = True
+        args.no_sparse = args.no_packed = True
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
@@ -699,6 +764,8 @@ def main():
         out["backward_exact"] = bench_backward(gdr2, hbm_gbs, x, chunked=False)
     if not args.no_sparse:
         out["sparse_write"] = bench_sparse(gdr2, hbm_gbs)
+    if not args.no_packed:
+        out["packed"] = bench_packed(gdr2, hbm_gbs, x)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x_host)
     if rank == 0:

@@ -50,6 +50,8 @@ def lib():
         L.gdr2_forward_segmented.restype = ci
         L.gdr2_forward_varlen.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, vp]
         L.gdr2_forward_varlen.restype = ci
+        L.gdr2_forward_varlen_segmented.argtypes = [vp] * 10 + [i64] * 5 + [ci, ci, i64, vp]
+        L.gdr2_forward_varlen_segmented.restype = ci
         L.gdr2_forward_cached.argtypes = [vp] * 10 + [i64] * 6 + [ci, ci, vp]
         L.gdr2_forward_cached.restype = ci
         L.gdr2_backward.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
@@ -190,11 +192,13 @@ def gdr2_forward_cached(q, k, v, b, w, log_decay, S0=None, *, cache_chunks: int,
 
 
 def gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, o=None, S_T=None,
-                        out_dtype=torch.float32, return_state: bool = True, stream=None):
+                        out_dtype=torch.float32, return_state: bool = True, segments=None, stream=None):
     """Prefill over N packed sequences of different lengths.  q, k, b,
     log_decay: [total_T, H, dk]; v, w: [total_T, H, dv]; cu_seqlens: int32
     [N + 1] on the same device (sequence n owns rows cu_seqlens[n] ..
-    cu_seqlens[n+1] - 1); S0: [N, H, dk, dv] fp32 or None.  Returns
+    cu_seqlens[n+1] - 1); S0: [N, H, dk, dv] fp32 or None.  ``segments`` (None:
+    the library's choice) fixes the segments per sequence of the chunk-parallel
+    scan (gdr2_forward_varlen_segmented).  Returns
     ``(o [total_T, H, dv], S_T [N, H, dk, dv])``."""
     if q.dim() != 3 or v.dim() != 3:
         raise ValueError("q and v must be [total_T, H, d]")
@@ -226,13 +230,15 @@ def gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, o=None
         S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     elif S_T is not None:
         _check_tokens("S_T", S_T, (N, H, dk, dv), torch.float32, dev)
+    entry = "gdr2_forward_varlen" if segments is None else "gdr2_forward_varlen_segmented"
+    extra = () if segments is None else (int(segments),)
     with torch.cuda.device(dev):
-        st = lib().gdr2_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
-                                       _ptr(S0), _ptr(o), _ptr(S_T), _ptr(cu_seqlens), N, total, H,
-                                       dk, dv, _DTYPES[dtype], _DTYPES[o.dtype],
-                                       ctypes.c_void_p(_stream_handle(stream)))
+        st = getattr(lib(), entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay),
+                                   _ptr(S0), _ptr(o), _ptr(S_T), _ptr(cu_seqlens), N, total, H,
+                                   dk, dv, _DTYPES[dtype], _DTYPES[o.dtype], *extra,
+                                   ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
-        raise GDR2Error(st, "gdr2_forward_varlen")
+        raise GDR2Error(st, entry)
     return o, S_T
 
 

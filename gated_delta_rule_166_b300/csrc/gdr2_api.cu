@@ -262,7 +262,48 @@ int forward_impl(const void* q, const void* k, const void* v, const void* b, con
             }
             return GDR2_OK;
         }
-        if (segments > 1 && (cu || padded)) return GDR2_ERR_UNSUPPORTED;
+        if (segments > 1 && padded) return GDR2_ERR_UNSUPPORTED;
+        if (exact && cu && bcache == 0 && segments != 1) {
+            // Packed sequences, few and long: the same segments per sequence (each
+            // sequence's chunks in G runs of ceil(chunks / G)), planned on the device.
+            // The library's choice takes the mean sequence length.
+            const int64_t nch_bound = (total + 63) / 64;
+            int64_t G = segments > 0 ? segments : auto_segments(bh, dv, (nch_bound + N - 1) / std::max<int64_t>(N, 1));
+            G = std::min<int64_t>(G, std::max<int64_t>(nch_bound, 1));
+            if (G > 1) {
+                SegArgs seg;
+                seg.G = static_cast<int>(G);
+                const int64_t chunks = prep_chunk_bound(a);
+                const size_t slot_bytes = round256(static_cast<size_t>(chunks) * static_cast<size_t>(H) * kSlot2Bytes);
+                const size_t nb_state = round256(static_cast<size_t>(N * G * H) * dk * dv * 4);   // also sT
+                const size_t nb_m = round256(static_cast<size_t>(N * G * H) * dk * dk * 4);
+                const size_t nb_o32 = round256(static_cast<size_t>(total * H) * dv * 4);
+                const size_t nb_r = round256(static_cast<size_t>(total * H) * dk * 4);
+                const size_t nb_cb = round256(static_cast<size_t>(N + 1) * 4);
+                const size_t nb_tb = round256(static_cast<size_t>(N * (G - 1) + 1) * 4);
+                void* ws = nullptr;
+                if ((st = ws_alloc(&ws, slot_bytes + 2 * nb_state + nb_m + nb_o32 + nb_r + nb_cb + nb_tb, stream)) !=
+                    GDR2_OK)
+                    return st;
+                uint8_t* p = static_cast<uint8_t*>(ws) + slot_bytes;
+                seg.seg_state = reinterpret_cast<float*>(p);
+                seg.sT = reinterpret_cast<float*>(p + nb_state);
+                seg.seg_m = reinterpret_cast<float*>(p + 2 * nb_state);
+                seg.o32 = reinterpret_cast<float*>(p + 2 * nb_state + nb_m);
+                seg.r = reinterpret_cast<float*>(p + 2 * nb_state + nb_m + nb_o32);
+                int* cbp = reinterpret_cast<int*>(p + 2 * nb_state + nb_m + nb_o32 + nb_r);
+                seg.chunk_base = cbp;
+                seg.tile_base = reinterpret_cast<int*>(p + 2 * nb_state + nb_m + nb_o32 + nb_r + nb_cb);
+                int rc = launch_chunk_base(a.cu, N, total, cbp, stream);
+                if (rc == GDR2_OK) rc = launch_prep2(a, static_cast<uint8_t*>(ws), cbp, chunks, stream, err);
+                if (rc == GDR2_OK) rc = launch_chain(a, static_cast<const uint8_t*>(ws), cbp, stream, err, seg);
+                if (rc == GDR2_OK) rc = launch_seg_plan(a, seg, stream);
+                if (rc == GDR2_OK) rc = launch_scan(a, seg, stream);
+                if (rc == GDR2_OK) rc = launch_correct(a, seg, stream, err);
+                if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
+                return rc;
+            }
+        }
         if (exact && !cu && bcache == 0 && segments != 1) {
             // Few long fixed-length sequences: segments of the chunk-parallel scan (prep2
             // over every chunk, the chain kernel over segments with value and transfer
@@ -340,6 +381,17 @@ extern "C" int gdr2_forward_varlen(const void* q, const void* k, const void* v,
     if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
     return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, cu_seqlens, N, 0, total_T, H, dk, dv,
                         in_dtype, out_dtype, stream);
+}
+
+extern "C" int gdr2_forward_varlen_segmented(const void* q, const void* k, const void* v,
+                                             const void* b, const void* w, const void* log_decay,
+                                             const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
+                                             int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                             int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream) {
+    if (N > 0 && !cu_seqlens) return GDR2_ERR_ARG;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
+    return forward_impl(q, k, v, b, w, log_decay, S0, o, S_T, cu_seqlens, N, 0, total_T, H, dk, dv,
+                        in_dtype, out_dtype, stream, /*noalloc=*/false, segments);
 }
 
 extern "C" int gdr2_forward_noalloc(const void* q, const void* k, const void* v,

@@ -94,8 +94,9 @@ struct ChainParams {
     int T, H, dk, dv, nch, total;   // dk, dv <= 128 / 64 per tile; channels past them are zero padding
     int out_bf16;
     long long wait_cycles;   // limit of each handshake wait (copy drains keep the default)
-    // Segments (fixed-length sequences, G > 1): blockIdx.x = (sequence * G + g) * H + head
-    // runs chunks g L .. g L + L - 1.  Value tiles of segment 0 start from S0 and write o;
+    // Segments (G > 1): blockIdx.x = (sequence * G + g) * H + head runs chunks g L ..
+    // g L + L - 1 (packed sequences: L = ceil(chunks / G) per sequence, o32 and r by
+    // global row, Tr unused).  Value tiles of segment 0 start from S0 and write o;
     // those of later segments start from zero and write fp32 rows to o32.  Transfer tiles
     // (blockIdx.y >= the value tiles, segments g >= 1) start from identity columns j0 ..
     // of d_k with U = 0: their O rows are r_t = M_t^T q_t (M_t the map from the segment
@@ -136,30 +137,31 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& tm_o, const CUtenso
     const int warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
     // this sequence's token rows and its first global chunk (offsets clamped as in prep2)
-    int T, tok0;
+    int T, tok0, Lc = prm.L;   // Lc: chunks per segment of this sequence
     int64_t chunk0;
     if (prm.cu) {
-        const int a = min(max(prm.cu[seq], 0), prm.total);
-        const int e = min(max(prm.cu[seq + 1], a), prm.total);
-        tok0 = a;
-        chunk0 = prm.chunk_base[seq];
         // only the chunks this sequence was given slots for (fewer than its length only
-        // for overlapping malformed offsets, see chunk_base_kernel)
-        T = static_cast<int>(min(static_cast<int64_t>(e - a),
-                                     static_cast<int64_t>(prm.chunk_base[seq + 1] - prm.chunk_base[seq]) * kC));
+        // for overlapping malformed offsets, see chunk_base_kernel); with segments,
+        // segment g's run of them
+        const PackedSegment ps = packed_segment(prm.cu, prm.chunk_base, prm.total, seq, prm.G, g);
+        if (prm.G > 1) Lc = ps.Lc;
+        tok0 = ps.a + ps.cs * kC;
+        T = max(ps.Ts - ps.cs * kC, 0);
+        chunk0 = prm.chunk_base[seq] + ps.cs;
     } else {
         // chunks c0 + g L .. of the sequence: tokens counted from the first of them
         T = prm.T - (prm.c0 + g * prm.L) * kC;
         tok0 = seq * prm.T + (prm.c0 + g * prm.L) * kC;
         chunk0 = static_cast<int64_t>(seq) * prm.nch + static_cast<int64_t>(g) * prm.L;
     }
-    const int n = min((T + kC - 1) / kC, prm.L);
+    const int n = min((T + kC - 1) / kC, Lc);
     // o rows: the caller's o (one pass, or segment 0), else fp32 scratch rows
     const bool to_o = prm.G == 1 || (!kTransfer && g == 0);
     const CUtensorMap* const om = to_o ? &tm_o : (kTransfer ? &tm_r : &tm_o32);
     const bool obf16 = to_o && prm.out_bf16;
     const int ow = kTransfer ? kPrepDK : prm.dv;   // width of an output row
-    const int orow0 = to_o ? tok0 : seq * prm.Tr + (g - 1) * prm.L * kC;
+    // o32 and r rows: per sequence after its first segment, or (packed) the global row
+    const int orow0 = to_o || prm.cu ? tok0 : seq * prm.Tr + (g - 1) * prm.L * kC;
     void* const obase = to_o ? prm.o : (kTransfer ? static_cast<void*>(prm.r) : static_cast<void*>(prm.o32));
     auto slot_of = [&](int c) {
         return prm.slots + ((chunk0 + c) * prm.H + h) * static_cast<int64_t>(kSlot2Bytes);
@@ -628,15 +630,17 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
     const int64_t nch = cpiece > 0 ? cpiece : (a.T + kC - 1) / kC;   // chunks per sequence in this launch
     if ((segmented || a.cu) && (c0 != 0 || cpiece > 0)) return GDR2_ERR_ARG;
     if (a.cu && a.S_cache && a.cache_chunks != 1) return GDR2_ERR_ARG;   // packed: every chunk's state
-    if (segmented && (a.cu || a.dk != kPrepDK || seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L >= nch ||
-                      !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r))
+    if (segmented && (a.dk != kPrepDK || !seg.seg_state || !seg.seg_m || !seg.o32 || !seg.r ||
+                      (!a.cu && (seg.L < 1 || static_cast<int64_t>(seg.G - 1) * seg.L >= nch)) ||
+                      (a.cu && a.S_cache)))
         return GDR2_ERR_ARG;
     const int64_t total = a.cu ? a.total : a.B * a.T;
     CUtensorMap mo, mo32, mr;
     if (!make_row_map(&mo, a.o, total, a.H, a.dv, a.out_dtype != GDR2_BF16)) return GDR2_ERR_CUDA;
     if (segmented) {
-        if (!make_row_map(&mo32, seg.o32, a.B * seg.Tr, a.H, a.dv, true) ||
-            !make_row_map(&mr, seg.r, a.B * seg.Tr, a.H, kPrepDK, true))
+        const int64_t srows = a.cu ? total : a.B * seg.Tr;   // rows of o32 and r
+        if (!make_row_map(&mo32, seg.o32, srows, a.H, a.dv, true) ||
+            !make_row_map(&mr, seg.r, srows, a.H, kPrepDK, true))
             return GDR2_ERR_CUDA;
     } else {
         mo32 = mo;   // not read
@@ -655,7 +659,7 @@ int launch_chain(const ForwardArgs& a, const uint8_t* slots, const int* chunk_ba
                     static_cast<int>(total),
                     a.out_dtype == GDR2_BF16 ? 1 : 0, 0,
                     segmented ? seg.G : 1,
-                    segmented ? seg.L : (a.cu ? 0x7fffffff : static_cast<int>(nch)),
+                    segmented && !a.cu ? seg.L : (a.cu ? 0x7fffffff : static_cast<int>(nch)),
                     segmented ? static_cast<int>(seg.Tr) : 0,
                     seg.seg_state, seg.seg_m, seg.o32, seg.r, c0, a.S_cache,
                     a.S_cache ? static_cast<int>(a.cache_chunks) : 1,

@@ -16,6 +16,27 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(x);
 }
 
+// Packed sequence `seq` of a call with token offsets cu and chunk offsets cb (the
+// first global chunk of each sequence, capped at the workspace's chunk bound): its
+// rows a .. a + Ts - 1 are the ones its `given` = cb[seq + 1] - cb[seq] chunks cover
+// (offsets clamped into [0, total], the end to at least the start).  With G segments
+// each holds Lc = ceil(given / G) chunks and segment g starts at chunk cs (segments
+// past the last chunk are empty).
+struct PackedSegment {
+    int a, Ts, given, Lc, cs;
+};
+__device__ __forceinline__ PackedSegment packed_segment(const int* cu, const int* cb, int total, int seq, int G,
+                                                        int g) {
+    PackedSegment p;
+    p.a = min(max(cu[seq], 0), total);
+    const int e = min(max(cu[seq + 1], p.a), total);
+    p.given = cb[seq + 1] - cb[seq];
+    p.Ts = static_cast<int>(min(static_cast<long long>(e - p.a), static_cast<long long>(p.given) * 64));
+    p.Lc = G > 1 ? (p.given + G - 1) / G : p.given;
+    p.cs = G > 1 ? min(g * p.Lc, p.given) : 0;
+    return p;
+}
+
 // Device-side failure codes written to the library's error word.
 enum : int { kDevOk = 0, kDevTimeout = 1 };
 
@@ -122,8 +143,12 @@ bool two_kernel_supports(const ForwardArgs& a);
 // chains the segments' affine maps S -> M S + N and launch_correct adds each later
 // segment's start-state term S_start^T r_t to its o rows.  G = 1: no segments.
 struct SegArgs {
-    int G = 1, L = 0;
-    int64_t Tr = 0;              // T - L * 64: rows per sequence of o32 and r
+    int G = 1, L = 0;            // packed sequences: L unused (ceil(chunks / G) per sequence)
+    int64_t Tr = 0;              // T - L * 64: rows per sequence of o32 and r (packed: o32 and r
+                                 // hold every global row, Tr unused)
+    const int* chunk_base = nullptr;   // packed: first global chunk of each sequence
+    int* tile_base = nullptr;    // packed: [N (G - 1) + 1] first correction tile of each
+                                 // (sequence, segment g >= 1), then the total
     float* seg_state = nullptr;  // [B][H][G][d_k][dv] value tiles' end states
     float* seg_m = nullptr;      // [B][H][G][d_k][d_k] transfer tiles' end states (g >= 1)
     float* o32 = nullptr;        // [B * Tr][H][dv] o of segments g >= 1 from a zero start
@@ -134,6 +159,8 @@ struct SegArgs {
 // segments g >= 1 = o32 + S_start^T r in the output dtype.
 int launch_scan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream);
 int launch_correct(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream, int* err);
+// packed sequences: the correction tiles of each (sequence, segment) into seg.tile_base
+int launch_seg_plan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream);
 // Fixed-length calls may prepare chunks [c0, c0 + cpiece) of every sequence only
 // (cpiece > 0; `chunks` = N * cpiece, slots numbered from 0 per sequence).
 // wy (non-null): also the backward record of every item, [chunks * H][kWyBytes].

@@ -161,11 +161,61 @@ constexpr uint32_t kCBar = 98304;    // mbarriers: operands, MMA done, o32 tile
 constexpr uint32_t kCSlot = kCBar + 32;
 constexpr uint32_t kCSmem = kCBar + 64 + 1024;
 
-template <bool kBf16Out>
+// Packed sequences: the 128-row correction tiles of segment g of sequence s start at
+// tile_base[s (G - 1) + g - 1] (segments g >= 1; each segment's rows tiled from its
+// first row, so that no tile straddles two segments), the total at tile_base[N (G - 1)].
+// One CTA.
+__global__ void seg_plan_kernel(const int* cu, const int* cb, int N, int G, int total, int* tile_base) {
+    __shared__ int part[1024];
+    const int tid = threadIdx.x;
+    const int per = (N + blockDim.x - 1) / blockDim.x;
+    const int s0 = tid * per, s1 = min(N, s0 + per);
+    auto tiles = [&](int s, int g) {
+        const PackedSegment ps = packed_segment(cu, cb, total, s, G, g);
+        const int r0 = ps.cs * kPrepC, r1 = min(min(ps.cs + ps.Lc, ps.given) * kPrepC, ps.Ts);
+        return r1 > r0 ? (r1 - r0 + kCorrRows - 1) / kCorrRows : 0;
+    };
+    int sum = 0;
+    for (int s = s0; s < s1; ++s)
+        for (int g = 1; g < G; ++g) sum += tiles(s, g);
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {   // exclusive scan of the partial sums
+        int run = 0;
+        for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
+            const int x = part[i];
+            part[i] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    int run = part[tid];
+    for (int s = s0; s < s1; ++s)
+        for (int g = 1; g < G; ++g) {
+            tile_base[s * (G - 1) + g - 1] = run;
+            run += tiles(s, g);
+        }
+    if (s1 == N && s0 < s1) tile_base[N * (G - 1)] = run;
+    if (N == 0 && tid == 0) tile_base[0] = 0;
+}
+
+// kPacked: packed sequences.  blockIdx.x / (dv / 64) numbers the tiles of all
+// (sequence, segment g >= 1) in turn (tile_base, from seg_plan_kernel; the grid is an
+// upper bound and later CTAs exit), r and o32 are indexed by global row (one-sequence
+// 4-D maps over all rows), and each thread stores its row of o itself, rows past the
+// segment's end left alone.
+struct PackedCorr {
+    const int* cu;
+    const int* cb;
+    const int* tile_base;
+    int N, total;
+};
+
+template <bool kBf16Out, bool kPacked>
 __global__ void __launch_bounds__(kCorrThreads)
 correct_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_st,
                const __grid_constant__ CUtensorMap tm_o32, const __grid_constant__ CUtensorMap tm_o, int G, int L,
-               int H, int dv, int* err) {
+               int H, int dv, int* err, const PackedCorr pk, void* o) {
     extern __shared__ uint8_t csm_raw[];
     using namespace tc;
     const uint32_t base = (smem_u32(csm_raw) + 1023u) & ~1023u;
@@ -174,9 +224,29 @@ correct_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__
     volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sgen + kCSlot);
     const int nh = dv / 64;
     const int tile = blockIdx.x / nh, j0 = (blockIdx.x % nh) * 64;
-    const int h = blockIdx.y, seq = blockIdx.z;
-    const int t0 = tile * kCorrRows;                  // row within the sequence's later-segment rows
-    const int g = 1 + t0 / (L * kPrepC);
+    const int h = blockIdx.y;
+    int seq, g, t0, nrows;   // t0: the tile's first row (within the sequence's later-segment rows;
+                             // packed: global); nrows: rows of the tile inside the segment
+    if constexpr (kPacked) {
+        const int nsg = pk.N * (G - 1);
+        if (tile >= pk.tile_base[nsg]) return;   // past the last tile (the grid is a bound)
+        int lo = 0, hi = nsg;                    // the last (sequence, segment) starting at or before it
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pk.tile_base[mid] <= tile) lo = mid; else hi = mid;
+        }
+        seq = lo / (G - 1);
+        g = 1 + lo % (G - 1);
+        const PackedSegment ps = packed_segment(pk.cu, pk.cb, pk.total, seq, G, g);
+        const int r0 = ps.cs * kPrepC, r1 = min(min(ps.cs + ps.Lc, ps.given) * kPrepC, ps.Ts);
+        t0 = ps.a + r0 + (tile - pk.tile_base[lo]) * kCorrRows;
+        nrows = min(kCorrRows, ps.a + r1 - t0);
+    } else {
+        seq = blockIdx.z;
+        t0 = tile * kCorrRows;
+        g = 1 + t0 / (L * kPrepC);
+        nrows = kCorrRows;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         mbar_init(bar_ab, 1);
@@ -193,8 +263,9 @@ correct_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__
     if (tid == 0) {
         mbar_expect_tx(bar_ab, 4u * 16384u + 4u * 8192u);
         const int srow = ((seq * H + h) * G + g) * dv + j0;   // S_start(g)^T rows j0 .. j0 + 63
+        const int mseq = kPacked ? 0 : seq;   // packed: one map over every row
         for (int kb = 0; kb < 4; ++kb) {
-            tma_load_4d(base + kCA + kb * 16384u, &tm_r, 32 * kb, h, t0, seq, bar_ab);
+            tma_load_4d(base + kCA + kb * 16384u, &tm_r, 32 * kb, h, t0, mseq, bar_ab);
             tma_load_2d(base + kCB + kb * 8192u, &tm_st, 32 * kb, srow, bar_ab);
         }
         ok = mbar_wait(bar_ab, 0);
@@ -209,8 +280,8 @@ correct_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__
             ok = mbar_wait(bar_mma, 0);
             if (ok) {
                 mbar_expect_tx(bar_o, 2u * 16384u);
-                tma_load_4d(base + kCA, &tm_o32, j0, h, t0, seq, bar_o);
-                tma_load_4d(base + kCA + 16384u, &tm_o32, j0 + 32, h, t0, seq, bar_o);
+                tma_load_4d(base + kCA, &tm_o32, j0, h, t0, mseq, bar_o);
+                tma_load_4d(base + kCA + 16384u, &tm_o32, j0 + 32, h, t0, mseq, bar_o);
             }
         }
         if (!ok) {
@@ -242,7 +313,28 @@ correct_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__
                 y[4 * q + 2] = x.z + __uint_as_float(acc[4 * q + 2]);
                 y[4 * q + 3] = x.w + __uint_as_float(acc[4 * q + 3]);
             }
-            if constexpr (!kBf16Out) {
+            if constexpr (kPacked) {
+                // this thread's row of o, columns j0 + 16 c16 .. + 15, if inside the segment
+                if (row < nrows) {
+                    const int64_t off = (static_cast<int64_t>(t0 + row) * H + h) * dv + j0 + 16 * c16;
+                    if constexpr (kBf16Out) {
+                        uint4 pk4[2];
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk4);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+                            pw[e] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+                        uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + off);
+                        op[0] = pk4[0];
+                        op[1] = pk4[1];
+                    } else {
+                        float4* op = reinterpret_cast<float4*>(static_cast<float*>(o) + off);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) op[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+                    }
+                }
+            } else if constexpr (!kBf16Out) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t a = rb + ((((4 * (c16 & 1) + q) ^ (row & 7)) & 7) << 4);
@@ -269,7 +361,7 @@ correct_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok) {
+    if (!kPacked && tid == 0 && ok) {
         const int orow = L * kPrepC + t0;   // row of o within the sequence
         if constexpr (kBf16Out) {
             tma_store_4d(&tm_o, base + kCA + 32768u, j0, h, orow, seq);
@@ -296,34 +388,59 @@ int launch_scan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream) {
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 
+int launch_seg_plan(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream) {
+    if (!a.cu || seg.G < 2 || !seg.chunk_base || !seg.tile_base) return GDR2_ERR_ARG;
+    seg_plan_kernel<<<1, 1024, 0, stream>>>(a.cu, seg.chunk_base, static_cast<int>(a.B), seg.G,
+                                            static_cast<int>(a.total), seg.tile_base);
+    return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+
 int launch_correct(const ForwardArgs& a, const SegArgs& seg, cudaStream_t stream, int* err) {
-    if (seg.G < 2 || seg.Tr <= 0 || (seg.L & 1) || !seg.sT) return GDR2_ERR_ARG;
+    const bool packed = a.cu != nullptr;
+    if (seg.G < 2 || !seg.sT || (packed ? !seg.chunk_base || !seg.tile_base : seg.Tr <= 0 || (seg.L & 1)))
+        return GDR2_ERR_ARG;
     if (a.B > 65535 || a.H > 65535) return GDR2_ERR_SHAPE;   // grid z and y
     const bool bf = a.out_dtype == GDR2_BF16;
     CUtensorMap mr, mst, mo32, mo;
-    if (!make_seq_map(&mr, seg.r, a.B, seg.Tr, a.H, kDK, true, 32) ||
-        !make_seq_map(&mo32, seg.o32, a.B, seg.Tr, a.H, a.dv, true, 32) ||
-        !make_seq_map(&mo, a.o, a.B, a.T, a.H, a.dv, !bf, bf ? 64 : 32) ||
-        !make_rows_map(&mst, seg.sT, a.B * a.H * seg.G * a.dv))
+    if (packed) {   // one map over every row; o is stored row by row
+        if (!make_seq_map(&mr, seg.r, 1, a.total, a.H, kDK, true, 32) ||
+            !make_seq_map(&mo32, seg.o32, 1, a.total, a.H, a.dv, true, 32) ||
+            !make_rows_map(&mst, seg.sT, a.B * a.H * seg.G * a.dv))
+            return GDR2_ERR_CUDA;
+        mo = mo32;   // not read
+    } else if (!make_seq_map(&mr, seg.r, a.B, seg.Tr, a.H, kDK, true, 32) ||
+               !make_seq_map(&mo32, seg.o32, a.B, seg.Tr, a.H, a.dv, true, 32) ||
+               !make_seq_map(&mo, a.o, a.B, a.T, a.H, a.dv, !bf, bf ? 64 : 32) ||
+               !make_rows_map(&mst, seg.sT, a.B * a.H * seg.G * a.dv)) {
         return GDR2_ERR_CUDA;
+    }
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(correct_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kCSmem));
-        if (attr == cudaSuccess)
-            attr = cudaFuncSetAttribute(correct_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kCSmem));
+        const void* kernels[4] = {reinterpret_cast<const void*>(correct_kernel<false, false>),
+                                  reinterpret_cast<const void*>(correct_kernel<true, false>),
+                                  reinterpret_cast<const void*>(correct_kernel<false, true>),
+                                  reinterpret_cast<const void*>(correct_kernel<true, true>)};
+        for (const void* k : kernels)
+            if (attr == cudaSuccess)
+                attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kCSmem));
     });
     if (attr != cudaSuccess) return GDR2_ERR_CUDA;
-    const dim3 grid(static_cast<unsigned>((seg.Tr + kCorrRows - 1) / kCorrRows * (a.dv / 64)),
-                    static_cast<unsigned>(a.H), static_cast<unsigned>(a.B));
-    if (bf)
-        correct_kernel<true><<<grid, kCorrThreads, kCSmem, stream>>>(mr, mst, mo32, mo, seg.G, seg.L,
-                                                                     static_cast<int>(a.H), static_cast<int>(a.dv), err);
-    else
-        correct_kernel<false><<<grid, kCorrThreads, kCSmem, stream>>>(mr, mst, mo32, mo, seg.G, seg.L,
-                                                                      static_cast<int>(a.H), static_cast<int>(a.dv), err);
+    const PackedCorr pk{a.cu, seg.chunk_base, seg.tile_base, static_cast<int>(a.B), static_cast<int>(a.total)};
+    const int nh = static_cast<int>(a.dv / 64);
+    // packed: at most total / 128 + N (G - 1) tiles (each segment adds at most one partial tile)
+    const int64_t tiles = packed ? a.total / kCorrRows + a.B * (seg.G - 1) + 1 : (seg.Tr + kCorrRows - 1) / kCorrRows;
+    if (tiles * nh >= (1ll << 31)) return GDR2_ERR_SHAPE;
+    const dim3 grid(static_cast<unsigned>(tiles * nh), static_cast<unsigned>(a.H),
+                    static_cast<unsigned>(packed ? 1 : a.B));
+    const int G = seg.G, L = seg.L, H = static_cast<int>(a.H), dv = static_cast<int>(a.dv);
+    if (packed) {
+        if (bf) correct_kernel<true, true><<<grid, kCorrThreads, kCSmem, stream>>>(mr, mst, mo32, mo, G, L, H, dv, err, pk, a.o);
+        else correct_kernel<false, true><<<grid, kCorrThreads, kCSmem, stream>>>(mr, mst, mo32, mo, G, L, H, dv, err, pk, a.o);
+    } else {
+        if (bf) correct_kernel<true, false><<<grid, kCorrThreads, kCSmem, stream>>>(mr, mst, mo32, mo, G, L, H, dv, err, pk, a.o);
+        else correct_kernel<false, false><<<grid, kCorrThreads, kCSmem, stream>>>(mr, mst, mo32, mo, G, L, H, dv, err, pk, a.o);
+    }
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 

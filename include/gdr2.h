@@ -210,6 +210,29 @@ int gdr2_forward_segmented(const void* q, const void* k, const void* v,
                            int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream);
 
 /*
+ * gdr2_forward_varlen_segmented -- gdr2_forward_varlen with an explicit number of
+ * segments per sequence for the chunk-parallel scan (see gdr2_forward_segmented).
+ * Sequence n's chunks are split into G runs of ceil(chunks_n / G) (runs past its
+ * last chunk are empty), the plan made on the device from cu_seqlens; the state
+ * pass runs every (sequence, segment) at once, then a scan over each sequence's
+ * segments and a tensor-core correction of the later segments' rows.  The
+ * results are those of the one-pass call within the bf16 bar.
+ *   segments : 0 = the library's choice (as gdr2_forward_varlen, which takes
+ *              segments only when few long sequences would leave SMs idle);
+ *              n >= 1 = n segments per sequence (1 = the sequential state pass)
+ * Workspace (the library's pool): the one-pass slots plus, per (sequence,
+ * segment, head), a state and a map (fp32), and fp32 partial outputs and r rows
+ * for every token row: total_T*H*(dk + dv)*4 bytes.  GDR2_ERR_ARG for segments
+ * < 0; GDR2_ERR_UNSUPPORTED for segments > 1 with fp32 inputs or head sizes
+ * other than dk = 128, dv in {64, 128}.
+ */
+int gdr2_forward_varlen_segmented(const void* q, const void* k, const void* v,
+                                  const void* b, const void* w, const void* log_decay,
+                                  const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
+                                  int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                  int in_dtype, int out_dtype, int64_t segments, cudaStream_t stream);
+
+/*
  * gdr2_forward_cached -- gdr2_forward that also keeps the state at segment ends.
  *
  * The "Memory Caching (MC)" page ("caching the memory" section) splits a

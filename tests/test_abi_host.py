@@ -140,6 +140,16 @@ def test_varlen_rejects_bad_args():
     assert L.gdr2_forward_varlen(*varlen_args(total=1 << 31)) == SHAPE
 
 
+def test_varlen_segmented_rejects_bad_args():
+    L = _lib.lib()
+    seg = lambda n, **kw: L.gdr2_forward_varlen_segmented(*(varlen_args(**kw)[:-1] + [n, None]))  # noqa: E731
+    assert seg(-1) == ARG
+    assert seg(2, cu=None) == ARG
+    assert seg(2, dk=48) == SHAPE
+    assert seg(2, total=1 << 31) == SHAPE
+    assert seg(2, o=ctypes.c_void_p(BASE + 9 * GAP)) == ALIAS   # o over cu
+
+
 def test_segmented_rejects_bad_args():
     L = _lib.lib()
 

@@ -44,3 +44,16 @@ def test_traffic_records_name_existing_sources_and_captures():
         assert r["dram_bytes_per_launch"] > 0, key
         if "per_kernel" in r:
             assert sum(r["per_kernel"].values()) == r["dram_bytes_per_launch"], key
+
+
+def test_packed_offsets_partition_the_rows():
+    """The packed-sequence leg's offsets: seeded, n strictly increasing ranges that
+    cover every row once, lengths not all multiples of the 64-token chunk."""
+    b = load_bench()
+    cu = b.packed_offsets(16384, 8)
+    assert cu.dtype.is_floating_point is False and cu.numel() == 9
+    assert int(cu[0]) == 0 and int(cu[-1]) == 16384
+    lengths = (cu[1:] - cu[:-1]).tolist()
+    assert all(L > 0 for L in lengths) and sum(lengths) == 16384
+    assert any(L % 64 for L in lengths)
+    assert b.packed_offsets(16384, 8).tolist() == cu.tolist()
