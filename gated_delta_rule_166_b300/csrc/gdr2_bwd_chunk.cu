@@ -420,7 +420,51 @@ struct Params {
     const int* cu;
     const int* chunk_base;
     int N, total;
+    // items in the grid, and the item distance to the one that runs on this SM next
+    // (the resident CTAs: one per SM); 0 turns the L2 prefetch of that item off
+    int items, pf_stride;
 };
+
+// Item `it` = (global chunk gc, head h): its sequence, chunk within the sequence,
+// token rows inside the sequence and first token row; false past the last chunk.
+struct CgItem {
+    int h, seq, c, nvalid;
+    int64_t row0;
+};
+__device__ __forceinline__ bool cg_locate(const Params& prm, int it, CgItem& x) {
+    const int gc = it / prm.H;
+    x.h = it - gc * prm.H;
+    if (prm.cu) {
+        // packed sequences: the last sequence whose first global chunk is at or before gc
+        // (offsets clamped as in the forward kernels)
+        const int* cbs = prm.chunk_base;
+        if (gc >= cbs[prm.N]) return false;
+        int lo = 0, hi = prm.N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cbs[mid] <= gc) lo = mid; else hi = mid;
+        }
+        x.seq = lo;
+        x.c = gc - cbs[lo];
+        const int a = min(max(prm.cu[lo], 0), prm.total);
+        const int e = min(max(prm.cu[lo + 1], a), prm.total);
+        x.nvalid = min(e - a - x.c * kC, kC);
+        x.row0 = static_cast<int64_t>(a) + static_cast<int64_t>(x.c) * kC;
+    } else {
+        x.seq = gc / prm.nch;
+        x.c = gc - x.seq * prm.nch;
+        x.nvalid = min(prm.T - x.c * kC, kC);
+        x.row0 = static_cast<int64_t>(x.seq) * prm.T + static_cast<int64_t>(x.c) * kC;
+    }
+    return true;
+}
+// The item's start state (null: zero), as the load phase reads it.
+__device__ __forceinline__ const float* cg_start_state(const Params& prm, int it, const CgItem& x) {
+    const int64_t bh = static_cast<int64_t>(x.seq) * prm.H + x.h;
+    return x.c == 0  ? (prm.S0 ? prm.S0 + bh * 16384 : nullptr)
+           : prm.cu ? prm.Sc + (static_cast<int64_t>(it) - prm.H) * 16384   // global chunk gc - 1
+                    : prm.Sc + (bh * prm.n_cache + (x.c - 1)) * 16384;
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -485,31 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
     const int a = 32 * quarter + lane;   // M = 128 accumulator row (key channel or d_v column)
 
     const int it = static_cast<int>(blockIdx.x);
-    const int gc = it / prm.H, h = it - gc * prm.H;   // global chunk, head
-    int seq, c, nvalid;
-    int64_t row0;   // first token row of the chunk
-    if (prm.cu) {
-        // packed sequences: the last sequence whose first global chunk is at or before gc
-        // (offsets clamped as in the forward kernels); items past the last chunk exit
-        const int* cbs = prm.chunk_base;
-        if (gc >= cbs[prm.N]) return;
-        int lo = 0, hi = prm.N;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cbs[mid] <= gc) lo = mid; else hi = mid;
-        }
-        seq = lo;
-        c = gc - cbs[lo];
-        const int a = min(max(prm.cu[seq], 0), prm.total);
-        const int e = min(max(prm.cu[seq + 1], a), prm.total);
-        nvalid = min(e - a - c * kC, kC);
-        row0 = static_cast<int64_t>(a) + static_cast<int64_t>(c) * kC;
-    } else {
-        seq = gc / prm.nch;
-        c = gc - seq * prm.nch;
-        nvalid = min(prm.T - c * kC, kC);
-        row0 = static_cast<int64_t>(seq) * prm.T + static_cast<int64_t>(c) * kC;
-    }
+    CgItem item;
+    if (!cg_locate(prm, it, item)) return;   // packed: past the last chunk (the grid is a bound)
+    const int h = item.h, seq = item.seq, c = item.c, nvalid = item.nvalid;
+    const int64_t row0 = item.row0;   // first token row of the chunk
     const int bh = seq * prm.H + h;
     auto gidx = [&](int r, int ch) { return ((row0 + r) * prm.H + h) * 128 + ch; };
 
@@ -542,9 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 
     // ---- S, dS' -> fp16 images [d_k][d_v]; rowsum(dS' * S) ----------------------------------
     {
-        const float* Sp = c == 0  ? (prm.S0 ? prm.S0 + static_cast<int64_t>(bh) * 16384 : nullptr)
-                          : prm.cu ? prm.Sc + (static_cast<int64_t>(it) - prm.H) * 16384   // global chunk gc - 1
-                                   : prm.Sc + (static_cast<int64_t>(bh) * prm.n_cache + (c - 1)) * 16384;
+        const float* Sp = cg_start_state(prm, it, item);
         const float* dSp = prm.dsn + static_cast<int64_t>(it) * 16384;   // global chunk gc, head h
         const int r = tid >> 2, e0 = 32 * (tid & 3);
         float part = 0.f;
@@ -600,6 +621,22 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
         put16_pair(sgen + kU, sgen + kUL, 8192u, static_cast<uint32_t>(r), static_cast<uint32_t>(e), uv);
     }
     operands_done();
+
+    // The item the next CTA on this SM will take is not in flight yet: one thread asks L2
+    // for its three contiguous inputs (backward record, start state, end-state gradient:
+    // 176 of its 320 KB) now, while this item's products and epilogues leave DRAM idle, so
+    // that its load phase finds them in L2 instead of every SM loading from DRAM at once.
+    // (The token rows, 64 strided 256- and 512-byte pieces each, are left to the load
+    // phase: prefetching them too, as bulk or as line prefetches, measured slower.)
+    if (tid == 32 && prm.pf_stride > 0 && it + prm.pf_stride < prm.items) {
+        const int nit = it + prm.pf_stride;
+        CgItem nx;
+        if (cg_locate(prm, nit, nx)) {
+            bulk_prefetch_l2(prm.wy + static_cast<int64_t>(nit) * kWyBytes, kWyBytes);
+            if (const float* ns = cg_start_state(prm, nit, nx)) bulk_prefetch_l2(ns, 65536u);
+            bulk_prefetch_l2(prm.dsn + static_cast<int64_t>(nit) * 16384, 65536u);
+        }
+    }
 
     // ---- 1. E^T = u^T T^T - S^T W^T  [d_v][token] ---------------------------------------------
     if (tid == 0) {
@@ -985,6 +1022,16 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 }  // namespace
 
 namespace {
+// The item distance between this CTA and the one that follows it on the same SM: one
+// CTA per SM is resident, so the SM count (0 if it cannot be read: no prefetch).
+int cgrad_prefetch_stride() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                    cudaSuccess)
+        return 0;
+    return sms > 0 ? sms : 0;
+}
+
 // Chunks of the call (packed sequences: an upper bound, every sequence adding at most
 // one partial chunk) and the workspace regions, in order: forward slots, backward
 // records, start states (the chain's cached states), end-state gradients, the
@@ -1070,7 +1117,8 @@ int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream
                    static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
                    a.d_q, a.d_k, a.d_b, a.d_g, a.d_v, a.d_w,
                    static_cast<int>(a.T), static_cast<int>(a.H), static_cast<int>(nch), static_cast<int>(n_cache), err,
-                   a.cu, cb, static_cast<int>(a.B), static_cast<int>(packed ? a.total : 0)};
+                   a.cu, cb, static_cast<int>(a.B), static_cast<int>(packed ? a.total : 0),
+                   static_cast<int>(items), cgrad_prefetch_stride()};
     cgr::cgrad_kernel<<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
