@@ -254,7 +254,7 @@ def gdr2_backward(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bo
 def gdr2_backward_chunked(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bool = True,
                           stream=None):
     """gdr2_backward through the chunkwise WY form on tensor cores: bf16 inputs
-    with dk = dv = 128, the same arguments and outputs."""
+    (dk, dv in {32, 64, 128}), the same arguments and outputs."""
     return _backward("gdr2_backward_chunked", q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream)
 
 
@@ -304,7 +304,7 @@ def gdr2_backward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T=No
 def gdr2_backward_chunked_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T=None, *,
                                  want_dS0: bool = True, stream=None):
     """gdr2_backward_varlen through the chunkwise WY form on tensor cores: bf16
-    inputs with dk = dv = 128, the same arguments and outputs."""
+    inputs (dk, dv in {32, 64, 128}), the same arguments and outputs."""
     return _backward_varlen("gdr2_backward_chunked_varlen", q, k, v, b, w, log_decay, cu_seqlens, S0, d_o,
                             d_S_T, want_dS0, stream)
 
@@ -348,7 +348,7 @@ class GatedDeltaRule2(torch.autograd.Function):
     """(o, S_T) = gdr2_forward(q, k, v, b, w, log_decay, S0) as a differentiable
     operation: the forward pass is gdr2_forward (fp32 o), the backward pass
     gdr2_backward, or gdr2_backward_chunked when ``chunked`` is set and the inputs
-    are bf16 with dk = dv = 128.  Gradients are fp32 and cast to each input's
+    are bf16.  Gradients are fp32 and cast to each input's
     dtype."""
 
     @staticmethod
@@ -356,7 +356,7 @@ class GatedDeltaRule2(torch.autograd.Function):
         o, S_T = gdr2_forward(q, k, v, b, w, log_decay, S0)
         ctx.save_for_backward(q, k, v, b, w, log_decay, S0)
         ctx.has_s0 = S0 is not None
-        ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16 and q.shape[-1] == 128 and v.shape[-1] == 128
+        ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16
         return o, S_T
 
     @staticmethod
@@ -373,8 +373,8 @@ class GatedDeltaRule2(torch.autograd.Function):
 
 def gdr2_apply(q, k, v, b, w, log_decay, S0=None, *, chunked_backward: bool = False):
     """Differentiable prefill: ``(o, S_T)`` with gradients through gdr2_backward
-    (exact fp32), or through gdr2_backward_chunked (tensor cores; bf16 inputs with
-    dk = dv = 128, else the exact path) when ``chunked_backward`` is set."""
+    (exact fp32), or through gdr2_backward_chunked (tensor cores; bf16 inputs, else
+    the exact path) when ``chunked_backward`` is set."""
     return GatedDeltaRule2.apply(q, k, v, b, w, log_decay, S0, chunked_backward)
 
 
@@ -382,8 +382,7 @@ class GatedDeltaRule2Varlen(torch.autograd.Function):
     """(o, S_T) = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0) as
     a differentiable operation over packed sequences: the forward pass is
     gdr2_forward_varlen (fp32 o), the backward pass gdr2_backward_varlen, or
-    gdr2_backward_chunked_varlen when ``chunked`` is set and the inputs are bf16
-    with dk = dv = 128.  Gradients are fp32 and cast to each input's dtype;
+    gdr2_backward_chunked_varlen when ``chunked`` is set and the inputs are bf16.  Gradients are fp32 and cast to each input's dtype;
     cu_seqlens gets none."""
 
     @staticmethod
@@ -391,7 +390,7 @@ class GatedDeltaRule2Varlen(torch.autograd.Function):
         o, S_T = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0)
         ctx.save_for_backward(q, k, v, b, w, log_decay, cu_seqlens, S0)
         ctx.has_s0 = S0 is not None
-        ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16 and q.shape[-1] == 128 and v.shape[-1] == 128
+        ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16
         return o, S_T
 
     @staticmethod
@@ -409,8 +408,8 @@ class GatedDeltaRule2Varlen(torch.autograd.Function):
 def gdr2_apply_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, chunked_backward: bool = False):
     """Differentiable prefill over packed sequences: ``(o, S_T)`` of
     gdr2_forward_varlen with gradients through gdr2_backward_varlen (exact fp32),
-    or through gdr2_backward_chunked_varlen (tensor cores; bf16 inputs with dk =
-    dv = 128, else the exact path) when ``chunked_backward`` is set."""
+    or through gdr2_backward_chunked_varlen (tensor cores; bf16 inputs, else the
+    exact path) when ``chunked_backward`` is set."""
     return GatedDeltaRule2Varlen.apply(q, k, v, b, w, log_decay, cu_seqlens, S0, chunked_backward)
 
 

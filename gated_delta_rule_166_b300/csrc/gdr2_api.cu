@@ -459,7 +459,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
             if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return GDR2_ERR_ALIAS;
         if (overlaps(outs[i], out_bytes[i], cu, bc)) return GDR2_ERR_ALIAS;
     }
-    if (chunked && (in_dtype != GDR2_BF16 || dk != kPrepDK || dv != 128)) return GDR2_ERR_UNSUPPORTED;
+    if (chunked && in_dtype != GDR2_BF16) return GDR2_ERR_UNSUPPORTED;
     int* err = nullptr;
     int st = device_setup(&err);
     if (st != GDR2_OK) return st;

@@ -95,6 +95,7 @@ struct Params {
     const int* cu;
     const int* chunk_base;
     int total;
+    int dk, dv;   // head sizes (up to 128; the state is zero-padded to 128 x 128 inside)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
@@ -256,12 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
         };
         // dO of chunk c for d_v column un, tokens 8 ug .. 8 ug + 7 (past the sequence end: 0)
         const int un = tid & 63, ug = tid >> 6;
-        const int64_t rs = static_cast<int64_t>(prm.H) * 128;
-        const float* const dcol = prm.dO + (tok0 * prm.H + h) * 128 + j0 + un;
+        // (value columns past d_v read as zero)
+        const int64_t rs = static_cast<int64_t>(prm.H) * prm.dv;
+        const bool col_ok = j0 + un < prm.dv;
+        const float* const dcol = prm.dO + (tok0 * prm.H + h) * prm.dv + (col_ok ? j0 + un : 0);
         auto fetch_do = [&](int c, float (&x)[8]) {
             const int t0 = c * kC + 8 * ug;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = t0 + e < T ? __ldg(dcol + static_cast<int64_t>(t0 + e) * rs) : 0.f;
+            for (int e = 0; e < 8; ++e) x[e] = col_ok && t0 + e < T ? __ldg(dcol + static_cast<int64_t>(t0 + e) * rs) : 0.f;
         };
         auto put_do = [&](int k, const float (&x)[8]) {
             uint4 hk, lk;
@@ -283,7 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
 
         float S[16];
         {
-            const float* s0 = prm.dST ? prm.dST + (static_cast<int64_t>(bh) * kPrepDK + j) * 128 + j0 + 16 * R : nullptr;
+            // d_S_T is [d_k][d_v]; rows past d_k and columns past d_v are zero padding
+            const bool live = j < prm.dk && j0 + 16 * R < prm.dv;
+            const float* s0 = prm.dST && live ? prm.dST + (static_cast<int64_t>(bh) * prm.dk + j) * prm.dv + j0 + 16 * R
+                                              : nullptr;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
                 const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -337,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1) rchain_kernel(const Params prm) {
         if (failed) {
             *abort_flag = 1;
             if (lane == 0) atomicExch(prm.err, kDevTimeout);
-        } else if (prm.dS0) {
-            float* p = prm.dS0 + (static_cast<int64_t>(bh) * kPrepDK + j) * 128 + j0 + 16 * R;
+        } else if (prm.dS0 && j < prm.dk && j0 + 16 * R < prm.dv) {
+            float* p = prm.dS0 + (static_cast<int64_t>(bh) * prm.dk + j) * prm.dv + j0 + 16 * R;
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4)
                 *reinterpret_cast<float4*>(p + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
@@ -423,6 +429,9 @@ struct Params {
     // items in the grid, and the item distance to the one that runs on this SM next
     // (the resident CTAs: one per SM); 0 turns the L2 prefetch of that item off
     int items, pf_stride;
+    // head sizes (up to 128): token rows are kdim or vdim wide, the states S0 and Sc
+    // are [kdim][vdim]; inside, every operand is zero-padded to 128 channels
+    int kdim, vdim;
 };
 
 // Item `it` = (global chunk gc, head h): its sequence, chunk within the sequence,
@@ -458,12 +467,13 @@ __device__ __forceinline__ bool cg_locate(const Params& prm, int it, CgItem& x) 
     }
     return true;
 }
-// The item's start state (null: zero), as the load phase reads it.
-__device__ __forceinline__ const float* cg_start_state(const Params& prm, int it, const CgItem& x) {
+// The item's start state ([d_k][d_v], st = d_k d_v floats; null: zero), as the load
+// phase reads it.
+__device__ __forceinline__ const float* cg_start_state(const Params& prm, int it, const CgItem& x, int64_t st) {
     const int64_t bh = static_cast<int64_t>(x.seq) * prm.H + x.h;
-    return x.c == 0  ? (prm.S0 ? prm.S0 + bh * 16384 : nullptr)
-           : prm.cu ? prm.Sc + (static_cast<int64_t>(it) - prm.H) * 16384   // global chunk gc - 1
-                    : prm.Sc + (bh * prm.n_cache + (x.c - 1)) * 16384;
+    return x.c == 0  ? (prm.S0 ? prm.S0 + bh * st : nullptr)
+           : prm.cu ? prm.Sc + (static_cast<int64_t>(it) - prm.H) * st   // global chunk gc - 1
+                    : prm.Sc + (bh * prm.n_cache + (x.c - 1)) * st;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -485,9 +495,10 @@ __device__ __forceinline__ void put16(uint8_t* img, uint32_t kblk, uint32_t row,
 // Lane l of a warp holds one key / value channel (a0 + l) at 16 tokens r0 .. r0 + 15;
 // the warp writes them to its 2 KB buffer and reads them back as 4 channels of one
 // token, so that each global store moves 16 bytes (8 lanes: one token's 32 channels)
-// instead of 4.  Rows at or past `nvalid` are not stored.
+// instead of 4.  Rows at or past `nvalid` and channels at or past `width` (the row
+// width of `out`, a multiple of 32) are not stored.
 __device__ __forceinline__ void store_tokens(float* buf, const float (&v)[16], float* out, int64_t row0, int H,
-                                             int h, int a0, int r0, int nvalid, int lane) {
+                                             int h, int a0, int r0, int nvalid, int lane, int width) {
 #pragma unroll
     for (int t = 0; t < 16; ++t) buf[t * 32 + lane] = v[t];
     __syncwarp();
@@ -495,8 +506,8 @@ __device__ __forceinline__ void store_tokens(float* buf, const float (&v)[16], f
     for (int s4 = 0; s4 < 4; ++s4) {
         const int t = 4 * s4 + (lane >> 3), c4 = 4 * (lane & 7);
         const float4 x = *reinterpret_cast<const float4*>(buf + t * 32 + c4);
-        if (r0 + t < nvalid)
-            *reinterpret_cast<float4*>(out + ((row0 + r0 + t) * H + h) * 128 + a0 + c4) = x;
+        if (r0 + t < nvalid && a0 < width)
+            *reinterpret_cast<float4*>(out + ((row0 + r0 + t) * H + h) * width + a0 + c4) = x;
     }
     __syncwarp();
 }
@@ -514,7 +525,11 @@ __device__ __forceinline__ void put16_pair(uint8_t* hi, uint8_t* lo, uint32_t kb
     put16(lo, kblk, row, k0, l);
 }
 
+// kPad: head sizes below 128 (zero-padded channels); the d_k = d_v = 128 instantiation
+// keeps compile-time row strides and no channel guards.
+template <bool kPad>
 __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
+    const int kdim = kPad ? prm.kdim : 128, vdim = kPad ? prm.vdim : 128;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (base - smem_u32(smem_raw));
@@ -534,7 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
     const int h = item.h, seq = item.seq, c = item.c, nvalid = item.nvalid;
     const int64_t row0 = item.row0;   // first token row of the chunk
     const int bh = seq * prm.H + h;
-    auto gidx = [&](int r, int ch) { return ((row0 + r) * prm.H + h) * 128 + ch; };
+    // element index of channel ch of token r in a key-side (dk wide) or value-side row
+    auto kidx = [&](int r, int ch) { return ((row0 + r) * prm.H + h) * kdim + ch; };
+    auto vidx = [&](int r, int ch) { return ((row0 + r) * prm.H + h) * vdim + ch; };
 
     if (tid == 0) {
         for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
@@ -565,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 
     // ---- S, dS' -> fp16 images [d_k][d_v]; rowsum(dS' * S) ----------------------------------
     {
-        const float* Sp = cg_start_state(prm, it, item);
+        const float* Sp = cg_start_state(prm, it, item, static_cast<int64_t>(kdim) * vdim);
         const float* dSp = prm.dsn + static_cast<int64_t>(it) * 16384;   // global chunk gc, head h
         const int r = tid >> 2, e0 = 32 * (tid & 3);
         float part = 0.f;
@@ -575,7 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             float sv[16], dv[16];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float4 x = Sp ? __ldg(reinterpret_cast<const float4*>(Sp + r * 128 + e) + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 x = Sp && r < kdim && e < vdim
+                                     ? __ldg(reinterpret_cast<const float4*>(Sp + r * vdim + e) + u)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float4 y = __ldg(reinterpret_cast<const float4*>(dSp + r * 128 + e) + u);
                 sv[4 * u] = x.x; sv[4 * u + 1] = x.y; sv[4 * u + 2] = x.z; sv[4 * u + 3] = x.w;
                 dv[4 * u] = y.x; dv[4 * u + 1] = y.y; dv[4 * u + 2] = y.z; dv[4 * u + 3] = y.w;
@@ -592,10 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
     // ---- dO and u = w v -> fp16 images [token][d_v] (tokens past the sequence end: 0) --------
     {
         const int r = tid >> 3, e = 16 * (tid & 7);
-        const bool valid = r < nvalid;
+        const bool valid = r < nvalid && e < vdim;   // value columns past d_v: zero
         float ov[16], uv[16];
         if (valid) {
-            const int64_t gi = gidx(r, e);
+            const int64_t gi = vidx(r, e);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 x = __ldg(reinterpret_cast<const float4*>(prm.dO + gi) + u);
@@ -633,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
         CgItem nx;
         if (cg_locate(prm, nit, nx)) {
             bulk_prefetch_l2(prm.wy + static_cast<int64_t>(nit) * kWyBytes, kWyBytes);
-            if (const float* ns = cg_start_state(prm, nit, nx)) bulk_prefetch_l2(ns, 65536u);
+            if (const float* ns = cg_start_state(prm, nit, nx, static_cast<int64_t>(kdim) * vdim))
+                bulk_prefetch_l2(ns, static_cast<uint32_t>(kdim * vdim * 4));
             bulk_prefetch_l2(prm.dsn + static_cast<int64_t>(nit) * 16384, 65536u);
         }
     }
@@ -754,8 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int r = 16 * cb + jj;
-            const bool valid = r < nvalid;
-            const int64_t gi = valid ? gidx(r, a) : 0;
+            const bool valid = r < nvalid && a < vdim;
+            const int64_t gi = valid ? vidx(r, a) : 0;
             vb[jj] = valid ? __ldg(reinterpret_cast<const unsigned short*>(prm.v) + gi) : 0;
             wb[jj] = valid ? __ldg(reinterpret_cast<const unsigned short*>(prm.w) + gi) : 0;
         }
@@ -771,10 +791,10 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             float t[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) t[jj] = v[jj] * bf(wb[jj]);
-            store_tokens(xb, t, prm.dv, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+            store_tokens(xb, t, prm.dv, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane, vdim);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) t[jj] = v[jj] * bf(vb[jj]);
-            store_tokens(xb, t, prm.dw, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+            store_tokens(xb, t, prm.dw, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane, vdim);
         }
         put16_pair(sgen + kdUt, sgen + kdUtL, 0u, static_cast<uint32_t>(a), 16u * cb, v);
     }
@@ -786,8 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
         for (int i = 0; i < 8; ++i) {
             const int p = tid + kThreads * i;
             const int tsel = p >> 10, r = (p >> 4) & 63, piece = p & 15;
-            const bool valid = r < nvalid;
-            const __nv_bfloat16* s = src[tsel] + gidx(valid ? r : 0, 8 * piece);
+            const bool valid = r < nvalid && 8 * piece < kdim;   // key channels past d_k: zero
+            const __nv_bfloat16* s = src[tsel] + (valid ? kidx(r, 8 * piece) : kidx(0, 0));
             cp_async16(base + kRaw + static_cast<uint32_t>(tsel) * 16384u + static_cast<uint32_t>(r) * 256u + 16u * piece, s,
                        valid ? 16u : 0u);
         }
@@ -924,8 +944,8 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
         }
         scr[cb * 128 + a] = zk;
         float* xb = reinterpret_cast<float*>(sgen + kXpB) + warp * 512;
-        store_tokens(xb, dqv, prm.dq, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
-        store_tokens(xb, dbv, prm.db, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+        store_tokens(xb, dqv, prm.dq, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane, kdim);
+        store_tokens(xb, dbv, prm.db, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane, kdim);
     }
     tc_fence_before();
     __syncthreads();
@@ -983,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             dgp[jj] -= y[jj] * tf32r(kv * fi);   // the K-group factor as rounded for X
         }
         float* xb = reinterpret_cast<float*>(sgen + kXpB) + warp * 512;
-        store_tokens(xb, dkp, prm.dk, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+        store_tokens(xb, dkp, prm.dk, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane, kdim);
         if (cb == 3) {
             // G_C's own terms land on the chunk's last token row
             float zk = 0.f;
@@ -1002,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) cgrad_kernel(const Params prm) {
             run += dgp[jj];
             dgp[jj] = run;
         }
-        store_tokens(xb, dgp, prm.dg, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane);
+        store_tokens(xb, dgp, prm.dg, row0, prm.H, h, 32 * quarter, 16 * cb, nvalid, lane, kdim);
     }
     if (!ok && tid == 0) atomicExch(prm.err, kDevTimeout);
     if (tid == 0) {
@@ -1064,7 +1084,9 @@ size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H, bool pa
 
 int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err) {
     const bool packed = a.cu != nullptr;
-    if (a.in_dtype != GDR2_BF16 || a.dk != kPrepDK || a.dv != 128 || (packed ? a.total <= 0 : a.T <= 0))
+    // head sizes below 128 run on channels zero-padded to 128, as in the forward
+    auto dim_ok = [](int64_t d) { return d == 32 || d == 64 || d == 128; };
+    if (a.in_dtype != GDR2_BF16 || !dim_ok(a.dk) || !dim_ok(a.dv) || (packed ? a.total <= 0 : a.T <= 0))
         return GDR2_ERR_UNSUPPORTED;
     const ChunkedLayout l = chunked_layout(a.B, a.T, a.H, packed, a.total);
     const int64_t chunks = l.chunks, items = chunks * a.H, n_cache = l.n_cache;
@@ -1103,12 +1125,16 @@ int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream
         attr_err = cudaFuncSetAttribute(rch::rchain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(rch::kSmemAlloc));
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(cgr::cgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            attr_err = cudaFuncSetAttribute(cgr::cgrad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(cgr::kSmemAlloc));
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(cgr::cgrad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(cgr::kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
     rch::Params rp{slots, a.dST, a.dO, dsn, a.d_S0, err, static_cast<int>(a.T), static_cast<int>(a.H),
-                   static_cast<int>(nch), kWaitCycles, a.cu, cb, static_cast<int>(packed ? a.total : 0)};
+                   static_cast<int>(nch), kWaitCycles, a.cu, cb, static_cast<int>(packed ? a.total : 0),
+                   static_cast<int>(a.dk), static_cast<int>(a.dv)};
     rch::rchain_kernel<<<dim3(static_cast<unsigned>(a.B * a.H), 2), rch::kThreads, rch::kSmemAlloc, stream>>>(rp);
     if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
     cgr::Params gp{wy, Sc, a.S0, dsn, a.dO,
@@ -1118,8 +1144,11 @@ int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream
                    a.d_q, a.d_k, a.d_b, a.d_g, a.d_v, a.d_w,
                    static_cast<int>(a.T), static_cast<int>(a.H), static_cast<int>(nch), static_cast<int>(n_cache), err,
                    a.cu, cb, static_cast<int>(a.B), static_cast<int>(packed ? a.total : 0),
-                   static_cast<int>(items), cgrad_prefetch_stride()};
-    cgr::cgrad_kernel<<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
+                   static_cast<int>(items), cgrad_prefetch_stride(), static_cast<int>(a.dk), static_cast<int>(a.dv)};
+    if (a.dk == 128 && a.dv == 128)
+        cgr::cgrad_kernel<false><<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
+    else
+        cgr::cgrad_kernel<true><<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
 }
 

@@ -338,8 +338,9 @@ int gdr2_backward_varlen(const void* q, const void* k, const void* v,
 
 /*
  * gdr2_backward_chunked -- the gradients of gdr2_backward (same arguments, same
- * outputs) through the chunkwise WY form on tensor cores, for bf16 inputs with
- * dk = dv = 128 (GDR2_ERR_UNSUPPORTED otherwise).  Per 64-token chunk, with
+ * outputs) through the chunkwise WY form on tensor cores, for bf16 inputs
+ * (GDR2_ERR_UNSUPPORTED for fp32); dk, dv in {32, 64, 128}, head sizes below 128
+ * computed on channels zero-padded to 128 as in the forward.  Per 64-token chunk, with
  * start state S, the gradient dS' at its end state and dO at its outputs
  * (Cb = c e^G, Qb = q e^G, Kb = k e^{G_C - G}, Kh = k e^{-G}, u = w (.) v,
  * A_kk = strict_tril(Cb Kh^T), A_qk = tril(Qb Kh^T), T = (I + A_kk)^-1,
@@ -375,7 +376,7 @@ int gdr2_backward_chunked(const void* q, const void* k, const void* v,
 /*
  * gdr2_backward_chunked_varlen -- gdr2_backward_chunked over N packed sequences:
  * the gradients of gdr2_forward_varlen through the chunkwise WY form on tensor
- * cores, for bf16 inputs with dk = dv = 128 (GDR2_ERR_UNSUPPORTED otherwise).
+ * cores, for bf16 inputs (dk, dv in {32, 64, 128}; GDR2_ERR_UNSUPPORTED for fp32).
  * Arguments, layouts and row ownership are those of gdr2_backward_varlen; the
  * precision is that of gdr2_backward_chunked, sequence by sequence.  Workspace
  * (the library's pool, released on the stream): per (chunk, head) 123,392

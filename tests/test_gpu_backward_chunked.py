@@ -5,7 +5,8 @@ The chunked path takes fp16 operands (tf32 for the decay-weighted products)
 with fp32 accumulation, like the chunked forward, so its bar is the bf16 one,
 max|err| / RMS(ref) <= 2e-2, on every gradient: dq, dk, dv, db, dw, dlog_decay
 and dS0.  Cases span several chunks with ragged tails, a single token, the
-slow, zero and mixed decay regimes, with and without S0 and a gradient at S_T.
+slow, zero and mixed decay regimes, with and without S0 and a gradient at S_T,
+and head sizes below 128 (zero-padded channels).
 Under fast decays db and dlog_decay have the derived bar stated below."""
 import numpy as np
 import pytest
@@ -74,9 +75,17 @@ def test_chunked_backward_empty_sequence_and_unsupported_shapes():
     d_o = torch.zeros(1, 8, 2, 128, device="cuda")
     with pytest.raises(gdr2.GDR2Error):   # fp32 inputs: the exact path is gdr2_backward
         gdr2.backward_chunked(*(t.float() for t in x.tensors()), x.S0, d_o, None)
-    y = make_prefill_inputs(1, 8, 2, 64, 128, dtype=torch.bfloat16, seed=941).to("cuda")
-    with pytest.raises(gdr2.GDR2Error):   # d_k = 64
-        gdr2.backward_chunked(*y.tensors(), None, d_o, None)
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 64), (128, 64), (64, 128), (32, 128), (128, 32)])
+def test_chunked_backward_small_head_sizes(dk, dv):
+    """Head sizes below 128 on channels zero-padded to 128 (as in the forward):
+    every gradient, dS0 included, against the oracle at the bf16 bar; ragged
+    chunks, a non-zero S0 and a gradient at S_T exercise the padded state rows and
+    columns in both directions."""
+    x = make_prefill_inputs(2, 150, 2, dk, dv, dtype=torch.bfloat16, seed=990 + dk + dv, decay_regime="slow",
+                            s0_std=0.4, b_scale=2.0)
+    check(x, *upstream(x, 50 + dk + dv), f"dk={dk} dv={dv}")
 
 
 def test_chunked_backward_agrees_with_exact_backward_on_ragged_batch():

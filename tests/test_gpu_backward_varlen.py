@@ -225,6 +225,19 @@ def test_chunked_varlen_without_initial_state_or_final_gradient_and_unsupported_
         gdr2.backward_chunked_varlen(*[t.float() for t in d], cu.cuda(), None, d_o.cuda(), None)
 
 
+def test_chunked_varlen_small_head_sizes():
+    """Packed sequences with d_k = 64, d_v = 32 on the zero-padded tensor-core path:
+    per-sequence oracle parity at the bf16 bar."""
+    lengths = [70, 129, 1]
+    H = 2
+    seqs, toks, S0, cu, d_o, d_ST = _packed(lengths, H, 64, 32, torch.bfloat16, seed=893, decay_regime="slow")
+    got = gdr2.backward_chunked_varlen(*[t.cuda() for t in toks], cu.cuda(), S0.cuda(), d_o.cuda(), d_ST.cuda())
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    for i, s in enumerate(seqs):
+        _check_sequence_chunked(got, s, i, int(cu[i]), int(cu[i + 1]), S0, d_o, d_ST, "chunked dk=64 dv=32")
+
+
 def test_autograd_varlen_chunked_backward():
     """gdr2_apply_varlen(chunked_backward=True) on bf16 inputs: gradients through
     the tensor-core path, returned in bf16 (bar 2e-2 plus one bf16 rounding)."""
