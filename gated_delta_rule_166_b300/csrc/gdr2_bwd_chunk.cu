@@ -1,5 +1,6 @@
-// Chunked gradients of the Gated Delta Rule-2 prefill: bf16 inputs, d_k = d_v = 128,
-// tensor cores for every contraction.
+// Chunked gradients of the Gated Delta Rule-2 prefill: bf16 inputs, d_k and d_v up to
+// 128 (smaller head sizes on channels zero-padded to 128, as in the forward), tensor
+// cores for every contraction; fixed-length batches or packed sequences.
 //
 // Method: reverse-mode differentiation of the chunkwise WY form of the "Gated
 // DeltaNet-2: Decoupling Erase and Write in Linear Attention" page (update equation;
