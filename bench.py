@@ -259,15 +259,23 @@ def launch_stats(per_launch):
             "first_ms": per_launch[0], "max_ms": max(per_launch), "calls": len(per_launch)}
 
 
-def bench_decode(gdr2, steps=1024, pool=16, seed=5):
+def bench_decode(gdr2, steps=1024, seed=5):
     """1024 in-place decode steps, launched eagerly and replayed from one CUDA
-    graph (the launch-bound inner loop of serving); GB/s from the graph replay."""
-    from gated_delta_rule_166_b300.inputs import DECODE_WORKLOAD, make_decode_state, make_decode_token
+    graph (the launch-bound inner loop of serving); GB/s from the graph replay.
+    Every step takes its own token (1024 sets, 6.4 GB, drawn on the device by
+    the seeded generator with the decode distributions), so no step's inputs
+    are in L2 from an earlier one."""
+    from gated_delta_rule_166_b300.inputs import DECODE_WORKLOAD, PrefillInputs, make_decode_state, \
+        make_prefill_inputs
 
     W = DECODE_WORKLOAD
     B, H, dk, dv = W["B"], W["H"], W["dk"], W["dv"]
     S = make_decode_state(B, H, dk, dv, seed=seed).cuda()
-    toks = [make_decode_token(B, H, dk, dv, seed=seed, step=s).to("cuda") for s in range(pool)]
+    allt = make_prefill_inputs(B, steps, H, dk, dv, dtype=torch.bfloat16, seed=seed * 1_000_003 + 1, device="cuda")
+    per_step = [t.transpose(0, 1).contiguous() for t in allt.tensors()]   # [steps, B, H, d]
+    del allt
+    toks = [PrefillInputs(*(t[s] for t in per_step), None) for s in range(steps)]
+    pool = steps
     o = torch.empty((B, H, dv), dtype=torch.float32, device="cuda")
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())

@@ -56,13 +56,13 @@ def _normalise_rows(x: torch.Tensor) -> torch.Tensor:
 
 
 def _decay(gen, shape, regime: str, shift: float) -> torch.Tensor:
-    z = torch.randn(shape, generator=gen)
+    z = torch.randn(shape, generator=gen, device=gen.device)
     if regime == "fast":
         return -F.softplus(z + shift)
     if regime == "slow":
         return -F.softplus(z - 4.0)
     if regime == "zero":
-        return torch.zeros(shape)
+        return torch.zeros(shape, device=gen.device)
     if regime == "mixed":
         fast = -F.softplus(z + shift)
         slow = -F.softplus(z - 4.0)
@@ -76,23 +76,27 @@ def make_prefill_inputs(B: int, T: int, H: int, dk: int, dv: int, *,
                         gates: str = "channel", decay: str = "channel",
                         decay_regime: str = "fast", decay_shift: float = 2.0,
                         s0_std: float | None = None,
-                        b_scale: float = 1.0) -> PrefillInputs:
+                        b_scale: float = 1.0, device: str = "cpu") -> PrefillInputs:
     """Draw one prefill problem.
 
     gates: "channel" (b, w per channel) or "tied" (KDA: b = w = one scalar per
     token and head).  decay: "channel" or "scalar" (one value per token and
     head, broadcast over d_k).  b_scale multiplies b after the sigmoid (the
-    page's ablation widens the erase range to [0, 2]).
+    page's ablation widens the erase range to [0, 2]).  device: where the
+    seeded generator draws (the same distributions; a CUDA generator gives other
+    values than the CPU one for the same seed, and is for inputs too large to
+    draw on the host in time, such as the decode bench's 1024 token sets).
     """
-    gen = torch.Generator().manual_seed(int(seed))
-    q = _normalise_rows(torch.randn(B, T, H, dk, generator=gen))
-    k = _normalise_rows(torch.randn(B, T, H, dk, generator=gen))
-    v = torch.randn(B, T, H, dv, generator=gen)
+    gen = torch.Generator(device=device).manual_seed(int(seed))
+    rn = lambda *shape: torch.randn(*shape, generator=gen, device=device)  # noqa: E731
+    q = _normalise_rows(rn(B, T, H, dk))
+    k = _normalise_rows(rn(B, T, H, dk))
+    v = rn(B, T, H, dv)
     if gates == "channel":
-        b = torch.sigmoid(torch.randn(B, T, H, dk, generator=gen))
-        w = torch.sigmoid(torch.randn(B, T, H, dv, generator=gen))
+        b = torch.sigmoid(rn(B, T, H, dk))
+        w = torch.sigmoid(rn(B, T, H, dv))
     elif gates == "tied":
-        s = torch.sigmoid(torch.randn(B, T, H, 1, generator=gen))
+        s = torch.sigmoid(rn(B, T, H, 1))
         b = s.expand(B, T, H, dk).contiguous()
         w = s.expand(B, T, H, dv).contiguous()
     else:
@@ -106,7 +110,7 @@ def make_prefill_inputs(B: int, T: int, H: int, dk: int, dv: int, *,
         raise ValueError(f"unknown decay mode {decay!r}")
     S0 = None
     if s0_std is not None:
-        S0 = torch.randn(B, H, dk, dv, generator=gen) * s0_std
+        S0 = rn(B, H, dk, dv) * s0_std
     cast = lambda t: t.to(dtype).contiguous()
     return PrefillInputs(cast(q), cast(k), cast(v), cast(b), cast(w), cast(g), S0)
 
