@@ -407,6 +407,57 @@ def bench_backward(gdr2, hbm_gbs, x, steps=5, warmup=3, batch=None, chunked=True
                          "kernel": kernels}}
 
 
+def bench_train_step(gdr2, hbm_gbs, x, steps=5, warmup=3):
+    """One training step of the layer (forward, then the gradients of all inputs
+    from a seeded fp32 gradient at o) at the GDN-2 layer workload, CUDA events
+    around `steps` steps, two ways: gdr2_forward_train + gdr2_backward_from_context
+    (the per-chunk context kept, 773 MB) and gdr2_forward + gdr2_backward_chunked
+    (recomputed)."""
+    B, T, H, dk = x.q.shape
+    dv = x.v.shape[-1]
+    gen = torch.Generator().manual_seed(11)
+    d_o = torch.randn(B, T, H, dv, generator=gen).to("cuda")
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    ctx = torch.empty(gdr2.gdr2_train_context_bytes(B, T, H, dk, dv), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def kept():
+        gdr2.forward_train(*x.tensors(), x.S0, o=o, S_T=S_T, ctx=ctx)
+        gdr2.backward_from_context(ctx, *x.tensors(), x.S0, d_o, None)
+
+    def recomputed():
+        gdr2.forward(*x.tensors(), x.S0, o=o, S_T=S_T)
+        gdr2.backward_chunked(*x.tensors(), x.S0, d_o, None)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if gdr2.gdr2_device_status() != 0:
+            raise RuntimeError("device-side failure in the training-step leg")
+        return a.elapsed_time(b) / steps
+
+    ms_kept, ms_rec = timed(kept), timed(recomputed)
+    return {"workload": f"{WORKLOAD} training step (B={B}): forward (bf16 o) and the gradients of all six "
+                        f"inputs, fp32, from a seeded fp32 gradient at o",
+            "context_kept": {"ms_per_step": ms_kept, "tokens_per_s": B * T / (ms_kept / 1e3),
+                             "context_bytes": ctx.numel(),
+                             "kernels": "gdr2_forward_train (prep2_kernel with backward records + chain_kernel "
+                                        "keeping every start state) + gdr2_backward_from_context (rchain_kernel + "
+                                        "cgrad_kernel)"},
+            "recomputed": {"ms_per_step": ms_rec, "tokens_per_s": B * T / (ms_rec / 1e3),
+                           "kernels": "gdr2_forward (prep2_kernel + chain_kernel) + gdr2_backward_chunked "
+                                      "(prep2_kernel + chain_kernel + rchain_kernel + cgrad_kernel)"},
+            "steps": steps, "warmup": warmup}
+
+
 def packed_offsets(total, n, seed=12):
     """cu_seqlens of `n` ragged sequences covering `total` token rows: n - 1 seeded
     cut points, distinct and uniform over the rows (lengths not multiples of 64)."""
@@ -614,7 +665,8 @@ def main():
                     help="profiling aid: the backward leg on the first N sequences only")
     ap.add_argument("--no-sparse", action="store_true", help="skip the sparse-write leg")
     ap.add_argument("--no-packed", action="store_true", help="skip the packed-sequence leg")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward", "sparse", "packed"],
+    ap.add_argument("--no-train", action="store_true", help="skip the training-step leg")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "backward", "sparse", "packed", "train"],
                     default="all",
                     help="profiling aid: run just one leg (decode and long print only that leg)")
     ap.add_argument("--decode-steps", type=int, default=1024)
@@ -705,6 +757,11 @@ def main():
         if rank == 0:
             print(json.dumps({"packed": pk}))
         return
+    if args.only == "train":
+        ts = bench_train_step(gdr2, hbm_gbs, x, steps=min(args.steps, 5), warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"train_step": ts}))
+        return
 
     with ClockSampler(local) as clk:
         ms, per_launch, launches = bench_prefill(gdr2, x, args.steps, args.warmup, world)
@@ -745,7 +802,7 @@ def main():
 
     if args.only == "prefill":
         args.no_e2e = args.no_decode = args.no_cpu_baseline = args.no_long = args.no_backward = True
-        args.no_sparse = args.no_packed = True
+        args.no_sparse = args.no_packed = args.no_train = True
     if not args.no_e2e:
         e2e_ms, h2d, d2h = bench_e2e(gdr2, x_host, max(3, args.steps // 4), 2)
         e2e_ms = max_over_ranks(e2e_ms, world)
@@ -774,6 +831,8 @@ def main():
         out["sparse_write"] = bench_sparse(gdr2, hbm_gbs)
     if not args.no_packed:
         out["packed"] = bench_packed(gdr2, hbm_gbs, x)
+    if not args.no_train:
+        out["train_step"] = bench_train_step(gdr2, hbm_gbs, x)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x_host)
     if rank == 0:

@@ -16,16 +16,19 @@ from ._lib import (  # noqa: F401
     gdr2_backward,
     gdr2_backward_chunked,
     gdr2_backward_chunked_varlen,
+    gdr2_backward_from_context,
     gdr2_backward_varlen,
     gdr2_decode_step,
     gdr2_device_status,
     gdr2_forward,
     gdr2_forward_cached,
     gdr2_forward_noalloc,
+    gdr2_forward_train,
     gdr2_forward_varlen,
     gdr2_release_workspace,
     gdr2_set_wait_limit,
     gdr2_sparse_write,
+    gdr2_train_context_bytes,
     gdr2_version,
     gdr2_workspace_stats,
 )
@@ -39,5 +42,7 @@ backward = gdr2_backward
 backward_chunked = gdr2_backward_chunked
 backward_varlen = gdr2_backward_varlen
 backward_chunked_varlen = gdr2_backward_chunked_varlen
+forward_train = gdr2_forward_train
+backward_from_context = gdr2_backward_from_context
 apply_varlen = gdr2_apply_varlen
 sparse_write = gdr2_sparse_write

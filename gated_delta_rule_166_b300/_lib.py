@@ -60,6 +60,12 @@ def lib():
         L.gdr2_backward_varlen.restype = ci
         L.gdr2_backward_chunked_varlen.argtypes = [vp] * 17 + [i64] * 5 + [ci, vp]
         L.gdr2_backward_chunked_varlen.restype = ci
+        L.gdr2_train_context_bytes.argtypes = [i64] * 5
+        L.gdr2_train_context_bytes.restype = i64
+        L.gdr2_forward_train.argtypes = [vp] * 10 + [i64] * 6 + [ci, ci, vp]
+        L.gdr2_forward_train.restype = ci
+        L.gdr2_backward_from_context.argtypes = [vp] * 10 + [i64] + [vp] * 7 + [i64] * 5 + [ci, vp]
+        L.gdr2_backward_from_context.restype = ci
         L.gdr2_backward_chunked.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
         L.gdr2_backward_chunked.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
@@ -258,7 +264,70 @@ def gdr2_backward_chunked(q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want
     return _backward("gdr2_backward_chunked", q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream)
 
 
-def _backward(fn, q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream):
+def gdr2_train_context_bytes(B: int, T: int, H: int, dk: int, dv: int) -> int:
+    """Bytes of the context gdr2_forward_train keeps for these sizes."""
+    n = lib().gdr2_train_context_bytes(B, T, H, dk, dv)
+    if n < 0:
+        raise GDR2Error(int(n), "gdr2_train_context_bytes")
+    return int(n)
+
+
+def gdr2_forward_train(q, k, v, b, w, log_decay, S0=None, *, o=None, S_T=None, out_dtype=torch.float32,
+                       ctx=None, stream=None):
+    """gdr2_forward that also keeps, in a device buffer, what the chunked backward
+    would recompute: every chunk's maps, backward records and start state (bf16
+    inputs).  Returns ``(o, S_T, ctx)``; ``ctx`` (uint8, or the given buffer) goes
+    to gdr2_backward_from_context with the same, unchanged inputs."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q and v must be [B, T, H, d]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_forward_train runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (B, T, H, d), dtype, dev)
+    if S0 is not None:
+        _check_tokens("S0", S0, (B, H, dk, dv), torch.float32, dev)
+    if o is None:
+        if out_dtype not in _DTYPES:
+            raise ValueError(f"unsupported out_dtype {out_dtype}")
+        o = torch.empty((B, T, H, dv), dtype=out_dtype, device=dev)
+    else:
+        _check_tokens("o", o, (B, T, H, dv), o.dtype, dev)
+    if S_T is None:
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    else:
+        _check_tokens("S_T", S_T, (B, H, dk, dv), torch.float32, dev)
+    need = gdr2_train_context_bytes(B, T, H, dk, dv)
+    if ctx is None:
+        ctx = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif ctx.device != dev or ctx.dtype != torch.uint8 or not ctx.is_contiguous() or ctx.numel() < need:
+        raise ValueError(f"ctx must be a contiguous uint8 tensor of at least {need} bytes on {dev}")
+    with torch.cuda.device(dev):
+        st = lib().gdr2_forward_train(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
+                                      _ptr(o), _ptr(S_T), _ptr(ctx), ctx.numel(), B, T, H, dk, dv,
+                                      _DTYPES[dtype], _DTYPES[o.dtype], ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_forward_train")
+    return o, S_T, ctx
+
+
+def gdr2_backward_from_context(ctx, q, k, v, b, w, log_decay, S0, d_o, d_S_T=None, *, want_dS0: bool = True,
+                               stream=None):
+    """gdr2_backward_chunked from the context gdr2_forward_train kept for these
+    inputs: the same arguments and fp32 outputs (dq, dk, dv, db, dw, dlog_decay,
+    dS0), without recomputing the forward."""
+    if ctx.dtype != torch.uint8 or not ctx.is_contiguous() or ctx.device != q.device:
+        raise ValueError("ctx must be the contiguous uint8 context of gdr2_forward_train")
+    return _backward("gdr2_backward_from_context", q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream,
+                     ctx=ctx)
+
+
+def _backward(fn, q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream, ctx=None):
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q and v must be [B, T, H, d]")
     B, T, H, dk = q.shape
@@ -279,10 +348,11 @@ def _backward(fn, q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0, stream):
     gq, gk, gb, gg = (torch.empty((B, T, H, dk), **f32) for _ in range(4))
     gv, gw = (torch.empty((B, T, H, dv), **f32) for _ in range(2))
     gS0 = torch.empty((B, H, dk, dv), **f32) if want_dS0 else None
+    ctx_args = () if ctx is None else (_ptr(ctx), ctx.numel())
     with torch.cuda.device(dev):
         st = getattr(lib(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
-                                _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
-                                _ptr(gg), _ptr(gS0), B, T, H, dk, dv, _DTYPES[dtype],
+                                _ptr(d_o), _ptr(d_S_T), *ctx_args, _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb),
+                                _ptr(gw), _ptr(gg), _ptr(gS0), B, T, H, dk, dv, _DTYPES[dtype],
                                 ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
         raise GDR2Error(st, fn)
@@ -347,35 +417,47 @@ def _backward_varlen(fn, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, w
 class GatedDeltaRule2(torch.autograd.Function):
     """(o, S_T) = gdr2_forward(q, k, v, b, w, log_decay, S0) as a differentiable
     operation: the forward pass is gdr2_forward (fp32 o), the backward pass
-    gdr2_backward, or gdr2_backward_chunked when ``chunked`` is set and the inputs
-    are bf16.  Gradients are fp32 and cast to each input's
-    dtype."""
+    gdr2_backward, or the chunked tensor-core backward when ``chunked`` is set and
+    the inputs are bf16.  The chunked backward either recomputes the forward's
+    per-chunk context (gdr2_backward_chunked) or, with ``keep_context``, the
+    forward pass is gdr2_forward_train and keeps it for
+    gdr2_backward_from_context (faster, 773 MB more memory per B4 H16 T4096 d128
+    call).  Gradients are fp32 and cast to each input's dtype."""
 
     @staticmethod
-    def forward(ctx, q, k, v, b, w, log_decay, S0=None, chunked=False):
-        o, S_T = gdr2_forward(q, k, v, b, w, log_decay, S0)
-        ctx.save_for_backward(q, k, v, b, w, log_decay, S0)
+    def forward(ctx, q, k, v, b, w, log_decay, S0=None, chunked=False, keep_context=True):
         ctx.has_s0 = S0 is not None
         ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16
+        kept = None
+        if ctx.chunked and keep_context and q.shape[0] * q.shape[1] * q.shape[2] > 0:
+            o, S_T, kept = gdr2_forward_train(q, k, v, b, w, log_decay, S0)
+        else:
+            o, S_T = gdr2_forward(q, k, v, b, w, log_decay, S0)
+        ctx.save_for_backward(q, k, v, b, w, log_decay, S0, kept)
         return o, S_T
 
     @staticmethod
     def backward(ctx, d_o, d_S_T):
-        q, k, v, b, w, log_decay, S0 = ctx.saved_tensors
+        q, k, v, b, w, log_decay, S0, kept = ctx.saved_tensors
         d_o = torch.zeros((*v.shape[:3], v.shape[-1]), dtype=torch.float32, device=q.device) if d_o is None \
             else d_o.float().contiguous()
         d_S_T = None if d_S_T is None else d_S_T.float().contiguous()
-        fn = gdr2_backward_chunked if ctx.chunked else gdr2_backward
-        g = fn(q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
+        if kept is not None:
+            g = gdr2_backward_from_context(kept, q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
+        else:
+            fn = gdr2_backward_chunked if ctx.chunked else gdr2_backward
+            g = fn(q, k, v, b, w, log_decay, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
         cast = [g[i].to(t.dtype) for i, t in enumerate((q, k, v, b, w, log_decay))]
-        return (*cast, g[6] if ctx.has_s0 else None, None)
+        return (*cast, g[6] if ctx.has_s0 else None, None, None)
 
 
-def gdr2_apply(q, k, v, b, w, log_decay, S0=None, *, chunked_backward: bool = False):
+def gdr2_apply(q, k, v, b, w, log_decay, S0=None, *, chunked_backward: bool = False, keep_context: bool = True):
     """Differentiable prefill: ``(o, S_T)`` with gradients through gdr2_backward
-    (exact fp32), or through gdr2_backward_chunked (tensor cores; bf16 inputs, else
-    the exact path) when ``chunked_backward`` is set."""
-    return GatedDeltaRule2.apply(q, k, v, b, w, log_decay, S0, chunked_backward)
+    (exact fp32), or through the chunked tensor-core backward (bf16 inputs, else
+    the exact path) when ``chunked_backward`` is set: from a context the forward
+    keeps (gdr2_forward_train, the default) or, with ``keep_context=False``,
+    recomputed by gdr2_backward_chunked."""
+    return GatedDeltaRule2.apply(q, k, v, b, w, log_decay, S0, chunked_backward, keep_context)
 
 
 class GatedDeltaRule2Varlen(torch.autograd.Function):

@@ -426,7 +426,8 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
                   const void* log_decay, const float* S0, const float* d_o, const float* d_S_T, float* d_q,
                   float* d_k, float* d_v, float* d_b, float* d_w, float* d_log_decay, float* d_S0, int64_t B,
                   int64_t T, int64_t H, int64_t dk, int64_t dv, int in_dtype, cudaStream_t stream, bool chunked,
-                  const int32_t* cu = nullptr, int64_t total = 0) {
+                  const int32_t* cu = nullptr, int64_t total = 0, const void* ctx = nullptr,
+                  int64_t ctx_bytes = 0) {
     if (B < 0 || T < 0 || H < 0 || total < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
@@ -460,6 +461,16 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
         if (overlaps(outs[i], out_bytes[i], cu, bc)) return GDR2_ERR_ALIAS;
     }
     if (chunked && in_dtype != GDR2_BF16) return GDR2_ERR_UNSUPPORTED;
+    // from a training forward's context: big enough, and no output inside it
+    size_t need_ctx = 0;
+    if (ctx || ctx_bytes) {
+        if (!has_tokens) need_ctx = 0;
+        else need_ctx = chunked_context_bytes(B, cu ? 0 : T, H, cu != nullptr, cu ? total : 0);
+        if ((need_ctx > 0 && !ctx) || ctx_bytes < 0 || static_cast<uint64_t>(ctx_bytes) < need_ctx) return GDR2_ERR_ARG;
+        if (ctx && !aligned16(ctx)) return GDR2_ERR_ALIGN;
+        for (int i = 0; i < 7; ++i)
+            if (overlaps(outs[i], out_bytes[i], ctx, need_ctx)) return GDR2_ERR_ALIAS;
+    }
     int* err = nullptr;
     int st = device_setup(&err);
     if (st != GDR2_OK) return st;
@@ -473,10 +484,13 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
     BackwardArgs a{q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                    B, cu ? 0 : T, H, dk, dv, in_dtype, reinterpret_cast<const int*>(cu), cu ? total : 0};
     void* ws = nullptr;
-    const size_t wsb = chunked ? backward_chunked_workspace_bytes(B, a.T, H, cu != nullptr, a.total)
+    const size_t wsb = ctx ? backward_from_context_workspace_bytes(B, a.T, H, cu != nullptr, a.total)
+                     : chunked ? backward_chunked_workspace_bytes(B, a.T, H, cu != nullptr, a.total)
                                : backward_workspace_bytes(B, a.T, H, dk, dv, cu != nullptr, a.total);
     if ((st = ws_alloc(&ws, wsb, stream)) != GDR2_OK) return st;
-    int rc = chunked ? launch_backward_chunked(a, ws, stream, err) : launch_backward(a, ws, stream);
+    int rc = ctx       ? launch_backward_from_context(a, ctx, ws, stream, err)
+             : chunked ? launch_backward_chunked(a, ws, stream, err)
+                       : launch_backward(a, ws, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GDR2_OK) rc = GDR2_ERR_CUDA;
     return rc;
 }
@@ -520,6 +534,78 @@ extern "C" int gdr2_backward_chunked_varlen(const void* q, const void* k, const 
     if (N < 0 || total_T < 0) return GDR2_ERR_ARG;
     return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
                          N, 0, H, dk, dv, in_dtype, stream, true, N > 0 ? cu_seqlens : nullptr, total_T);
+}
+
+extern "C" int64_t gdr2_train_context_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv) {
+    if (B < 0 || T < 0 || H < 0) return GDR2_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
+    int64_t rows = 0, bh = 0;
+    if (!mul_ok(B, T, &rows) || !mul_ok(rows, H, &rows) || !mul_ok(B, H, &bh) || rows >= (1ll << 40))
+        return GDR2_ERR_SHAPE;
+    return rows == 0 ? 0 : static_cast<int64_t>(chunked_context_bytes(B, T, H));
+}
+
+extern "C" int gdr2_forward_train(const void* q, const void* k, const void* v,
+                                  const void* b, const void* w, const void* log_decay,
+                                  const float* S0, void* o, float* S_T, void* ctx, int64_t ctx_bytes,
+                                  int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                  int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (B < 0 || T < 0 || H < 0 || ctx_bytes < 0) return GDR2_ERR_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
+    if (in_dtype != GDR2_BF16) return GDR2_ERR_UNSUPPORTED;
+    int64_t rows = 0, bh = 0, nk = 0, nv = 0, ns = 0;
+    if (!mul_ok(B, T, &rows) || !mul_ok(rows, H, &rows) || !mul_ok(B, H, &bh) || !mul_ok(rows, dk, &nk) ||
+        !mul_ok(rows, dv, &nv) || !mul_ok(bh, dk * dv, &ns) || nk > INT64_MAX / 8 || ns > INT64_MAX / 8 ||
+        bh >= 0x7fffffffLL)
+        return GDR2_ERR_SHAPE;
+    const bool has_tokens = rows > 0;
+    if (has_tokens && (!q || !k || !v || !b || !w || !log_decay || !o)) return GDR2_ERR_ARG;
+    for (const void* p : {q, k, v, b, w, log_decay, (const void*)S0, (const void*)o, (const void*)S_T,
+                          (const void*)ctx})
+        if (p && !aligned16(p)) return GDR2_ERR_ALIGN;
+    const size_t need = has_tokens ? chunked_context_bytes(B, T, H) : 0;
+    if ((need > 0 && !ctx) || static_cast<uint64_t>(ctx_bytes) < need) return GDR2_ERR_ARG;
+    const size_t bk = (size_t)nk * 2, bv = (size_t)nv * 2, bs = (size_t)ns * 4;
+    const size_t bo = (size_t)nv * (out_dtype == GDR2_F32 ? 4 : 2);
+    const void* ins[7] = {q, k, b, log_decay, v, w, S0};
+    const size_t in_bytes[7] = {bk, bk, bk, bk, bv, bv, bs};
+    for (int i = 0; i < 7; ++i) {
+        if (has_tokens && overlaps(o, bo, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
+        if (i < 6 && overlaps(S_T, bs, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
+        if (overlaps(ctx, need, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
+    }
+    if (S_T && S0 && S_T != S0 && overlaps(S_T, bs, S0, bs)) return GDR2_ERR_ALIAS;
+    if ((has_tokens && overlaps(o, bo, S_T, bs)) || overlaps(ctx, need, o, has_tokens ? bo : 0) ||
+        overlaps(ctx, need, S_T, bs))
+        return GDR2_ERR_ALIAS;
+    int* err = nullptr;
+    int st = device_setup(&err);
+    if (st != GDR2_OK) return st;
+    if (bh == 0) return GDR2_OK;
+    if (!has_tokens) {   // no tokens: S_T = S0 (or zeros), nothing to keep
+        if (!S_T) return GDR2_OK;
+        const cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
+                                              : cudaMemcpyAsync(S_T, S0, bs, cudaMemcpyDeviceToDevice, stream))
+                                 : cudaMemsetAsync(S_T, 0, bs, stream);
+        return e == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+    }
+    BackwardArgs a{q, k, v, b, w, log_decay, S0, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                   nullptr, nullptr, B, T, H, dk, dv, in_dtype};
+    return launch_forward_train(a, o, out_dtype, S_T, ctx, stream, err);
+}
+
+extern "C" int gdr2_backward_from_context(const void* q, const void* k, const void* v,
+                                          const void* b, const void* w, const void* log_decay,
+                                          const float* S0, const float* d_o, const float* d_S_T,
+                                          const void* ctx, int64_t ctx_bytes,
+                                          float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                          float* d_log_decay, float* d_S0,
+                                          int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                          int in_dtype, cudaStream_t stream) {
+    if (!ctx && ctx_bytes == 0 && B > 0 && T > 0 && H > 0) return GDR2_ERR_ARG;
+    return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                         B, T, H, dk, dv, in_dtype, stream, true, nullptr, 0, ctx, ctx_bytes);
 }
 
 extern "C" int gdr2_backward_chunked(const void* q, const void* k, const void* v,

@@ -1054,12 +1054,13 @@ int cgrad_prefetch_stride() {
 }
 
 // Chunks of the call (packed sequences: an upper bound, every sequence adding at most
-// one partial chunk) and the workspace regions, in order: forward slots, backward
-// records, start states (the chain's cached states), end-state gradients, the
-// recomputed forward's o, and (packed) the first global chunk of each sequence.
+// one partial chunk) and the workspace regions, in order: the context that the forward
+// part leaves for the backward part (forward slots, backward records, start states --
+// the chain's cached states -- and, packed, the first global chunk of each sequence),
+// then the end-state gradients and the recomputed forward's o.
 struct ChunkedLayout {
     int64_t chunks, n_cache;
-    size_t slots, wy, sc, dsn, o, cb, total;
+    size_t slots, wy, sc, cb, ctx, dsn, o, total;
 };
 ChunkedLayout chunked_layout(int64_t B, int64_t T, int64_t H, bool packed, int64_t total_rows) {
     auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -1071,55 +1072,61 @@ ChunkedLayout chunked_layout(int64_t B, int64_t T, int64_t H, bool packed, int64
     l.slots = r256(items * kSlot2Bytes);
     l.wy = r256(items * kWyBytes);
     l.sc = r256((packed ? items : static_cast<size_t>(B * H * l.n_cache)) * 16384 * 4);
+    l.cb = packed ? r256(static_cast<size_t>(B + 1) * 4) : 0;
+    l.ctx = l.slots + l.wy + l.sc + l.cb;
     l.dsn = r256(items * 16384 * 4);
     l.o = r256(static_cast<size_t>(rows * H) * 128 * 2);
-    l.cb = packed ? r256(static_cast<size_t>(B + 1) * 4) : 0;
-    l.total = l.slots + l.wy + l.sc + l.dsn + l.o + l.cb;
+    l.total = l.ctx + l.dsn + l.o;
     return l;
 }
-}  // namespace
 
-size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed, int64_t total) {
-    return chunked_layout(B, T, H, packed, total).total;
+struct ChunkedCtx {
+    uint8_t* slots;
+    uint8_t* wy;
+    float* Sc;
+    int* cb;
+};
+ChunkedCtx chunked_ctx(uint8_t* base, const ChunkedLayout& l, bool packed) {
+    return ChunkedCtx{base, base + l.slots, reinterpret_cast<float*>(base + l.slots + l.wy),
+                      packed ? reinterpret_cast<int*>(base + l.slots + l.wy + l.sc) : nullptr};
 }
 
-int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err) {
+// bf16 inputs, head sizes in {32, 64, 128} (below 128 on channels zero-padded to 128,
+// as in the forward), at least one token; the grid limits of the kernels.
+int chunked_check(const BackwardArgs& a, const ChunkedLayout& l) {
     const bool packed = a.cu != nullptr;
-    // head sizes below 128 run on channels zero-padded to 128, as in the forward
     auto dim_ok = [](int64_t d) { return d == 32 || d == 64 || d == 128; };
     if (a.in_dtype != GDR2_BF16 || !dim_ok(a.dk) || !dim_ok(a.dv) || (packed ? a.total <= 0 : a.T <= 0))
         return GDR2_ERR_UNSUPPORTED;
-    const ChunkedLayout l = chunked_layout(a.B, a.T, a.H, packed, a.total);
-    const int64_t chunks = l.chunks, items = chunks * a.H, n_cache = l.n_cache;
-    const int64_t nch = packed ? 0 : (a.T + kC - 1) / kC;
-    if (items >= (1ll << 31) || a.B * a.H >= 65536ll * 32768ll || (packed && a.total >= (1ll << 31)))
+    if (l.chunks * a.H >= (1ll << 31) || a.B * a.H >= 65536ll * 32768ll || (packed && a.total >= (1ll << 31)))
         return GDR2_ERR_SHAPE;
-    uint8_t* p = static_cast<uint8_t*>(ws);
-    uint8_t* slots = p;
-    p += l.slots;
-    uint8_t* wy = p;
-    p += l.wy;
-    float* Sc = reinterpret_cast<float*>(p);
-    p += l.sc;
-    float* dsn = reinterpret_cast<float*>(p);
-    p += l.dsn;
-    void* o_scratch = p;
-    p += l.o;
-    int* cb = packed ? reinterpret_cast<int*>(p) : nullptr;
+    return GDR2_OK;
+}
 
-    // forward: every chunk's maps and backward record, and its start state (the chain's
-    // cached state after each chunk)
-    ForwardArgs f{a.q, a.k, a.v, a.b, a.w, a.g, a.S0, o_scratch, nullptr, a.B, packed ? 0 : a.T, a.H, a.dk, a.dv,
-                  a.cu, packed ? a.total : a.B * a.T, GDR2_BF16, GDR2_BF16};
-    if (packed || n_cache > 0) {
-        f.S_cache = Sc;
+// The forward part: every chunk's maps and backward record, and its start state (the
+// chain's cached state after each chunk) into the context; o (out_dtype) and S_T (or
+// null) as gdr2_forward writes them.
+int chunked_forward_part(const BackwardArgs& a, const ChunkedLayout& l, const ChunkedCtx& c, void* o, int out_dtype,
+                         float* S_T, cudaStream_t stream, int* err) {
+    const bool packed = a.cu != nullptr;
+    ForwardArgs f{a.q, a.k, a.v, a.b, a.w, a.g, a.S0, o, S_T, a.B, packed ? 0 : a.T, a.H, a.dk, a.dv,
+                  a.cu, packed ? a.total : a.B * a.T, GDR2_BF16, out_dtype};
+    if (packed || l.n_cache > 0) {
+        f.S_cache = c.Sc;
         f.cache_chunks = 1;
     }
-    int rc = packed ? launch_chunk_base(a.cu, a.B, a.total, cb, stream) : GDR2_OK;
-    if (rc == GDR2_OK) rc = launch_prep2(f, slots, cb, chunks, stream, err, 0, 0, wy);
-    if (rc == GDR2_OK) rc = launch_chain(f, slots, cb, stream, err);
-    if (rc != GDR2_OK) return rc;
+    int rc = packed ? launch_chunk_base(a.cu, a.B, a.total, c.cb, stream) : GDR2_OK;
+    if (rc == GDR2_OK) rc = launch_prep2(f, c.slots, c.cb, l.chunks, stream, err, 0, 0, c.wy);
+    if (rc == GDR2_OK) rc = launch_chain(f, c.slots, c.cb, stream, err);
+    return rc;
+}
 
+// The backward part, from the context: dS from the last chunk to the first (end-state
+// gradients into dsn), then every chunk's token gradients.
+int chunked_backward_part(const BackwardArgs& a, const ChunkedLayout& l, const ChunkedCtx& c, float* dsn,
+                          cudaStream_t stream, int* err) {
+    const bool packed = a.cu != nullptr;
+    const int64_t items = l.chunks * a.H, nch = packed ? 0 : (a.T + kC - 1) / kC;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -1133,24 +1140,71 @@ int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream
                                             static_cast<int>(cgr::kSmemAlloc));
     });
     if (attr_err != cudaSuccess) return GDR2_ERR_CUDA;
-    rch::Params rp{slots, a.dST, a.dO, dsn, a.d_S0, err, static_cast<int>(a.T), static_cast<int>(a.H),
-                   static_cast<int>(nch), kWaitCycles, a.cu, cb, static_cast<int>(packed ? a.total : 0),
+    rch::Params rp{c.slots, a.dST, a.dO, dsn, a.d_S0, err, static_cast<int>(a.T), static_cast<int>(a.H),
+                   static_cast<int>(nch), kWaitCycles, a.cu, c.cb, static_cast<int>(packed ? a.total : 0),
                    static_cast<int>(a.dk), static_cast<int>(a.dv)};
     rch::rchain_kernel<<<dim3(static_cast<unsigned>(a.B * a.H), 2), rch::kThreads, rch::kSmemAlloc, stream>>>(rp);
     if (cudaPeekAtLastError() != cudaSuccess) return GDR2_ERR_CUDA;
-    cgr::Params gp{wy, Sc, a.S0, dsn, a.dO,
+    cgr::Params gp{c.wy, c.Sc, a.S0, dsn, a.dO,
                    static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
                    static_cast<const __nv_bfloat16*>(a.b), static_cast<const __nv_bfloat16*>(a.g),
                    static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.w),
                    a.d_q, a.d_k, a.d_b, a.d_g, a.d_v, a.d_w,
-                   static_cast<int>(a.T), static_cast<int>(a.H), static_cast<int>(nch), static_cast<int>(n_cache), err,
-                   a.cu, cb, static_cast<int>(a.B), static_cast<int>(packed ? a.total : 0),
+                   static_cast<int>(a.T), static_cast<int>(a.H), static_cast<int>(nch), static_cast<int>(l.n_cache), err,
+                   a.cu, c.cb, static_cast<int>(a.B), static_cast<int>(packed ? a.total : 0),
                    static_cast<int>(items), cgrad_prefetch_stride(), static_cast<int>(a.dk), static_cast<int>(a.dv)};
     if (a.dk == 128 && a.dv == 128)
         cgr::cgrad_kernel<false><<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
     else
         cgr::cgrad_kernel<true><<<static_cast<unsigned>(items), cgr::kThreads, cgr::kSmemAlloc, stream>>>(gp);
     return cudaPeekAtLastError() == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
+}
+}  // namespace
+
+size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed, int64_t total) {
+    return chunked_layout(B, T, H, packed, total).total;
+}
+
+size_t chunked_context_bytes(int64_t B, int64_t T, int64_t H, bool packed, int64_t total) {
+    return chunked_layout(B, T, H, packed, total).ctx;
+}
+
+int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err) {
+    const bool packed = a.cu != nullptr;
+    const ChunkedLayout l = chunked_layout(a.B, a.T, a.H, packed, a.total);
+    int rc = chunked_check(a, l);
+    if (rc != GDR2_OK) return rc;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const ChunkedCtx c = chunked_ctx(base, l, packed);
+    float* dsn = reinterpret_cast<float*>(base + l.ctx);
+    void* o_scratch = base + l.ctx + l.dsn;
+    rc = chunked_forward_part(a, l, c, o_scratch, GDR2_BF16, nullptr, stream, err);
+    if (rc == GDR2_OK) rc = chunked_backward_part(a, l, c, dsn, stream, err);
+    return rc;
+}
+
+int launch_forward_train(const BackwardArgs& a, void* o, int out_dtype, float* S_T, void* ctx, cudaStream_t stream,
+                         int* err) {
+    const bool packed = a.cu != nullptr;
+    const ChunkedLayout l = chunked_layout(a.B, a.T, a.H, packed, a.total);
+    const int rc = chunked_check(a, l);
+    if (rc != GDR2_OK) return rc;
+    return chunked_forward_part(a, l, chunked_ctx(static_cast<uint8_t*>(ctx), l, packed), o, out_dtype, S_T, stream,
+                                err);
+}
+
+size_t backward_from_context_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed, int64_t total) {
+    return chunked_layout(B, T, H, packed, total).dsn;
+}
+
+int launch_backward_from_context(const BackwardArgs& a, const void* ctx, void* ws, cudaStream_t stream, int* err) {
+    const bool packed = a.cu != nullptr;
+    const ChunkedLayout l = chunked_layout(a.B, a.T, a.H, packed, a.total);
+    const int rc = chunked_check(a, l);
+    if (rc != GDR2_OK) return rc;
+    // the kernels only read the context
+    const ChunkedCtx c = chunked_ctx(static_cast<uint8_t*>(const_cast<void*>(ctx)), l, packed);
+    return chunked_backward_part(a, l, c, static_cast<float*>(ws), stream, err);
 }
 
 }  // namespace gdr2

@@ -106,6 +106,13 @@ int launch_backward(const BackwardArgs& a, void* ws, cudaStream_t stream);
 // token gradients (gdr2_bwd_chunk.cu).
 size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed = false, int64_t total = 0);
 int launch_backward_chunked(const BackwardArgs& a, void* ws, cudaStream_t stream, int* err);
+// The chunked backward in two halves around a context kept by the caller: the forward
+// part (writing o and S_T as gdr2_forward does) and the backward part from it.
+size_t chunked_context_bytes(int64_t B, int64_t T, int64_t H, bool packed = false, int64_t total = 0);
+int launch_forward_train(const BackwardArgs& a, void* o, int out_dtype, float* S_T, void* ctx, cudaStream_t stream,
+                         int* err);
+size_t backward_from_context_workspace_bytes(int64_t B, int64_t T, int64_t H, bool packed = false, int64_t total = 0);
+int launch_backward_from_context(const BackwardArgs& a, const void* ctx, void* ws, cudaStream_t stream, int* err);
 
 // ---- chunked prefill in affine form (bf16 inputs) -----------------------------------
 // prep2 writes, for every 64-token chunk of every (sequence, head), the maps of the

@@ -374,6 +374,53 @@ int gdr2_backward_chunked(const void* q, const void* k, const void* v,
                           int in_dtype, cudaStream_t stream);
 
 /*
+ * Training with a kept context.  gdr2_backward_chunked recomputes the forward's
+ * per-chunk maps and states before its backward products.  A training step that
+ * runs the forward anyway can keep them instead: gdr2_forward_train is
+ * gdr2_forward that also writes, into a caller-owned device buffer `ctx`, every
+ * chunk's maps and backward record and its start state, and
+ * gdr2_backward_from_context takes the gradients from that context (the same
+ * kernels on the same values as gdr2_backward_chunked, so the same results bit
+ * for bit).  The trade is memory for time: the context holds, per (64-token
+ * chunk, head), 123,392 bytes of maps and records and a 64 KB fp32 state, 773 MB
+ * at B4 H16 T4096 d128.
+ *
+ * gdr2_train_context_bytes -- the bytes `ctx` must hold for a fixed-length call
+ * of these sizes (0 without tokens), or a negative status (GDR2_ERR_ARG,
+ * GDR2_ERR_SHAPE).
+ *
+ * gdr2_forward_train -- gdr2_forward's arguments and results (o in out_dtype,
+ * S_T or NULL) plus ctx (device, 16-byte aligned, ctx_bytes >= the size above,
+ * overlapping no input or output).  bf16 inputs, dk, dv in {32, 64, 128}
+ * (GDR2_ERR_UNSUPPORTED for fp32).  It always runs the one-pass chunked kernels
+ * (no sequence segments).  The context stays valid while the caller keeps the
+ * inputs unchanged.
+ *
+ * gdr2_backward_from_context -- gdr2_backward_chunked's arguments and results,
+ * plus the ctx (and its size) that gdr2_forward_train wrote for the same inputs
+ * and sizes.  Outputs may not overlap the context (GDR2_ERR_ALIAS); a NULL ctx
+ * with tokens is GDR2_ERR_ARG.  Workspace (the library's pool): the end-state
+ * gradients, 64 KB per (chunk, head).  What they compute is what
+ * gdr2_forward and gdr2_backward_chunked compute (the page's update equation,
+ * its chunkwise WY form and the chain rule through it); the two calls only split
+ * gdr2_backward_chunked where its forward recomputation ends.
+ */
+int64_t gdr2_train_context_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
+int gdr2_forward_train(const void* q, const void* k, const void* v,
+                       const void* b, const void* w, const void* log_decay,
+                       const float* S0, void* o, float* S_T, void* ctx, int64_t ctx_bytes,
+                       int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                       int in_dtype, int out_dtype, cudaStream_t stream);
+int gdr2_backward_from_context(const void* q, const void* k, const void* v,
+                               const void* b, const void* w, const void* log_decay,
+                               const float* S0, const float* d_o, const float* d_S_T,
+                               const void* ctx, int64_t ctx_bytes,
+                               float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                               float* d_log_decay, float* d_S0,
+                               int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                               int in_dtype, cudaStream_t stream);
+
+/*
  * gdr2_backward_chunked_varlen -- gdr2_backward_chunked over N packed sequences:
  * the gradients of gdr2_forward_varlen through the chunkwise WY form on tensor
  * cores, for bf16 inputs (dk, dv in {32, 64, 128}; GDR2_ERR_UNSUPPORTED for fp32).

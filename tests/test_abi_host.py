@@ -222,6 +222,51 @@ def test_backward_chunked_varlen_rejects_bad_args():
     assert call(gq=ctypes.c_void_p(BASE + 16 * GAP), dk=128, dv=128) == ALIAS   # d_q over cu_seqlens
 
 
+def test_train_context_bytes_by_hand_and_bad_sizes():
+    L = _lib.lib()
+    L.gdr2_train_context_bytes.restype = ctypes.c_int64
+    # one 64-token chunk of one head: the forward slot (74,240 B), the backward record
+    # (49,152 B) and one fp32 start state (65,536 B), each region rounded to 256 B
+    assert L.gdr2_train_context_bytes(1, 64, 1, 128, 128) == 74240 + 49152 + 65536
+    # a ragged second chunk adds a slot and a record but no cached state (the state after
+    # the last, partial chunk is never a start state)
+    assert L.gdr2_train_context_bytes(1, 65, 1, 128, 128) == 2 * 74240 + 2 * 49152 + 65536
+    assert L.gdr2_train_context_bytes(1, 0, 3, 128, 128) == 0
+    assert L.gdr2_train_context_bytes(-1, 64, 1, 128, 128) == ARG
+    assert L.gdr2_train_context_bytes(1, 64, 1, 48, 128) == SHAPE
+
+
+def test_forward_train_and_backward_from_context_reject_bad_args():
+    L = _lib.lib()
+    names = ["q", "k", "v", "b", "w", "g", "S0", "o", "ST", "ctx"]
+    p = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in enumerate(names)}
+
+    def fwd(ctx_bytes=1 << 30, dtype=1, **over):
+        q = dict(p)
+        q.update(over)
+        return L.gdr2_forward_train(*[q[n] for n in names], ctx_bytes, 1, 64, 2, 128, 128, dtype, 0, None)
+
+    assert fwd(ctx=None) == ARG
+    assert fwd(ctx_bytes=100) == ARG                              # smaller than the context
+    assert fwd(ctx=ctypes.c_void_p(BASE + 9 * GAP + 8)) == ALIGN
+    assert fwd(ctx=ctypes.c_void_p(BASE + 1 * GAP)) == ALIAS       # over k
+    assert fwd(ctx=ctypes.c_void_p(BASE + 7 * GAP)) == ALIAS       # over o
+    assert fwd(dtype=0) == UNSUP                                   # fp32 inputs
+    bnames = ["q", "k", "v", "b", "w", "g", "S0", "do", "dST", "ctx",
+              "gq", "gk", "gv", "gb", "gw", "gg", "gS0"]
+    bp = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in enumerate(bnames)}
+
+    def bwd(ctx_bytes=1 << 30, **over):
+        q = dict(bp)
+        q.update(over)
+        a = [q[n] for n in bnames]
+        return L.gdr2_backward_from_context(*a[:10], ctx_bytes, *a[10:], 1, 64, 2, 128, 128, 1, None)
+
+    assert bwd(ctx=None, ctx_bytes=0) == ARG
+    assert bwd(ctx_bytes=100) == ARG
+    assert bwd(gq=ctypes.c_void_p(BASE + 9 * GAP)) == ALIAS       # d_q over the context
+
+
 def test_cached_rejects_bad_args():
     L = _lib.lib()
 
