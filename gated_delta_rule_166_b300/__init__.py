@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     gdr2_backward_chunked,
     gdr2_backward_chunked_varlen,
     gdr2_backward_from_context,
+    gdr2_backward_from_context_varlen,
     gdr2_backward_varlen,
     gdr2_decode_step,
     gdr2_device_status,
@@ -24,6 +25,7 @@ from ._lib import (  # noqa: F401
     gdr2_forward_cached,
     gdr2_forward_noalloc,
     gdr2_forward_train,
+    gdr2_forward_train_varlen,
     gdr2_forward_varlen,
     gdr2_release_workspace,
     gdr2_set_wait_limit,
@@ -44,5 +46,7 @@ backward_varlen = gdr2_backward_varlen
 backward_chunked_varlen = gdr2_backward_chunked_varlen
 forward_train = gdr2_forward_train
 backward_from_context = gdr2_backward_from_context
+forward_train_varlen = gdr2_forward_train_varlen
+backward_from_context_varlen = gdr2_backward_from_context_varlen
 apply_varlen = gdr2_apply_varlen
 sparse_write = gdr2_sparse_write

@@ -66,6 +66,12 @@ def lib():
         L.gdr2_forward_train.restype = ci
         L.gdr2_backward_from_context.argtypes = [vp] * 10 + [i64] + [vp] * 7 + [i64] * 5 + [ci, vp]
         L.gdr2_backward_from_context.restype = ci
+        L.gdr2_train_context_bytes_varlen.argtypes = [i64] * 5
+        L.gdr2_train_context_bytes_varlen.restype = i64
+        L.gdr2_forward_train_varlen.argtypes = [vp] * 11 + [i64] * 6 + [ci, ci, vp]
+        L.gdr2_forward_train_varlen.restype = ci
+        L.gdr2_backward_from_context_varlen.argtypes = [vp] * 11 + [i64] + [vp] * 7 + [i64] * 5 + [ci, vp]
+        L.gdr2_backward_from_context_varlen.restype = ci
         L.gdr2_backward_chunked.argtypes = [vp] * 16 + [i64] * 5 + [ci, vp]
         L.gdr2_backward_chunked.restype = ci
         L.gdr2_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, ci, vp]
@@ -379,7 +385,60 @@ def gdr2_backward_chunked_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, 
                             d_S_T, want_dS0, stream)
 
 
-def _backward_varlen(fn, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0, stream):
+def gdr2_forward_train_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, out_dtype=torch.float32,
+                              ctx=None, stream=None):
+    """gdr2_forward_varlen that keeps the per-chunk context for
+    gdr2_backward_from_context_varlen (bf16 inputs; the packed form of
+    gdr2_forward_train).  Returns ``(o, S_T, ctx)``."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q and v must be [total_T, H, d]")
+    total, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype, dev = q.dtype, q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr2_forward_train_varlen runs on CUDA tensors only")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, d in (("k", k, dk), ("b", b, dk), ("log_decay", log_decay, dk),
+                       ("v", v, dv), ("w", w, dv)):
+        _check_tokens(name, t, (total, H, d), dtype, dev)
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D tensor of N + 1 offsets")
+    _check_tokens("cu_seqlens", cu_seqlens, cu_seqlens.shape, torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    if S0 is not None:
+        _check_tokens("S0", S0, (N, H, dk, dv), torch.float32, dev)
+    if out_dtype not in _DTYPES:
+        raise ValueError(f"unsupported out_dtype {out_dtype}")
+    o = torch.empty((total, H, dv), dtype=out_dtype, device=dev)
+    S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    need = int(lib().gdr2_train_context_bytes_varlen(N, total, H, dk, dv))
+    if need < 0:
+        raise GDR2Error(need, "gdr2_train_context_bytes_varlen")
+    if ctx is None:
+        ctx = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif ctx.device != dev or ctx.dtype != torch.uint8 or not ctx.is_contiguous() or ctx.numel() < need:
+        raise ValueError(f"ctx must be a contiguous uint8 tensor of at least {need} bytes on {dev}")
+    with torch.cuda.device(dev):
+        st = lib().gdr2_forward_train_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
+                                             _ptr(o), _ptr(S_T), _ptr(cu_seqlens), _ptr(ctx), ctx.numel(), N, total,
+                                             H, dk, dv, _DTYPES[dtype], _DTYPES[out_dtype],
+                                             ctypes.c_void_p(_stream_handle(stream)))
+    if st != 0:
+        raise GDR2Error(st, "gdr2_forward_train_varlen")
+    return o, S_T, ctx
+
+
+def gdr2_backward_from_context_varlen(ctx, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T=None, *,
+                                      want_dS0: bool = True, stream=None):
+    """gdr2_backward_chunked_varlen from the context gdr2_forward_train_varlen kept."""
+    if ctx.dtype != torch.uint8 or not ctx.is_contiguous() or ctx.device != q.device:
+        raise ValueError("ctx must be the contiguous uint8 context of gdr2_forward_train_varlen")
+    return _backward_varlen("gdr2_backward_from_context_varlen", q, k, v, b, w, log_decay, cu_seqlens, S0, d_o,
+                            d_S_T, want_dS0, stream, ctx=ctx)
+
+
+def _backward_varlen(fn, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0, stream, ctx=None):
     if q.dim() != 3 or v.dim() != 3:
         raise ValueError("q and v must be [total_T, H, d]")
     total, H, dk = q.shape
@@ -404,10 +463,14 @@ def _backward_varlen(fn, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, w
     gq, gk, gb, gg = (torch.zeros((total, H, dk), **f32) for _ in range(4))
     gv, gw = (torch.zeros((total, H, dv), **f32) for _ in range(2))
     gS0 = torch.empty((N, H, dk, dv), **f32) if want_dS0 else None
+    if ctx is None:
+        ptrs = (_ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw), _ptr(gg), _ptr(gS0), _ptr(cu_seqlens))
+    else:   # the context entry takes cu_seqlens and the context before the outputs
+        ptrs = (_ptr(cu_seqlens), _ptr(ctx), ctx.numel(), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
+                _ptr(gg), _ptr(gS0))
     with torch.cuda.device(dev):
         st = getattr(lib(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(w), _ptr(log_decay), _ptr(S0),
-                                _ptr(d_o), _ptr(d_S_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw),
-                                _ptr(gg), _ptr(gS0), _ptr(cu_seqlens), N, total, H, dk, dv,
+                                _ptr(d_o), _ptr(d_S_T), *ptrs, N, total, H, dk, dv,
                                 _DTYPES[dtype], ctypes.c_void_p(_stream_handle(stream)))
     if st != 0:
         raise GDR2Error(st, fn)
@@ -463,36 +526,49 @@ def gdr2_apply(q, k, v, b, w, log_decay, S0=None, *, chunked_backward: bool = Fa
 class GatedDeltaRule2Varlen(torch.autograd.Function):
     """(o, S_T) = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0) as
     a differentiable operation over packed sequences: the forward pass is
-    gdr2_forward_varlen (fp32 o), the backward pass gdr2_backward_varlen, or
-    gdr2_backward_chunked_varlen when ``chunked`` is set and the inputs are bf16.  Gradients are fp32 and cast to each input's dtype;
-    cu_seqlens gets none."""
+    gdr2_forward_varlen (fp32 o), the backward pass gdr2_backward_varlen, or the
+    chunked tensor-core backward when ``chunked`` is set and the inputs are bf16
+    (from the context gdr2_forward_train_varlen keeps with ``keep_context``, else
+    recomputed by gdr2_backward_chunked_varlen).  Gradients are fp32 and cast to
+    each input's dtype; cu_seqlens gets none."""
 
     @staticmethod
-    def forward(ctx, q, k, v, b, w, log_decay, cu_seqlens, S0=None, chunked=False):
-        o, S_T = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0)
-        ctx.save_for_backward(q, k, v, b, w, log_decay, cu_seqlens, S0)
+    def forward(ctx, q, k, v, b, w, log_decay, cu_seqlens, S0=None, chunked=False, keep_context=True):
         ctx.has_s0 = S0 is not None
         ctx.chunked = bool(chunked) and q.dtype == torch.bfloat16
+        kept = None
+        if ctx.chunked and keep_context and q.shape[0] * q.shape[1] > 0 and cu_seqlens.numel() > 1:
+            o, S_T, kept = gdr2_forward_train_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0)
+        else:
+            o, S_T = gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0)
+        ctx.save_for_backward(q, k, v, b, w, log_decay, cu_seqlens, S0, kept)
         return o, S_T
 
     @staticmethod
     def backward(ctx, d_o, d_S_T):
-        q, k, v, b, w, log_decay, cu_seqlens, S0 = ctx.saved_tensors
+        q, k, v, b, w, log_decay, cu_seqlens, S0, kept = ctx.saved_tensors
         d_o = torch.zeros(v.shape, dtype=torch.float32, device=q.device) if d_o is None \
             else d_o.float().contiguous()
         d_S_T = None if d_S_T is None else d_S_T.float().contiguous()
-        fn = gdr2_backward_chunked_varlen if ctx.chunked else gdr2_backward_varlen
-        g = fn(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
+        if kept is not None:
+            g = gdr2_backward_from_context_varlen(kept, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T,
+                                                  want_dS0=ctx.has_s0)
+        else:
+            fn = gdr2_backward_chunked_varlen if ctx.chunked else gdr2_backward_varlen
+            g = fn(q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, want_dS0=ctx.has_s0)
         cast = [g[i].to(t.dtype) for i, t in enumerate((q, k, v, b, w, log_decay))]
-        return (*cast, None, g[6] if ctx.has_s0 else None, None)
+        return (*cast, None, g[6] if ctx.has_s0 else None, None, None)
 
 
-def gdr2_apply_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, chunked_backward: bool = False):
+def gdr2_apply_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, chunked_backward: bool = False,
+                      keep_context: bool = True):
     """Differentiable prefill over packed sequences: ``(o, S_T)`` of
     gdr2_forward_varlen with gradients through gdr2_backward_varlen (exact fp32),
-    or through gdr2_backward_chunked_varlen (tensor cores; bf16 inputs, else the
-    exact path) when ``chunked_backward`` is set."""
-    return GatedDeltaRule2Varlen.apply(q, k, v, b, w, log_decay, cu_seqlens, S0, chunked_backward)
+    or through the chunked tensor-core backward (bf16 inputs, else the exact path)
+    when ``chunked_backward`` is set: from a context the forward keeps
+    (gdr2_forward_train_varlen, the default) or recomputed
+    (gdr2_backward_chunked_varlen, ``keep_context=False``)."""
+    return GatedDeltaRule2Varlen.apply(q, k, v, b, w, log_decay, cu_seqlens, S0, chunked_backward, keep_context)
 
 
 def gdr2_decode_step(q, k, v, b, w, log_decay, S, *, o=None, out_dtype=torch.float32,

@@ -545,17 +545,28 @@ extern "C" int64_t gdr2_train_context_bytes(int64_t B, int64_t T, int64_t H, int
     return rows == 0 ? 0 : static_cast<int64_t>(chunked_context_bytes(B, T, H));
 }
 
-extern "C" int gdr2_forward_train(const void* q, const void* k, const void* v,
-                                  const void* b, const void* w, const void* log_decay,
-                                  const float* S0, void* o, float* S_T, void* ctx, int64_t ctx_bytes,
-                                  int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
-                                  int in_dtype, int out_dtype, cudaStream_t stream) {
-    if (B < 0 || T < 0 || H < 0 || ctx_bytes < 0) return GDR2_ERR_ARG;
+extern "C" int64_t gdr2_train_context_bytes_varlen(int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv) {
+    if (N < 0 || total_T < 0 || H < 0) return GDR2_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
+    int64_t rows = 0, bh = 0;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL || !mul_ok(total_T, H, &rows) || !mul_ok(N, H, &bh))
+        return GDR2_ERR_SHAPE;
+    return rows == 0 || N == 0 ? 0 : static_cast<int64_t>(chunked_context_bytes(N, 0, H, true, total_T));
+}
+
+namespace {
+
+// gdr2_forward_train and its packed form (cu: device offsets [N + 1] over `total` rows).
+int forward_train_impl(const void* q, const void* k, const void* v, const void* b, const void* w,
+                       const void* log_decay, const float* S0, void* o, float* S_T, void* ctx, int64_t ctx_bytes,
+                       const int32_t* cu, int64_t N, int64_t T, int64_t total, int64_t H, int64_t dk, int64_t dv,
+                       int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (N < 0 || T < 0 || total < 0 || H < 0 || ctx_bytes < 0) return GDR2_ERR_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return GDR2_ERR_UNSUPPORTED;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDR2_ERR_SHAPE;
     if (in_dtype != GDR2_BF16) return GDR2_ERR_UNSUPPORTED;
-    int64_t rows = 0, bh = 0, nk = 0, nv = 0, ns = 0;
-    if (!mul_ok(B, T, &rows) || !mul_ok(rows, H, &rows) || !mul_ok(B, H, &bh) || !mul_ok(rows, dk, &nk) ||
+    int64_t rows = cu ? total : 0, bh = 0, nk = 0, nv = 0, ns = 0;
+    if ((!cu && !mul_ok(N, T, &rows)) || !mul_ok(rows, H, &rows) || !mul_ok(N, H, &bh) || !mul_ok(rows, dk, &nk) ||
         !mul_ok(rows, dv, &nv) || !mul_ok(bh, dk * dv, &ns) || nk > INT64_MAX / 8 || ns > INT64_MAX / 8 ||
         bh >= 0x7fffffffLL)
         return GDR2_ERR_SHAPE;
@@ -564,15 +575,16 @@ extern "C" int gdr2_forward_train(const void* q, const void* k, const void* v,
     for (const void* p : {q, k, v, b, w, log_decay, (const void*)S0, (const void*)o, (const void*)S_T,
                           (const void*)ctx})
         if (p && !aligned16(p)) return GDR2_ERR_ALIGN;
-    const size_t need = has_tokens ? chunked_context_bytes(B, T, H) : 0;
+    if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u)) return GDR2_ERR_ALIGN;
+    const size_t need = has_tokens && bh > 0 ? chunked_context_bytes(N, cu ? 0 : T, H, cu != nullptr, total) : 0;
     if ((need > 0 && !ctx) || static_cast<uint64_t>(ctx_bytes) < need) return GDR2_ERR_ARG;
     const size_t bk = (size_t)nk * 2, bv = (size_t)nv * 2, bs = (size_t)ns * 4;
-    const size_t bo = (size_t)nv * (out_dtype == GDR2_F32 ? 4 : 2);
-    const void* ins[7] = {q, k, b, log_decay, v, w, S0};
-    const size_t in_bytes[7] = {bk, bk, bk, bk, bv, bv, bs};
-    for (int i = 0; i < 7; ++i) {
+    const size_t bo = (size_t)nv * (out_dtype == GDR2_F32 ? 4 : 2), bc = cu ? static_cast<size_t>(N + 1) * 4 : 0;
+    const void* ins[8] = {q, k, b, log_decay, v, w, S0, cu};
+    const size_t in_bytes[8] = {bk, bk, bk, bk, bv, bv, bs, bc};
+    for (int i = 0; i < 8; ++i) {
         if (has_tokens && overlaps(o, bo, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
-        if (i < 6 && overlaps(S_T, bs, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
+        if (i != 6 && overlaps(S_T, bs, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
         if (overlaps(ctx, need, ins[i], in_bytes[i])) return GDR2_ERR_ALIAS;
     }
     if (S_T && S0 && S_T != S0 && overlaps(S_T, bs, S0, bs)) return GDR2_ERR_ALIAS;
@@ -591,8 +603,49 @@ extern "C" int gdr2_forward_train(const void* q, const void* k, const void* v,
         return e == cudaSuccess ? GDR2_OK : GDR2_ERR_CUDA;
     }
     BackwardArgs a{q, k, v, b, w, log_decay, S0, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                   nullptr, nullptr, B, T, H, dk, dv, in_dtype};
+                   nullptr, nullptr, N, cu ? 0 : T, H, dk, dv, in_dtype, reinterpret_cast<const int*>(cu),
+                   cu ? total : 0};
     return launch_forward_train(a, o, out_dtype, S_T, ctx, stream, err);
+}
+
+}  // namespace
+
+extern "C" int gdr2_forward_train(const void* q, const void* k, const void* v,
+                                  const void* b, const void* w, const void* log_decay,
+                                  const float* S0, void* o, float* S_T, void* ctx, int64_t ctx_bytes,
+                                  int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                  int in_dtype, int out_dtype, cudaStream_t stream) {
+    return forward_train_impl(q, k, v, b, w, log_decay, S0, o, S_T, ctx, ctx_bytes, nullptr, B, T, 0, H, dk, dv,
+                              in_dtype, out_dtype, stream);
+}
+
+extern "C" int gdr2_forward_train_varlen(const void* q, const void* k, const void* v,
+                                         const void* b, const void* w, const void* log_decay,
+                                         const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
+                                         void* ctx, int64_t ctx_bytes,
+                                         int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                         int in_dtype, int out_dtype, cudaStream_t stream) {
+    if (N > 0 && !cu_seqlens) return GDR2_ERR_ARG;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
+    return forward_train_impl(q, k, v, b, w, log_decay, S0, o, S_T, ctx, ctx_bytes, N > 0 ? cu_seqlens : nullptr, N,
+                              0, total_T, H, dk, dv, in_dtype, out_dtype, stream);
+}
+
+extern "C" int gdr2_backward_from_context_varlen(const void* q, const void* k, const void* v,
+                                                 const void* b, const void* w, const void* log_decay,
+                                                 const float* S0, const float* d_o, const float* d_S_T,
+                                                 const int32_t* cu_seqlens, const void* ctx, int64_t ctx_bytes,
+                                                 float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                                 float* d_log_decay, float* d_S0,
+                                                 int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                                 int in_dtype, cudaStream_t stream) {
+    if (N > 0 && !cu_seqlens) return GDR2_ERR_ARG;
+    if (N >= 0x7fffffffLL || total_T >= 0x7fffffffLL) return GDR2_ERR_SHAPE;
+    if (N < 0 || total_T < 0) return GDR2_ERR_ARG;
+    if (!ctx && ctx_bytes == 0 && N > 0 && total_T > 0 && H > 0) return GDR2_ERR_ARG;
+    return backward_impl(q, k, v, b, w, log_decay, S0, d_o, d_S_T, d_q, d_k, d_v, d_b, d_w, d_log_decay, d_S0,
+                         N, 0, H, dk, dv, in_dtype, stream, true, N > 0 ? cu_seqlens : nullptr, total_T, ctx,
+                         ctx_bytes);
 }
 
 extern "C" int gdr2_backward_from_context(const void* q, const void* k, const void* v,

@@ -421,6 +421,30 @@ int gdr2_backward_from_context(const void* q, const void* k, const void* v,
                                int in_dtype, cudaStream_t stream);
 
 /*
+ * The same over N packed sequences (layouts, offsets and row ownership as in
+ * gdr2_forward_varlen and gdr2_backward_varlen; the context also keeps each
+ * sequence's first chunk).  The context holds ceil(total_T / 64) + N chunks (an
+ * upper bound: each sequence adds at most one partial chunk), 0 bytes without
+ * tokens or sequences.  The backward's gradients are gdr2_backward_chunked_varlen's
+ * bit for bit.
+ */
+int64_t gdr2_train_context_bytes_varlen(int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv);
+int gdr2_forward_train_varlen(const void* q, const void* k, const void* v,
+                              const void* b, const void* w, const void* log_decay,
+                              const float* S0, void* o, float* S_T, const int32_t* cu_seqlens,
+                              void* ctx, int64_t ctx_bytes,
+                              int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                              int in_dtype, int out_dtype, cudaStream_t stream);
+int gdr2_backward_from_context_varlen(const void* q, const void* k, const void* v,
+                                      const void* b, const void* w, const void* log_decay,
+                                      const float* S0, const float* d_o, const float* d_S_T,
+                                      const int32_t* cu_seqlens, const void* ctx, int64_t ctx_bytes,
+                                      float* d_q, float* d_k, float* d_v, float* d_b, float* d_w,
+                                      float* d_log_decay, float* d_S0,
+                                      int64_t N, int64_t total_T, int64_t H, int64_t dk, int64_t dv,
+                                      int in_dtype, cudaStream_t stream);
+
+/*
  * gdr2_backward_chunked_varlen -- gdr2_backward_chunked over N packed sequences:
  * the gradients of gdr2_forward_varlen through the chunkwise WY form on tensor
  * cores, for bf16 inputs (dk, dv in {32, 64, 128}; GDR2_ERR_UNSUPPORTED for fp32).

@@ -267,6 +267,28 @@ def test_forward_train_and_backward_from_context_reject_bad_args():
     assert bwd(gq=ctypes.c_void_p(BASE + 9 * GAP)) == ALIAS       # d_q over the context
 
 
+def test_packed_train_context_bytes_and_bad_args():
+    L = _lib.lib()
+    L.gdr2_train_context_bytes_varlen.restype = ctypes.c_int64
+    # 2 sequences over 65 rows: ceil(65 / 64) + 2 = 4 chunk slots, records and states per
+    # head, plus the sequences' first chunks (3 ints, one 256-byte region)
+    assert L.gdr2_train_context_bytes_varlen(2, 65, 1, 128, 128) == 4 * (74240 + 49152 + 65536) + 256
+    assert L.gdr2_train_context_bytes_varlen(0, 65, 1, 128, 128) == 0
+    assert L.gdr2_train_context_bytes_varlen(-1, 65, 1, 128, 128) == ARG
+    names = ["q", "k", "v", "b", "w", "g", "S0", "o", "ST", "cu", "ctx"]
+    p = {n: ctypes.c_void_p(BASE + i * GAP) for i, n in enumerate(names)}
+
+    def fwd(**over):
+        q = dict(p)
+        q.update(over)
+        return L.gdr2_forward_train_varlen(*[q[n] for n in names], 1 << 30, 2, 100, 2, 128, 128, 1, 0, None)
+
+    assert fwd(cu=None) == ARG
+    assert fwd(ctx=None) == ARG
+    assert fwd(cu=ctypes.c_void_p(BASE + 9 * GAP + 2)) == ALIGN
+    assert fwd(ctx=ctypes.c_void_p(BASE + 9 * GAP)) == ALIAS      # context over cu_seqlens
+
+
 def test_cached_rejects_bad_args():
     L = _lib.lib()
 

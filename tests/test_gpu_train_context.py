@@ -99,3 +99,39 @@ def test_autograd_keep_context_and_recompute_agree_and_match_oracle():
         bar = 2e-2 + float(np.abs(rf).max()) * 2.0 ** -8 / float(np.sqrt(np.mean(rf * rf)))
         e = err_over_rms(g.float().cpu().numpy(), rf)
         assert e <= bar, f"{n}: {e:.3e} (bar {bar:.3g})"
+
+
+def test_packed_train_context_reproduces_varlen_forward_and_chunked_backward():
+    """Packed sequences (an empty one and ragged chunks among them): the training
+    forward's o and S_T are gdr2_forward_varlen's and the gradients from its context
+    gdr2_backward_chunked_varlen's, bit for bit; gdr2_apply_varlen with the default
+    kept context gives the recomputing path's gradients."""
+    lengths = [130, 0, 64, 257, 1]
+    H = 2
+    seqs = [make_prefill_inputs(1, L, H, 128, 64, dtype=torch.bfloat16, seed=1250 + 7 * i, s0_std=0.3,
+                                decay_regime="slow") for i, L in enumerate(lengths)]
+    toks = [torch.cat([s.tensors()[i][0] for s in seqs]).contiguous().cuda() for i in range(6)]
+    S0 = torch.stack([s.S0[0] for s in seqs]).contiguous().cuda()
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device="cuda")
+    total = int(cu[-1])
+    o_f, S_f = gdr2.forward_varlen(*toks, cu, S0)
+    o_t, S_t, kept = gdr2.forward_train_varlen(*toks, cu, S0)
+    torch.cuda.synchronize()
+    assert torch.equal(o_t, o_f) and torch.equal(S_t, S_f)
+    gen = torch.Generator().manual_seed(1260)
+    d_o = torch.randn(total, H, 64, generator=gen).cuda()
+    d_ST = torch.randn(len(lengths), H, 128, 64, generator=gen).cuda()
+    ref = gdr2.backward_chunked_varlen(*toks, cu, S0, d_o, d_ST)
+    got = gdr2.backward_from_context_varlen(kept, *toks, cu, S0, d_o, d_ST)
+    torch.cuda.synchronize()
+    assert gdr2.gdr2_device_status() == 0
+    for n, g, r in zip(NAMES, got, ref):
+        assert torch.equal(g, r), n
+    grads = []
+    for keep in (True, False):
+        leaves = [t.clone().requires_grad_(True) for t in toks] + [S0.clone().requires_grad_(True)]
+        o, S_T = gdr2.gdr2_apply_varlen(*leaves[:6], cu, leaves[6], chunked_backward=True, keep_context=keep)
+        ((o * d_o).sum() + (S_T * d_ST).sum()).backward()
+        grads.append([leaf.grad for leaf in leaves])
+    for n, a, b in zip(NAMES, *grads):
+        assert torch.equal(a, b), n
