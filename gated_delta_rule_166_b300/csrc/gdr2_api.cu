@@ -464,8 +464,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* b, co
     // from a training forward's context: big enough, and no output inside it
     size_t need_ctx = 0;
     if (ctx || ctx_bytes) {
-        if (!has_tokens) need_ctx = 0;
-        else need_ctx = chunked_context_bytes(B, cu ? 0 : T, H, cu != nullptr, cu ? total : 0);
+        if (has_tokens && bh > 0) need_ctx = chunked_context_bytes(B, cu ? 0 : T, H, cu != nullptr, cu ? total : 0);
         if ((need_ctx > 0 && !ctx) || ctx_bytes < 0 || static_cast<uint64_t>(ctx_bytes) < need_ctx) return GDR2_ERR_ARG;
         if (ctx && !aligned16(ctx)) return GDR2_ERR_ALIGN;
         for (int i = 0; i < 7; ++i)
