@@ -294,41 +294,60 @@ sparse_tile_kernel(const SparseParams p) {
         const int buf = ch & 1;
         if (ch + 1 < nchunks) fetch(ch + 1, raw);   // in flight during this chunk
         const int t0 = ch * TC, nt = min(TC, p.T - t0);
+        // A token's slot offsets, key-side values and u come from the staging buffer,
+        // not the memory tile, so the next token's are loaded while this one reduces;
+        // only the gathers wait for the previous token's scatter.
+        struct Staged {
+            uint32_t ad[KPL];   // shared-memory address of each selected slot's column c
+            float4 a[KPL];      // {e^g, b k, k, q} of each selected slot
+            float u;            // w v of column c
+        };
+        auto stage_of = [&](int tt) {
+            Staged x;
+            x.u = lds_f(a_su + 4u * static_cast<uint32_t>((buf * TC + tt) * W + c));
+            const uint32_t so = a_soff + 4u * static_cast<uint32_t>((buf * TC + tt) * KPAD + g);
+            const uint32_t sv = a_sval + 16u * static_cast<uint32_t>((buf * TC + tt) * KPAD + g);
+#pragma unroll
+            for (int i = 0; i < KPL; ++i) {
+                x.ad[i] = a_tile + 4u * static_cast<uint32_t>(lds_i(so + 4u * G * i) + c);
+                x.a[i] = lds_f4(sv + 16u * G * i);
+            }
+            return x;
+        };
+        Staged cur = stage_of(0);   // nt >= 1: chunks hold at least one token
 #pragma unroll 1
         for (int tt = 0; tt < nt; ++tt) {
             const int t = t0 + tt;
-            const float u = lds_f(a_su + 4u * static_cast<uint32_t>((buf * TC + tt) * W + c));
-            const uint32_t so = a_soff + 4u * static_cast<uint32_t>((buf * TC + tt) * KPAD + g);
-            const uint32_t sv = a_sval + 16u * static_cast<uint32_t>((buf * TC + tt) * KPAD + g);
-            uint32_t ad[KPL];
+            const uint32_t (&ad)[KPL] = cur.ad;
+            const float4 (&a)[KPL] = cur.a;
+            const float u = cur.u;
             float sd[KPL];
-            float4 a[KPL];
 #pragma unroll
-            for (int i = 0; i < KPL; ++i) {
-                ad[i] = a_tile + 4u * static_cast<uint32_t>(lds_i(so + 4u * G * i) + c);
-                a[i] = lds_f4(sv + 16u * G * i);
-                sd[i] = lds_f(ad[i]);
-            }
-            float x = 0.f;
+            for (int i = 0; i < KPL; ++i) sd[i] = lds_f(ad[i]);
+            const Staged nxt = stage_of(tt + 1 < nt ? tt + 1 : tt);   // the last token re-reads its own
+            float x0 = 0.f, x1 = 0.f;   // two accumulators: half the dependent chain
 #pragma unroll
             for (int i = 0; i < KPL; ++i) {
                 sd[i] *= a[i].x;
-                x = fmaf(a[i].y, sd[i], x);
+                if (i & 1) x1 = fmaf(a[i].y, sd[i], x1); else x0 = fmaf(a[i].y, sd[i], x0);
             }
+            float x = x0 + x1;
 #pragma unroll
             for (int off = W; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
             const float d = u - x;
-            float ov = 0.f;
+            float o0 = 0.f, o1 = 0.f;
 #pragma unroll
             for (int i = 0; i < KPL; ++i) {
                 const float nv = fmaf(a[i].z, d, sd[i]);
                 sts_f(ad[i], nv);
-                ov = fmaf(a[i].w, nv, ov);
+                if (i & 1) o1 = fmaf(a[i].w, nv, o1); else o0 = fmaf(a[i].w, nv, o0);
             }
+            float ov = o0 + o1;
 #pragma unroll
             for (int off = W; off < 32; off <<= 1) ov += __shfl_xor_sync(0xffffffffu, ov, off);
             if (g == 0) oo[uoff(t)] = from_f32<Tout>(ov);
             __syncwarp();   // this token's scatter is visible to the next token's gathers
+            cur = nxt;
         }
         if (ch + 1 < nchunks) {
             put(ch + 1, buf ^ 1, raw);
