@@ -630,12 +630,14 @@ def oracle_sample(x, pairs):
 
 def cpu_baseline(x, budget_s=15.0):
     """Time the oracle on a bounded sample: whole sequences of as many heads
-    as fit ~budget_s, taken from batch 0 first."""
+    as fit ~budget_s, taken from batch 0 first; also its one-thread times for one
+    head of this workload and for the tiny fp32 workload."""
     B, T, H, _ = x.q.shape
     probe = [(0, 0)]
-    dt, th, _ = oracle_sample(x, probe)
-    rate1 = th / max(dt, 1e-6)                       # token-heads/s on one thread
+    dt1, th, _ = oracle_sample(x, probe)            # one head, one thread
+    rate1 = th / max(dt1, 1e-6)                     # token-heads/s on one thread
     import oracle
+    from gated_delta_rule_166_b300.inputs import make_workload
 
     cores = oracle.default_threads()
     n_pairs = max(1, min(B * H, int(budget_s * rate1 * cores / T)))
@@ -644,9 +646,14 @@ def cpu_baseline(x, budget_s=15.0):
         n_rows = n_pairs // H
         pairs = [(bi, h) for bi in range(n_rows) for h in range(H)]
     dt, tokheads, threads = oracle_sample(x, pairs)
+    tiny = make_workload("tiny_f32")
+    t0 = time.perf_counter()
+    oracle.forward(*tiny.tensors(), tiny.S0, nthreads=1)
+    dt_tiny = time.perf_counter() - t0
     return {"value": (tokheads / H) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(pairs)} of {B * H} (batch, head) sequences x {T} tokens "
-                      f"({tokheads} token-heads, {dt:.1f} s)"}
+                      f"({tokheads} token-heads, {dt:.1f} s)",
+            "one_thread_s": {f"{WORKLOAD}_one_head": dt1, "tiny_f32": dt_tiny}}
 
 
 # --------------------------------------------------------------------------

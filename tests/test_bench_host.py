@@ -57,3 +57,19 @@ def test_packed_offsets_partition_the_rows():
     assert all(L > 0 for L in lengths) and sum(lengths) == 16384
     assert any(L % 64 for L in lengths)
     assert b.packed_offsets(16384, 8).tolist() == cu.tolist()
+
+
+def test_cpu_baseline_reports_one_thread_times():
+    """The oracle baseline on a small synthetic problem (CPU only): its record
+    carries the sampled rate and the one-thread times of one head and of the tiny
+    fp32 workload."""
+    import torch
+
+    from gated_delta_rule_166_b300.inputs import make_prefill_inputs
+
+    b = load_bench()
+    x = make_prefill_inputs(1, 64, 2, 32, 32, dtype=torch.bfloat16, seed=3)
+    rec = b.cpu_baseline(x, budget_s=0.01)
+    assert rec["kind"] == "oracle" and rec["value"] > 0 and rec["cores"] >= 1
+    assert set(rec["one_thread_s"]) == {"gdn2_layer_T4096_one_head", "tiny_f32"}
+    assert all(v > 0 for v in rec["one_thread_s"].values())
