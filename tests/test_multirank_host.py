@@ -42,7 +42,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_max_time_and_independent_batches():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of a multi-threaded process
         out = mgr.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
