@@ -50,8 +50,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-# The B300's nominal HBM3e bandwidth (the roofline's spec figure; the measured copy
-# rate in MEASURED_PEAKS.json is the one the fractions are graded against)
+# The B300's nominal HBM3e bandwidth: the roofline's spec figure, reported beside the
+# fraction of the measured copy rate (the "peak" of every roofline record)
 SPEC_HBM_GBS = 8000.0
 METRIC = "GDR-2 fwd tokens/sec at H16 d128 T4K (1×B300); % of roofline; decode GB/s"
 WORKLOAD = "gdn2_layer_T4096"
