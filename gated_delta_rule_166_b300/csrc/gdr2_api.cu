@@ -815,4 +815,4 @@ extern "C" const char* gdr2_status_string(int status) {
     }
 }
 
-extern "C" int gdr2_version(void) { return 100; }
+extern "C" int gdr2_version(void) { return 200; }

@@ -555,7 +555,10 @@ int64_t gdr2_set_wait_limit(int64_t cycles);
 /* Human-readable name of a gdr2_status value (static storage). */
 const char* gdr2_status_string(int status);
 
-/* Library ABI version: major * 10000 + minor * 100 + patch. */
+/* Library ABI version: major * 10000 + minor * 100 + patch.  0.2.0 added the
+ * backward over packed sequences (both paths), segments for packed sequences,
+ * the training forward and backward around a kept context, and the chunked
+ * backward for head sizes below 128; every 0.1.0 entry point is unchanged. */
 int gdr2_version(void);
 
 #ifdef __cplusplus
