@@ -460,8 +460,13 @@ def _backward_varlen(fn, q, k, v, b, w, log_decay, cu_seqlens, S0, d_o, d_S_T, w
         if t is not None:
             _check_tokens(name, t, (N, H, dk, dv), torch.float32, dev)
     f32 = dict(dtype=torch.float32, device=dev)
-    gq, gk, gb, gg = (torch.zeros((total, H, dk), **f32) for _ in range(4))
-    gv, gw = (torch.zeros((total, H, dv), **f32) for _ in range(2))
+    # rows outside every sequence are left to the caller: zero, as their gradients
+    # are.  One fill over one buffer of the six (disjoint, 16-byte-aligned views)
+    # runs at full bandwidth; six small fills do not.
+    nk, nv = total * H * dk, total * H * dv
+    flat = torch.zeros(4 * nk + 2 * nv, **f32)
+    gq, gk, gb, gg = (flat[i * nk:(i + 1) * nk].view(total, H, dk) for i in range(4))
+    gv, gw = (flat[4 * nk + i * nv:4 * nk + (i + 1) * nv].view(total, H, dv) for i in range(2))
     gS0 = torch.empty((N, H, dk, dv), **f32) if want_dS0 else None
     if ctx is None:
         ptrs = (_ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gw), _ptr(gg), _ptr(gS0), _ptr(cu_seqlens))
