@@ -211,7 +211,9 @@ def gdr2_forward_varlen(q, k, v, b, w, log_decay, cu_seqlens, S0=None, *, o=None
     cu_seqlens[n+1] - 1); S0: [N, H, dk, dv] fp32 or None.  ``segments`` (None:
     the library's choice) fixes the segments per sequence of the chunk-parallel
     scan (gdr2_forward_varlen_segmented).  Returns
-    ``(o [total_T, H, dv], S_T [N, H, dk, dv])``."""
+    ``(o [total_T, H, dv], S_T [N, H, dk, dv])``.  Offsets from 0 to total_T
+    cover every row; rows that other offsets leave to no sequence are not
+    written in ``o`` (a new ``o`` holds whatever its memory held there)."""
     if q.dim() != 3 or v.dim() != 3:
         raise ValueError("q and v must be [total_T, H, d]")
     total, H, dk = q.shape
